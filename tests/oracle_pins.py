@@ -1,0 +1,308 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix,
+never against a retyping of the oracle's own formula.
+
+Each pin is a plain function of the oracle module (so the mutation test can
+run the same pins against deliberately broken builds of the oracle).  They
+raise AssertionError when the oracle is wrong.
+
+  * closed forms of softmax attention: one position returns V; identical keys,
+    a zero query or a zero scale return the mean of V; two positions give the
+    logistic weights; constant V returns the constant; one dominant logit
+    returns that position's V;
+  * an independent library routine (torch fp64 softmax) on tiny inputs;
+  * gather special cases that reduce to array reshapes (identity block
+    table, request rows), plus invariance under relabelling physical blocks,
+    plus contiguous == paged with bs = S and a one-entry table
+    ("Leveraging Low-Level CUDA APIs for vAttention's Dynamic Memory",
+    section 5.2.3; "Running Out of Cache", block tables);
+  * GQA: repeating each KV head G times (plain MHA) gives the same result;
+  * append then gather finds the new token at the last position; untouched
+    bytes stay untouched; copy on write makes dst equal src.
+"""
+import math
+
+import numpy as np
+import torch
+
+D = 128
+
+
+def _bf16(x):
+    """float array -> uint16 bf16 bits (round to nearest even via torch)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _val(u16):
+    """uint16 bf16 bits -> float64 values (exact)."""
+    return (np.asarray(u16, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _rand_bf16(rng, shape, scale=1.0):
+    return _bf16(rng.standard_normal(shape) * scale)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def pin_single_position_returns_v(orc):
+    rng = np.random.default_rng(1)
+    for _ in range(5):
+        q, K, V = _rand_bf16(rng, D), _rand_bf16(rng, (1, D)), _rand_bf16(rng, (1, D))
+        o = orc.attend(q, K, V, 1 / math.sqrt(D))
+        assert np.array_equal(o, _val(V[0])), "ctx=1 must return v_0 exactly"
+
+
+def pin_identical_keys_give_mean(orc):
+    rng = np.random.default_rng(2)
+    k = _rand_bf16(rng, D)
+    K = np.tile(k, (37, 1))
+    V = _rand_bf16(rng, (37, D))
+    q = _rand_bf16(rng, D, 3.0)
+    o = orc.attend(q, K, V, 1 / math.sqrt(D))
+    assert np.allclose(o, _val(V).mean(axis=0), rtol=0, atol=1e-12)
+
+
+def pin_zero_query_or_scale_gives_mean(orc):
+    rng = np.random.default_rng(3)
+    K, V = _rand_bf16(rng, (23, D)), _rand_bf16(rng, (23, D))
+    mean = _val(V).mean(axis=0)
+    o = orc.attend(np.zeros(D, np.uint16), K, V, 0.7)
+    assert np.allclose(o, mean, rtol=0, atol=1e-12)
+    o = orc.attend(_rand_bf16(rng, D), K, V, 0.0)
+    assert np.allclose(o, mean, rtol=0, atol=1e-12)
+
+
+def pin_two_positions_logistic(orc):
+    rng = np.random.default_rng(4)
+    for trial in range(6):
+        q, K, V = _rand_bf16(rng, D), _rand_bf16(rng, (2, D)), _rand_bf16(rng, (2, D))
+        scale = [0.088, 0.5, 1.0, 0.01, 0.3, 2.0][trial]
+        qv, Kv, Vv = _val(q), _val(K), _val(V)
+        delta = scale * (math.fsum(qv * Kv[0]) - math.fsum(qv * Kv[1]))
+        w0 = 1.0 / (1.0 + math.exp(-delta))   # logistic sigma(s0 - s1)
+        w1 = 1.0 / (1.0 + math.exp(delta))
+        expect = w0 * Vv[0] + w1 * Vv[1]
+        o = orc.attend(q, K, V, scale)
+        assert np.allclose(o, expect, rtol=1e-12, atol=1e-12)
+
+
+def pin_constant_v(orc):
+    rng = np.random.default_rng(5)
+    K = _rand_bf16(rng, (50, D))
+    row = _rand_bf16(rng, D)
+    V = np.tile(row, (50, 1))
+    o = orc.attend(_rand_bf16(rng, D), K, V, 1 / math.sqrt(D))
+    assert np.allclose(o, _val(row), rtol=1e-14, atol=1e-14)
+
+
+def pin_dominant_logit(orc):
+    rng = np.random.default_rng(6)
+    ctx = 100
+    K = np.zeros((ctx, D), np.float64)
+    for j in range(ctx):
+        K[j, j % D] = 1.0
+    V = _rand_bf16(rng, (ctx, D))
+    for star in (0, 41, 99):
+        q = np.zeros(D)
+        q[star % D] = 1000.0
+        o = orc.attend(_bf16(q), _bf16(K), V, 1 / math.sqrt(D))
+        assert np.allclose(o, _val(V[star]), rtol=1e-12, atol=1e-12)
+
+
+def pin_empty_context_gives_zeros(orc):
+    o = orc.attend(np.ones(D, np.uint16), np.zeros((0, D), np.uint16),
+                   np.zeros((0, D), np.uint16), 1.0)
+    assert np.array_equal(o, np.zeros(D))
+
+
+def pin_library_softmax(orc):
+    """torch fp64 softmax(q K^T * scale) V on random tiny inputs."""
+    rng = np.random.default_rng(7)
+    for ctx in (1, 2, 3, 17, 64, 130):
+        q, K, V = _rand_bf16(rng, D, 2.0), _rand_bf16(rng, (ctx, D)), _rand_bf16(rng, (ctx, D))
+        scale = 1 / math.sqrt(D)
+        qt, Kt, Vt = (torch.from_numpy(_val(a)) for a in (q, K, V))
+        ref = (torch.softmax((Kt @ qt) * scale, dim=0) @ Vt).numpy()
+        o = orc.attend(q, K, V, scale)
+        assert np.allclose(o, ref, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------- gathers
+
+def _pool(rng, nb, hkv, bs):
+    return _rand_bf16(rng, (nb, hkv, bs, D))
+
+
+def pin_identity_table_is_reshape(orc):
+    """With block table [0, 1, 2, ...] the logical rows of KV head h are the
+    pool's head-h rows read in order (a reshape)."""
+    rng = np.random.default_rng(8)
+    for bs in (1, 5, 16):
+        nb, hkv = 9, 3
+        cache = _pool(rng, nb, hkv, bs)
+        table = np.arange(nb, dtype=np.int32)
+        for ctx in (1, bs, nb * bs - 2, nb * bs):
+            for h in range(hkv):
+                got = orc.gather_paged(cache, table, ctx, bs, h)
+                assert np.array_equal(got, cache[:, h].reshape(-1, D)[:ctx])
+
+
+def pin_request_rows_are_subtensors(orc):
+    rng = np.random.default_rng(9)
+    buf = _rand_bf16(rng, (4, 2, 33, D))
+    for r in range(4):
+        for h in range(2):
+            got = orc.gather_contig(buf, r, 20, h)
+            assert np.array_equal(got, buf[r, h, :20])
+
+
+def pin_block_relabel_invariance(orc):
+    """Relabelling physical blocks (moving storage and table together) leaves
+    the decode output bit-identical."""
+    rng = np.random.default_rng(10)
+    hq, hkv, bs, nb = 8, 2, 16, 40
+    ctx = np.array([1, 16, 17, 100, 33], np.int32)
+    need = (ctx + bs - 1) // bs
+    table = np.zeros((len(ctx), need.max()), np.int32)
+    ids = rng.permutation(nb)
+    pos = 0
+    for i, n in enumerate(need):
+        table[i, :n] = ids[pos:pos + n]
+        pos += n
+    kc, vc = _pool(rng, nb, hkv, bs), _pool(rng, nb, hkv, bs)
+    q = _rand_bf16(rng, (len(ctx), hq, D))
+    base = orc.paged_decode(q, kc, vc, table, ctx, 1 / math.sqrt(D))
+    perm = rng.permutation(nb)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[perm], vc2[perm] = kc, vc
+    out = orc.paged_decode(q, kc2, vc2, perm[table].astype(np.int32), ctx,
+                           1 / math.sqrt(D))
+    assert np.array_equal(out, base)
+    # and the output really depends on the table (guards a table-blind oracle)
+    shuffled = table.copy()
+    shuffled[3, :2] = shuffled[3, [1, 0]]
+    other = orc.paged_decode(q, kc, vc, shuffled, ctx, 1 / math.sqrt(D))
+    assert not np.array_equal(other[3], base[3])
+
+
+def pin_contig_equals_paged_with_bs_S(orc):
+    """[max_reqs, Hkv, S, D] read at reqId x S is the paged pool with bs = S
+    and the one-entry table [reqId]."""
+    rng = np.random.default_rng(11)
+    max_reqs, hkv, hq, S = 6, 2, 8, 48
+    kb, vb = _rand_bf16(rng, (max_reqs, hkv, S, D)), _rand_bf16(rng, (max_reqs, hkv, S, D))
+    req = np.array([4, 0, 5, 2], np.int32)
+    ctx = np.array([48, 1, 30, 0], np.int32)
+    q = _rand_bf16(rng, (4, hq, D))
+    a = orc.contig_decode(q, kb, vb, req, ctx, 0.1)
+    b = orc.paged_decode(q, kb, vb, req.reshape(-1, 1), ctx, 0.1)
+    assert np.array_equal(a, b)
+    assert np.array_equal(a[3], np.zeros((hq, D)))
+
+
+def pin_paged_equals_logical_attend(orc):
+    """Paged decode of one (sequence, head) equals attention over the rows the
+    identity-table reshape exposes (brute force on a contiguous copy)."""
+    rng = np.random.default_rng(12)
+    nb, hkv, hq, bs = 7, 1, 3, 4
+    kc, vc = _pool(rng, nb, hkv, bs), _pool(rng, nb, hkv, bs)
+    table = np.arange(nb, dtype=np.int32).reshape(1, -1)
+    ctx = np.array([25], np.int32)
+    q = _rand_bf16(rng, (1, hq, D))
+    out = orc.paged_decode(q, kc, vc, table, ctx, 0.2)
+    Kl, Vl = kc[:, 0].reshape(-1, D)[:25], vc[:, 0].reshape(-1, D)[:25]
+    for h in range(hq):
+        assert np.array_equal(out[0, h], orc.attend(q[0, h], Kl, Vl, 0.2))
+
+
+def pin_gqa_equals_repeated_mha(orc):
+    rng = np.random.default_rng(13)
+    hkv, G, bs, nb = 3, 4, 8, 30
+    hq = hkv * G
+    ctx = np.array([9, 40, 1], np.int32)
+    table = rng.permutation(nb)[:15].reshape(3, 5).astype(np.int32)
+    kc, vc = _pool(rng, nb, hkv, bs), _pool(rng, nb, hkv, bs)
+    q = _rand_bf16(rng, (3, hq, D))
+    gqa = orc.paged_decode(q, kc, vc, table, ctx, 0.09)
+    kr = np.ascontiguousarray(np.repeat(kc, G, axis=1))  # head h -> h // G
+    vr = np.ascontiguousarray(np.repeat(vc, G, axis=1))
+    mha = orc.paged_decode(q, kr, vr, table, ctx, 0.09)
+    assert np.array_equal(gqa, mha)
+
+
+def pin_threads_do_not_change_results(orc):
+    rng = np.random.default_rng(14)
+    kc, vc = _pool(rng, 20, 2, 16), _pool(rng, 20, 2, 16)
+    table = rng.permutation(20)[:12].reshape(3, 4).astype(np.int32)
+    ctx = np.array([64, 3, 50], np.int32)
+    q = _rand_bf16(rng, (3, 8, D))
+    a = orc.paged_decode(q, kc, vc, table, ctx, 0.1, nthreads=1)
+    b = orc.paged_decode(q, kc, vc, table, ctx, 0.1, nthreads=7)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ append and copy
+
+def pin_append_then_gather(orc):
+    """Observation-1: each step adds exactly one token.  After appending at the
+    slot of position ctx-1, the gather through the block table returns the new
+    row last, every earlier row unchanged, and no other byte of the pool moved."""
+    rng = np.random.default_rng(15)
+    hkv, bs, nb = 2, 16, 24
+    kc, vc = _pool(rng, nb, hkv, bs), _pool(rng, nb, hkv, bs)
+    table = rng.permutation(nb)[:12].reshape(3, 4).astype(np.int32)
+    ctx_pre = np.array([0, 16, 40], np.int64)
+    slots = np.array([table[i, p // bs] * bs + p % bs for i, p in enumerate(ctx_pre)],
+                     np.int64)
+    k_new, v_new = _rand_bf16(rng, (3, hkv, D)), _rand_bf16(rng, (3, hkv, D))
+    before_k = [[orc.gather_paged(kc, table[i], int(ctx_pre[i]), bs, h)
+                 for h in range(hkv)] for i in range(3)]
+    k0, v0 = kc.copy(), vc.copy()
+    orc.kv_append(slots, k_new, v_new, kc, vc)
+    for i in range(3):
+        c = int(ctx_pre[i]) + 1
+        for h in range(hkv):
+            gk = orc.gather_paged(kc, table[i], c, bs, h)
+            gv = orc.gather_paged(vc, table[i], c, bs, h)
+            assert np.array_equal(gk[-1], k_new[i, h])
+            assert np.array_equal(gv[-1], v_new[i, h])
+            assert np.array_equal(gk[:-1], before_k[i][h])
+    changed = np.count_nonzero(kc != k0) + np.count_nonzero(vc != v0)
+    assert changed <= 2 * 3 * hkv * D
+    # a padding slot (-1) writes nothing
+    k1 = kc.copy()
+    orc.kv_append(np.array([-1], np.int64), k_new[:1], v_new[:1], kc, vc)
+    assert np.array_equal(kc, k1)
+
+
+def pin_append_contig_positions(orc):
+    """In the contiguous layout slot reqId*S + pos puts the row at position pos
+    of request reqId's sub-tensor."""
+    rng = np.random.default_rng(16)
+    S, hkv = 12, 2
+    kb, vb = _rand_bf16(rng, (3, hkv, S, D)), _rand_bf16(rng, (3, hkv, S, D))
+    k_new, v_new = _rand_bf16(rng, (2, hkv, D)), _rand_bf16(rng, (2, hkv, D))
+    orc.kv_append(np.array([2 * S + 7, 0 * S + 11], np.int64), k_new, v_new, kb, vb)
+    for h in range(hkv):
+        assert np.array_equal(orc.gather_contig(kb, 2, 8, h)[7], k_new[0, h])
+        assert np.array_equal(orc.gather_contig(vb, 0, 12, h)[11], v_new[1, h])
+
+
+def pin_block_copy(orc):
+    rng = np.random.default_rng(17)
+    L, nb, hkv, bs = 3, 10, 2, 4
+    ks = [_pool(rng, nb, hkv, bs) for _ in range(L)]
+    vs = [_pool(rng, nb, hkv, bs) for _ in range(L)]
+    k0, v0 = [a.copy() for a in ks], [a.copy() for a in vs]
+    pairs = np.array([[3, 7], [0, 9], [5, 2]], np.int64)
+    orc.block_copy(pairs, ks, vs)
+    for l in range(L):
+        for src, dst in pairs:
+            assert np.array_equal(ks[l][dst], k0[l][src])
+            assert np.array_equal(vs[l][dst], v0[l][src])
+        untouched = [b for b in range(nb) if b not in pairs[:, 1]]
+        assert np.array_equal(ks[l][untouched], k0[l][untouched])
+        assert np.array_equal(vs[l][untouched], v0[l][untouched])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
