@@ -1,0 +1,550 @@
+"""Decode-step benchmark: KV append + paged decode attention over every layer
+of a Llama-3-8B-shaped decode batch (batch 64, context 1024, block_size 16,
+32 layers), through the C ABI on one GB300 per rank.
+
+One JSON line (rank 0):
+  value       decode tokens/s per layer, whole job (all ranks), inputs resident
+  e2e         the same metric with per-step inputs copied from pinned host
+              memory and the outputs read back inside the timed region
+  roofline    achieved HBM bandwidth of the paged attention call (main +
+              split-combine kernels) from CUDA events in the timed region,
+              against the measured copy bandwidth of this GPU model
+  cpu_baseline  the CPU fp64 oracle on a bounded sample of the same workload
+  legs        contiguous-layout attention on the same logical KV, the append
+              kernel alone, and a Yi-34B-shaped copy-on-write block copy
+
+--impl reference times the CPU oracle instead (the only reference there is).
+Multi-GPU (torchrun): every rank runs its own replica of the batch (weak
+scaling, no collective on the data path); the barrier and the max over ranks
+of the timed region use torch.distributed.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode-attn achieved HBM TB/s (% of GB300 8 TB/s); decode tokens/s/layer"
+UNIT = "tokens/s/layer"
+WORKLOADS = {
+    # name: (shape, batch, context, block_size, seed)
+    "llama3_8b_b64": (W.LLAMA3_8B, 64, 1024, 16, W.SEED_LLAMA),
+    "yi6b_b64": (W.YI_6B, 64, 1024, 16, W.SEED_YI6B),
+}
+for _b in W.LLAMA_SWEEP_BATCHES:
+    WORKLOADS["llama3_8b_b%d" % _b] = (W.LLAMA3_8B, _b, 1024, 16, W.SEED_LLAMA)
+DEFAULT_WORKLOAD = "llama3_8b_b64"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _describe(name):
+    shape, B, ctx, bs, _ = WORKLOADS[name]
+    return ("%s-shaped decode: batch %d, context %d, block_size %d, %d layers, "
+            "%d query / %d KV heads, head_dim %d"
+            % (shape.name, B, ctx, bs, shape.num_layers, shape.num_q_heads,
+               shape.num_kv_heads, shape.head_dim))
+
+
+def algorithmic_bytes(batch):
+    """Bytes one paged attention call must move: K and V of every attended
+    position, Q and O, the block-table entries read and the context lengths."""
+    s = batch.shape
+    ctx = batch.ctx.astype(np.int64)
+    kv = int(ctx.sum()) * s.num_kv_heads * s.head_dim * 2 * 2
+    qo = 2 * batch.B * s.num_q_heads * s.head_dim * 2
+    tables = int(((ctx + batch.block_size - 1) // batch.block_size).sum()) * 4
+    return kv + qo + tables + 4 * batch.B
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_245_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "paged_decode_%s.md" % name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != _source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class DeviceWorkload:
+    def __init__(self, name, dev, rank):
+        import paged_kv_cache_245_gb300 as pkv
+        self.pkv = pkv
+        shape, B, ctx, bs, seed = WORKLOADS[name]
+        self.name = name
+        self.shape = shape
+        self.batch = W.uniform_batch(shape, B, ctx, bs, seed=seed + 1000 * rank)
+        self.dev = dev
+        b = self.batch
+        self.layers = []
+        for l in range(shape.num_layers):
+            li = W.layer_inputs(b, l, device=dev, fast_cache=True)
+            self.layers.append(li)
+        self.tables = torch.as_tensor(b.block_tables, device=dev)
+        self.ctx = torch.as_tensor(b.ctx, device=dev)
+        self.slots = torch.as_tensor(b.slot_mapping, device=dev)
+        self.scale = W.default_scale(shape)
+        self.out = [torch.empty_like(li.q) for li in self.layers]
+        nbytes = pkv.decode_workspace_size(b.B, shape.num_q_heads, shape.num_kv_heads,
+                                           b.max_context)
+        self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        self.nsplit = pkv.decode_num_splits(b.B, shape.num_q_heads, shape.num_kv_heads,
+                                            b.max_context)
+
+    def launches_per_step(self):
+        return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0))
+
+    def layer(self, l, events=None):
+        li = self.layers[l]
+        self.pkv.kv_append(self.slots, li.k_new, li.v_new, li.k_cache, li.v_cache)
+        if events is not None:
+            events[0].record()
+        self.pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, self.tables, self.ctx,
+                                        self.batch.max_context, self.scale, out=self.out[l],
+                                        workspace=self.workspace)
+        if events is not None:
+            events[1].record()
+
+    def step(self, events=None):
+        for l in range(self.shape.num_layers):
+            self.layer(l, None if events is None else events[l])
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_gpu(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from __graft_entry__ import build
+    if rank == 0 or world == 1:
+        build()
+    _barrier(world)
+    wl = DeviceWorkload(args.workload, dev, rank)
+    nl = wl.shape.num_layers
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        wl.step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K decode steps, attention calls bracketed by events
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nl)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0.record(stream)
+    for k in range(args.steps):
+        wl.step(ev[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    clock_info = clocks.stop()
+    elapsed_ms = _max_over_ranks(t0.elapsed_time(t1), world, dev)
+    attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
+    attn_avg_ms = _max_over_ranks(float(np.mean(attn_ms)), world, dev)
+
+    B = wl.batch.B
+    ms_per_step = elapsed_ms / args.steps
+    value = world * B / (ms_per_step / 1e3 / nl)
+    alg = algorithmic_bytes(wl.batch)
+    peak, peak_kind = _peaks()
+    achieved_gbs = alg / (attn_avg_ms / 1e3) / 1e9
+
+    legs = {}
+    e2e = None
+    cpu = None
+    if rank == 0 and not args.skip_legs:
+        legs = measure_legs(wl, dev, args)
+    if not args.skip_e2e:
+        e2e = measure_e2e(wl, dev, args, world)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        cpu = cpu_baseline(wl, args)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _describe(args.workload), "global_batch": B * world,
+                   "seq_len": int(wl.batch.ctx.max()), "layers": nl,
+                   "block_size": wl.batch.block_size, "num_splits": wl.nsplit,
+                   "parallelism": "replicas (one batch per GPU, no collective)" if world > 1
+                   else "single GPU",
+                   "l2": "inputs larger than L2: %.1f GB of distinct K/V per step, "
+                         "%.0f MB per layer" % (nl * alg / 1e9, alg / 1e6),
+                   "step": "per layer: kv_append + paged_decode_attention (main + combine)"},
+        "hbm_tbs": round(achieved_gbs / 1e3, 4),
+        "hbm_pct_of_8tbs": round(100 * achieved_gbs / 8000.0, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
+                     "traffic": _profiled_traffic(args.workload),
+                     "kernel": "paged_decode_attention call (decode_attention_kernel + "
+                               "decode_combine_kernel)",
+                     "algorithmic_bytes_per_launch": alg,
+                     "avg_launch_us": round(attn_avg_ms * 1e3, 3),
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
+        "gpu_launches": wl.launches_per_step() * args.steps,
+        "clocks": clock_info,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if legs:
+        line["legs"] = legs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _time_calls(fn, iters, dev):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    torch.cuda.synchronize(dev)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / iters
+
+
+def measure_legs(wl, dev, args):
+    """Per-kernel figures beside the step: contiguous-layout attention over the
+    same logical K/V, the append alone, and a copy-on-write block copy."""
+    pkv = wl.pkv
+    b = wl.batch
+    nl = min(8, wl.shape.num_layers)   # 8 distinct layers: > 2 GB, far above L2
+    alg = algorithmic_bytes(b)
+    S = int(b.ctx.max())
+    bufs = []
+    for l in range(nl):
+        li = wl.layers[l]
+        bufs.append((W.paged_to_contig(li.k_cache, b, S), W.paged_to_contig(li.v_cache, b, S)))
+    req = torch.arange(b.B, dtype=torch.int32, device=dev)
+    it = {"i": 0}
+
+    def contig():
+        l = it["i"] % nl
+        it["i"] += 1
+        pkv.contig_decode_attention(wl.layers[l].q, bufs[l][0], bufs[l][1], req, wl.ctx,
+                                    b.max_context, wl.scale, out=wl.out[l],
+                                    workspace=wl.workspace)
+
+    def paged():
+        l = it["i"] % nl
+        it["i"] += 1
+        li = wl.layers[l]
+        pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, wl.tables, wl.ctx,
+                                   b.max_context, wl.scale, out=wl.out[l],
+                                   workspace=wl.workspace)
+
+    iters = max(20, args.steps // 4)
+    t_contig = _time_calls(contig, iters, dev)
+    t_paged = _time_calls(paged, iters, dev)
+    del bufs
+
+    def append():
+        l = it["i"] % wl.shape.num_layers
+        it["i"] += 1
+        li = wl.layers[l]
+        pkv.kv_append(wl.slots, li.k_new, li.v_new, li.k_cache, li.v_cache)
+
+    t_append = _time_calls(append, iters, dev)
+    append_bytes = 2 * 2 * b.B * wl.shape.num_kv_heads * wl.shape.head_dim * 2 + 8 * b.B
+
+    # Yi-34B-shaped copy on write: 96 block pairs x 60 layers of 32 KiB blocks
+    L, nb = 60, 192
+    g = torch.Generator(device=dev)
+    g.manual_seed(W.SEED_YI34B)
+    ks = [torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    vs = [torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    pairs = torch.stack([torch.arange(0, 96), torch.arange(96, 192)], 1).to(dev)
+    t_copy = _time_calls(lambda: pkv.block_copy(pairs, ks, vs), 20, dev)
+    copy_bytes = 2 * 96 * L * 2 * 8 * 16 * 128 * 2
+    del ks, vs
+    return {
+        "paged_attention_us": round(t_paged * 1e3, 3),
+        "contig_attention_us": round(t_contig * 1e3, 3),
+        "paged_over_contig_time": round(t_paged / t_contig, 4),
+        "contig_hbm_gbs": round(alg / (t_contig / 1e3) / 1e9, 1),
+        "kv_append_us": round(t_append * 1e3, 3),
+        "kv_append_gbs": round(append_bytes / (t_append / 1e3) / 1e9, 1),
+        "block_copy_us": round(t_copy * 1e3, 3),
+        "block_copy_gbs": round(copy_bytes / (t_copy / 1e3) / 1e9, 1),
+        "block_copy_shape": "96 pairs x 60 layers x (K,V) of 32 KiB blocks (read + write)",
+    }
+
+
+def measure_e2e(wl, dev, args, world):
+    """Each step copies its inputs (q, new k/v, slots, tables, context lengths
+    per layer) from pinned host memory, runs the step through the C ABI, and
+    reads every layer's output back to pinned host memory."""
+    nl = wl.shape.num_layers
+    host_in, dev_in, host_out = [], [], []
+    for l in range(nl):
+        li = wl.layers[l]
+        hi = [t.detach().to("cpu").pin_memory() for t in (li.q, li.k_new, li.v_new)]
+        host_in.append(hi)
+        dev_in.append([torch.empty_like(t) for t in (li.q, li.k_new, li.v_new)])
+        host_out.append(torch.empty(li.q.shape, dtype=li.q.dtype, pin_memory=True))
+    h_meta = [torch.as_tensor(a).pin_memory() for a in
+              (wl.batch.slot_mapping, wl.batch.block_tables, wl.batch.ctx)]
+    d_meta = [torch.empty_like(t, device=dev) for t in h_meta]
+    h2d = sum(t.numel() * t.element_size() for row in host_in for t in row)
+    h2d += nl * sum(t.numel() * t.element_size() for t in h_meta)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    pkv = wl.pkv
+    b = wl.batch
+
+    def step():
+        for l in range(nl):
+            for d, h in zip(d_meta, h_meta):
+                d.copy_(h, non_blocking=True)
+            q, kn, vn = dev_in[l]
+            for d, h in zip(dev_in[l], host_in[l]):
+                d.copy_(h, non_blocking=True)
+            li = wl.layers[l]
+            pkv.kv_append(d_meta[0], kn, vn, li.k_cache, li.v_cache)
+            pkv.paged_decode_attention(q, li.k_cache, li.v_cache, d_meta[1], d_meta[2],
+                                       b.max_context, wl.scale, out=wl.out[l],
+                                       workspace=wl.workspace)
+            host_out[l].copy_(wl.out[l], non_blocking=True)
+
+    iters = max(10, args.steps // 10)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        step()
+    c.record()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    ms = _max_over_ranks(a.elapsed_time(c) / iters, world, dev)
+    return {"value": round(world * b.B / (ms / 1e3 / nl), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 4), "steps": iters}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_layer_host(name, layer=0, rank=0):
+    shape, B, ctx, bs, seed = WORKLOADS[name]
+    b = W.uniform_batch(shape, B, ctx, bs, seed=seed + 1000 * rank)
+    li = W.layer_inputs(b, layer, device="cpu")
+    return b, {"q": W.to_u16(li.q), "k_new": W.to_u16(li.k_new), "v_new": W.to_u16(li.v_new),
+               "k": W.to_u16(li.k_cache).copy(), "v": W.to_u16(li.v_cache).copy()}
+
+
+def _oracle_step(oracle, b, h, scale, nthreads):
+    oracle.kv_append(b.slot_mapping, h["k_new"], h["v_new"], h["k"], h["v"])
+    oracle.paged_decode(h["q"], h["k"], h["v"], b.block_tables, b.ctx, scale, nthreads)
+
+
+def cpu_baseline(wl, args, budget_s=15.0):
+    """The oracle as it stands, on all host cores, on layers of the same
+    workload until about budget_s seconds of work."""
+    import oracle
+    cores = os.cpu_count() or 1
+    b, h = _oracle_layer_host(args.workload)
+    scale = W.default_scale(b.shape)
+    _oracle_step(oracle, b, h, scale, cores)       # warm
+    done, t_total = 0, 0.0
+    while t_total < budget_s and done < 64:
+        t = time.perf_counter()
+        _oracle_step(oracle, b, h, scale, cores)
+        t_total += time.perf_counter() - t
+        done += 1
+    return {"value": round(b.B * done / t_total, 2), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": "%d repetitions of one layer (append + attention, all %d sequences) of "
+                      "the same workload, fp64 C oracle, %d threads" % (done, b.B, cores)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from oracle.build_oracle import build as build_oracle
+    build_oracle()
+    cores = os.cpu_count() or 1
+    b, h = _oracle_layer_host(args.workload)
+    scale = W.default_scale(b.shape)
+    for _ in range(max(args.warmup, 0)):
+        _oracle_step(oracle, b, h, scale, cores)
+    steps = args.steps
+    t = time.perf_counter()
+    for _ in range(steps):
+        _oracle_step(oracle, b, h, scale, cores)
+    el = time.perf_counter() - t
+    value = b.B * steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * el / steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _describe(args.workload), "global_batch": b.B,
+                       "seq_len": int(b.ctx.max()), "layers_per_step": 1,
+                       "step": "one layer of the workload (append + attention, all sequences)"},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
+                             "kind": "oracle",
+                             "sample": "one layer per step, all %d sequences" % b.B},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--skip-legs", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        # CPU-only arm: rank 0 runs it; other ranks exit without work.
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        run_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * pkv.h -- C ABI of the paged / contiguous KV-cache decode library (sm_103a).
+ *
+ * Four operations make one decode step over a KV cache:
+ *   pkv_kv_append                 write each new token's K and V into its slot
+ *   pkv_paged_decode_attention    single-query attention through block tables
+ *   pkv_contig_decode_attention   the same over per-request sub-tensors
+ *   pkv_block_copy                copy whole blocks (copy on write)
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *     owned by the caller; the library never allocates or frees them and
+ *     keeps no per-call state.  `stream` is a cudaStream_t (NULL = the legacy
+ *     default stream); every call is asynchronous on it.
+ *   - Element types: K, V, Q and outputs are bf16 (passed as void*), block
+ *     tables, context lengths and request ids are int32, slots and copy
+ *     pairs are int64.  head_dim must be 128 (PKV_ERR_UNSUPPORTED otherwise);
+ *     num_q_heads must be a multiple of num_kv_heads with a ratio of 1..8.
+ *   - bf16 base pointers must be 16-byte aligned, int32 arrays 4-byte and
+ *     int64 arrays 8-byte aligned (PKV_ERR_INVALID_ARG otherwise).
+ *   - The return value covers host-side validation and the launch
+ *     (cudaGetLastError).  Device-side index checks run only in checked mode
+ *     (pkv_set_checked); they record the first violation in a per-device
+ *     error word read by pkv_get_device_error and skip the bad access.  In
+ *     the default mode indices are trusted, as a page table is.
+ *   - A query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Layouts (the pages fix none; these are this library's contracts):
+ *   paged cache     [num_blocks][num_kv_heads][block_size][head_dim]
+ *   contig buffer   [max_reqs][num_kv_heads][S][head_dim]
+ *   q, out          [num_seqs][num_q_heads][head_dim]
+ *   new k, v        [num_tokens][num_kv_heads][head_dim]
+ *   block_tables    [num_seqs][max_blocks_per_seq]
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size        */
+    PKV_ERR_UNSUPPORTED = 2,   /* head_dim != 128, group ratio > 8, ...     */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than needed  */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime call failed                */
+    PKV_ERR_DEVICE_BOUNDS = 5  /* pkv_get_device_error found a device error */
+} pkv_status;
+
+/* Codes stored in the device error word (checked mode, and wait limits). */
+enum {
+    PKV_DEVERR_NONE = 0,
+    PKV_DEVERR_BLOCK_ID = 1,   /* block table entry outside [0, num_blocks) */
+    PKV_DEVERR_SLOT = 2,       /* slot outside [0, num_slots)               */
+    PKV_DEVERR_REQ_ID = 3,     /* request id outside [0, max_reqs)          */
+    PKV_DEVERR_CONTEXT = 4,    /* context longer than max_context, than the
+                                  block table holds, or than S             */
+    PKV_DEVERR_COPY_PAIR = 5,  /* block_copy id outside [0, num_blocks)     */
+    PKV_DEVERR_TIMEOUT = 6     /* a copy into shared memory never completed */
+};
+
+typedef struct pkv_heads {
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} pkv_heads;
+
+/*
+ * KV append.  "Insights into LLM Serving Systems: KV-Cache Memory Allocation
+ * Patterns", section 4, Observation-1: each decode iteration grows every
+ * request's KV cache by exactly one token; "Running Out of Cache": a new
+ * block is taken only when the last one is full.
+ *
+ * For each token t < num_tokens and KV head h, copies k[t][h][:] to
+ * k_cache[slot / block_size][h][slot % block_size][:] and v likewise, where
+ * slot = slot_mapping[t] (device, int64).  A negative slot skips the token
+ * (padding).  For the contiguous layout pass block_size = S and slot =
+ * reqId * S + position.  num_slots = num_blocks * block_size bounds the
+ * slots in checked mode.  Bit-exact: the bytes are moved, not converted.
+ */
+PKV_API pkv_status pkv_kv_append(const int64_t *slot_mapping, int64_t num_tokens,
+                         const void *k, const void *v,
+                         void *k_cache, void *v_cache,
+                         int64_t num_slots, int64_t block_size,
+                         pkv_heads heads, void *stream);
+
+/*
+ * Number of context splits the decode calls use, and the fp32 workspace they
+ * need, for num_seqs sequences of at most max_context positions on the
+ * current device.  The split count depends only on these arguments, the
+ * device's SM count and pkv_set_split_tiles; both decode calls use the same
+ * rule.  A workspace size of 0 means no workspace is needed.
+ */
+PKV_API int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads,
+                              int32_t max_context);
+PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, pkv_heads heads,
+                                 int32_t max_context);
+
+/*
+ * Paged decode attention.  "Running Out of Cache": the cache is divided into
+ * fixed blocks, a sequence's blocks need not be adjacent, and a block table
+ * maps positions to blocks as a page table maps virtual to physical memory;
+ * "Efficient Memory Management for Large Language Model Serving with
+ * PagedAttention" (summary): the PagedAttention algorithm over such blocks.
+ *
+ * For sequence i and query head h, with ctx = context_lens[i]:
+ *   K_j = k_cache[block_tables[i][j / block_size]][h / G][j % block_size]
+ *   out[i][h] = sum_j softmax_j(scale * q[i][h] . K_j) V_j,  j < ctx
+ * accumulated in fp32, rounded to bf16.  ctx <= 0 writes zeros.  Entries of
+ * a block table past ceil(ctx / block_size) are never read.
+ * max_context is a host-side upper bound on every context_lens[i] (it sizes
+ * the grid without reading device memory); max_blocks_per_seq *
+ * block_size must be >= max_context.  workspace must hold
+ * pkv_decode_workspace_size(num_seqs, heads, max_context) bytes (16-byte
+ * aligned) when that size is non-zero; its contents need no initialisation.
+ */
+PKV_API pkv_status pkv_paged_decode_attention(
+    const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_blocks,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int32_t block_size, float scale, pkv_heads heads, void *out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Contiguous-layout decode attention.  "Leveraging Low-Level CUDA APIs for
+ * vAttention's Dynamic Memory", section 5.2.3: each layer's K (and V) tensor
+ * holds the maximum batch; the sub-tensor of a request sits at offset
+ * reqId x S, S being the per-request maximum (counted here in tokens).
+ *
+ * Same result as the paged call with K_j = k_buf[req_ids[i]][h / G][j],
+ * i.e. the paged layout with block_size = S and the table [req_ids[i]].
+ * Requires context_lens[i] <= S and 0 <= req_ids[i] < max_reqs.
+ */
+PKV_API pkv_status pkv_contig_decode_attention(
+    const void *q, const void *k_buf, const void *v_buf,
+    const int32_t *req_ids, int32_t max_reqs,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int64_t S, float scale, pkv_heads heads, void *out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Copy-on-write block copy.  "Running Out of Cache" (section "Fragmentation
+ * is lost users") and the PagedAttention summary: sequences share physical
+ * blocks and copy a block only when one of them writes into it.
+ *
+ * For each pair c < n of src_dst_pairs (device, int64 [n][2]) and each layer
+ * l < num_layers, copies block_bytes bytes from block src to block dst of
+ * k_caches[l] and of v_caches[l].  k_caches and v_caches are HOST arrays of
+ * num_layers device pointers (each 16-byte aligned); block_bytes must be a
+ * multiple of 16.  num_blocks bounds the ids in checked mode.  Pairs must
+ * not overlap (no dst is another pair's src).  Bit-exact.
+ */
+PKV_API pkv_status pkv_block_copy(const int64_t *src_dst_pairs, int64_t n,
+                          void *const *k_caches, void *const *v_caches,
+                          int32_t num_layers, int64_t num_blocks,
+                          int64_t block_bytes, void *stream);
+
+/* Checked mode on (1) or off (0, the default) for later calls. */
+PKV_API void pkv_set_checked(int enable);
+PKV_API int pkv_get_checked(void);
+
+/*
+ * Tokens-per-split override in units of 16-token tiles (0 restores the
+ * automatic rule).  Changes pkv_decode_num_splits/_workspace_size for later
+ * calls; meant for tuning and tests.
+ */
+PKV_API void pkv_set_split_tiles(int32_t tiles);
+
+/*
+ * Reads and clears the error word of the current device (synchronises the
+ * device).  *code_out receives a PKV_DEVERR_* code.  Returns PKV_OK when the
+ * word was clear, PKV_ERR_DEVICE_BOUNDS when it held an error, PKV_ERR_CUDA
+ * if the read failed.
+ */
+PKV_API pkv_status pkv_get_device_error(int *code_out);
+
+/* Static description of a status code. */
+PKV_API const char *pkv_status_string(pkv_status status);
+
+/* Detail message of the last failing call on this host thread ("" if none). */
+PKV_API const char *pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,11 @@
+"""Decode attention over a paged (block-table) or contiguous (reqId x S) KV
+cache, with KV append and copy-on-write block copy, as hand-written sm_103a
+CUDA kernels behind a C ABI (include/pkv.h).  This package is the thin
+Python binding; build the library with ``build.build()``."""
+from .binding import (PkvError, block_copy, contig_decode_attention, decode_num_splits,
+                      decode_workspace_size, get_checked, get_device_error, kv_append, lib,
+                      paged_decode_attention, set_checked, set_split_tiles)
+
+__all__ = ["PkvError", "block_copy", "contig_decode_attention", "decode_num_splits",
+           "decode_workspace_size", "get_checked", "get_device_error", "kv_append", "lib",
+           "paged_decode_attention", "set_checked", "set_split_tiles"]

@@ -1,0 +1,244 @@
+"""Python binding of the C ABI in ``include/pkv.h`` (argument marshalling only).
+
+Every function takes torch CUDA tensors, checks their dtype/shape/contiguity,
+and passes raw device pointers and the current CUDA stream to the compiled
+library ``libpkv.so``.  All computation happens in the library's kernels;
+there is no fallback of any kind: if the library is missing or fails to load,
+every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+                3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_BOUNDS"}
+DEVERR_NAMES = {0: "none", 1: "block_id", 2: "slot", 3: "req_id", 4: "context",
+                5: "copy_pair", 6: "timeout"}
+
+EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size",
+            "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
+            "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
+            "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class Heads(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libpkv.so is not built (%s); run __graft_entry__.build() "
+                           "or paged_kv_cache_245_gb300/build.py" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    L.pkv_kv_append.argtypes = [vp, i64, vp, vp, vp, vp, i64, i64, Heads, vp]
+    L.pkv_decode_num_splits.argtypes = [i32, Heads, i32]
+    L.pkv_decode_num_splits.restype = i32
+    L.pkv_decode_workspace_size.argtypes = [i32, Heads, i32]
+    L.pkv_decode_workspace_size.restype = sz
+    L.pkv_paged_decode_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
+                                             ctypes.c_float, Heads, vp, vp, sz, vp]
+    L.pkv_contig_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i64,
+                                              ctypes.c_float, Heads, vp, vp, sz, vp]
+    L.pkv_block_copy.argtypes = [vp, i64, vp, vp, i32, i64, i64, vp]
+    L.pkv_set_checked.argtypes = [ctypes.c_int]
+    L.pkv_set_checked.restype = None
+    L.pkv_get_checked.restype = ctypes.c_int
+    L.pkv_set_split_tiles.argtypes = [i32]
+    L.pkv_set_split_tiles.restype = None
+    L.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    L.pkv_status_string.argtypes = [ctypes.c_int]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_last_error.restype = ctypes.c_char_p
+    for name in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_contig_decode_attention",
+                 "pkv_block_copy", "pkv_get_device_error"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != PKV_OK:
+        raise PkvError(status, lib().pkv_last_error().decode())
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+
+
+def heads(num_q_heads, num_kv_heads, head_dim=128):
+    return Heads(int(num_q_heads), int(num_kv_heads), int(head_dim))
+
+
+# ---------------------------------------------------------------- operations
+
+def kv_append(slot_mapping, k, v, k_cache, v_cache):
+    """Write new rows k, v [T, Hkv, D] into the caches at slot_mapping [T]
+    (int64; slot = block * block_size + offset; negative = skip).  The caches
+    are [num_blocks, Hkv, block_size, D] (or [max_reqs, Hkv, S, D])."""
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, 4)
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k.shape != v.shape:
+        raise ValueError("k/v and cache shapes must match")
+    if k.shape[1] != hkv or k.shape[2] != d or k.shape[0] != slot_mapping.shape[0]:
+        raise ValueError("k must be [T, Hkv, D] matching the cache and slot_mapping")
+    _check(lib().pkv_kv_append(_ptr(slot_mapping), k.shape[0], _ptr(k), _ptr(v),
+                               _ptr(k_cache), _ptr(v_cache), nb * bs, bs,
+                               heads(hkv, hkv, d), _stream(k_cache)))
+
+
+def decode_num_splits(num_seqs, num_q_heads, num_kv_heads, max_context, head_dim=128):
+    return int(lib().pkv_decode_num_splits(num_seqs, heads(num_q_heads, num_kv_heads, head_dim),
+                                           max_context))
+
+
+def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, max_context, head_dim=128):
+    return int(lib().pkv_decode_workspace_size(num_seqs, heads(num_q_heads, num_kv_heads,
+                                                               head_dim), max_context))
+
+
+def _workspace(workspace, q, nbytes):
+    if nbytes == 0:
+        return workspace
+    if workspace is None:
+        # convenience for callers without their own buffer; the C ABI itself never allocates
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    return workspace
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, max_context,
+                           scale, out=None, workspace=None):
+    """out[i, h] = softmax(scale * q[i, h] . K) V over the context_lens[i]
+    positions that block_tables[i] maps into the paged caches."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d != d2 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shapes disagree")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    h = heads(hq, hkv, d)
+    nbytes = lib().pkv_decode_workspace_size(B, h, int(max_context)) if B > 0 else 0
+    workspace = _workspace(workspace, q, nbytes)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pkv_paged_decode_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], nb,
+        _ptr(context_lens), B, int(max_context), bs, float(scale), h, _ptr(out), ws_ptr,
+        ws_len, _stream(q)))
+    return out
+
+
+def contig_decode_attention(q, k_buf, v_buf, req_ids, context_lens, max_context, scale,
+                            out=None, workspace=None):
+    """Decode attention over per-request sub-tensors: request i's rows are
+    k_buf[req_ids[i], h, :context_lens[i]] (offset reqId x S)."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_buf, "k_buf"), (v_buf, "v_buf")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(req_ids, torch.int32, "req_ids", 1)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, hq, d = q.shape
+    max_reqs, hkv, S, d2 = k_buf.shape
+    if d != d2 or tuple(v_buf.shape) != tuple(k_buf.shape):
+        raise ValueError("q / buffer shapes disagree")
+    if req_ids.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("req_ids / context_lens must have num_seqs rows")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    h = heads(hq, hkv, d)
+    nbytes = lib().pkv_decode_workspace_size(B, h, int(max_context)) if B > 0 else 0
+    workspace = _workspace(workspace, q, nbytes)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pkv_contig_decode_attention(
+        _ptr(q), _ptr(k_buf), _ptr(v_buf), _ptr(req_ids), max_reqs, _ptr(context_lens), B,
+        int(max_context), S, float(scale), h, _ptr(out), ws_ptr, ws_len, _stream(q)))
+    return out
+
+
+def block_copy(src_dst_pairs, k_caches, v_caches):
+    """Copy whole blocks src -> dst (pairs [n, 2] int64 on the device) in every
+    layer's K and V cache (lists of [num_blocks, ...] bf16 tensors)."""
+    _need(src_dst_pairs, torch.int64, "src_dst_pairs", 2)
+    L = len(k_caches)
+    if L != len(v_caches) or L == 0:
+        raise ValueError("need one K and one V cache per layer")
+    shape = tuple(k_caches[0].shape)
+    for t in list(k_caches) + list(v_caches):
+        _need(t, torch.bfloat16, "cache")
+        if tuple(t.shape) != shape:
+            raise ValueError("all caches must have one shape")
+    nb = shape[0]
+    block_bytes = k_caches[0][0].numel() * 2
+    kp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_caches])
+    vp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
+    _check(lib().pkv_block_copy(_ptr(src_dst_pairs), src_dst_pairs.shape[0], kp, vp, L, nb,
+                                block_bytes, _stream(k_caches[0])))
+
+
+def set_checked(enable):
+    lib().pkv_set_checked(1 if enable else 0)
+
+
+def get_checked():
+    return bool(lib().pkv_get_checked())
+
+
+def set_split_tiles(tiles):
+    lib().pkv_set_split_tiles(int(tiles))
+
+
+def get_device_error():
+    """Read and clear the device error word; returns its code name."""
+    code = ctypes.c_int(0)
+    st = lib().pkv_get_device_error(ctypes.byref(code))
+    if st not in (0, 5):
+        _check(st)
+    return DEVERR_NAMES.get(code.value, code.value)

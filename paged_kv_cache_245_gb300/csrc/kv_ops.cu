@@ -1,0 +1,84 @@
+// kv_ops.cu -- the two data-movement kernels of a decode step: KV append
+// (write each new token's K/V row into its cache slot) and the
+// copy-on-write block copy.  Both move bytes unchanged (bit-exact) with
+// 16-byte vector loads and stores.
+#include "kv_ops.cuh"
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// One 16-lane group per 256-byte row; a 256-thread CTA moves 16 rows.
+// Rows are numbered (which in {K, V}, token t, KV head h), K first.
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int lane16 = threadIdx.x & 15;
+  const int64_t per_kind = p.num_tokens * p.Hkv;
+  if (row >= 2 * per_kind) return;
+  const bool is_v = row >= per_kind;
+  const int64_t r = is_v ? row - per_kind : row;
+  const int64_t t = r / p.Hkv;
+  const int64_t h = r % p.Hkv;
+  const int64_t slot = p.slot_mapping[t];
+  if (slot < 0) return;  // padding token
+  if (slot >= p.num_slots && p.checked) {
+    if (lane16 == 0 && !is_v) record_error(p.err, kErrSlot);
+    return;
+  }
+  const int64_t blk = slot / p.bs;
+  const int64_t off = slot % p.bs;
+  const uint16_t* src = (is_v ? p.v : p.k) + (t * p.Hkv + h) * kHeadDim + lane16 * 8;
+  uint16_t* dst = (is_v ? p.v_cache : p.k_cache) + ((blk * p.Hkv + h) * p.bs + off) * kHeadDim +
+                  lane16 * 8;
+  *reinterpret_cast<uint4*>(dst) = ld_global_nc_v4(src);
+}
+
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
+  const int64_t rows = 2 * p.num_tokens * p.Hkv;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows + 15) / 16;
+  kv_append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Block copy: blockIdx.x strides over the block's 16-byte chunks, blockIdx.y
+// is the pair, blockIdx.z = 2 * layer + (0 for K, 1 for V).
+__global__ void __launch_bounds__(256) block_copy_kernel(const CopyParams p) {
+  const int64_t pair = blockIdx.y;
+  const int layer = blockIdx.z >> 1;
+  const bool is_v = blockIdx.z & 1;
+  const int64_t src = p.pairs[2 * pair];
+  const int64_t dst = p.pairs[2 * pair + 1];
+  if (p.checked && (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrCopyPair);
+    return;
+  }
+  unsigned char* base = static_cast<unsigned char*>(is_v ? p.v[layer] : p.k[layer]);
+  const uint4* s = reinterpret_cast<const uint4*>(base + src * p.block_bytes);
+  uint4* d = reinterpret_cast<uint4*>(base + dst * p.block_bytes);
+  const int64_t n16 = p.block_bytes / 16;
+  constexpr int kUnroll = 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + (kUnroll - 1) * stride < n16; i += kUnroll * stride) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = ld_global_nc_v4(s + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) d[i + u * stride] = v[u];
+  }
+  for (; i < n16; i += stride) d[i] = ld_global_nc_v4(s + i);
+}
+
+cudaError_t launch_block_copy(const CopyParams& p, int64_t num_pairs, cudaStream_t stream) {
+  if (num_pairs == 0 || p.num_layers == 0) return cudaSuccess;
+  const int64_t n16 = p.block_bytes / 16;
+  int64_t bx = (n16 + 256 * 4 - 1) / (256 * 4);
+  if (bx < 1) bx = 1;
+  if (bx > 64) bx = 64;
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(num_pairs),
+                  static_cast<unsigned>(2 * p.num_layers));
+  block_copy_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,40 @@
+// kv_ops.cuh -- parameters and launchers of the KV append and block copy
+// kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct AppendParams {
+  const int64_t* slot_mapping;  // [T]
+  const uint16_t* k;            // [T][Hkv][128]
+  const uint16_t* v;
+  uint16_t* k_cache;            // [.][Hkv][bs][128]
+  uint16_t* v_cache;
+  int64_t num_tokens;
+  int64_t num_slots;
+  int64_t bs;
+  int64_t Hkv;
+  int32_t checked;
+  int* err;
+};
+
+constexpr int kMaxCopyLayers = 64;  // layers per launch (pointers passed by value)
+
+struct CopyParams {
+  const int64_t* pairs;  // [n][2] (src, dst)
+  void* k[kMaxCopyLayers];
+  void* v[kMaxCopyLayers];
+  int32_t num_layers;    // <= kMaxCopyLayers for this launch
+  int64_t num_blocks;
+  int64_t block_bytes;
+  int32_t checked;
+  int* err;
+};
+
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_block_copy(const CopyParams& p, int64_t num_pairs, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,363 @@
+// pkv_api.cu -- the C ABI declared in include/pkv.h: host-side validation,
+// split policy, launches, checked mode and the per-device error word.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/pkv.h"
+#include "decode_launch.cuh"
+#include "kv_ops.cuh"
+
+namespace {
+
+std::atomic<int> g_checked{0};
+std::atomic<int> g_split_tiles{0};
+thread_local char g_last_error[256] = "";
+
+// The device error word: one int per device (module-scope __device__).
+__device__ int g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+pkv_status fail(pkv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device id, its error-word address and SM count (cached per device).
+pkv_status device_info(int* dev_out, int** err_out, int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device id %d", dev);
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+  }
+  if (dev_out) *dev_out = dev;
+  if (err_out) *err_out = g_err_ptr[dev];
+  if (sms_out) *sms_out = g_num_sms[dev];
+  return PKV_OK;
+}
+
+pkv_status check_heads(const pkv_heads& h) {
+  if (h.num_q_heads <= 0 || h.num_kv_heads <= 0 || h.head_dim <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "head counts must be positive");
+  if (h.head_dim != pkv::kHeadDim)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (only 128 is built)", h.head_dim);
+  if (h.num_q_heads % h.num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                h.num_q_heads, h.num_kv_heads);
+  const int g = h.num_q_heads / h.num_kv_heads;
+  if (g > 8) return fail(PKV_ERR_UNSUPPORTED, "query heads per KV head %d > 8", g);
+  if (h.num_kv_heads > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  return PKV_OK;
+}
+
+// Split rule.  A split is a run of `chunk` 16-token tiles of one (sequence,
+// KV head); a CTA handles one split.  The rule picks the chunk (a multiple
+// of the warp count) that minimises a simple makespan model: waves of
+// resident CTAs x (tiles per CTA + a fixed per-CTA overhead of 2 tiles),
+// capped at 64 tiles so that one long context cannot dominate a batch.
+int32_t choose_chunk_tiles(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context,
+                           int num_sms) {
+  const int64_t ntiles = max_context > 0 ? (static_cast<int64_t>(max_context) + 15) / 16 : 0;
+  const int forced = g_split_tiles.load();
+  if (forced > 0) return forced;
+  if (ntiles <= pkv::kDecodeWarps) return pkv::kDecodeWarps;
+  const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 2;
+  int64_t best_chunk = pkv::kDecodeWarps;
+  double best_cost = 1e300;
+  const int64_t cap = 64;
+  for (int64_t chunk = pkv::kDecodeWarps; chunk <= cap; chunk += pkv::kDecodeWarps) {
+    const int64_t nsplit = (ntiles + chunk - 1) / chunk;
+    const int64_t ctas = pairs * nsplit;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const int64_t used = chunk < ntiles ? chunk : ntiles;
+    const double cost = static_cast<double>(waves) * static_cast<double>(used + 2);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best_chunk = chunk;
+    }
+    if (chunk >= ntiles) break;
+  }
+  return static_cast<int32_t>(best_chunk);
+}
+
+struct SplitPlan {
+  int32_t chunk_tiles;
+  int32_t nsplit;
+  size_t workspace_bytes;
+};
+
+SplitPlan plan_splits(int32_t num_seqs, const pkv_heads& h, int32_t max_context, int num_sms) {
+  SplitPlan s;
+  s.chunk_tiles = choose_chunk_tiles(num_seqs, h.num_kv_heads, max_context, num_sms);
+  const int64_t ntiles = max_context > 0 ? (static_cast<int64_t>(max_context) + 15) / 16 : 0;
+  int64_t n = (ntiles + s.chunk_tiles - 1) / s.chunk_tiles;
+  if (n < 1) n = 1;
+  s.nsplit = static_cast<int32_t>(n);
+  s.workspace_bytes = s.nsplit > 1 ? static_cast<size_t>(num_seqs) * h.num_q_heads *
+                                         static_cast<size_t>(s.nsplit) *
+                                         (pkv::kHeadDim + 2) * sizeof(float)
+                                   : 0;
+  return s;
+}
+
+pkv_status decode_common(bool contig, const void* q, const void* k, const void* v,
+                         const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
+                         const int32_t* req_ids, int32_t max_reqs, const int32_t* context_lens,
+                         int32_t num_seqs, int32_t max_context, int64_t bs_or_S, float scale,
+                         pkv_heads h, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  pkv_status st = check_heads(h);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_context < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_seqs > 65535");
+  if (!q || !k || !v || !out || !context_lens)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return fail(PKV_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  if (!aligned(context_lens, 4)) return fail(PKV_ERR_INVALID_ARG, "context_lens misaligned");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (bs_or_S <= 0) return fail(PKV_ERR_INVALID_ARG, contig ? "S must be >= 1" : "block_size must be >= 1");
+  if (contig) {
+    if (!req_ids || !aligned(req_ids, 4)) return fail(PKV_ERR_INVALID_ARG, "req_ids null or misaligned");
+    if (max_reqs <= 0) return fail(PKV_ERR_INVALID_ARG, "max_reqs must be >= 1");
+    if (max_context > bs_or_S) return fail(PKV_ERR_INVALID_ARG, "max_context %d > S %lld",
+                                            max_context, static_cast<long long>(bs_or_S));
+  } else {
+    if (!block_tables || !aligned(block_tables, 4))
+      return fail(PKV_ERR_INVALID_ARG, "block_tables null or misaligned");
+    if (max_blocks <= 0 || num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "empty block table or pool");
+    if (static_cast<int64_t>(max_blocks) * bs_or_S < max_context)
+      return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq * block_size < max_context");
+    if (static_cast<int64_t>(num_blocks) * h.num_kv_heads * bs_or_S > (int64_t{1} << 40))
+      return fail(PKV_ERR_UNSUPPORTED, "cache too large");
+  }
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  st = device_info(&dev, &err, &sms);
+  if (st != PKV_OK) return st;
+  const SplitPlan plan = plan_splits(num_seqs, h, max_context, sms);
+  if (plan.nsplit > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
+  if (plan.workspace_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+      return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", plan.workspace_bytes,
+                  workspace ? workspace_bytes : size_t{0});
+    if (!aligned(workspace, 16)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  }
+
+  pkv::DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.out = static_cast<uint16_t*>(out);
+  if (plan.nsplit > 1) {
+    p.part_o = static_cast<float*>(workspace);
+    p.part_ml = p.part_o + static_cast<size_t>(num_seqs) * h.num_q_heads * plan.nsplit * pkv::kHeadDim;
+  }
+  p.ctx_lens = context_lens;
+  p.block_tables = block_tables;
+  p.req_ids = req_ids;
+  p.bs = bs_or_S;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks;
+  p.max_reqs = max_reqs;
+  p.num_seqs = num_seqs;
+  p.Hq = h.num_q_heads;
+  p.Hkv = h.num_kv_heads;
+  p.max_context = max_context;
+  p.chunk_tiles = plan.chunk_tiles;
+  p.nsplit = plan.nsplit;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e)
+  p.checked = g_checked.load();
+  p.err = err;
+  const int group = h.num_q_heads / h.num_kv_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = contig ? pkv::launch_decode_contig(p, group, s)
+                               : pkv::launch_decode_paged(p, group, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_kv_append(const int64_t* slot_mapping, int64_t num_tokens, const void* k,
+                         const void* v, void* k_cache, void* v_cache, int64_t num_slots,
+                         int64_t block_size, pkv_heads heads, void* stream) {
+  if (heads.num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads must be positive");
+  if (heads.head_dim != pkv::kHeadDim)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (only 128 is built)", heads.head_dim);
+  if (num_tokens < 0 || num_slots < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (num_tokens == 0) return PKV_OK;
+  if (block_size <= 0) return fail(PKV_ERR_INVALID_ARG, "block_size must be >= 1");
+  if (!slot_mapping || !k || !v || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(slot_mapping, 8)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping misaligned");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  int* err = nullptr;
+  pkv_status st = device_info(nullptr, &err, nullptr);
+  if (st != PKV_OK) return st;
+  pkv::AppendParams p;
+  p.slot_mapping = slot_mapping;
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.k_cache = static_cast<uint16_t*>(k_cache);
+  p.v_cache = static_cast<uint16_t*>(v_cache);
+  p.num_tokens = num_tokens;
+  p.num_slots = num_slots;
+  p.bs = block_size;
+  p.Hkv = heads.num_kv_heads;
+  p.checked = g_checked.load();
+  p.err = err;
+  const int64_t rows = 2 * num_tokens * heads.num_kv_heads;
+  if ((rows + 15) / 16 > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens");
+  const cudaError_t e = pkv::launch_kv_append(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return PKV_OK;
+}
+
+int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads, int32_t max_context) {
+  int sms = 0;
+  if (device_info(nullptr, nullptr, &sms) != PKV_OK) return -1;
+  if (check_heads(heads) != PKV_OK || num_seqs < 0 || max_context < 0) return -1;
+  return plan_splits(num_seqs, heads, max_context, sms).nsplit;
+}
+
+size_t pkv_decode_workspace_size(int32_t num_seqs, pkv_heads heads, int32_t max_context) {
+  int sms = 0;
+  if (device_info(nullptr, nullptr, &sms) != PKV_OK) return 0;
+  if (check_heads(heads) != PKV_OK || num_seqs <= 0 || max_context < 0) return 0;
+  return plan_splits(num_seqs, heads, max_context, sms).workspace_bytes;
+}
+
+pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      int32_t num_blocks, const int32_t* context_lens,
+                                      int32_t num_seqs, int32_t max_context, int32_t block_size,
+                                      float scale, pkv_heads heads, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq, num_blocks,
+                       nullptr, 0, context_lens, num_seqs, max_context, block_size, scale, heads,
+                       out, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_contig_decode_attention(const void* q, const void* k_buf, const void* v_buf,
+                                       const int32_t* req_ids, int32_t max_reqs,
+                                       const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t max_context, int64_t S, float scale,
+                                       pkv_heads heads, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
+                       num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
+                       stream);
+}
+
+pkv_status pkv_block_copy(const int64_t* src_dst_pairs, int64_t n, void* const* k_caches,
+                          void* const* v_caches, int32_t num_layers, int64_t num_blocks,
+                          int64_t block_bytes, void* stream) {
+  if (n < 0 || num_layers < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (n == 0 || num_layers == 0) return PKV_OK;
+  if (!src_dst_pairs || !aligned(src_dst_pairs, 8))
+    return fail(PKV_ERR_INVALID_ARG, "src_dst_pairs null or misaligned");
+  if (!k_caches || !v_caches) return fail(PKV_ERR_INVALID_ARG, "null cache pointer array");
+  if (block_bytes <= 0 || block_bytes % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "block_bytes must be a positive multiple of 16");
+  if (num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_blocks must be >= 1");
+  for (int32_t l = 0; l < num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l] || !aligned(k_caches[l], 16) || !aligned(v_caches[l], 16))
+      return fail(PKV_ERR_INVALID_ARG, "cache pointer of layer %d null or misaligned", l);
+  }
+  int* err = nullptr;
+  pkv_status st = device_info(nullptr, &err, nullptr);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t p0 = 0; p0 < n; p0 += 65535) {
+    const int64_t np = (n - p0) < 65535 ? (n - p0) : 65535;
+    for (int32_t l0 = 0; l0 < num_layers; l0 += pkv::kMaxCopyLayers) {
+      pkv::CopyParams p;
+      std::memset(&p, 0, sizeof p);
+      p.pairs = src_dst_pairs + 2 * p0;
+      p.num_layers = (num_layers - l0) < pkv::kMaxCopyLayers ? (num_layers - l0) : pkv::kMaxCopyLayers;
+      for (int32_t l = 0; l < p.num_layers; ++l) {
+        p.k[l] = k_caches[l0 + l];
+        p.v[l] = v_caches[l0 + l];
+      }
+      p.num_blocks = num_blocks;
+      p.block_bytes = block_bytes;
+      p.checked = g_checked.load();
+      p.err = err;
+      const cudaError_t e = pkv::launch_block_copy(p, np, s);
+      if (e != cudaSuccess) return cuda_fail(e, "block_copy launch");
+    }
+  }
+  return PKV_OK;
+}
+
+void pkv_set_checked(int enable) { g_checked.store(enable ? 1 : 0); }
+int pkv_get_checked(void) { return g_checked.load(); }
+void pkv_set_split_tiles(int32_t tiles) {
+  if (tiles > 0) tiles = (tiles + pkv::kDecodeWarps - 1) / pkv::kDecodeWarps * pkv::kDecodeWarps;
+  g_split_tiles.store(tiles > 0 ? tiles : 0);
+}
+
+pkv_status pkv_get_device_error(int* code_out) {
+  if (!code_out) return fail(PKV_ERR_INVALID_ARG, "code_out is null");
+  int* err = nullptr;
+  pkv_status st = device_info(nullptr, &err, nullptr);
+  if (st != PKV_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int code = 0;
+  e = cudaMemcpy(&code, err, sizeof code, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  const int zero = 0;
+  e = cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  *code_out = code;
+  return code == 0 ? PKV_OK : PKV_ERR_DEVICE_BOUNDS;
+}
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime error";
+    case PKV_ERR_DEVICE_BOUNDS: return "device-side bounds error recorded";
+  }
+  return "unknown status";
+}
+
+const char* pkv_last_error(void) { return g_last_error; }
+
+}  // extern "C"

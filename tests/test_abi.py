@@ -1,0 +1,112 @@
+"""The C-ABI library loads on a machine without a GPU and exports every
+symbol include/pkv.h declares; host-side validation rejects bad arguments
+before any CUDA call.  No GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_245_gb300 as pkv
+from paged_kv_cache_245_gb300 import binding
+from paged_kv_cache_245_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return pkv.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    return set(re.findall(r"PKV_API[^;(]*?\b(pkv_\w+)\s*\(", text))
+
+
+def test_header_declares_the_calls(L):
+    names = _declared()
+    for call in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_contig_decode_attention",
+                 "pkv_block_copy", "pkv_decode_workspace_size", "pkv_get_device_error"):
+        assert call in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert set(binding.EXPORTED) <= _declared()
+
+
+def _h(hq=8, hkv=2, d=128):
+    return binding.Heads(hq, hkv, d)
+
+
+FAKE = ctypes.c_void_p(0x10000)        # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def test_status_strings(L):
+    assert L.pkv_status_string(0) == b"ok"
+    assert L.pkv_status_string(3).startswith(b"workspace")
+
+
+def test_decode_rejects_bad_heads(L):
+    st = L.pkv_paged_decode_attention(FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 16, 0.1,
+                                      _h(d=64), FAKE, None, 0, None)
+    assert st == 2 and b"head_dim" in L.pkv_last_error()
+    st = L.pkv_paged_decode_attention(FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 16, 0.1,
+                                      _h(32, 2), FAKE, None, 0, None)
+    assert st == 2
+    st = L.pkv_paged_decode_attention(FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 16, 0.1,
+                                      _h(9, 2), FAKE, None, 0, None)
+    assert st == 1
+
+
+def test_decode_rejects_null_and_misaligned(L):
+    st = L.pkv_paged_decode_attention(None, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 16, 0.1,
+                                      _h(), FAKE, None, 0, None)
+    assert st == 1
+    st = L.pkv_paged_decode_attention(MISALIGNED, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 16,
+                                      0.1, _h(), FAKE, None, 0, None)
+    assert st == 1 and b"aligned" in L.pkv_last_error()
+    st = L.pkv_paged_decode_attention(FAKE, FAKE, FAKE, FAKE, 3, 10, FAKE, 2, 64, 16, 0.1,
+                                      _h(), FAKE, None, 0, None)
+    assert st == 1 and b"max_blocks" in L.pkv_last_error()
+    st = L.pkv_paged_decode_attention(FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 0, 0.1,
+                                      _h(), FAKE, None, 0, None)
+    assert st == 1
+    st = L.pkv_paged_decode_attention(FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 2, 64, 16,
+                                      float("nan"), _h(), FAKE, None, 0, None)
+    assert st == 1
+
+
+def test_contig_rejects_context_beyond_S(L):
+    st = L.pkv_contig_decode_attention(FAKE, FAKE, FAKE, FAKE, 4, FAKE, 2, 65, 64, 0.1, _h(),
+                                       FAKE, None, 0, None)
+    assert st == 1 and b"S" in L.pkv_last_error()
+
+
+def test_empty_batch_is_a_no_op(L):
+    st = L.pkv_paged_decode_attention(None, None, None, None, 0, 0, None, 0, 0, 16, 0.1, _h(),
+                                      None, None, 0, None)
+    assert st == 0
+    assert L.pkv_kv_append(None, 0, None, None, None, None, 0, 16, _h(), None) == 0
+    assert L.pkv_block_copy(None, 0, None, None, 3, 10, 1024, None) == 0
+
+
+def test_append_and_copy_validation(L):
+    assert L.pkv_kv_append(FAKE, 4, FAKE, FAKE, FAKE, FAKE, 100, 0, _h(), None) == 1
+    assert L.pkv_kv_append(MISALIGNED, 4, FAKE, FAKE, FAKE, MISALIGNED, 100, 16, _h(), None) == 1
+    assert L.pkv_kv_append(FAKE, 4, FAKE, FAKE, FAKE, FAKE, 100, 16, _h(d=256), None) == 2
+    arr = (ctypes.c_void_p * 2)(0x10000, 0x10008)
+    assert L.pkv_block_copy(FAKE, 2, arr, arr, 2, 10, 1024, None) == 1
+    assert L.pkv_block_copy(FAKE, 2, arr, arr, 1, 10, 1000, None) == 1
+
+
+def test_checked_flag_and_split_override_round_trip(L):
+    pkv.set_checked(True)
+    assert pkv.get_checked()
+    pkv.set_checked(False)
+    assert not pkv.get_checked()
+    pkv.set_split_tiles(0)
