@@ -165,6 +165,32 @@ PKV_API pkv_status pkv_block_copy(const int64_t *src_dst_pairs, int64_t n,
                           int32_t num_layers, int64_t num_blocks,
                           int64_t block_bytes, void *stream);
 
+/*
+ * Paged decode attention without a caller workspace.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory,
+ * for instance an engine whose allocator owns all of the GPU's memory for its
+ * KV-cache pool, or a latency-critical caller that must not call cudaMalloc
+ * or cudaFree (they can synchronise the device).
+ *
+ * Same arguments and result as pkv_paged_decode_attention, minus the
+ * workspace.  The split partials go to a fixed device array of
+ * PKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits; nothing is allocated per call.  A batch whose partials
+ * need more (pkv_decode_workspace_size above the maximum) is rejected with
+ * PKV_ERR_WORKSPACE and a message in pkv_last_error.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture.  All calls on a
+ * device share the one array: calls whose kernels overlap on the GPU (on
+ * different streams, unordered) race and give wrong results.  The array
+ * keeps the last call's contents; nothing in it needs to start at zero.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+PKV_API pkv_status pkv_paged_decode_attention_noalloc(
+    const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_blocks,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int32_t block_size, float scale, pkv_heads heads, void *out, void *stream);
+
 /* Checked mode on (1) or off (0, the default) for later calls. */
 PKV_API void pkv_set_checked(int enable);
 PKV_API int pkv_get_checked(void);

@@ -361,3 +361,13 @@ const char* pkv_status_string(pkv_status s) {
 const char* pkv_last_error(void) { return g_last_error; }
 
 }  // extern "C"
+
+namespace pkv {
+
+// Lets other translation units of the library report a failure through
+// pkv_last_error().
+void set_last_error_message(const char* msg) {
+  snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+}
+
+}  // namespace pkv
