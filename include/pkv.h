@@ -99,7 +99,7 @@ PKV_API pkv_status pkv_kv_append(const int64_t *slot_mapping, int64_t num_tokens
  * need, for num_seqs sequences of at most max_context positions on the
  * current device.  The split count depends only on these arguments, the
  * device's SM count and pkv_set_split_tiles; both decode calls use the same
- * rule.  A workspace size of 0 means no workspace is needed.
+ * rule.  The size covers whichever decode kernel the call selects.
  */
 PKV_API int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads,
                               int32_t max_context);
@@ -190,6 +190,17 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
     const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_blocks,
     const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
     int32_t block_size, float scale, pkv_heads heads, void *out, void *stream);
+
+/*
+ * Which decode kernel later calls use: 0 automatic (the default: the
+ * tensor-core kernel wherever it applies -- contiguous layout, or a paged
+ * block size that is a multiple of 16 -- else the split kernel), 1 always the
+ * split (CUDA-core) kernel, 2 / 3 the tensor-core kernel with 4 warps x 4
+ * stages / 8 warps x 2 stages per CTA (PKV_ERR_UNSUPPORTED where it does not
+ * apply).  Meant for tests and tuning; both kernels compute the same result.
+ */
+PKV_API void pkv_set_decode_variant(int variant);
+PKV_API int pkv_get_decode_variant(void);
 
 /* Checked mode on (1) or off (0, the default) for later calls. */
 PKV_API void pkv_set_checked(int enable);

@@ -23,6 +23,7 @@ DEVERR_NAMES = {0: "none", 1: "block_id", 2: "slot", 3: "req_id", 4: "context",
 EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size",
             "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
+            "pkv_set_decode_variant", "pkv_get_decode_variant",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -63,6 +64,9 @@ def lib():
     L.pkv_set_checked.argtypes = [ctypes.c_int]
     L.pkv_set_checked.restype = None
     L.pkv_get_checked.restype = ctypes.c_int
+    L.pkv_set_decode_variant.argtypes = [ctypes.c_int]
+    L.pkv_set_decode_variant.restype = None
+    L.pkv_get_decode_variant.restype = ctypes.c_int
     L.pkv_set_split_tiles.argtypes = [i32]
     L.pkv_set_split_tiles.restype = None
     L.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -229,6 +233,19 @@ def set_checked(enable):
 
 def get_checked():
     return bool(lib().pkv_get_checked())
+
+
+# decode kernel selection: automatic, the split (CUDA-core) kernel, or the
+# tensor-core kernel in its 4-warp x 4-stage / 8-warp x 2-stage shapes
+VARIANT_AUTO, VARIANT_SPLIT, VARIANT_TC_4X4, VARIANT_TC_8X2 = 0, 1, 2, 3
+
+
+def set_decode_variant(variant):
+    lib().pkv_set_decode_variant(int(variant))
+
+
+def get_decode_variant():
+    return int(lib().pkv_get_decode_variant())
 
 
 def set_split_tiles(tiles):

@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["pkv_api.cu", "kv_ops.cu", "decode_paged.cu", "decode_contig.cu", "pkv_noalloc.cu"]
+SOURCES = ["pkv_api.cu", "kv_ops.cu", "decode_paged.cu", "decode_contig.cu", "decode_tc.cu",
+           "pkv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

@@ -1,0 +1,112 @@
+// decode_tc.cu -- host launch of the tensor-core / stream-K decode kernels:
+// tensor-map encoding, batch chunking, kernel instantiations.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "decode_tc.cuh"
+#include "decode_tc_launch.h"
+
+namespace pkv {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [rows][128] bf16 viewed as a 2-D tensor; boxes of 16 rows x 64 columns
+// (128 bytes), 128-byte swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+  const cuuint32_t box[2] = {64u, 16u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kContig, int W, int S>
+cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,
+                       int num_ctas, cudaStream_t stream) {
+  using L = TcSmem<W, S>;
+  static unsigned long long done_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  auto kernel = decode_tc_kernel<kContig, W, S>;
+  if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
+  }
+  // Batches above kTcMaxSeqs run as consecutive chunks reusing the workspace.
+  for (int s0 = 0; s0 < p0.num_seqs; s0 += kTcMaxSeqs) {
+    TcParams p = p0;
+    p.num_seqs = (p0.num_seqs - s0) < kTcMaxSeqs ? (p0.num_seqs - s0) : kTcMaxSeqs;
+    p.q += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
+    p.out += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
+    p.ctx_lens += s0;
+    if (kContig) p.req_ids += s0;
+    else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
+    kernel<<<num_ctas, W * 32, L::kTotal, stream>>>(tk, tv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
+    decode_tc_combine_kernel<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p, num_ctas);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t tc_workspace_bytes(int num_ctas) {
+  const size_t rec = static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float);
+  const size_t prefix = (static_cast<size_t>(kTcMaxSeqs + 1) * sizeof(int32_t) + 255) / 256 * 256;
+  return rec + prefix;
+}
+
+TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, const void* v,
+                          int64_t rows_total, int cfg, int num_ctas, void* workspace,
+                          cudaStream_t stream, cudaError_t* cuda_err) {
+  *cuda_err = cudaSuccess;
+  alignas(64) CUtensorMap tk;
+  alignas(64) CUtensorMap tv;
+  if (!encode_rows(&tk, k, rows_total) || !encode_rows(&tv, v, rows_total))
+    return TcStatus::kEncodeFailed;
+  TcParams p = p_in;
+  p.rec = static_cast<float*>(workspace);
+  p.prefix_out = reinterpret_cast<int32_t*>(
+      static_cast<unsigned char*>(workspace) +
+      static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float));
+  cudaError_t e;
+  if (contig) {
+    e = cfg == 1 ? launch_cfg<true, 8, 2>(tk, tv, p, num_ctas, stream)
+                 : launch_cfg<true, 4, 4>(tk, tv, p, num_ctas, stream);
+  } else {
+    e = cfg == 1 ? launch_cfg<false, 8, 2>(tk, tv, p, num_ctas, stream)
+                 : launch_cfg<false, 4, 4>(tk, tv, p, num_ctas, stream);
+  }
+  *cuda_err = e;
+  return e == cudaSuccess ? TcStatus::kOk : TcStatus::kCudaError;
+}
+
+}  // namespace pkv

@@ -1,0 +1,502 @@
+// decode_tc.cuh -- decode attention over a paged (block size a multiple of 16)
+// or contiguous KV cache with warp-level tensor-core math and a persistent,
+// evenly balanced ("stream-K") schedule.  sm_103a.
+//
+// Same result as decode_attention.cuh: for sequence i, query head h, KV head
+// h / G, out[i][h] = sum_j softmax_j(scale * q . K_j) V_j over j < ctx_i
+// ("Running Out of Cache": block tables map positions to blocks;
+// "Leveraging Low-Level CUDA APIs for vAttention's Dynamic Memory" 5.2.3:
+// request sub-tensor at reqId x S).
+//
+// Schedule.  The work is the flattened list of 16-token tiles of every
+// (sequence, KV head) pair, pair p = seq * Hkv + kvh in order.  The grid has
+// one CTA per SM; CTA c takes tiles [c*T/P, (c+1)*T/P) -- every CTA gets the
+// same number of tiles whatever the context lengths.  A CTA walks its range
+// pair by pair ("segments"); its warps take the segment's tiles round-robin.
+// A segment that covers a whole pair writes the bf16 output directly; the at
+// most two partial segments of a CTA (its first and its last) write an fp32
+// record (o, m, l) that the combine kernel merges.
+//
+// Data movement.  K and V tiles (16 rows x 256 B) come in through the TMA
+// engine from a 2-D tensor map over the cache's rows, as two 64-column boxes
+// with 128-byte swizzling (so ldmatrix reads are free of bank conflicts),
+// into a per-warp ring of shared-memory stages completed by mbarriers.  The
+// group's query rows ride along with a warp's first tile of each segment.
+//
+// Math per tile (one warp): S^T[16 tokens x 8 heads] = K . Q^T with 8
+// mma.m16n8k16 (bf16 in, fp32 accumulate); fp32 online softmax in base 2 on
+// the accumulator fragment; P is packed to bf16 and transposed in registers
+// (movmatrix) into the B operand of O^T[128 x 8] += V^T . P^T (8 more mma,
+// V^T fetched with ldmatrix.trans).  Query heads beyond G are zero padding.
+#pragma once
+
+#include <cuda.h>
+#include <math.h>
+
+#include "decode_tc_launch.h"
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+constexpr int kTcMaxSeqs = 1024;      // sequences per launch (host splits larger batches)
+constexpr int kTcHeads = 8;           // mma N: query heads of one KV head, padded
+constexpr int kRecStride = 132;       // floats per head record: o[128], m, l, pad
+constexpr int kTcStageBytes = 10240;  // K tile 4 KiB, V tile 4 KiB, Q rows 2 KiB
+constexpr int kBoxBytes = 2048;       // 16 rows x 128 B: half a head_dim row
+
+
+template <int W, int S>
+struct TcSmem {
+  static constexpr int kStagesOff = 0;
+  static constexpr int kBarsOff = W * S * kTcStageBytes;
+  static constexpr int kMergeOff = kBarsOff + W * S * 8;
+  static constexpr int kMLOff = kMergeOff + W * kTcHeads * kRecStride * 4;
+  static constexpr int kCtxOff = kMLOff + W * kTcHeads * 2 * 4;
+  static constexpr int kReqOff = kCtxOff + kTcMaxSeqs * 4;
+  static constexpr int kPrefixOff = kReqOff + kTcMaxSeqs * 4;
+  static constexpr int kEnd = kPrefixOff + (kTcMaxSeqs + 1) * 4;
+  static constexpr int kTotal = kEnd + 1024;  // slack to align the base to 1 KiB
+};
+
+// Context length as the kernels use it (checked mode: clamp and report).
+__device__ __forceinline__ int tc_context(const TcParams& p, int i, bool contig, bool report) {
+  int ctx = p.ctx_lens[i];
+  if (ctx < 0) ctx = 0;
+  if (p.checked) {
+    int64_t cap = contig ? p.bs : static_cast<int64_t>(p.max_blocks) * p.bs;
+    if (cap > p.max_context) cap = p.max_context;
+    if (ctx > cap) {
+      if (report) record_error(p.err, kErrContext);
+      ctx = static_cast<int>(cap);
+    }
+    if (contig) {
+      const int r = p.req_ids[i];
+      if (r < 0 || r >= p.max_reqs) {
+        if (report) record_error(p.err, kErrReqId);
+        ctx = 0;
+      }
+    }
+  }
+  return ctx;
+}
+
+// A run of tiles of one pair inside a CTA's range.
+struct TcSeg {
+  int64_t x0, x1;        // tiles [x0, x1) of the flattened list
+  int64_t pstart, pend;  // the whole pair's tiles
+  int seq, kvh;
+};
+
+// Segment starting at tile x (x < hi <= T).  prefix[i] = tiles of sequences
+// before i; pair (i, h) holds tiles [Hkv*prefix[i] + h*n_i, + n_i).
+__device__ __forceinline__ TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_t* prefix,
+                                             int B, int Hkv) {
+  int a = 0, b = B - 1;
+  while (a < b) {
+    const int mid = (a + b + 1) >> 1;
+    if (static_cast<int64_t>(Hkv) * prefix[mid] <= x) a = mid; else b = mid - 1;
+  }
+  const int64_t base = static_cast<int64_t>(Hkv) * prefix[a];
+  const int n = prefix[a + 1] - prefix[a];  // > 0 because x < Hkv*prefix[a+1]
+  TcSeg s;
+  s.seq = a;
+  s.kvh = static_cast<int>((x - base) / n);
+  s.pstart = base + static_cast<int64_t>(s.kvh) * n;
+  s.pend = s.pstart + n;
+  s.x0 = x;
+  s.x1 = s.pend < hi ? s.pend : hi;
+  return s;
+}
+
+// The CTA that owns tile x when T tiles are split evenly over P CTAs
+// (CTA c owns [floor(c*T/P), floor((c+1)*T/P))).
+__device__ __forceinline__ int tc_owner(int64_t x, int64_t T, int P) {
+  return static_cast<int>(((x + 1) * P + T - 1) / T) - 1;
+}
+
+template <bool kContig, int W, int S>
+__global__ void __launch_bounds__(W * 32, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const TcParams p) {
+  using L = TcSmem<W, S>;
+  constexpr unsigned kFull = 0xffffffffu;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int c = blockIdx.x;
+  const int P = gridDim.x;
+  const int B = p.num_seqs;
+  const int G = p.G;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarsOff) + warp * S;
+  float* merge = reinterpret_cast<float*>(smem + L::kMergeOff);
+  float* ml = reinterpret_cast<float*>(smem + L::kMLOff);
+  int32_t* ctx_s = reinterpret_cast<int32_t*>(smem + L::kCtxOff);
+  int32_t* req_s = reinterpret_cast<int32_t*>(smem + L::kReqOff);
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefixOff);
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+
+  // ---- tile counts and their prefix over sequences (every CTA, once)
+  for (int i = tid; i < B; i += W * 32) {
+    const int ctx = tc_context(p, i, kContig, c == 0);
+    ctx_s[i] = ctx;
+    if (kContig) req_s[i] = ctx > 0 ? p.req_ids[i] : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (B + 31) / 32;
+    const int i0 = lane * per;
+    int sum = 0;
+    for (int i = i0; i < i0 + per && i < B; ++i) sum += (ctx_s[i] + 15) >> 4;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = i0; i < i0 + per && i < B; ++i) {
+      prefix[i] = run;
+      run += (ctx_s[i] + 15) >> 4;
+    }
+    if (lane == 31) prefix[B] = incl;
+  }
+  __syncthreads();
+  if (c == 0)
+    for (int i = tid; i <= B; i += W * 32) p.prefix_out[i] = prefix[i];
+  const int64_t T = static_cast<int64_t>(p.Hkv) * prefix[B];
+  const int64_t lo = static_cast<int64_t>(c) * T / P;
+  const int64_t hi = static_cast<int64_t>(c + 1) * T / P;
+  if (lo >= hi) return;  // uniform across the CTA
+
+  const uint64_t policy = l2_policy_evict_first();
+  unsigned char* stage0 = smem + L::kStagesOff + warp * S * kTcStageBytes;
+
+  // ---- this warp's tile stream: segment by segment, tiles x0 + warp, + W, ...
+  TcSeg iseg = tc_find_seg(lo, hi, prefix, B, p.Hkv);
+  int64_t ix = iseg.x0 + warp;
+  bool ivalid = true;
+  auto settle = [&]() {
+    while (ix >= iseg.x1) {
+      if (iseg.x1 >= hi) {
+        ivalid = false;
+        return;
+      }
+      iseg = tc_find_seg(iseg.x1, hi, prefix, B, p.Hkv);
+      ix = iseg.x0 + warp;
+    }
+  };
+  settle();
+
+  // block-table entry of the tile at the issue cursor (lane 0 only)
+  auto load_entry = [&]() -> int32_t {
+    if (kContig || lane != 0 || !ivalid) return 0;
+    const int64_t pos = (ix - iseg.pstart) * 16;
+    return __ldg(p.block_tables + static_cast<int64_t>(iseg.seq) * p.max_blocks + pos / p.bs);
+  };
+
+  auto issue = [&](int stage, int32_t entry) {
+    if (lane == 0) {
+      unsigned char* st = stage0 + stage * kTcStageBytes;
+      const bool first = ix == iseg.x0 + warp;
+      const int64_t pos = (ix - iseg.pstart) * 16;
+      bool kv_ok = true;
+      int64_t row;
+      if (kContig) {
+        row = (static_cast<int64_t>(req_s[iseg.seq]) * p.Hkv + iseg.kvh) * p.bs + pos;
+      } else {
+        if (p.checked && (entry < 0 || entry >= p.num_blocks)) {
+          record_error(p.err, kErrBlockId);
+          kv_ok = false;  // skip the copy: stale rows, undefined output, no fault
+        }
+        row = (static_cast<int64_t>(entry) * p.Hkv + iseg.kvh) * p.bs + pos % p.bs;
+      }
+      const uint32_t bytes = (kv_ok ? 4u * kBoxBytes : 0u) +
+                             (first ? static_cast<uint32_t>(G) * kRowBytes : 0u);
+      mbar_arrive_expect_tx(&bars[stage], bytes);
+      if (kv_ok) {
+        const int32_t y = static_cast<int32_t>(row);
+        tma_load_2d(st, &tmk, 0, y, &bars[stage], policy);
+        tma_load_2d(st + kBoxBytes, &tmk, 64, y, &bars[stage], policy);
+        tma_load_2d(st + 2 * kBoxBytes, &tmv, 0, y, &bars[stage], policy);
+        tma_load_2d(st + 3 * kBoxBytes, &tmv, 64, y, &bars[stage], policy);
+      }
+      if (first) {
+        const uint16_t* qsrc =
+            p.q + (static_cast<int64_t>(iseg.seq) * p.Hq + iseg.kvh * G) * kHeadDim;
+        bulk_copy_g2s(st + 4 * kBoxBytes, qsrc, G * kRowBytes, &bars[stage], policy);
+      }
+    }
+  };
+
+  int issued = 0;
+  for (int s = 0; s < S && ivalid; ++s) {
+    issue(s, load_entry());
+    ++issued;
+    ix += W;
+    settle();
+  }
+  int32_t next_entry = load_entry();
+
+  // ---- per-lane fragment geometry
+  const int g = lane >> 2;   // accumulator row group
+  const int tq = lane & 3;   // accumulator column pair
+  uint32_t koff[4], voff[4];
+  {
+    const int rk = (lane & 7) + 8 * ((lane >> 3) & 1), hk = lane >> 4;
+    const int rv = (lane & 7) + 8 * (lane >> 4), hv = (lane >> 3) & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      koff[j] = rk * 128 + ((((2 * j + hk) ^ (rk & 7))) << 4);
+      voff[j] = rv * 128 + ((((2 * j + hv) ^ (rv & 7))) << 4);
+    }
+  }
+
+  uint32_t qb[8][2];
+  float acc[8][4];
+  float m0, m1, l0, l1;
+  int consumed = 0;
+  bool dead = false;
+
+  TcSeg seg = tc_find_seg(lo, hi, prefix, B, p.Hkv);
+  while (true) {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const int ctx = ctx_s[seg.seq];
+
+    for (int64_t x = seg.x0 + warp; x < seg.x1 && !dead; x += W) {
+      const int stage = consumed % S;
+      const uint32_t parity = static_cast<uint32_t>(consumed / S) & 1u;
+      if (!__all_sync(kFull, mbar_wait_bounded(&bars[stage], parity))) {
+        dead = true;
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      ++consumed;
+      unsigned char* st = stage0 + stage * kTcStageBytes;
+      const uint32_t kaddr = smem_addr(st);
+      const uint32_t vaddr = kaddr + 2 * kBoxBytes;
+      const int nvalid = min(16, ctx - static_cast<int>((x - seg.pstart) * 16));
+
+      if (x == seg.x0 + warp) {  // this warp's first tile of the segment: load Q^T fragments
+        const uint32_t* qs = reinterpret_cast<const uint32_t*>(st + 4 * kBoxBytes);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          qb[ks][0] = g < G ? qs[g * 64 + ks * 8 + tq] : 0u;
+          qb[ks][1] = g < G ? qs[g * 64 + ks * 8 + 4 + tq] : 0u;
+        }
+      }
+      if (nvalid < 16) {  // rows past the context must not feed p.V (0 * NaN)
+        for (int idx = lane; idx < (16 - nvalid) * 16; idx += 32) {
+          const int r = nvalid + (idx >> 4);
+          const int ch = idx & 15;
+          *reinterpret_cast<uint4*>(st + 2 * kBoxBytes + (ch >> 3) * kBoxBytes + r * 128 +
+                                    (ch & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+
+      // ---- S^T = K . Q^T  (two accumulation chains)
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a[4];
+        ldmatrix_x4(a, kaddr + (ks >> 2) * kBoxBytes + koff[ks & 3]);
+        if (ks & 1) mma_bf16_16816(sb, a, qb[ks][0], qb[ks][1]);
+        else mma_bf16_16816(sa, a, qb[ks][0], qb[ks][1]);
+      }
+      const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+      const float s0 = v0 ? (sa[0] + sb[0]) * p.qscale : -INFINITY;  // token g,   head 2tq
+      const float s1 = v0 ? (sa[1] + sb[1]) * p.qscale : -INFINITY;  // token g,   head 2tq+1
+      const float s2 = v1 ? (sa[2] + sb[2]) * p.qscale : -INFINITY;  // token g+8, head 2tq
+      const float s3 = v1 ? (sa[3] + sb[3]) * p.qscale : -INFINITY;  // token g+8, head 2tq+1
+
+      // ---- online softmax, per head column
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+      }
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      if (n0 > m0) {
+        const float a = fast_exp2(m0 - n0);
+        l0 *= a;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { acc[i][0] *= a; acc[i][2] *= a; }
+        m0 = n0;
+      }
+      if (n1 > m1) {
+        const float a = fast_exp2(m1 - n1);
+        l1 *= a;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { acc[i][1] *= a; acc[i][3] *= a; }
+        m1 = n1;
+      }
+      const float p0 = fast_exp2(s0 - m0), p2 = fast_exp2(s2 - m0);
+      const float p1 = fast_exp2(s1 - m1), p3 = fast_exp2(s3 - m1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));  // P^T rows: tokens 0..7
+      const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8..15
+
+      // ---- O^T += V^T . P^T
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vaddr + (i >> 2) * kBoxBytes + voff[i & 3]);
+        mma_bf16_16816(acc[i], a, b0, b1);
+      }
+      __syncwarp();
+
+      // ---- refill this stage with the next tile of the stream
+      if (ivalid) {
+        fence_proxy_async_smem();
+        issue(stage, next_entry);
+        ++issued;
+        ix += W;
+        settle();
+        next_entry = load_entry();
+      }
+    }
+
+    // ---- merge the warps' partial results for this segment
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, o);
+      l1 += __shfl_xor_sync(kFull, l1, o);
+    }
+    float* mb = merge + warp * kTcHeads * kRecStride;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mb[(2 * tq) * kRecStride + 16 * i + g] = acc[i][0];
+      mb[(2 * tq + 1) * kRecStride + 16 * i + g] = acc[i][1];
+      mb[(2 * tq) * kRecStride + 16 * i + g + 8] = acc[i][2];
+      mb[(2 * tq + 1) * kRecStride + 16 * i + g + 8] = acc[i][3];
+    }
+    if (g == 0) {
+      ml[(warp * kTcHeads + 2 * tq) * 2] = m0;
+      ml[(warp * kTcHeads + 2 * tq) * 2 + 1] = l0;
+      ml[(warp * kTcHeads + 2 * tq + 1) * 2] = m1;
+      ml[(warp * kTcHeads + 2 * tq + 1) * 2 + 1] = l1;
+    }
+    __syncthreads();
+    const bool whole = seg.x0 == seg.pstart && seg.x1 == seg.pend;
+    const int slot = seg.x0 == lo ? 0 : 1;
+    for (int idx = tid; idx < G * kHeadDim; idx += W * 32) {
+      const int hh = idx >> 7;
+      const int d = idx & 127;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < W; ++w) M = fmaxf(M, ml[(w * kTcHeads + hh) * 2]);
+      float Ls = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float f = fast_exp2(ml[(w * kTcHeads + hh) * 2] - M);
+          Ls = fmaf(ml[(w * kTcHeads + hh) * 2 + 1], f, Ls);
+          O = fmaf(merge[(w * kTcHeads + hh) * kRecStride + d], f, O);
+        }
+      }
+      const float o = Ls > 0.f ? O / Ls : 0.f;
+      if (whole) {
+        p.out[((static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) * kHeadDim) + d] =
+            f32_to_bf16_bits(o);
+      } else {
+        float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcHeads + hh) * kRecStride;
+        r[d] = o;
+        if (d == 0) {
+          r[128] = Ls > 0.f ? M : -INFINITY;
+          r[129] = Ls;
+        }
+      }
+    }
+    __syncthreads();
+    if (seg.x1 >= hi) break;
+    seg = tc_find_seg(seg.x1, hi, prefix, B, p.Hkv);
+  }
+
+  if (dead) {
+    // give the copies still in flight a bounded chance to land before exit
+    for (int k = consumed; k < issued; ++k)
+      mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>(k / S) & 1u);
+  }
+}
+
+// One warp per (sequence, query head): zeros for an empty context; nothing
+// when one CTA covered the whole pair (it wrote the output); otherwise merge
+// the records of the CTAs that share the pair:
+//   M = max m_c,  w_c = l_c 2^(m_c - M),  out = sum w_c o_c / sum w_c.
+__global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (idx >= static_cast<int64_t>(p.num_seqs) * p.Hq) return;
+  const int seq = static_cast<int>(idx / p.Hq);
+  const int hq = static_cast<int>(idx % p.Hq);
+  const int kvh = hq / p.G;
+  const int gi = hq % p.G;
+  const int32_t* prefix = p.prefix_out;
+  const int n = prefix[seq + 1] - prefix[seq];
+  uint2* dst = reinterpret_cast<uint2*>(p.out + idx * kHeadDim + lane * 4);
+  if (n == 0) {
+    *dst = make_uint2(0u, 0u);
+    return;
+  }
+  const int64_t T = static_cast<int64_t>(p.Hkv) * prefix[p.num_seqs];
+  const int64_t pstart = static_cast<int64_t>(p.Hkv) * prefix[seq] + static_cast<int64_t>(kvh) * n;
+  const int64_t pend = pstart + n;
+  const int cf = tc_owner(pstart, T, P);
+  const int cl = tc_owner(pend - 1, T, P);
+  if (cf == cl) return;
+  // CTA cc's record for this pair: slot 0 if the pair began before cc's range
+  // (or exactly at its start), slot 1 if it began inside; CTAs whose range
+  // is empty wrote nothing and are skipped.
+  auto record = [&](int cc) -> const float* {
+    const int64_t lo_c = static_cast<int64_t>(cc) * T / P;
+    const int64_t hi_c = static_cast<int64_t>(cc + 1) * T / P;
+    if (lo_c >= hi_c) return nullptr;
+    const int slot = lo_c >= pstart ? 0 : 1;
+    return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcHeads + gi) * kRecStride;
+  };
+  float M = -INFINITY;
+  for (int cc = cf; cc <= cl; ++cc) {
+    const float* r = record(cc);
+    if (r != nullptr) M = fmaxf(M, r[128]);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float Wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int cc = cf; cc <= cl; ++cc) {
+      const float* r = record(cc);
+      if (r == nullptr) continue;
+      const float ls = r[129];
+      if (ls > 0.f) {
+        const float w = ls * fast_exp2(r[128] - M);
+        const float4 o = *reinterpret_cast<const float4*>(r + lane * 4);
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+        Wsum += w;
+      }
+    }
+  }
+  const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
+  const uint32_t lo16 = f32_to_bf16_bits(acc.x * inv) | (uint32_t(f32_to_bf16_bits(acc.y * inv)) << 16);
+  const uint32_t hi16 = f32_to_bf16_bits(acc.z * inv) | (uint32_t(f32_to_bf16_bits(acc.w * inv)) << 16);
+  *dst = make_uint2(lo16, hi16);
+}
+
+}  // namespace pkv

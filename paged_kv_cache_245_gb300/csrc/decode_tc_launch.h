@@ -1,0 +1,39 @@
+// decode_tc_launch.h -- host interface of the tensor-core / stream-K decode
+// path (decode_tc.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct TcParams {
+  const uint16_t* q;        // [B][Hq][128]
+  uint16_t* out;            // [B][Hq][128]
+  const int32_t* ctx_lens;  // [B]
+  const int32_t* block_tables;  // paged [B][max_blocks]
+  const int32_t* req_ids;       // contig [B]
+  float* rec;               // [gridDim.x][2][8][kRecStride]
+  int32_t* prefix_out;      // [B + 1] tile prefix per sequence (CTA 0 writes it)
+  int64_t bs;               // paged block size (multiple of 16); contig S
+  int64_t num_blocks;       // paged pool size (checked mode)
+  int32_t max_blocks, max_reqs;
+  int32_t num_seqs, Hq, Hkv, G, max_context;
+  float qscale;             // scale * log2(e)
+  int32_t checked;
+  int* err;
+};
+
+
+enum class TcStatus { kOk, kEncodeFailed, kCudaError };
+
+// Workspace bytes for the per-CTA partial records and the tile prefix.
+size_t tc_workspace_bytes(int num_ctas);
+
+// cfg 0: 4 warps x 4 stages per CTA; cfg 1: 8 warps x 2 stages.
+TcStatus launch_decode_tc(const TcParams& p, bool contig, const void* k, const void* v,
+                          int64_t rows_total, int cfg, int num_ctas, void* workspace,
+                          cudaStream_t stream, cudaError_t* cuda_err);
+
+}  // namespace pkv

@@ -10,12 +10,15 @@
 
 #include "../../include/pkv.h"
 #include "decode_launch.cuh"
+#include "decode_tc_launch.h"
 #include "kv_ops.cuh"
 
 namespace {
 
 std::atomic<int> g_checked{0};
 std::atomic<int> g_split_tiles{0};
+// 0 automatic, 1 CUDA-core split kernel, 2 tensor-core 4x4, 3 tensor-core 8x2
+std::atomic<int> g_variant{0};
 thread_local char g_last_error[256] = "";
 
 // The device error word: one int per device (module-scope __device__).
@@ -126,6 +129,18 @@ SplitPlan plan_splits(int32_t num_seqs, const pkv_heads& h, int32_t max_context,
   return s;
 }
 
+// Persistent tensor-core kernel: one CTA per SM.
+int tc_ctas(int num_sms) { return num_sms > 0 ? num_sms : 1; }
+
+// Workspace the decode calls may need: the larger of the two kernels'
+// requirements (the query does not know the layout or block size).
+size_t decode_workspace_need(int32_t num_seqs, const pkv_heads& h, int32_t max_context,
+                             int num_sms) {
+  const size_t split = plan_splits(num_seqs, h, max_context, num_sms).workspace_bytes;
+  const size_t tc = pkv::tc_workspace_bytes(tc_ctas(num_sms));
+  return split > tc ? split : tc;
+}
+
 pkv_status decode_common(bool contig, const void* q, const void* k, const void* v,
                          const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
                          const int32_t* req_ids, int32_t max_reqs, const int32_t* context_lens,
@@ -162,6 +177,47 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
   int* err = nullptr;
   st = device_info(&dev, &err, &sms);
   if (st != PKV_OK) return st;
+  const int group = h.num_q_heads / h.num_kv_heads;
+  const int64_t rows_total = contig ? static_cast<int64_t>(max_reqs) * h.num_kv_heads * bs_or_S
+                                    : static_cast<int64_t>(num_blocks) * h.num_kv_heads * bs_or_S;
+  const bool tc_ok = (contig || bs_or_S % 16 == 0) && rows_total <= 0x7fffffffLL;
+  const int variant = g_variant.load();
+  if (variant >= 2 && !tc_ok)
+    return fail(PKV_ERR_UNSUPPORTED, "tensor-core kernel needs block_size %% 16 == 0 and < 2^31 rows");
+  if (variant != 1 && tc_ok) {
+    const size_t need = pkv::tc_workspace_bytes(tc_ctas(sms));
+    if (!workspace || workspace_bytes < need)
+      return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need,
+                  workspace ? workspace_bytes : size_t{0});
+    if (!aligned(workspace, 16)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    pkv::TcParams t;
+    std::memset(&t, 0, sizeof t);
+    t.q = static_cast<const uint16_t*>(q);
+    t.out = static_cast<uint16_t*>(out);
+    t.ctx_lens = context_lens;
+    t.block_tables = block_tables;
+    t.req_ids = req_ids;
+    t.bs = bs_or_S;
+    t.num_blocks = num_blocks;
+    t.max_blocks = max_blocks;
+    t.max_reqs = max_reqs;
+    t.num_seqs = num_seqs;
+    t.Hq = h.num_q_heads;
+    t.Hkv = h.num_kv_heads;
+    t.G = group;
+    t.max_context = max_context;
+    t.qscale = scale * 1.4426950408889634f;  // log2(e)
+    t.checked = g_checked.load();
+    t.err = err;
+    cudaError_t ce = cudaSuccess;
+    const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total,
+                                                   variant == 3 ? 1 : 0, tc_ctas(sms), workspace,
+                                                   static_cast<cudaStream_t>(stream), &ce);
+    if (ts == pkv::TcStatus::kEncodeFailed)
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
+    if (ts != pkv::TcStatus::kOk) return cuda_fail(ce, "decode launch");
+    return PKV_OK;
+  }
   const SplitPlan plan = plan_splits(num_seqs, h, max_context, sms);
   if (plan.nsplit > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
   if (plan.workspace_bytes > 0) {
@@ -197,7 +253,6 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
   p.qscale = scale * 1.4426950408889634f;  // log2(e)
   p.checked = g_checked.load();
   p.err = err;
-  const int group = h.num_q_heads / h.num_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = contig ? pkv::launch_decode_contig(p, group, s)
                                : pkv::launch_decode_paged(p, group, s);
@@ -256,7 +311,7 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, pkv_heads heads, int32_t max_
   int sms = 0;
   if (device_info(nullptr, nullptr, &sms) != PKV_OK) return 0;
   if (check_heads(heads) != PKV_OK || num_seqs <= 0 || max_context < 0) return 0;
-  return plan_splits(num_seqs, heads, max_context, sms).workspace_bytes;
+  return decode_workspace_need(num_seqs, heads, max_context, sms);
 }
 
 pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -323,6 +378,8 @@ pkv_status pkv_block_copy(const int64_t* src_dst_pairs, int64_t n, void* const* 
 }
 
 void pkv_set_checked(int enable) { g_checked.store(enable ? 1 : 0); }
+void pkv_set_decode_variant(int variant) { g_variant.store(variant >= 0 && variant <= 3 ? variant : 0); }
+int pkv_get_decode_variant(void) { return g_variant.load(); }
 int pkv_get_checked(void) { return g_checked.load(); }
 void pkv_set_split_tiles(int32_t tiles) {
   if (tiles > 0) tiles = (tiles + pkv::kDecodeWarps - 1) / pkv::kDecodeWarps * pkv::kDecodeWarps;

@@ -21,10 +21,17 @@ DEV = torch.device("cuda:0")
 def _reset_modes():
     pkv.set_split_tiles(0)
     pkv.set_checked(False)
+    pkv.set_decode_variant(pkv.VARIANT_AUTO)
     yield
     pkv.set_split_tiles(0)
     pkv.set_checked(False)
+    pkv.set_decode_variant(pkv.VARIANT_AUTO)
     torch.cuda.synchronize()
+
+
+# every decode kernel shape: automatic (tensor-core where it applies), the
+# split CUDA-core kernel, and the tensor-core kernel's 8-warp shape
+VARIANTS = [pkv.VARIANT_AUTO, pkv.VARIANT_SPLIT, pkv.VARIANT_TC_8X2]
 
 
 def _batch(hq, hkv, ctx, bs, seed=5, spare=3):
@@ -48,9 +55,11 @@ def test_tiny_workload_before_and_after_append():
     assert_attention_close(L.gpu_attend(), L.oracle_attend(), "after append")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (6, 2), (8, 2), (10, 2), (12, 2), (14, 2),
                                     (16, 2), (56, 8), (32, 4)])
-def test_every_group_size(hq, hkv):
+def test_every_group_size(hq, hkv, variant):
+    pkv.set_decode_variant(variant)
     ctx = [1, 2, 15, 16, 17, 31, 33, 64, 100, 257, 700]
     L = DeviceLayer(_batch(hq, hkv, ctx, 16), 0, DEV)
     L.gpu_append()
@@ -60,8 +69,12 @@ def test_every_group_size(hq, hkv):
     assert_attention_close(L.gpu_attend(), L.oracle_attend(), "G=%d" % (hq // hkv))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("bs", [1, 3, 8, 16, 24, 32, 64, 128, 256])
-def test_block_sizes(bs):
+def test_block_sizes(bs, variant):
+    if variant == pkv.VARIANT_TC_8X2 and bs % 16:
+        pytest.skip("the tensor-core kernel takes block sizes that are multiples of 16")
+    pkv.set_decode_variant(variant)
     ctx = [1, 5, 16, 17, 48, 129, 300, 513]
     L = DeviceLayer(_batch(8, 2, ctx, bs, seed=bs), 0, DEV)
     L.gpu_append()
@@ -75,6 +88,7 @@ def test_block_sizes(bs):
 def test_split_counts_agree_with_oracle(tiles):
     """Any number of context splits gives the oracle's result (the split
     combine is exercised whenever a context spans more than one split)."""
+    pkv.set_decode_variant(pkv.VARIANT_SPLIT)
     pkv.set_split_tiles(tiles)
     ctx = [1, 63, 64, 65, 250, 1024, 2049]
     L = DeviceLayer(_batch(32, 8, ctx, 16, seed=11), 0, DEV)
@@ -83,8 +97,10 @@ def test_split_counts_agree_with_oracle(tiles):
     assert_attention_close(L.gpu_attend(), L.oracle_attend(), "tiles=%d" % tiles)
 
 
-def test_zero_and_single_contexts():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_zero_and_single_contexts(variant):
     """ctx = 0 gives zeros; ctx = 1 returns v_0 exactly (bf16 round trip)."""
+    pkv.set_decode_variant(variant)
     b = _batch(8, 2, [1, 1, 5], 16)
     b.ctx = np.array([0, 1, 5], np.int32)
     L = DeviceLayer(b, 0, DEV)
@@ -99,7 +115,9 @@ def test_zero_and_single_contexts():
     assert_attention_close(out, L.oracle_attend(), "ctx 0/1/5")
 
 
-def test_all_empty_batch_and_empty_call():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_all_empty_batch_and_empty_call(variant):
+    pkv.set_decode_variant(variant)
     b = _batch(8, 2, [3, 3], 16)
     b.ctx = np.zeros(2, np.int32)
     L = DeviceLayer(b, 0, DEV)
@@ -111,7 +129,9 @@ def test_all_empty_batch_and_empty_call():
     pkv.paged_decode_attention(empty_q, L.k_cache, L.v_cache, L.tables[:0], L.ctx[:0], 0, 1.0)
 
 
-def test_block_relabelling_is_bit_exact():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_block_relabelling_is_bit_exact(variant):
+    pkv.set_decode_variant(variant)
     ctx = [7, 100, 333, 1025]
     b = _batch(32, 8, ctx, 16, seed=21)
     L = DeviceLayer(b, 0, DEV)
@@ -127,10 +147,12 @@ def test_block_relabelling_is_bit_exact():
     assert torch.equal(out, base)
 
 
-def test_block_size_and_layout_do_not_change_bits():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_block_size_and_layout_do_not_change_bits(variant):
     """The kernels tile the logical sequence in 16-token tiles whatever the
     layout, so block sizes 16..128 and the contiguous layout give identical
     bits for identical logical K/V."""
+    pkv.set_decode_variant(variant)
     ctx = W.ragged_lengths(24, seed=3, max_len=1500)
     ref = None
     base = W.make_paged_batch(W.LLAMA3_8B, ctx, 16, seed=9)
@@ -174,12 +196,13 @@ def test_contig_against_oracle_with_permuted_request_rows():
     vb = torch.randn((max_reqs, hkv, S, 128), generator=g).to(torch.bfloat16)
     q = torch.randn((len(ctx), hq, 128), generator=g).to(torch.bfloat16)
     ref = oracle.contig_decode(W.to_u16(q), W.to_u16(kb), W.to_u16(vb), req, ctx, 0.1)
-    for tiles in (0, 4):
+    for variant, tiles in ((0, 0), (1, 0), (1, 4), (3, 0)):
+        pkv.set_decode_variant(variant)
         pkv.set_split_tiles(tiles)
         out = pkv.contig_decode_attention(q.to(DEV), kb.to(DEV), vb.to(DEV),
                                           torch.as_tensor(req, device=DEV),
                                           torch.as_tensor(ctx, device=DEV), S, 0.1)
-        assert_attention_close(out, ref, "contig tiles=%d" % tiles)
+        assert_attention_close(out, ref, "contig variant=%d tiles=%d" % (variant, tiles))
 
 
 def test_contig_append_positions():
@@ -250,7 +273,9 @@ def test_large_block_copy():
 
 # ------------------------------------------------------------- checked mode
 
-def test_checked_mode_reports_bad_block_id_without_fault():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_checked_mode_reports_bad_block_id_without_fault(variant):
+    pkv.set_decode_variant(variant)
     b = _batch(8, 2, [20, 40], 16)
     L = DeviceLayer(b, 0, DEV)
     assert pkv.get_device_error() == "none"
@@ -265,7 +290,9 @@ def test_checked_mode_reports_bad_block_id_without_fault():
     assert pkv.get_device_error() == "none"
 
 
-def test_checked_mode_reports_bad_slot_and_context_and_request():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_checked_mode_reports_bad_slot_and_context_and_request(variant):
+    pkv.set_decode_variant(variant)
     b = _batch(8, 2, [20, 40], 16)
     L = DeviceLayer(b, 0, DEV)
     pkv.set_checked(True)
@@ -302,3 +329,24 @@ def test_workspace_is_checked():
     out = pkv.paged_decode_attention(L.q, L.k_cache, L.v_cache, L.tables, L.ctx, b.max_context,
                                      L.scale, workspace=ws)
     assert_attention_close(out, L.oracle_attend(), "explicit workspace")
+
+
+def test_large_batch_is_chunked():
+    """More sequences than one tensor-core launch takes (1024) run as
+    consecutive chunks; ragged short contexts, many of them empty."""
+    ctx = np.random.default_rng(8).integers(0, 40, size=1500).astype(np.int32)
+    ctx[:3] = [1, 39, 0]
+    b = _batch(16, 4, np.maximum(ctx, 1), 16, seed=12)
+    b.ctx = ctx
+    L = DeviceLayer(b, 0, DEV)
+    L.set_step(b)
+    assert_attention_close(L.gpu_attend(), L.oracle_attend(), "1500 sequences")
+
+
+def test_variant_knob_rejects_tensor_core_for_odd_block_size():
+    pkv.set_decode_variant(pkv.VARIANT_TC_4X4)
+    b = _batch(8, 2, [20, 40], 24)
+    L = DeviceLayer(b, 0, DEV)
+    with pytest.raises(pkv.PkvError) as e:
+        L.gpu_attend()
+    assert e.value.status == 2
