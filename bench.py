@@ -203,7 +203,14 @@ class DeviceWorkload:
         self.nsplit = pkv.decode_num_splits(b.B, shape.num_q_heads, shape.num_kv_heads,
                                             b.max_context)
 
+    @property
+    def uses_tc(self):
+        return self.batch.block_size % 16 == 0 and self.pkv.get_decode_variant() != 1
+
     def launches_per_step(self):
+        # kv_append, the attention kernel and its combine kernel per layer
+        if self.uses_tc:
+            return self.shape.num_layers * 3
         return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0))
 
     def layer(self, l, events=None):
@@ -220,6 +227,13 @@ class DeviceWorkload:
     def step(self, events=None):
         for l in range(self.shape.num_layers):
             self.layer(l, None if events is None else events[l])
+
+    def attention_only(self):
+        for l in range(self.shape.num_layers):
+            li = self.layers[l]
+            self.pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, self.tables, self.ctx,
+                                            self.batch.max_context, self.scale, out=self.out[l],
+                                            workspace=self.workspace)
 
 
 def _barrier(world):
@@ -246,28 +260,47 @@ def run_gpu(args, world, rank, local):
     nl = wl.shape.num_layers
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(max(args.warmup, 3)):
+    # Direct launches first (sets kernel attributes, warms caches), then the
+    # step and the attention calls alone are captured as CUDA graphs: a decode
+    # loop replays the same launches every step, so the host's per-call
+    # overhead stays out of the device-time measurement.
+    for _ in range(3):
         wl.step()
     torch.cuda.synchronize(dev)
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph):
+        wl.step()
+    attn_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(attn_graph):
+        wl.attention_only()
+    torch.cuda.synchronize(dev)
+    for _ in range(max(args.warmup, 3)):
+        step_graph.replay()
+    torch.cuda.synchronize(dev)
 
-    # ---- timed region: K decode steps, attention calls bracketed by events
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(nl)] for _ in range(args.steps)]
+    # ---- timed region: K decode steps (graph replays) between two events
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     _barrier(world)
     torch.cuda.synchronize(dev)
     clocks.start()
-    t0.record(stream)
+    t0.record()
     for k in range(args.steps):
-        wl.step(ev[k])
-    t1.record(stream)
+        step_graph.replay()
+    t1.record()
     torch.cuda.synchronize(dev)
     _barrier(world)
+    # ---- the attention calls alone (same calls, same data), for the roofline
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    attn_reps = max(args.steps // 2, 3)
+    a0.record()
+    for k in range(attn_reps):
+        attn_graph.replay()
+    a1.record()
+    torch.cuda.synchronize(dev)
     clock_info = clocks.stop()
     elapsed_ms = _max_over_ranks(t0.elapsed_time(t1), world, dev)
-    attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
-    attn_avg_ms = _max_over_ranks(float(np.mean(attn_ms)), world, dev)
+    attn_avg_ms = _max_over_ranks(a0.elapsed_time(a1) / (attn_reps * nl), world, dev)
 
     B = wl.batch.B
     ms_per_step = elapsed_ms / args.steps
@@ -304,12 +337,17 @@ def run_gpu(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                      "traffic": _profiled_traffic(args.workload),
-                     "kernel": "paged_decode_attention call (decode_attention_kernel + "
+                     "kernel": "paged_decode_attention call (decode_tc_kernel + "
+                               "decode_tc_combine_kernel)" if wl.uses_tc else
+                               "paged_decode_attention call (decode_attention_kernel + "
                                "decode_combine_kernel)",
                      "algorithmic_bytes_per_launch": alg,
                      "avg_launch_us": round(attn_avg_ms * 1e3, 3),
+                     "timed_over": "%d replays of the step's %d attention calls" % (attn_reps, nl),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
         "gpu_launches": wl.launches_per_step() * args.steps,
+        "timing": "CUDA-graph replay of the step; roofline from a replay of the 32 "
+                  "attention calls alone",
         "clocks": clock_info,
     }
     if e2e is not None:
@@ -322,16 +360,24 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def _time_calls(fn, iters, dev):
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+def _time_graph(fn, reps, dev, calls=1):
+    """Device time of one call of fn: `calls` calls captured in a CUDA graph,
+    replayed `reps` times between CUDA events (after a warm replay)."""
     fn()
     torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(iters):
-        fn()
+    for _ in range(reps):
+        g.replay()
     b.record()
     torch.cuda.synchronize(dev)
-    return a.elapsed_time(b) / iters
+    return a.elapsed_time(b) / (reps * calls)
 
 
 def measure_legs(wl, dev, args):
@@ -364,10 +410,16 @@ def measure_legs(wl, dev, args):
                                    b.max_context, wl.scale, out=wl.out[l],
                                    workspace=wl.workspace)
 
-    iters = max(20, args.steps // 4)
-    t_contig = _time_calls(contig, iters, dev)
-    t_paged = _time_calls(paged, iters, dev)
+    reps = max(10, args.steps // 20)
+    t_contig = _time_graph(contig, reps, dev, calls=nl)
+    t_paged = _time_graph(paged, reps, dev, calls=nl)
     del bufs
+    # the split (CUDA-core) kernel on the same calls, for comparison
+    pkv.set_decode_variant(pkv.VARIANT_SPLIT)
+    try:
+        t_split = _time_graph(paged, reps, dev, calls=nl)
+    finally:
+        pkv.set_decode_variant(pkv.VARIANT_AUTO)
 
     def append():
         l = it["i"] % wl.shape.num_layers
@@ -375,7 +427,7 @@ def measure_legs(wl, dev, args):
         li = wl.layers[l]
         pkv.kv_append(wl.slots, li.k_new, li.v_new, li.k_cache, li.v_cache)
 
-    t_append = _time_calls(append, iters, dev)
+    t_append = _time_graph(append, reps, dev, calls=wl.shape.num_layers)
     append_bytes = 2 * 2 * b.B * wl.shape.num_kv_heads * wl.shape.head_dim * 2 + 8 * b.B
 
     # Yi-34B-shaped copy on write: 96 block pairs x 60 layers of 32 KiB blocks
@@ -385,13 +437,15 @@ def measure_legs(wl, dev, args):
     ks = [torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev) for _ in range(L)]
     vs = [torch.empty((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev) for _ in range(L)]
     pairs = torch.stack([torch.arange(0, 96), torch.arange(96, 192)], 1).to(dev)
-    t_copy = _time_calls(lambda: pkv.block_copy(pairs, ks, vs), 20, dev)
+    t_copy = _time_graph(lambda: pkv.block_copy(pairs, ks, vs), 20, dev)
     copy_bytes = 2 * 96 * L * 2 * 8 * 16 * 128 * 2
     del ks, vs
     return {
         "paged_attention_us": round(t_paged * 1e3, 3),
         "contig_attention_us": round(t_contig * 1e3, 3),
         "paged_over_contig_time": round(t_paged / t_contig, 4),
+        "split_kernel_attention_us": round(t_split * 1e3, 3),
+        "split_kernel_hbm_gbs": round(alg / (t_split / 1e3) / 1e9, 1),
         "contig_hbm_gbs": round(alg / (t_contig / 1e3) / 1e9, 1),
         "kv_append_us": round(t_append * 1e3, 3),
         "kv_append_gbs": round(append_bytes / (t_append / 1e3) / 1e9, 1),

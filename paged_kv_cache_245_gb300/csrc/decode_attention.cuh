@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int kvh = blockIdx.y;
   const int seq = blockIdx.z;
 
+  grid_dependency_trigger();
+  grid_dependency_wait();
   const int ctx = effective_context(p, seq, kContig, threadIdx.x == 0 && split == 0);
   const int ntiles = ctx > 0 ? (ctx + kTileTokens - 1) / kTileTokens : 0;
   const int t_begin = split * p.chunk_tiles;
@@ -426,6 +428,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
 //   M = max_s m_s,  w_s = l_s 2^(m_s - M),  out = sum_s w_s o_s / sum_s w_s.
 template <bool kContig>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  grid_dependency_trigger();
+  grid_dependency_wait();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;

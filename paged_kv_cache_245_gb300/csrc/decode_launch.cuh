@@ -32,12 +32,11 @@ cudaError_t launch_decode_group(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = ensure_smem_limit(kernel, L::kTotal, &done_mask);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, p.Hkv, p.num_seqs);
-  kernel<<<grid, kDecodeThreads, L::kTotal, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(kernel, grid, dim3(kDecodeThreads), L::kTotal, stream, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
-  decode_combine_kernel<kContig><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_combine_kernel<kContig>, dim3(static_cast<unsigned>((rows + 3) / 4)),
+                    dim3(128), 0, stream, p);
 }
 
 template <bool kContig>

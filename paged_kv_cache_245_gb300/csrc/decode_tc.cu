@@ -65,12 +65,11 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     p.ctx_lens += s0;
     if (kContig) p.req_ids += s0;
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
-    kernel<<<num_ctas, W * 32, L::kTotal, stream>>>(tk, tv, p);
-    e = cudaGetLastError();
+    e = launch_pdl(kernel, dim3(num_ctas), dim3(W * 32), L::kTotal, stream, tk, tv, p);
     if (e != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
-    decode_tc_combine_kernel<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p, num_ctas);
-    e = cudaGetLastError();
+    e = launch_pdl(decode_tc_combine_kernel, dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128),
+                   0, stream, p, num_ctas);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -99,11 +98,11 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
       static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float));
   cudaError_t e;
   if (contig) {
-    e = cfg == 1 ? launch_cfg<true, 8, 2>(tk, tv, p, num_ctas, stream)
-                 : launch_cfg<true, 4, 4>(tk, tv, p, num_ctas, stream);
+    e = cfg == 1 ? launch_cfg<true, 12, 2>(tk, tv, p, num_ctas, stream)
+                 : launch_cfg<true, 8, 3>(tk, tv, p, num_ctas, stream);
   } else {
-    e = cfg == 1 ? launch_cfg<false, 8, 2>(tk, tv, p, num_ctas, stream)
-                 : launch_cfg<false, 4, 4>(tk, tv, p, num_ctas, stream);
+    e = cfg == 1 ? launch_cfg<false, 12, 2>(tk, tv, p, num_ctas, stream)
+                 : launch_cfg<false, 8, 3>(tk, tv, p, num_ctas, stream);
   }
   *cuda_err = e;
   return e == cudaSuccess ? TcStatus::kOk : TcStatus::kCudaError;

@@ -38,10 +38,9 @@
 
 namespace pkv {
 
-constexpr int kTcMaxSeqs = 1024;      // sequences per launch (host splits larger batches)
 constexpr int kTcHeads = 8;           // mma N: query heads of one KV head, padded
-constexpr int kRecStride = 132;       // floats per head record: o[128], m, l, pad
-constexpr int kTcStageBytes = 10240;  // K tile 4 KiB, V tile 4 KiB, Q rows 2 KiB
+constexpr int kTcMergeHeads = 4;      // heads merged per pass through shared memory
+constexpr int kTcStageBytes = 8192;   // K tile 4 KiB, V tile 4 KiB
 constexpr int kBoxBytes = 2048;       // 16 rows x 128 B: half a head_dim row
 
 
@@ -50,12 +49,13 @@ struct TcSmem {
   static constexpr int kStagesOff = 0;
   static constexpr int kBarsOff = W * S * kTcStageBytes;
   static constexpr int kMergeOff = kBarsOff + W * S * 8;
-  static constexpr int kMLOff = kMergeOff + W * kTcHeads * kRecStride * 4;
+  static constexpr int kMLOff = kMergeOff + W * kTcMergeHeads * kRecStride * 4;
   static constexpr int kCtxOff = kMLOff + W * kTcHeads * 2 * 4;
   static constexpr int kReqOff = kCtxOff + kTcMaxSeqs * 4;
   static constexpr int kPrefixOff = kReqOff + kTcMaxSeqs * 4;
   static constexpr int kEnd = kPrefixOff + (kTcMaxSeqs + 1) * 4;
   static constexpr int kTotal = kEnd + 1024;  // slack to align the base to 1 KiB
+  static_assert(kTotal <= 232448, "shared memory per CTA exceeds 227 KiB");
 };
 
 // Context length as the kernels use it (checked mode: clamp and report).
@@ -144,6 +144,11 @@ __global__ void __launch_bounds__(W * 32, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  // Programmatic dependent launch: let the next kernel in the stream get
+  // scheduled now, and wait for the previous one to finish before reading
+  // any input (no-ops without the launch attribute).
+  grid_dependency_trigger();
+  grid_dependency_wait();
 
   // ---- tile counts and their prefix over sequences (every CTA, once)
   for (int i = tid; i < B; i += W * 32) {
@@ -180,6 +185,20 @@ __global__ void __launch_bounds__(W * 32, 1)
 
   const uint64_t policy = l2_policy_evict_first();
   unsigned char* stage0 = smem + L::kStagesOff + warp * S * kTcStageBytes;
+  const int g = lane >> 2;   // accumulator row group
+  const int tq = lane & 3;   // accumulator column pair
+
+  // Q^T fragments of one segment straight from global memory:
+  // b0 = Q[g][16ks + 2tq, +1], b1 = Q[g][16ks + 2tq + 8, +9] (heads >= G are 0).
+  auto load_q = [&](uint32_t (&qf)[8][2], int seq, int kvh) {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        p.q + (static_cast<int64_t>(seq) * p.Hq + kvh * G + (g < G ? g : 0)) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[ks][0] = g < G ? __ldg(qrow + ks * 8 + tq) : 0u;
+      qf[ks][1] = g < G ? __ldg(qrow + ks * 8 + 4 + tq) : 0u;
+    }
+  };
 
   // ---- this warp's tile stream: segment by segment, tiles x0 + warp, + W, ...
   TcSeg iseg = tc_find_seg(lo, hi, prefix, B, p.Hkv);
@@ -197,6 +216,11 @@ __global__ void __launch_bounds__(W * 32, 1)
   };
   settle();
 
+  // The next segment's Q fragments are fetched into qn when the stream first
+  // reaches it (if qn is free), so the segment start does not wait on them.
+  uint32_t qn[8][2];
+  int64_t qn_pair = -1;
+
   // block-table entry of the tile at the issue cursor (lane 0 only)
   auto load_entry = [&]() -> int32_t {
     if (kContig || lane != 0 || !ivalid) return 0;
@@ -205,9 +229,12 @@ __global__ void __launch_bounds__(W * 32, 1)
   };
 
   auto issue = [&](int stage, int32_t entry) {
+    if (ix == iseg.x0 + warp && qn_pair < 0) {  // whole warp
+      load_q(qn, iseg.seq, iseg.kvh);
+      qn_pair = iseg.pstart;
+    }
     if (lane == 0) {
       unsigned char* st = stage0 + stage * kTcStageBytes;
-      const bool first = ix == iseg.x0 + warp;
       const int64_t pos = (ix - iseg.pstart) * 16;
       bool kv_ok = true;
       int64_t row;
@@ -220,20 +247,13 @@ __global__ void __launch_bounds__(W * 32, 1)
         }
         row = (static_cast<int64_t>(entry) * p.Hkv + iseg.kvh) * p.bs + pos % p.bs;
       }
-      const uint32_t bytes = (kv_ok ? 4u * kBoxBytes : 0u) +
-                             (first ? static_cast<uint32_t>(G) * kRowBytes : 0u);
-      mbar_arrive_expect_tx(&bars[stage], bytes);
+      mbar_arrive_expect_tx(&bars[stage], kv_ok ? 4u * kBoxBytes : 0u);
       if (kv_ok) {
         const int32_t y = static_cast<int32_t>(row);
         tma_load_2d(st, &tmk, 0, y, &bars[stage], policy);
         tma_load_2d(st + kBoxBytes, &tmk, 64, y, &bars[stage], policy);
         tma_load_2d(st + 2 * kBoxBytes, &tmv, 0, y, &bars[stage], policy);
         tma_load_2d(st + 3 * kBoxBytes, &tmv, 64, y, &bars[stage], policy);
-      }
-      if (first) {
-        const uint16_t* qsrc =
-            p.q + (static_cast<int64_t>(iseg.seq) * p.Hq + iseg.kvh * G) * kHeadDim;
-        bulk_copy_g2s(st + 4 * kBoxBytes, qsrc, G * kRowBytes, &bars[stage], policy);
       }
     }
   };
@@ -247,9 +267,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   }
   int32_t next_entry = load_entry();
 
-  // ---- per-lane fragment geometry
-  const int g = lane >> 2;   // accumulator row group
-  const int tq = lane & 3;   // accumulator column pair
+  // ---- per-lane ldmatrix offsets inside a 128-byte-swizzled 16 x 128 B box
   uint32_t koff[4], voff[4];
   {
     const int rk = (lane & 7) + 8 * ((lane >> 3) & 1), hk = lane >> 4;
@@ -276,6 +294,18 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int ctx = ctx_s[seg.seq];
 
     for (int64_t x = seg.x0 + warp; x < seg.x1 && !dead; x += W) {
+      if (x == seg.x0 + warp) {  // this warp's first tile of the segment
+        if (qn_pair == seg.pstart) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            qb[ks][0] = qn[ks][0];
+            qb[ks][1] = qn[ks][1];
+          }
+          qn_pair = -1;
+        } else {
+          load_q(qb, seg.seq, seg.kvh);
+        }
+      }
       const int stage = consumed % S;
       const uint32_t parity = static_cast<uint32_t>(consumed / S) & 1u;
       if (!__all_sync(kFull, mbar_wait_bounded(&bars[stage], parity))) {
@@ -289,14 +319,6 @@ __global__ void __launch_bounds__(W * 32, 1)
       const uint32_t vaddr = kaddr + 2 * kBoxBytes;
       const int nvalid = min(16, ctx - static_cast<int>((x - seg.pstart) * 16));
 
-      if (x == seg.x0 + warp) {  // this warp's first tile of the segment: load Q^T fragments
-        const uint32_t* qs = reinterpret_cast<const uint32_t*>(st + 4 * kBoxBytes);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          qb[ks][0] = g < G ? qs[g * 64 + ks * 8 + tq] : 0u;
-          qb[ks][1] = g < G ? qs[g * 64 + ks * 8 + 4 + tq] : 0u;
-        }
-      }
       if (nvalid < 16) {  // rows past the context must not feed p.V (0 * NaN)
         for (int idx = lane; idx < (16 - nvalid) * 16; idx += 32) {
           const int r = nvalid + (idx >> 4);
@@ -371,19 +393,11 @@ __global__ void __launch_bounds__(W * 32, 1)
       }
     }
 
-    // ---- merge the warps' partial results for this segment
+    // ---- merge the warps' partial results for this segment (4 heads a pass)
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l0 += __shfl_xor_sync(kFull, l0, o);
       l1 += __shfl_xor_sync(kFull, l1, o);
-    }
-    float* mb = merge + warp * kTcHeads * kRecStride;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      mb[(2 * tq) * kRecStride + 16 * i + g] = acc[i][0];
-      mb[(2 * tq + 1) * kRecStride + 16 * i + g] = acc[i][1];
-      mb[(2 * tq) * kRecStride + 16 * i + g + 8] = acc[i][2];
-      mb[(2 * tq + 1) * kRecStride + 16 * i + g + 8] = acc[i][3];
     }
     if (g == 0) {
       ml[(warp * kTcHeads + 2 * tq) * 2] = m0;
@@ -391,38 +405,53 @@ __global__ void __launch_bounds__(W * 32, 1)
       ml[(warp * kTcHeads + 2 * tq + 1) * 2] = m1;
       ml[(warp * kTcHeads + 2 * tq + 1) * 2 + 1] = l1;
     }
-    __syncthreads();
     const bool whole = seg.x0 == seg.pstart && seg.x1 == seg.pend;
     const int slot = seg.x0 == lo ? 0 : 1;
-    for (int idx = tid; idx < G * kHeadDim; idx += W * 32) {
-      const int hh = idx >> 7;
-      const int d = idx & 127;
-      float M = -INFINITY;
+    for (int h0 = 0; h0 < G; h0 += kTcMergeHeads) {
+      // lanes whose head pair (2tq, 2tq+1) falls in [h0, h0 + 4) write it
+      if ((2 * tq) >= h0 && (2 * tq) < h0 + kTcMergeHeads) {
+        float* mb = merge + (warp * kTcMergeHeads + (2 * tq - h0)) * kRecStride;
 #pragma unroll
-      for (int w = 0; w < W; ++w) M = fmaxf(M, ml[(w * kTcHeads + hh) * 2]);
-      float Ls = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float f = fast_exp2(ml[(w * kTcHeads + hh) * 2] - M);
-          Ls = fmaf(ml[(w * kTcHeads + hh) * 2 + 1], f, Ls);
-          O = fmaf(merge[(w * kTcHeads + hh) * kRecStride + d], f, O);
+        for (int i = 0; i < 8; ++i) {
+          mb[16 * i + g] = acc[i][0];
+          mb[kRecStride + 16 * i + g] = acc[i][1];
+          mb[16 * i + g + 8] = acc[i][2];
+          mb[kRecStride + 16 * i + g + 8] = acc[i][3];
         }
       }
-      const float o = Ls > 0.f ? O / Ls : 0.f;
-      if (whole) {
-        p.out[((static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) * kHeadDim) + d] =
-            f32_to_bf16_bits(o);
-      } else {
-        float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcHeads + hh) * kRecStride;
-        r[d] = o;
-        if (d == 0) {
-          r[128] = Ls > 0.f ? M : -INFINITY;
-          r[129] = Ls;
+      __syncthreads();
+      const int nh = min(kTcMergeHeads, G - h0);
+      for (int idx = tid; idx < nh * kHeadDim; idx += W * 32) {
+        const int hl = idx >> 7;
+        const int hh = h0 + hl;
+        const int d = idx & 127;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, ml[(w * kTcHeads + hh) * 2]);
+        float Ls = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            const float f = fast_exp2(ml[(w * kTcHeads + hh) * 2] - M);
+            Ls = fmaf(ml[(w * kTcHeads + hh) * 2 + 1], f, Ls);
+            O = fmaf(merge[(w * kTcMergeHeads + hl) * kRecStride + d], f, O);
+          }
+        }
+        const float o = Ls > 0.f ? O / Ls : 0.f;
+        if (whole) {
+          p.out[((static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) * kHeadDim) + d] =
+              f32_to_bf16_bits(o);
+        } else {
+          float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcHeads + hh) * kRecStride;
+          r[d] = o;
+          if (d == 0) {
+            r[128] = Ls > 0.f ? M : -INFINITY;
+            r[129] = Ls;
+          }
         }
       }
+      __syncthreads();
     }
-    __syncthreads();
     if (seg.x1 >= hi) break;
     seg = tc_find_seg(seg.x1, hi, prefix, B, p.Hkv);
   }
@@ -439,6 +468,8 @@ __global__ void __launch_bounds__(W * 32, 1)
 // the records of the CTAs that share the pair:
 //   M = max m_c,  w_c = l_c 2^(m_c - M),  out = sum w_c o_c / sum w_c.
 __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P) {
+  grid_dependency_trigger();
+  grid_dependency_wait();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;

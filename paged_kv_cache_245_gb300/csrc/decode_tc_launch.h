@@ -8,6 +8,9 @@
 
 namespace pkv {
 
+constexpr int kTcMaxSeqs = 512;  // sequences per launch (larger batches run in chunks)
+constexpr int kRecStride = 132;  // floats per head record: o[128], m, l, pad
+
 struct TcParams {
   const uint16_t* q;        // [B][Hq][128]
   uint16_t* out;            // [B][Hq][128]
@@ -31,7 +34,7 @@ enum class TcStatus { kOk, kEncodeFailed, kCudaError };
 // Workspace bytes for the per-CTA partial records and the tile prefix.
 size_t tc_workspace_bytes(int num_ctas);
 
-// cfg 0: 4 warps x 4 stages per CTA; cfg 1: 8 warps x 2 stages.
+// cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages.
 TcStatus launch_decode_tc(const TcParams& p, bool contig, const void* k, const void* v,
                           int64_t rows_total, int cfg, int num_ctas, void* workspace,
                           cudaStream_t stream, cudaError_t* cuda_err);

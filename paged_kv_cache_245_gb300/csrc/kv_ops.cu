@@ -10,6 +10,8 @@ namespace pkv {
 // One 16-lane group per 256-byte row; a 256-thread CTA moves 16 rows.
 // Rows are numbered (which in {K, V}, token t, KV head h), K first.
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  grid_dependency_trigger();
+  grid_dependency_wait();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 16 + (threadIdx.x >> 4);
   const int lane16 = threadIdx.x & 15;
   const int64_t per_kind = p.num_tokens * p.Hkv;
@@ -36,13 +38,14 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
   const int64_t rows = 2 * p.num_tokens * p.Hkv;
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + 15) / 16;
-  kv_append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 // Block copy: blockIdx.x strides over the block's 16-byte chunks, blockIdx.y
 // is the pair, blockIdx.z = 2 * layer + (0 for K, 1 for V).
 __global__ void __launch_bounds__(256) block_copy_kernel(const CopyParams p) {
+  grid_dependency_trigger();
+  grid_dependency_wait();
   const int64_t pair = blockIdx.y;
   const int layer = blockIdx.z >> 1;
   const bool is_v = blockIdx.z & 1;
@@ -77,8 +80,7 @@ cudaError_t launch_block_copy(const CopyParams& p, int64_t num_pairs, cudaStream
   if (bx > 64) bx = 64;
   const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(num_pairs),
                   static_cast<unsigned>(2 * p.num_layers));
-  block_copy_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(block_copy_kernel, grid, dim3(256), 0, stream, p);
 }
 
 }  // namespace pkv

@@ -5,6 +5,9 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+
+#include <utility>
 
 namespace pkv {
 
@@ -104,6 +107,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gm
       : "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Allow the next kernel in the stream to be scheduled now.
+__device__ __forceinline__ void grid_dependency_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the kernels this one depends on have completed and their memory
+// is visible.  Returns at once when the launch had no programmatic dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- math -------------------------------------------------------------------
 // 2^x with the hardware approximation (ex2.approx; -inf -> +0).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -185,6 +199,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Host: launch `kernel` on `stream` allowing programmatic dependent launch
+// (the kernel may be scheduled while the previous kernel of the stream is
+// still running; every kernel here calls grid_dependency_wait() before it
+// touches memory another kernel could write).  PKV_NO_PDL=1 turns it off.
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("PKV_NO_PDL");
+    return !(v != nullptr && v[0] == '1');
+  }();
+  return on;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace pkv
