@@ -64,6 +64,13 @@ def _describe(name):
                shape.num_kv_heads, shape.head_dim))
 
 
+def rank_batch(name, rank):
+    """The batch a rank decodes: every rank gets the workload's full shape
+    (weak scaling) with its own seed, so ranks hold different sequences."""
+    shape, B, ctx, bs, seed = WORKLOADS[name]
+    return W.uniform_batch(shape, B, ctx, bs, seed=seed + 1000 * rank)
+
+
 def algorithmic_bytes(batch):
     """Bytes one paged attention call must move: K and V of every attended
     position, Q and O, the block-table entries read and the context lengths."""
@@ -185,7 +192,7 @@ class DeviceWorkload:
         shape, B, ctx, bs, seed = WORKLOADS[name]
         self.name = name
         self.shape = shape
-        self.batch = W.uniform_batch(shape, B, ctx, bs, seed=seed + 1000 * rank)
+        self.batch = rank_batch(name, rank)
         self.dev = dev
         b = self.batch
         self.layers = []
@@ -242,6 +249,7 @@ def _barrier(world):
 
 
 def _max_over_ranks(x, world, dev):
+    """Max of a per-rank value over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     t = torch.tensor([x], dtype=torch.float64, device=dev)
@@ -511,8 +519,7 @@ def measure_e2e(wl, dev, args, world):
 # ------------------------------------------------------------------ CPU oracle
 
 def _oracle_layer_host(name, layer=0, rank=0):
-    shape, B, ctx, bs, seed = WORKLOADS[name]
-    b = W.uniform_batch(shape, B, ctx, bs, seed=seed + 1000 * rank)
+    b = rank_batch(name, rank)
     li = W.layer_inputs(b, layer, device="cpu")
     return b, {"q": W.to_u16(li.q), "k_new": W.to_u16(li.k_new), "v_new": W.to_u16(li.v_new),
                "k": W.to_u16(li.k_cache).copy(), "v": W.to_u16(li.v_cache).copy()}

@@ -194,10 +194,13 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
 /*
  * Which decode kernel later calls use: 0 automatic (the default: the
  * tensor-core kernel wherever it applies -- contiguous layout, or a paged
- * block size that is a multiple of 16 -- else the split kernel), 1 always the
- * split (CUDA-core) kernel, 2 / 3 the tensor-core kernel with 4 warps x 4
- * stages / 8 warps x 2 stages per CTA (PKV_ERR_UNSUPPORTED where it does not
- * apply).  Meant for tests and tuning; both kernels compute the same result.
+ * block size that is a multiple of 16 -- and the batch holds at least 32
+ * sixteen-token tiles per SM when every context is max_context long; else
+ * the split kernel, which fills the GPU better for small batches), 1 always the
+ * split (CUDA-core) kernel, 2 / 3 the tensor-core kernel with 8 warps x 3
+ * stages / 12 warps x 2 stages per CTA (the automatic choice uses 12 x 2;
+ * PKV_ERR_UNSUPPORTED where the kernel does not apply).  Meant for tests and
+ * tuning; every kernel computes the same result.
  */
 PKV_API void pkv_set_decode_variant(int variant);
 PKV_API int pkv_get_decode_variant(void);

@@ -5,11 +5,11 @@ Python binding; build the library with ``build.build()``."""
 from .binding import (PkvError, block_copy, contig_decode_attention, decode_num_splits,
                       decode_workspace_size, get_checked, get_device_error, kv_append, lib,
                       paged_decode_attention, set_checked, set_decode_variant, get_decode_variant,
-                      set_split_tiles, VARIANT_AUTO, VARIANT_SPLIT, VARIANT_TC_4X4,
-                      VARIANT_TC_8X2)
+                      set_split_tiles, VARIANT_AUTO, VARIANT_SPLIT, VARIANT_TC_8X3,
+                      VARIANT_TC_12X2)
 
 __all__ = ["PkvError", "block_copy", "contig_decode_attention", "decode_num_splits",
            "decode_workspace_size", "get_checked", "get_device_error", "kv_append", "lib",
            "paged_decode_attention", "set_checked", "set_split_tiles", "set_decode_variant",
-           "get_decode_variant", "VARIANT_AUTO", "VARIANT_SPLIT", "VARIANT_TC_4X4",
-           "VARIANT_TC_8X2"]
+           "get_decode_variant", "VARIANT_AUTO", "VARIANT_SPLIT", "VARIANT_TC_8X3",
+           "VARIANT_TC_12X2"]

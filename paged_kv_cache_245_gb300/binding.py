@@ -236,8 +236,8 @@ def get_checked():
 
 
 # decode kernel selection: automatic, the split (CUDA-core) kernel, or the
-# tensor-core kernel in its 4-warp x 4-stage / 8-warp x 2-stage shapes
-VARIANT_AUTO, VARIANT_SPLIT, VARIANT_TC_4X4, VARIANT_TC_8X2 = 0, 1, 2, 3
+# tensor-core kernel in its 8-warp x 3-stage / 12-warp x 2-stage CTA shapes
+VARIANT_AUTO, VARIANT_SPLIT, VARIANT_TC_8X3, VARIANT_TC_12X2 = 0, 1, 2, 3
 
 
 def set_decode_variant(variant):

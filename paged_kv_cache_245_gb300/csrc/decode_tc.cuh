@@ -258,9 +258,33 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
   };
 
+  // Prologue: walk the stream S tiles ahead so that lane s fetches the block
+  // table entry of tile s (one memory latency for all of them), then fill
+  // the stages.
+  int32_t pre_entry = 0;
+  if (!kContig) {
+    TcSeg cs = iseg;
+    int64_t cx = ix;
+    bool cv = ivalid;
+    for (int s = 0; s < S && cv; ++s) {
+      if (lane == s) {
+        const int64_t pos = (cx - cs.pstart) * 16;
+        pre_entry = __ldg(p.block_tables + static_cast<int64_t>(cs.seq) * p.max_blocks + pos / p.bs);
+      }
+      cx += W;
+      while (cx >= cs.x1) {
+        if (cs.x1 >= hi) {
+          cv = false;
+          break;
+        }
+        cs = tc_find_seg(cs.x1, hi, prefix, B, p.Hkv);
+        cx = cs.x0 + warp;
+      }
+    }
+  }
   int issued = 0;
   for (int s = 0; s < S && ivalid; ++s) {
-    issue(s, load_entry());
+    issue(s, __shfl_sync(kFull, pre_entry, s));
     ++issued;
     ix += W;
     settle();

@@ -17,7 +17,7 @@ namespace {
 
 std::atomic<int> g_checked{0};
 std::atomic<int> g_split_tiles{0};
-// 0 automatic, 1 CUDA-core split kernel, 2 tensor-core 4x4, 3 tensor-core 8x2
+// 0 automatic, 1 CUDA-core split kernel, 2 tensor-core 8x3, 3 tensor-core 12x2
 std::atomic<int> g_variant{0};
 thread_local char g_last_error[256] = "";
 
@@ -184,7 +184,14 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
   const int variant = g_variant.load();
   if (variant >= 2 && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "tensor-core kernel needs block_size %% 16 == 0 and < 2^31 rows");
-  if (variant != 1 && tc_ok) {
+  // Automatic choice: the persistent tensor-core kernel needs enough tiles
+  // to spread over one CTA per SM; for batches whose upper-bound tile count
+  // (all contexts at max_context) is under 32 tiles per SM the many-CTA
+  // split kernel finishes sooner.
+  const int64_t tile_bound = static_cast<int64_t>(num_seqs) * h.num_kv_heads *
+                             ((static_cast<int64_t>(max_context) + 15) / 16);
+  const bool tc_pick = variant >= 2 || (variant == 0 && tile_bound >= 32LL * tc_ctas(sms));
+  if (tc_pick && tc_ok) {
     const size_t need = pkv::tc_workspace_bytes(tc_ctas(sms));
     if (!workspace || workspace_bytes < need)
       return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need,
@@ -211,7 +218,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     t.err = err;
     cudaError_t ce = cudaSuccess;
     const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total,
-                                                   variant == 3 ? 1 : 0, tc_ctas(sms), workspace,
+                                                   variant == 2 ? 0 : 1, tc_ctas(sms), workspace,
                                                    static_cast<cudaStream_t>(stream), &ce);
     if (ts == pkv::TcStatus::kEncodeFailed)
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");

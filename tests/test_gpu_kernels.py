@@ -29,9 +29,10 @@ def _reset_modes():
     torch.cuda.synchronize()
 
 
-# every decode kernel shape: automatic (tensor-core where it applies), the
-# split CUDA-core kernel, and the tensor-core kernel's 8-warp shape
-VARIANTS = [pkv.VARIANT_AUTO, pkv.VARIANT_SPLIT, pkv.VARIANT_TC_8X2]
+# every decode kernel: automatic choice, the split CUDA-core kernel, and the
+# tensor-core kernel in both of its CTA shapes
+VARIANTS = [pkv.VARIANT_AUTO, pkv.VARIANT_SPLIT, pkv.VARIANT_TC_8X3, pkv.VARIANT_TC_12X2]
+TC_VARIANTS = (pkv.VARIANT_TC_8X3, pkv.VARIANT_TC_12X2)
 
 
 def _batch(hq, hkv, ctx, bs, seed=5, spare=3):
@@ -72,7 +73,7 @@ def test_every_group_size(hq, hkv, variant):
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("bs", [1, 3, 8, 16, 24, 32, 64, 128, 256])
 def test_block_sizes(bs, variant):
-    if variant == pkv.VARIANT_TC_8X2 and bs % 16:
+    if variant in TC_VARIANTS and bs % 16:
         pytest.skip("the tensor-core kernel takes block sizes that are multiples of 16")
     pkv.set_decode_variant(variant)
     ctx = [1, 5, 16, 17, 48, 129, 300, 513]
@@ -315,12 +316,15 @@ def test_checked_mode_reports_bad_slot_and_context_and_request(variant):
     assert pkv.get_device_error() == "copy_pair"
 
 
-def test_workspace_is_checked():
+@pytest.mark.parametrize("variant", [pkv.VARIANT_SPLIT, pkv.VARIANT_TC_12X2])
+def test_workspace_is_checked(variant):
+    pkv.set_decode_variant(variant)
     b = _batch(32, 8, [4000, 4000], 16)
     L = DeviceLayer(b, 0, DEV)
     need = pkv.decode_workspace_size(2, 32, 8, b.max_context)
-    assert need > 0
-    small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    assert need > 1024
+    small = torch.empty(1024 if variant == pkv.VARIANT_TC_12X2 else 16, dtype=torch.uint8,
+                        device=DEV)
     with pytest.raises(pkv.PkvError) as e:
         pkv.paged_decode_attention(L.q, L.k_cache, L.v_cache, L.tables, L.ctx, b.max_context,
                                    L.scale, workspace=small)
@@ -331,9 +335,11 @@ def test_workspace_is_checked():
     assert_attention_close(out, L.oracle_attend(), "explicit workspace")
 
 
-def test_large_batch_is_chunked():
-    """More sequences than one tensor-core launch takes (1024) run as
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_large_batch_is_chunked(variant):
+    """More sequences than one tensor-core launch takes (512) run as
     consecutive chunks; ragged short contexts, many of them empty."""
+    pkv.set_decode_variant(variant)
     ctx = np.random.default_rng(8).integers(0, 40, size=1500).astype(np.int32)
     ctx[:3] = [1, 39, 0]
     b = _batch(16, 4, np.maximum(ctx, 1), 16, seed=12)
@@ -344,7 +350,7 @@ def test_large_batch_is_chunked():
 
 
 def test_variant_knob_rejects_tensor_core_for_odd_block_size():
-    pkv.set_decode_variant(pkv.VARIANT_TC_4X4)
+    pkv.set_decode_variant(pkv.VARIANT_TC_8X3)
     b = _batch(8, 2, [20, 40], 24)
     L = DeviceLayer(b, 0, DEV)
     with pytest.raises(pkv.PkvError) as e:
