@@ -148,7 +148,7 @@ def _source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_245_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+        if f.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -464,39 +464,43 @@ def measure_legs(wl, dev, args):
 
 
 def measure_e2e(wl, dev, args, world):
-    """Each step copies its inputs (q, new k/v, slots, tables, context lengths
-    per layer) from pinned host memory, runs the step through the C ABI, and
-    reads every layer's output back to pinned host memory."""
+    """Each step copies its inputs -- every layer's q and new k/v rows plus the
+    batch's slots, block tables and context lengths -- from one pinned host
+    buffer to the device, runs the step through the C ABI (append + attention
+    per layer), and reads every layer's output back to pinned host memory."""
     nl = wl.shape.num_layers
-    host_in, dev_in, host_out = [], [], []
+    b = wl.batch
+    parts = []
     for l in range(nl):
         li = wl.layers[l]
-        hi = [t.detach().to("cpu").pin_memory() for t in (li.q, li.k_new, li.v_new)]
-        host_in.append(hi)
-        dev_in.append([torch.empty_like(t) for t in (li.q, li.k_new, li.v_new)])
-        host_out.append(torch.empty(li.q.shape, dtype=li.q.dtype, pin_memory=True))
-    h_meta = [torch.as_tensor(a).pin_memory() for a in
-              (wl.batch.slot_mapping, wl.batch.block_tables, wl.batch.ctx)]
-    d_meta = [torch.empty_like(t, device=dev) for t in h_meta]
-    h2d = sum(t.numel() * t.element_size() for row in host_in for t in row)
-    h2d += nl * sum(t.numel() * t.element_size() for t in h_meta)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+        parts += [li.q, li.k_new, li.v_new]
+    parts += [torch.as_tensor(b.slot_mapping), torch.as_tensor(b.block_tables),
+              torch.as_tensor(b.ctx)]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = [0]
+    for n in sizes:
+        offs.append(offs[-1] + (n + 255) // 256 * 256)
+    host_in = torch.empty(offs[-1], dtype=torch.uint8, pin_memory=True)
+    for t, o, n in zip(parts, offs, sizes):
+        host_in[o:o + n].copy_(t.detach().to("cpu").contiguous().view(-1).view(torch.uint8))
+    dev_in = torch.empty(offs[-1], dtype=torch.uint8, device=dev)
+    views = [dev_in[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, sizes)]
+    out_all = torch.empty((nl,) + tuple(wl.layers[0].q.shape), dtype=torch.bfloat16, device=dev)
+    host_out = torch.empty(out_all.shape, dtype=out_all.dtype, pin_memory=True)
+    h2d = sum(sizes)
+    d2h = out_all.numel() * out_all.element_size()
     pkv = wl.pkv
-    b = wl.batch
+    slots, tables, ctx = views[3 * nl:]
 
     def step():
+        dev_in.copy_(host_in, non_blocking=True)
         for l in range(nl):
-            for d, h in zip(d_meta, h_meta):
-                d.copy_(h, non_blocking=True)
-            q, kn, vn = dev_in[l]
-            for d, h in zip(dev_in[l], host_in[l]):
-                d.copy_(h, non_blocking=True)
+            q, kn, vn = views[3 * l:3 * l + 3]
             li = wl.layers[l]
-            pkv.kv_append(d_meta[0], kn, vn, li.k_cache, li.v_cache)
-            pkv.paged_decode_attention(q, li.k_cache, li.v_cache, d_meta[1], d_meta[2],
-                                       b.max_context, wl.scale, out=wl.out[l],
-                                       workspace=wl.workspace)
-            host_out[l].copy_(wl.out[l], non_blocking=True)
+            pkv.kv_append(slots, kn, vn, li.k_cache, li.v_cache)
+            pkv.paged_decode_attention(q, li.k_cache, li.v_cache, tables, ctx, b.max_context,
+                                       wl.scale, out=out_all[l], workspace=wl.workspace)
+        host_out.copy_(out_all, non_blocking=True)
 
     iters = max(10, args.steps // 10)
     for _ in range(3):
@@ -513,7 +517,9 @@ def measure_e2e(wl, dev, args, world):
     ms = _max_over_ranks(a.elapsed_time(c) / iters, world, dev)
     return {"value": round(world * b.B / (ms / 1e3 / nl), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(ms, 4), "steps": iters}
+            "ms_per_step": round(ms, 4), "steps": iters,
+            "how": "direct C-ABI calls (no graph); one pinned H2D of the step's inputs, "
+                   "one D2H of all layers' outputs, inside the timed region"}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -582,6 +588,24 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args):
+    """A small case for ncu: 4 layers of the workload (about 1 GB), a few
+    paged attention calls through the C ABI."""
+    import paged_kv_cache_245_gb300 as pkv
+    from __graft_entry__ import build
+    build()
+    dev = torch.device("cuda", 0)
+    b = rank_batch(args.workload, 0)
+    layers = [W.layer_inputs(b, l, device=dev, fast_cache=True) for l in range(4)]
+    tables = torch.as_tensor(b.block_tables, device=dev)
+    ctx = torch.as_tensor(b.ctx, device=dev)
+    for i in range(args.profile_calls):
+        li = layers[i % 4]
+        pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, tables, ctx, b.max_context,
+                                   W.default_scale(b.shape))
+    torch.cuda.synchronize(dev)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -592,8 +616,14 @@ def main():
     ap.add_argument("--skip-legs", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="profiling case: run this many paged attention calls over 4 layers "
+                         "of the workload and exit (no timing, no JSON)")
     args = ap.parse_args()
     world, rank, local = _dist()
+    if args.profile_calls > 0:
+        profile_case(args)
+        return
     if args.impl == "reference":
         # CPU-only arm: rank 0 runs it; other ranks exit without work.
         run_reference(args, world, rank)

@@ -108,12 +108,6 @@ __device__ __forceinline__ TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_
   return s;
 }
 
-// The CTA that owns tile x when T tiles are split evenly over P CTAs
-// (CTA c owns [floor(c*T/P), floor((c+1)*T/P))).
-__device__ __forceinline__ int tc_owner(int64_t x, int64_t T, int P) {
-  return static_cast<int>(((x + 1) * P + T - 1) / T) - 1;
-}
-
 template <bool kContig, int W, int S>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -179,8 +173,8 @@ __global__ void __launch_bounds__(W * 32, 1)
   if (c == 0)
     for (int i = tid; i <= B; i += W * 32) p.prefix_out[i] = prefix[i];
   const int64_t T = static_cast<int64_t>(p.Hkv) * prefix[B];
-  const int64_t lo = static_cast<int64_t>(c) * T / P;
-  const int64_t hi = static_cast<int64_t>(c + 1) * T / P;
+  const int64_t lo = tc_range_lo(c, T, P);
+  const int64_t hi = tc_range_lo(c + 1, T, P);
   if (lo >= hi) return;  // uniform across the CTA
 
   const uint64_t policy = l2_policy_evict_first();
@@ -512,15 +506,15 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
   const int64_t T = static_cast<int64_t>(p.Hkv) * prefix[p.num_seqs];
   const int64_t pstart = static_cast<int64_t>(p.Hkv) * prefix[seq] + static_cast<int64_t>(kvh) * n;
   const int64_t pend = pstart + n;
-  const int cf = tc_owner(pstart, T, P);
-  const int cl = tc_owner(pend - 1, T, P);
+  const int cf = static_cast<int>(tc_owner(pstart, T, P));
+  const int cl = static_cast<int>(tc_owner(pend - 1, T, P));
   if (cf == cl) return;
   // CTA cc's record for this pair: slot 0 if the pair began before cc's range
   // (or exactly at its start), slot 1 if it began inside; CTAs whose range
   // is empty wrote nothing and are skipped.
   auto record = [&](int cc) -> const float* {
-    const int64_t lo_c = static_cast<int64_t>(cc) * T / P;
-    const int64_t hi_c = static_cast<int64_t>(cc + 1) * T / P;
+    const int64_t lo_c = tc_range_lo(cc, T, P);
+    const int64_t hi_c = tc_range_lo(cc + 1, T, P);
     if (lo_c >= hi_c) return nullptr;
     const int slot = lo_c >= pstart ? 0 : 1;
     return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcHeads + gi) * kRecStride;

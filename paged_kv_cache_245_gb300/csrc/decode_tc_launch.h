@@ -31,6 +31,17 @@ struct TcParams {
 
 enum class TcStatus { kOk, kEncodeFailed, kCudaError };
 
+// Static partition of the flattened tile list [0, T) over P CTAs: CTA c owns
+// [floor(c*T/P), floor((c+1)*T/P)).
+__host__ __device__ inline int64_t tc_range_lo(int64_t c, int64_t T, int64_t P) {
+  return c * T / P;
+}
+
+// The CTA that owns tile x (the largest c with range_lo(c) <= x).
+__host__ __device__ inline int64_t tc_owner(int64_t x, int64_t T, int64_t P) {
+  return ((x + 1) * P + T - 1) / T - 1;
+}
+
 // Workspace bytes for the per-CTA partial records and the tile prefix.
 size_t tc_workspace_bytes(int num_ctas);
 

@@ -204,11 +204,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Host: launch `kernel` on `stream` allowing programmatic dependent launch
 // (the kernel may be scheduled while the previous kernel of the stream is
 // still running; every kernel here calls grid_dependency_wait() before it
-// touches memory another kernel could write).  PKV_NO_PDL=1 turns it off.
+// touches memory another kernel could write).  Off unless PKV_PDL=1: on the
+// decode step it measured about 1 % slower than plain stream order.
 inline bool pdl_enabled() {
   static const bool on = [] {
-    const char* v = getenv("PKV_NO_PDL");
-    return !(v != nullptr && v[0] == '1');
+    const char* v = getenv("PKV_PDL");
+    return v != nullptr && v[0] == '1';
   }();
   return on;
 }
