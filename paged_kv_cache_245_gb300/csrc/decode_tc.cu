@@ -2,6 +2,7 @@
 // tensor-map encoding, batch chunking, kernel instantiations.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "decode_tc.cuh"
@@ -68,8 +69,15 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     e = launch_pdl(kernel, dim3(num_ctas), dim3(W * 32), L::kTotal, stream, tk, tv, p);
     if (e != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
-    e = launch_pdl(decode_tc_combine_kernel, dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128),
-                   0, stream, p, num_ctas);
+    // The combine may be scheduled while the main kernel drains (it waits
+    // for it before reading anything); PKV_COMBINE_PDL=0 turns that off.
+    static const bool combine_pdl = [] {
+      const char* v = getenv("PKV_COMBINE_PDL");
+      return !(v != nullptr && v[0] == '0');
+    }();
+    e = launch_pdl_if(combine_pdl || pdl_enabled(), decode_tc_combine_kernel,
+                      dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128), 0, stream, p,
+                      num_ctas);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

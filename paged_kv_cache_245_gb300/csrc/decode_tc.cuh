@@ -511,7 +511,10 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
   if (cf == cl) return;
   // CTA cc's record for this pair: slot 0 if the pair began before cc's range
   // (or exactly at its start), slot 1 if it began inside; CTAs whose range
-  // is empty wrote nothing and are skipped.
+  // is empty wrote nothing and are skipped.  Lane j loads record cf + j's
+  // (m, l) so that all records cost one round trip, then every lane loads its
+  // four output elements of the records four at a time.
+  constexpr unsigned kFull = 0xffffffffu;
   auto record = [&](int cc) -> const float* {
     const int64_t lo_c = tc_range_lo(cc, T, P);
     const int64_t hi_c = tc_range_lo(cc + 1, T, P);
@@ -519,20 +522,51 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
     const int slot = lo_c >= pstart ? 0 : 1;
     return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcHeads + gi) * kRecStride;
   };
-  float M = -INFINITY;
-  for (int cc = cf; cc <= cl; ++cc) {
-    const float* r = record(cc);
-    if (r != nullptr) M = fmaxf(M, r[128]);
-  }
+  const int K = cl - cf + 1;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float Wsum = 0.f;
-  if (M != -INFINITY) {
+  if (K <= 32) {
+    const float* rj = lane < K ? record(cf + lane) : nullptr;
+    const float mj = rj != nullptr ? __ldcg(rj + 128) : -INFINITY;
+    const float lj = rj != nullptr ? __ldcg(rj + 129) : 0.f;
+    float M = lj > 0.f ? mj : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    const float wj = (lj > 0.f && M != -INFINITY) ? lj * fast_exp2(mj - M) : 0.f;
+    const unsigned long long rbits = reinterpret_cast<unsigned long long>(rj);
+    for (int j = 0; j < K; j += 4) {
+      float4 o[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int jj = min(j + u, K - 1);
+        const float wu = __shfl_sync(kFull, wj, jj);
+        const float* r = reinterpret_cast<const float*>(__shfl_sync(kFull, rbits, jj));
+        w[u] = (j + u < K) ? wu : 0.f;
+        o[u] = w[u] > 0.f ? __ldcg(reinterpret_cast<const float4*>(r) + lane)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x = fmaf(w[u], o[u].x, acc.x);
+        acc.y = fmaf(w[u], o[u].y, acc.y);
+        acc.z = fmaf(w[u], o[u].z, acc.z);
+        acc.w = fmaf(w[u], o[u].w, acc.w);
+        Wsum += w[u];
+      }
+    }
+  } else {
+    // more than 32 CTAs share the pair (tiny batches): two passes
+    float M = -INFINITY;
     for (int cc = cf; cc <= cl; ++cc) {
       const float* r = record(cc);
-      if (r == nullptr) continue;
-      const float ls = r[129];
-      if (ls > 0.f) {
-        const float w = ls * fast_exp2(r[128] - M);
+      if (r != nullptr && r[129] > 0.f) M = fmaxf(M, r[128]);
+    }
+    if (M != -INFINITY) {
+      for (int cc = cf; cc <= cl; ++cc) {
+        const float* r = record(cc);
+        if (r == nullptr || !(r[129] > 0.f)) continue;
+        const float w = r[129] * fast_exp2(r[128] - M);
         const float4 o = *reinterpret_cast<const float4*>(r + lane * 4);
         acc.x = fmaf(w, o.x, acc.x);
         acc.y = fmaf(w, o.y, acc.y);
