@@ -46,6 +46,11 @@ WORKLOADS = {
 }
 for _b in W.LLAMA_SWEEP_BATCHES:
     WORKLOADS["llama3_8b_b%d" % _b] = (W.LLAMA3_8B, _b, 1024, 16, W.SEED_LLAMA)
+# ragged serving batch (context = prompt + generated so far, max 8192)
+for _bs in W.RAGGED_BLOCK_SIZES:
+    WORKLOADS["llama3_8b_ragged_bs%d" % _bs] = (W.LLAMA3_8B, 256, "ragged", _bs, W.SEED_RAGGED)
+# parallel sampling over shared prompts: the first decode step after copy on write
+WORKLOADS["yi34b_sharing"] = (W.YI_34B, 128, "sharing", 16, W.SEED_YI34B)
 DEFAULT_WORKLOAD = "llama3_8b_b64"
 
 
@@ -58,17 +63,33 @@ def _dist():
 
 def _describe(name):
     shape, B, ctx, bs, _ = WORKLOADS[name]
-    return ("%s-shaped decode: batch %d, context %d, block_size %d, %d layers, "
+    ctx_text = {"ragged": "ragged contexts (prompt ~ Exp(1024) + generated ~ U{0..Exp(256)}, "
+                          "max 8192)",
+                "sharing": "32 prompts ~ U[1024, 8192] x 4 sampled branches sharing prompt "
+                           "blocks, first step after copy on write"}.get(ctx, "context %s" % ctx)
+    return ("%s-shaped decode: batch %d, %s, block_size %d, %d layers, "
             "%d query / %d KV heads, head_dim %d"
-            % (shape.name, B, ctx, bs, shape.num_layers, shape.num_q_heads,
+            % (shape.name, B, ctx_text, bs, shape.num_layers, shape.num_q_heads,
                shape.num_kv_heads, shape.head_dim))
 
 
-def rank_batch(name, rank):
-    """The batch a rank decodes: every rank gets the workload's full shape
-    (weak scaling) with its own seed, so ranks hold different sequences."""
+def rank_workload(name, rank):
+    """(batch, copy-on-write pairs [n, 2] or None) that a rank decodes: every
+    rank gets the workload's full shape (weak scaling) with its own seed, so
+    ranks hold different sequences.  The sharing workload's step is the first
+    decode step after forking, so it starts with the copies on write."""
     shape, B, ctx, bs, seed = WORKLOADS[name]
-    return W.uniform_batch(shape, B, ctx, bs, seed=seed + 1000 * rank)
+    seed = seed + 1000 * rank
+    if ctx == "ragged":
+        return W.make_paged_batch(shape, W.ragged_lengths(B, seed=seed), bs, seed), None
+    if ctx == "sharing":
+        sc = W.sharing_scenario(seed=seed, decode_steps=1)
+        return sc.steps[0], (sc.cow_pairs if len(sc.cow_pairs) else None)
+    return W.uniform_batch(shape, B, ctx, bs, seed=seed), None
+
+
+def rank_batch(name, rank):
+    return rank_workload(name, rank)[0]
 
 
 def algorithmic_bytes(batch):
@@ -192,13 +213,16 @@ class DeviceWorkload:
         shape, B, ctx, bs, seed = WORKLOADS[name]
         self.name = name
         self.shape = shape
-        self.batch = rank_batch(name, rank)
+        self.batch, pairs = rank_workload(name, rank)
         self.dev = dev
         b = self.batch
         self.layers = []
         for l in range(shape.num_layers):
             li = W.layer_inputs(b, l, device=dev, fast_cache=True)
             self.layers.append(li)
+        self.cow = None if pairs is None else torch.as_tensor(pairs, device=dev)
+        self.k_caches = [li.k_cache for li in self.layers]
+        self.v_caches = [li.v_cache for li in self.layers]
         self.tables = torch.as_tensor(b.block_tables, device=dev)
         self.ctx = torch.as_tensor(b.ctx, device=dev)
         self.slots = torch.as_tensor(b.slot_mapping, device=dev)
@@ -215,10 +239,17 @@ class DeviceWorkload:
         return self.batch.block_size % 16 == 0 and self.pkv.get_decode_variant() != 1
 
     def launches_per_step(self):
-        # kv_append, the attention kernel and its combine kernel per layer
+        # kv_append, the attention kernel and its combine kernel per layer,
+        # plus one block copy launch (all layers) when the step copies on write
+        cow = 0 if self.cow is None else 1
         if self.uses_tc:
-            return self.shape.num_layers * 3
-        return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0))
+            return self.shape.num_layers * 3 + cow
+        return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0)) + cow
+
+    def copy_on_write(self, pairs=None):
+        pairs = self.cow if pairs is None else pairs
+        if pairs is not None:
+            self.pkv.block_copy(pairs, self.k_caches, self.v_caches)
 
     def layer(self, l, events=None):
         li = self.layers[l]
@@ -232,6 +263,7 @@ class DeviceWorkload:
             events[1].record()
 
     def step(self, events=None):
+        self.copy_on_write()
         for l in range(self.shape.num_layers):
             self.layer(l, None if events is None else events[l])
 
@@ -333,13 +365,16 @@ def run_gpu(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": _describe(args.workload), "global_batch": B * world,
-                   "seq_len": int(wl.batch.ctx.max()), "layers": nl,
+                   "seq_len": int(wl.batch.ctx.max()), "mean_context": round(float(wl.batch.ctx.mean()), 1),
+                   "layers": nl,
                    "block_size": wl.batch.block_size, "num_splits": wl.nsplit,
                    "parallelism": "replicas (one batch per GPU, no collective)" if world > 1
                    else "single GPU",
                    "l2": "inputs larger than L2: %.1f GB of distinct K/V per step, "
                          "%.0f MB per layer" % (nl * alg / 1e9, alg / 1e6),
-                   "step": "per layer: kv_append + paged_decode_attention (main + combine)"},
+                   "step": ("block_copy of %d copy-on-write pairs (all layers), then "
+                            % len(wl.cow) if wl.cow is not None else "")
+                           + "per layer: kv_append + paged_decode_attention (main + combine)"},
         "hbm_tbs": round(achieved_gbs / 1e3, 4),
         "hbm_pct_of_8tbs": round(100 * achieved_gbs / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
@@ -393,9 +428,13 @@ def measure_legs(wl, dev, args):
     same logical K/V, the append alone, and a copy-on-write block copy."""
     pkv = wl.pkv
     b = wl.batch
-    nl = min(8, wl.shape.num_layers)   # 8 distinct layers: > 2 GB, far above L2
     alg = algorithmic_bytes(b)
-    S = int(b.ctx.max())
+    # the contiguous layout's per-request capacity S: the ragged batch's
+    # maximum length (8192), else the longest context of the batch
+    S = 8192 if WORKLOADS[wl.name][2] == "ragged" else int(b.ctx.max())
+    # distinct layers cycled (far above L2), within about 24 GB of buffers
+    buf_bytes = 2 * b.B * wl.shape.num_kv_heads * S * wl.shape.head_dim * 2
+    nl = max(1, min(8, wl.shape.num_layers, int(24e9 // buf_bytes)))
     bufs = []
     for l in range(nl):
         li = wl.layers[l]
@@ -452,6 +491,7 @@ def measure_legs(wl, dev, args):
         "paged_attention_us": round(t_paged * 1e3, 3),
         "contig_attention_us": round(t_contig * 1e3, 3),
         "paged_over_contig_time": round(t_paged / t_contig, 4),
+        "contig_S": S, "contig_layers": nl,
         "split_kernel_attention_us": round(t_split * 1e3, 3),
         "split_kernel_hbm_gbs": round(alg / (t_split / 1e3) / 1e9, 1),
         "contig_hbm_gbs": round(alg / (t_contig / 1e3) / 1e9, 1),
@@ -476,6 +516,8 @@ def measure_e2e(wl, dev, args, world):
         parts += [li.q, li.k_new, li.v_new]
     parts += [torch.as_tensor(b.slot_mapping), torch.as_tensor(b.block_tables),
               torch.as_tensor(b.ctx)]
+    if wl.cow is not None:
+        parts.append(wl.cow)
     sizes = [t.numel() * t.element_size() for t in parts]
     offs = [0]
     for n in sizes:
@@ -490,10 +532,12 @@ def measure_e2e(wl, dev, args, world):
     h2d = sum(sizes)
     d2h = out_all.numel() * out_all.element_size()
     pkv = wl.pkv
-    slots, tables, ctx = views[3 * nl:]
+    slots, tables, ctx = views[3 * nl:3 * nl + 3]
+    cow = views[3 * nl + 3] if wl.cow is not None else None
 
     def step():
         dev_in.copy_(host_in, non_blocking=True)
+        wl.copy_on_write(cow)
         for l in range(nl):
             q, kn, vn = views[3 * l:3 * l + 3]
             li = wl.layers[l]
@@ -502,7 +546,7 @@ def measure_e2e(wl, dev, args, world):
                                        wl.scale, out=out_all[l], workspace=wl.workspace)
         host_out.copy_(out_all, non_blocking=True)
 
-    iters = max(10, args.steps // 10)
+    iters = max(20, args.steps // 10)
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
@@ -525,13 +569,20 @@ def measure_e2e(wl, dev, args, world):
 # ------------------------------------------------------------------ CPU oracle
 
 def _oracle_layer_host(name, layer=0, rank=0):
-    b = rank_batch(name, rank)
+    b, pairs = rank_workload(name, rank)
     li = W.layer_inputs(b, layer, device="cpu")
     return b, {"q": W.to_u16(li.q), "k_new": W.to_u16(li.k_new), "v_new": W.to_u16(li.v_new),
-               "k": W.to_u16(li.k_cache).copy(), "v": W.to_u16(li.v_cache).copy()}
+               "k": W.to_u16(li.k_cache).copy(), "v": W.to_u16(li.v_cache).copy(),
+               "cow": pairs}
+
+
+def _oracle_step_text(h):
+    return ("copy on write + " if h["cow"] is not None else "") + "append + attention"
 
 
 def _oracle_step(oracle, b, h, scale, nthreads):
+    if h["cow"] is not None:
+        oracle.block_copy(h["cow"], [h["k"]], [h["v"]])
     oracle.kv_append(b.slot_mapping, h["k_new"], h["v_new"], h["k"], h["v"])
     oracle.paged_decode(h["q"], h["k"], h["v"], b.block_tables, b.ctx, scale, nthreads)
 
@@ -552,8 +603,9 @@ def cpu_baseline(wl, args, budget_s=15.0):
         done += 1
     return {"value": round(b.B * done / t_total, 2), "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": "%d repetitions of one layer (append + attention, all %d sequences) of "
-                      "the same workload, fp64 C oracle, %d threads" % (done, b.B, cores)}
+            "sample": "%d repetitions of one layer (%s, all %d sequences) of "
+                      "the same workload, fp64 C oracle, %d threads"
+                      % (done, _oracle_step_text(h), b.B, cores)}
 
 
 def run_reference(args, world, rank):
@@ -579,7 +631,8 @@ def run_reference(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": _describe(args.workload), "global_batch": b.B,
                        "seq_len": int(b.ctx.max()), "layers_per_step": 1,
-                       "step": "one layer of the workload (append + attention, all sequences)"},
+                       "step": "one layer of the workload (%s, all sequences)"
+                               % _oracle_step_text(h)},
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
                              "kind": "oracle",
                              "sample": "one layer per step, all %d sequences" % b.B},

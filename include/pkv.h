@@ -205,6 +205,14 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
 PKV_API void pkv_set_decode_variant(int variant);
 PKV_API int pkv_get_decode_variant(void);
 
+/*
+ * Test hook for the bounded waits.  The next tensor-core decode call makes
+ * one warp wait for 16 bytes that never arrive: that wait gives up after its
+ * time limit (2 s), the call records PKV_DEVERR_TIMEOUT in the device error
+ * word, the output of that call is undefined, and the context stays usable.
+ */
+PKV_API void pkv_debug_stall_next_decode(void);
+
 /* Checked mode on (1) or off (0, the default) for later calls. */
 PKV_API void pkv_set_checked(int enable);
 PKV_API int pkv_get_checked(void);

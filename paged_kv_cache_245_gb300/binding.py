@@ -23,7 +23,7 @@ DEVERR_NAMES = {0: "none", 1: "block_id", 2: "slot", 3: "req_id", 4: "context",
 EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size",
             "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
-            "pkv_set_decode_variant", "pkv_get_decode_variant",
+            "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -64,6 +64,7 @@ def lib():
     L.pkv_set_checked.argtypes = [ctypes.c_int]
     L.pkv_set_checked.restype = None
     L.pkv_get_checked.restype = ctypes.c_int
+    L.pkv_debug_stall_next_decode.restype = None
     L.pkv_set_decode_variant.argtypes = [ctypes.c_int]
     L.pkv_set_decode_variant.restype = None
     L.pkv_get_decode_variant.restype = ctypes.c_int

@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     return __ldg(p.block_tables + static_cast<int64_t>(iseg.seq) * p.max_blocks + pos / p.bs);
   };
 
+  int issued = 0;  // tiles issued by this warp so far
   auto issue = [&](int stage, int32_t entry) {
     if (ix == iseg.x0 + warp && qn_pair < 0) {  // whole warp
       load_q(qn, iseg.seq, iseg.kvh);
@@ -241,7 +242,10 @@ __global__ void __launch_bounds__(W * 32, 1)
         }
         row = (static_cast<int64_t>(entry) * p.Hkv + iseg.kvh) * p.bs + pos % p.bs;
       }
-      mbar_arrive_expect_tx(&bars[stage], kv_ok ? 4u * kBoxBytes : 0u);
+      // (test hook: on its first tile, CTA 0's warp 0 announces 16 more bytes
+      // than its copies bring, so that wait runs into its time limit)
+      const uint32_t extra = (p.stall_test && c == 0 && warp == 0 && issued == 0) ? 16u : 0u;
+      mbar_arrive_expect_tx(&bars[stage], (kv_ok ? 4u * kBoxBytes : 0u) + extra);
       if (kv_ok) {
         const int32_t y = static_cast<int32_t>(row);
         tma_load_2d(st, &tmk, 0, y, &bars[stage], policy);
@@ -276,7 +280,6 @@ __global__ void __launch_bounds__(W * 32, 1)
       }
     }
   }
-  int issued = 0;
   for (int s = 0; s < S && ivalid; ++s) {
     issue(s, __shfl_sync(kFull, pre_entry, s));
     ++issued;

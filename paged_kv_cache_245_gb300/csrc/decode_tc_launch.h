@@ -25,6 +25,7 @@ struct TcParams {
   int32_t num_seqs, Hq, Hkv, G, max_context;
   float qscale;             // scale * log2(e)
   int32_t checked;
+  int32_t stall_test;       // test hook: CTA 0's warp 0 expects 16 bytes that never come
   int* err;
 };
 

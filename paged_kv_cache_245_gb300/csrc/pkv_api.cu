@@ -19,6 +19,7 @@ std::atomic<int> g_checked{0};
 std::atomic<int> g_split_tiles{0};
 // 0 automatic, 1 CUDA-core split kernel, 2 tensor-core 8x3, 3 tensor-core 12x2
 std::atomic<int> g_variant{0};
+std::atomic<int> g_stall_test{0};
 thread_local char g_last_error[256] = "";
 
 // The device error word: one int per device (module-scope __device__).
@@ -215,6 +216,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     t.max_context = max_context;
     t.qscale = scale * 1.4426950408889634f;  // log2(e)
     t.checked = g_checked.load();
+    t.stall_test = g_stall_test.exchange(0);
     t.err = err;
     cudaError_t ce = cudaSuccess;
     const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total,
@@ -385,6 +387,7 @@ pkv_status pkv_block_copy(const int64_t* src_dst_pairs, int64_t n, void* const* 
 }
 
 void pkv_set_checked(int enable) { g_checked.store(enable ? 1 : 0); }
+void pkv_debug_stall_next_decode(void) { g_stall_test.store(1); }
 void pkv_set_decode_variant(int variant) { g_variant.store(variant >= 0 && variant <= 3 ? variant : 0); }
 int pkv_get_decode_variant(void) { return g_variant.load(); }
 int pkv_get_checked(void) { return g_checked.load(); }

@@ -356,3 +356,52 @@ def test_variant_knob_rejects_tensor_core_for_odd_block_size():
     with pytest.raises(pkv.PkvError) as e:
         L.gpu_attend()
     assert e.value.status == 2
+
+
+def test_wait_limit_reports_timeout_and_context_survives():
+    """A wait that can never complete (test hook: one warp announces 16 bytes
+    no copy brings) gives up after its time limit and reports a timeout in
+    the device error word; the next call on the same context is correct."""
+    pkv.set_decode_variant(pkv.VARIANT_TC_12X2)
+    b = _batch(32, 8, [1024] * 64, 16, seed=31)
+    L = DeviceLayer(b, 0, DEV)
+    assert pkv.get_device_error() == "none"
+    pkv.lib().pkv_debug_stall_next_decode()
+    L.gpu_attend()
+    assert pkv.get_device_error() == "timeout"
+    out = L.gpu_attend()
+    assert pkv.get_device_error() == "none"
+    assert_attention_close(out, L.oracle_attend(), "after a timed-out call")
+
+
+def test_cuda_graph_replay_matches_direct_calls():
+    """The decode step (append + attention) captured in a CUDA graph and
+    replayed gives the same bytes as direct calls."""
+    b = _batch(32, 8, [300, 1024, 17, 700] * 16, 16, seed=41)
+    L = DeviceLayer(b, 0, DEV)
+    k0, v0 = L.k_cache.clone(), L.v_cache.clone()
+    ws = torch.empty(pkv.decode_workspace_size(b.B, 32, 8, b.max_context), dtype=torch.uint8,
+                     device=DEV)
+    out = torch.empty_like(L.q)
+
+    def step():
+        pkv.kv_append(L.slots, L.k_new, L.v_new, L.k_cache, L.v_cache)
+        pkv.paged_decode_attention(L.q, L.k_cache, L.v_cache, L.tables, L.ctx, b.max_context,
+                                   L.scale, out=out, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    direct = out.clone()
+    L.k_cache.copy_(k0)
+    L.v_cache.copy_(v0)
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    L.k_cache.copy_(k0)
+    L.v_cache.copy_(v0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, direct)
+    L.oracle_append()
+    assert_attention_close(out, L.oracle_attend(), "graph replay")
