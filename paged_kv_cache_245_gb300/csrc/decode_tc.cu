@@ -57,10 +57,16 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  // Batches above kTcMaxSeqs run as consecutive chunks reusing the workspace.
-  for (int s0 = 0; s0 < p0.num_seqs; s0 += kTcMaxSeqs) {
+  // Batches above kTcMaxSeqs run as consecutive chunks reusing the workspace;
+  // a chunk's tile prefix (int32) must hold chunk * ceil(max_context / 16).
+  const int64_t max_tiles = (static_cast<int64_t>(p0.max_context) + 15) / 16;
+  int chunk = kTcMaxSeqs;
+  if (max_tiles > 0 && static_cast<int64_t>(chunk) * max_tiles > 0x7fffffffLL)
+    chunk = static_cast<int>(0x7fffffffLL / max_tiles);
+  if (chunk < 1) chunk = 1;
+  for (int s0 = 0; s0 < p0.num_seqs; s0 += chunk) {
     TcParams p = p0;
-    p.num_seqs = (p0.num_seqs - s0) < kTcMaxSeqs ? (p0.num_seqs - s0) : kTcMaxSeqs;
+    p.num_seqs = (p0.num_seqs - s0) < chunk ? (p0.num_seqs - s0) : chunk;
     p.q += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
     p.out += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
     p.ctx_lens += s0;
@@ -100,6 +106,16 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
   if (!encode_rows(&tk, k, rows_total) || !encode_rows(&tv, v, rows_total))
     return TcStatus::kEncodeFailed;
   TcParams p = p_in;
+  // The cost of a segment in tiles.  Measured per-CTA timelines grow by about
+  // 2-2.7 us per extra segment at 5.7-7 tiles/us per CTA (12-19 tiles); a
+  // sweep of 0..48 on GB300 was fastest at 24 (ragged batches gain most).
+  // PKV_TC_SEG_COST overrides it (0: an even split of the tiles alone).
+  static const int seg_cost = [] {
+    const char* v = getenv("PKV_TC_SEG_COST");
+    const int x = v != nullptr ? atoi(v) : 24;
+    return x < 0 ? 0 : (x > 4096 ? 4096 : x);
+  }();
+  p.seg_cost = seg_cost;
   p.rec = static_cast<float*>(workspace);
   p.prefix_out = reinterpret_cast<int32_t*>(
       static_cast<unsigned char*>(workspace) +

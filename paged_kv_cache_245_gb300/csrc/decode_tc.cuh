@@ -10,12 +10,14 @@
 //
 // Schedule.  The work is the flattened list of 16-token tiles of every
 // (sequence, KV head) pair, pair p = seq * Hkv + kvh in order.  The grid has
-// one CTA per SM; CTA c takes tiles [c*T/P, (c+1)*T/P) -- every CTA gets the
-// same number of tiles whatever the context lengths.  A CTA walks its range
-// pair by pair ("segments"); its warps take the segment's tiles round-robin.
-// A segment that covers a whole pair writes the bf16 output directly; the at
-// most two partial segments of a CTA (its first and its last) write an fp32
-// record (o, m, l) that the combine kernel merges.
+// one CTA per SM, and each CTA takes a contiguous run of tiles.  The runs are
+// cut so that every CTA gets the same cost, counting a tile as 1 and each
+// pair it touches as seg_cost more (tc_unit_to_tile), whatever the context
+// lengths.  A CTA walks its run pair by pair ("segments"); its warps take
+// the segment's tiles round-robin.  A segment that covers a whole pair writes
+// the bf16 output directly; the at most two partial segments of a CTA (its
+// first and its last) write an fp32 record (o, m, l) that the combine kernel
+// merges.
 //
 // Data movement.  K and V tiles (16 rows x 256 B) come in through the TMA
 // engine from a 2-D tensor map over the cache's rows, as two 64-column boxes
@@ -172,9 +174,9 @@ __global__ void __launch_bounds__(W * 32, 1)
   __syncthreads();
   if (c == 0)
     for (int i = tid; i <= B; i += W * 32) p.prefix_out[i] = prefix[i];
-  const int64_t T = static_cast<int64_t>(p.Hkv) * prefix[B];
-  const int64_t lo = tc_range_lo(c, T, P);
-  const int64_t hi = tc_range_lo(c + 1, T, P);
+  const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
+  const int64_t lo = tc_unit_to_tile(tc_range_lo(c, V, P), prefix, B, p.Hkv, p.seg_cost);
+  const int64_t hi = tc_unit_to_tile(tc_range_lo(c + 1, V, P), prefix, B, p.Hkv, p.seg_cost);
   if (lo >= hi) return;  // uniform across the CTA
 
   const uint64_t policy = l2_policy_evict_first();
@@ -427,7 +429,9 @@ __global__ void __launch_bounds__(W * 32, 1)
       ml[(warp * kTcHeads + 2 * tq + 1) * 2 + 1] = l1;
     }
     const bool whole = seg.x0 == seg.pstart && seg.x1 == seg.pend;
-    const int slot = seg.x0 == lo ? 0 : 1;
+    // record slot: 0 for a segment that began in an earlier CTA's range (it
+    // starts this range), 1 for one that starts the pair (and ends this range)
+    const int slot = seg.x0 > seg.pstart ? 0 : 1;
     for (int h0 = 0; h0 < G; h0 += kTcMergeHeads) {
       // lanes whose head pair (2tq, 2tq+1) falls in [h0, h0 + 4) write it
       if ((2 * tq) >= h0 && (2 * tq) < h0 + kTcMergeHeads) {
@@ -506,23 +510,24 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
     *dst = make_uint2(0u, 0u);
     return;
   }
-  const int64_t T = static_cast<int64_t>(p.Hkv) * prefix[p.num_seqs];
-  const int64_t pstart = static_cast<int64_t>(p.Hkv) * prefix[seq] + static_cast<int64_t>(kvh) * n;
-  const int64_t pend = pstart + n;
-  const int cf = static_cast<int>(tc_owner(pstart, T, P));
-  const int cl = static_cast<int>(tc_owner(pend - 1, T, P));
+  const int alpha = p.seg_cost;
+  const int64_t V = tc_vseq(prefix, p.num_seqs, p.Hkv, alpha);
+  // units of the pair's first and last tiles
+  const int64_t u0 = tc_vseq(prefix, seq, p.Hkv, alpha) + static_cast<int64_t>(kvh) * (n + alpha) + alpha;
+  const int cf = static_cast<int>(tc_owner(u0, V, P));
+  const int cl = static_cast<int>(tc_owner(u0 + n - 1, V, P));
   if (cf == cl) return;
-  // CTA cc's record for this pair: slot 0 if the pair began before cc's range
-  // (or exactly at its start), slot 1 if it began inside; CTAs whose range
+  // CTA cc's record for this pair: slot 1 in cf (where the pair begins), slot
+  // 0 in the later CTAs (the pair began before their range); CTAs whose range
   // is empty wrote nothing and are skipped.  Lane j loads record cf + j's
   // (m, l) so that all records cost one round trip, then every lane loads its
   // four output elements of the records four at a time.
   constexpr unsigned kFull = 0xffffffffu;
   auto record = [&](int cc) -> const float* {
-    const int64_t lo_c = tc_range_lo(cc, T, P);
-    const int64_t hi_c = tc_range_lo(cc + 1, T, P);
-    if (lo_c >= hi_c) return nullptr;
-    const int slot = lo_c >= pstart ? 0 : 1;
+    // a CTA strictly between cf and cl with a non-empty range holds tiles of
+    // the pair (its units lie inside the pair's run of tiles)
+    if (tc_range_lo(cc, V, P) >= tc_range_lo(cc + 1, V, P)) return nullptr;
+    const int slot = cc == cf ? 1 : 0;
     return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcHeads + gi) * kRecStride;
   };
   const int K = cl - cf + 1;

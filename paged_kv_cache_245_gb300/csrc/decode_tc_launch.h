@@ -19,6 +19,7 @@ struct TcParams {
   const int32_t* req_ids;       // contig [B]
   float* rec;               // [gridDim.x][2][8][kRecStride]
   int32_t* prefix_out;      // [B + 1] tile prefix per sequence (CTA 0 writes it)
+  int32_t seg_cost;         // schedule weight of one segment, in tiles (alpha below)
   int64_t bs;               // paged block size (multiple of 16); contig S
   int64_t num_blocks;       // paged pool size (checked mode)
   int32_t max_blocks, max_reqs;
@@ -32,15 +33,45 @@ struct TcParams {
 
 enum class TcStatus { kOk, kEncodeFailed, kCudaError };
 
-// Static partition of the flattened tile list [0, T) over P CTAs: CTA c owns
-// [floor(c*T/P), floor((c+1)*T/P)).
-__host__ __device__ inline int64_t tc_range_lo(int64_t c, int64_t T, int64_t P) {
-  return c * T / P;
+// Even partition of [0, V) over P CTAs: CTA c owns [floor(c*V/P), floor((c+1)*V/P)).
+__host__ __device__ inline int64_t tc_range_lo(int64_t c, int64_t V, int64_t P) {
+  return c * V / P;
 }
 
-// The CTA that owns tile x (the largest c with range_lo(c) <= x).
-__host__ __device__ inline int64_t tc_owner(int64_t x, int64_t T, int64_t P) {
-  return ((x + 1) * P + T - 1) / T - 1;
+// The CTA whose range holds position u (the largest c with range_lo(c) <= u).
+__host__ __device__ inline int64_t tc_owner(int64_t u, int64_t V, int64_t P) {
+  return ((u + 1) * P + V - 1) / V - 1;
+}
+
+// Cost-weighted schedule.  A CTA's time grows with its tiles and, about as
+// much as alpha more tiles would, with each (sequence, KV head) segment it
+// walks (the per-segment merge, Q load and table lookups).  So the partition
+// is even over "virtual units": pair (i, h) spans n_i + alpha units, alpha
+// units of padding followed by its n_i tiles, pairs in order.  Sequence i's
+// pairs start at unit Hkv * (prefix[i] + alpha * i) (prefix[i] = tiles of
+// sequences before i; an empty sequence is padding only).  Tile j of pair
+// (i, h) is unit tc_vseq(i) + h * (n_i + alpha) + alpha + j.  A CTA's units
+// hold a contiguous run of tiles; a range that falls inside padding holds
+// none, and a cut inside padding leaves the next pair whole.
+__host__ __device__ inline int64_t tc_vseq(const int32_t* prefix, int i, int Hkv, int alpha) {
+  return static_cast<int64_t>(Hkv) * (static_cast<int64_t>(prefix[i]) + static_cast<int64_t>(alpha) * i);
+}
+
+// First tile whose unit is >= u (u in [0, V]; u == V gives T).
+__host__ __device__ inline int64_t tc_unit_to_tile(int64_t u, const int32_t* prefix, int B, int Hkv,
+                                                   int alpha) {
+  if (u >= tc_vseq(prefix, B, Hkv, alpha)) return static_cast<int64_t>(Hkv) * prefix[B];
+  int a = 0, b = B - 1;  // largest i with tc_vseq(i) <= u
+  while (a < b) {
+    const int mid = (a + b + 1) >> 1;
+    if (tc_vseq(prefix, mid, Hkv, alpha) <= u) a = mid; else b = mid - 1;
+  }
+  const int64_t n = prefix[a + 1] - prefix[a];
+  if (n + alpha <= 0) return static_cast<int64_t>(Hkv) * prefix[a];  // (not reached: see above)
+  const int64_t r = u - tc_vseq(prefix, a, Hkv, alpha);
+  const int64_t h = r / (n + alpha);
+  const int64_t o = r % (n + alpha) - alpha;
+  return static_cast<int64_t>(Hkv) * prefix[a] + h * n + (o > 0 ? o : 0);
 }
 
 // Workspace bytes for the per-CTA partial records and the tile prefix.
