@@ -445,31 +445,42 @@ __global__ void __launch_bounds__(W * 32, 1)
         }
       }
       __syncthreads();
+      // warp hl merges head h0 + hl: lane j < W derives warp j's weight
+      // 2^(m_j - M) / sum_k l_k 2^(m_k - M) once, then every lane sums its four
+      // output elements over the W partials
       const int nh = min(kTcMergeHeads, G - h0);
-      for (int idx = tid; idx < nh * kHeadDim; idx += W * 32) {
-        const int hl = idx >> 7;
-        const int hh = h0 + hl;
-        const int d = idx & 127;
-        float M = -INFINITY;
+      if (warp < nh) {
+        const int hh = h0 + warp;
+        const float mj = lane < W ? ml[(lane * kTcHeads + hh) * 2] : -INFINITY;
+        const float lj = lane < W ? ml[(lane * kTcHeads + hh) * 2 + 1] : 0.f;
+        float M = mj;
 #pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, ml[(w * kTcHeads + hh) * 2]);
-        float Ls = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const float fj = mj == -INFINITY ? 0.f : fast_exp2(mj - M);
+        float Ls = lj * fj;
 #pragma unroll
-          for (int w = 0; w < W; ++w) {
-            const float f = fast_exp2(ml[(w * kTcHeads + hh) * 2] - M);
-            Ls = fmaf(ml[(w * kTcHeads + hh) * 2 + 1], f, Ls);
-            O = fmaf(merge[(w * kTcMergeHeads + hl) * kRecStride + d], f, O);
-          }
+        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(kFull, Ls, o);
+        const float wj = Ls > 0.f ? fj / Ls : 0.f;
+        float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float ww = __shfl_sync(kFull, wj, w);
+          const float4 v =
+              *reinterpret_cast<const float4*>(merge + (w * kTcMergeHeads + warp) * kRecStride + lane * 4);
+          o4.x = fmaf(v.x, ww, o4.x);
+          o4.y = fmaf(v.y, ww, o4.y);
+          o4.z = fmaf(v.z, ww, o4.z);
+          o4.w = fmaf(v.w, ww, o4.w);
         }
-        const float o = Ls > 0.f ? O / Ls : 0.f;
         if (whole) {
-          p.out[((static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) * kHeadDim) + d] =
-              f32_to_bf16_bits(o);
+          const uint32_t lo16 = f32_to_bf16_bits(o4.x) | (uint32_t(f32_to_bf16_bits(o4.y)) << 16);
+          const uint32_t hi16 = f32_to_bf16_bits(o4.z) | (uint32_t(f32_to_bf16_bits(o4.w)) << 16);
+          *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) *
+                                                kHeadDim + lane * 4) = make_uint2(lo16, hi16);
         } else {
           float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcHeads + hh) * kRecStride;
-          r[d] = o;
-          if (d == 0) {
+          *reinterpret_cast<float4*>(r + lane * 4) = o4;
+          if (lane == 0) {
             r[128] = Ls > 0.f ? M : -INFINITY;
             r[129] = Ls;
           }
