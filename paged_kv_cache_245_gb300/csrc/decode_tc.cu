@@ -74,16 +74,18 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
     e = launch_pdl(kernel, dim3(num_ctas), dim3(W * 32), L::kTotal, stream, tk, tv, p);
     if (e != cudaSuccess) return e;
-    const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hq;
+    if (num_ctas < 2) continue;  // one CTA: every pair was written whole
     // The combine may be scheduled while the main kernel drains (it waits
-    // for it before reading anything); PKV_COMBINE_PDL=0 turns that off.
+    // for it before reading the records); PKV_COMBINE_PDL=0 turns that off.
     static const bool combine_pdl = [] {
       const char* v = getenv("PKV_COMBINE_PDL");
       return !(v != nullptr && v[0] == '0');
     }();
-    e = launch_pdl_if(combine_pdl || pdl_enabled(), decode_tc_combine_kernel,
-                      dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128), 0, stream, p,
-                      num_ctas);
+    const int64_t warps = static_cast<int64_t>(num_ctas - 1) * p.G;
+    const int early = pdl_enabled() ? 0 : 1;  // main kernel in plain stream order
+    e = launch_pdl_if(combine_pdl || pdl_enabled(), decode_tc_combine_kernel<kContig>,
+                      dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0, stream, p,
+                      num_ctas, early);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -92,9 +94,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
 }  // namespace
 
 size_t tc_workspace_bytes(int num_ctas) {
-  const size_t rec = static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float);
-  const size_t prefix = (static_cast<size_t>(kTcMaxSeqs + 1) * sizeof(int32_t) + 255) / 256 * 256;
-  return rec + prefix;
+  return static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float);
 }
 
 TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, const void* v,
@@ -117,9 +117,6 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
   }();
   p.seg_cost = seg_cost;
   p.rec = static_cast<float*>(workspace);
-  p.prefix_out = reinterpret_cast<int32_t*>(
-      static_cast<unsigned char*>(workspace) +
-      static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float));
   cudaError_t e;
   if (contig) {
     e = cfg == 1 ? launch_cfg<true, 12, 2>(tk, tv, p, num_ctas, stream)

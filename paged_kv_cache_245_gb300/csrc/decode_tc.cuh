@@ -82,34 +82,6 @@ __device__ __forceinline__ int tc_context(const TcParams& p, int i, bool contig,
   return ctx;
 }
 
-// A run of tiles of one pair inside a CTA's range.
-struct TcSeg {
-  int64_t x0, x1;        // tiles [x0, x1) of the flattened list
-  int64_t pstart, pend;  // the whole pair's tiles
-  int seq, kvh;
-};
-
-// Segment starting at tile x (x < hi <= T).  prefix[i] = tiles of sequences
-// before i; pair (i, h) holds tiles [Hkv*prefix[i] + h*n_i, + n_i).
-__device__ __forceinline__ TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_t* prefix,
-                                             int B, int Hkv) {
-  int a = 0, b = B - 1;
-  while (a < b) {
-    const int mid = (a + b + 1) >> 1;
-    if (static_cast<int64_t>(Hkv) * prefix[mid] <= x) a = mid; else b = mid - 1;
-  }
-  const int64_t base = static_cast<int64_t>(Hkv) * prefix[a];
-  const int n = prefix[a + 1] - prefix[a];  // > 0 because x < Hkv*prefix[a+1]
-  TcSeg s;
-  s.seq = a;
-  s.kvh = static_cast<int>((x - base) / n);
-  s.pstart = base + static_cast<int64_t>(s.kvh) * n;
-  s.pend = s.pstart + n;
-  s.x0 = x;
-  s.x1 = s.pend < hi ? s.pend : hi;
-  return s;
-}
-
 template <bool kContig, int W, int S>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -172,8 +144,12 @@ __global__ void __launch_bounds__(W * 32, 1)
     if (lane == 31) prefix[B] = incl;
   }
   __syncthreads();
-  if (c == 0)
-    for (int i = tid; i <= B; i += W * 32) p.prefix_out[i] = prefix[i];
+  // outputs of empty contexts are zeros (sequences c, c + P, ... of this CTA)
+  for (int i = c; i < B; i += P) {
+    if (ctx_s[i] != 0) continue;
+    uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(i) * p.Hq * kHeadDim);
+    for (int k = tid; k < p.Hq * kHeadDim / 8; k += W * 32) o[k] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
   const int64_t lo = tc_unit_to_tile(tc_range_lo(c, V, P), prefix, B, p.Hkv, p.seg_cost);
   const int64_t hi = tc_unit_to_tile(tc_range_lo(c + 1, V, P), prefix, B, p.Hkv, p.seg_cost);
@@ -499,35 +475,68 @@ __global__ void __launch_bounds__(W * 32, 1)
   }
 }
 
-// One warp per (sequence, query head): zeros for an empty context; nothing
-// when one CTA covered the whole pair (it wrote the output); otherwise merge
-// the records of the CTAs that share the pair:
-//   M = max m_c,  w_c = l_c 2^(m_c - M),  out = sum w_c o_c / sum w_c.
-__global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P) {
+// Split-pair combine.  One warp per (CTA boundary b = 1 .. P-1, query head
+// gi < G).  The warp finds the pair that holds the first tile of CTA b's
+// range; if b is the first boundary inside that pair (CTA b - 1 holds its
+// first tile), the warp merges the records of the CTAs cf .. cl that share
+// the pair:  M = max m_c,  w_c = l_c 2^(m_c - M),  out = sum w_c o_c / sum w_c.
+// Every other pair was written whole by the main kernel.  The classification
+// reads only context_lens (and req_ids): with `early` set, the main kernel
+// was launched in plain stream order, so those inputs were complete before
+// it started and the warp classifies before waiting for the main kernel;
+// only the record loads and the merge follow the wait.
+template <bool kContig>
+__global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P, int early) {
+  __shared__ int32_t prefix[kTcMaxSeqs + 1];
+  __shared__ int32_t wsum[4];
   grid_dependency_trigger();
-  grid_dependency_wait();
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (idx >= static_cast<int64_t>(p.num_seqs) * p.Hq) return;
-  const int seq = static_cast<int>(idx / p.Hq);
-  const int hq = static_cast<int>(idx % p.Hq);
-  const int kvh = hq / p.G;
-  const int gi = hq % p.G;
-  const int32_t* prefix = p.prefix_out;
-  const int n = prefix[seq + 1] - prefix[seq];
-  uint2* dst = reinterpret_cast<uint2*>(p.out + idx * kHeadDim + lane * 4);
-  if (n == 0) {
-    *dst = make_uint2(0u, 0u);
-    return;
+  if (!early) grid_dependency_wait();
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int B = p.num_seqs;
+  // tile prefix over sequences, as the main kernel computes it (4 per thread)
+  int n4[4];
+  int tsum = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid * 4 + k;
+    n4[k] = i < B ? (tc_context(p, i, kContig, false) + 15) >> 4 : 0;
+    tsum += n4[k];
   }
+  int incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - tsum;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid * 4 + k;
+    if (i < B) prefix[i] = run;
+    run += n4[k];
+  }
+  if (tid == 127) prefix[B] = run;
+  __syncthreads();
+
+  // classify: does this warp merge a pair, and which
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  const int bnd = 1 + static_cast<int>(idx / p.G);
+  const int gi = static_cast<int>(idx % p.G);
   const int alpha = p.seg_cost;
-  const int64_t V = tc_vseq(prefix, p.num_seqs, p.Hkv, alpha);
-  // units of the pair's first and last tiles
-  const int64_t u0 = tc_vseq(prefix, seq, p.Hkv, alpha) + static_cast<int64_t>(kvh) * (n + alpha) + alpha;
-  const int cf = static_cast<int>(tc_owner(u0, V, P));
-  const int cl = static_cast<int>(tc_owner(u0 + n - 1, V, P));
-  if (cf == cl) return;
+  const int64_t V = tc_vseq(prefix, B, p.Hkv, alpha);
+  int seq = 0, kvh = 0, cf = 0, cl = 0;
+  const bool merge_it = tc_boundary_pair(bnd, prefix, B, p.Hkv, alpha, P, &seq, &kvh, &cf, &cl);
+  // Every thread waits here, so that the combine never completes before the
+  // main kernel (whose outputs later work in the stream may read).
+  if (early) grid_dependency_wait();
+  if (!merge_it) return;
+  uint2* dst = reinterpret_cast<uint2*>(
+      p.out + ((static_cast<int64_t>(seq) * p.Hq + kvh * p.G + gi) * kHeadDim) + lane * 4);
   // CTA cc's record for this pair: slot 1 in cf (where the pair begins), slot
   // 0 in the later CTAs (the pair began before their range); CTAs whose range
   // is empty wrote nothing and are skipped.  Lane j loads record cf + j's

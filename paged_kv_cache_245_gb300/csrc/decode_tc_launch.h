@@ -18,7 +18,6 @@ struct TcParams {
   const int32_t* block_tables;  // paged [B][max_blocks]
   const int32_t* req_ids;       // contig [B]
   float* rec;               // [gridDim.x][2][8][kRecStride]
-  int32_t* prefix_out;      // [B + 1] tile prefix per sequence (CTA 0 writes it)
   int32_t seg_cost;         // schedule weight of one segment, in tiles (alpha below)
   int64_t bs;               // paged block size (multiple of 16); contig S
   int64_t num_blocks;       // paged pool size (checked mode)
@@ -74,7 +73,60 @@ __host__ __device__ inline int64_t tc_unit_to_tile(int64_t u, const int32_t* pre
   return static_cast<int64_t>(Hkv) * prefix[a] + h * n + (o > 0 ? o : 0);
 }
 
-// Workspace bytes for the per-CTA partial records and the tile prefix.
+// A run of tiles of one pair inside a CTA's range.
+struct TcSeg {
+  int64_t x0, x1;        // tiles [x0, x1) of the flattened list
+  int64_t pstart, pend;  // the whole pair's tiles
+  int seq, kvh;
+};
+
+// Segment starting at tile x (x < hi <= T).  prefix[i] = tiles of sequences
+// before i; pair (i, h) holds tiles [Hkv*prefix[i] + h*n_i, + n_i).
+__host__ __device__ inline TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_t* prefix,
+                                             int B, int Hkv) {
+  int a = 0, b = B - 1;
+  while (a < b) {
+    const int mid = (a + b + 1) >> 1;
+    if (static_cast<int64_t>(Hkv) * prefix[mid] <= x) a = mid; else b = mid - 1;
+  }
+  const int64_t base = static_cast<int64_t>(Hkv) * prefix[a];
+  const int n = prefix[a + 1] - prefix[a];  // > 0 because x < Hkv*prefix[a+1]
+  TcSeg s;
+  s.seq = a;
+  s.kvh = static_cast<int>((x - base) / n);
+  s.pstart = base + static_cast<int64_t>(s.kvh) * n;
+  s.pend = s.pstart + n;
+  s.x0 = x;
+  s.x1 = s.pend < hi ? s.pend : hi;
+  return s;
+}
+
+// The pair that the combine warp of CTA boundary bnd (1 <= bnd < P) merges:
+// the pair holding the first tile of CTA bnd's range, if bnd is the first
+// boundary inside it (CTA bnd - 1 holds its first tile).  Returns false if
+// that boundary merges nothing; else its sequence, KV head and the CTAs
+// cf .. cl whose ranges share the pair.
+__host__ __device__ inline bool tc_boundary_pair(int bnd, const int32_t* prefix, int B, int Hkv,
+                                                 int alpha, int64_t P, int* seq, int* kvh, int* cf,
+                                                 int* cl) {
+  if (bnd < 1 || bnd >= P) return false;
+  const int64_t V = tc_vseq(prefix, B, Hkv, alpha);
+  const int64_t T = static_cast<int64_t>(Hkv) * prefix[B];
+  const int64_t x = tc_unit_to_tile(tc_range_lo(bnd, V, P), prefix, B, Hkv, alpha);
+  if (x >= T) return false;
+  const TcSeg seg = tc_find_seg(x, T, prefix, B, Hkv);
+  if (seg.pstart == x) return false;  // a boundary between pairs cuts nothing
+  const int64_t n = seg.pend - seg.pstart;
+  // units of the pair's first and last tiles
+  const int64_t u0 = tc_vseq(prefix, seg.seq, Hkv, alpha) + seg.kvh * (n + alpha) + alpha;
+  *seq = seg.seq;
+  *kvh = seg.kvh;
+  *cf = static_cast<int>(tc_owner(u0, V, P));
+  *cl = static_cast<int>(tc_owner(u0 + n - 1, V, P));
+  return *cf + 1 == bnd;
+}
+
+// Workspace bytes for the per-CTA partial records.
 size_t tc_workspace_bytes(int num_ctas);
 
 // cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages.

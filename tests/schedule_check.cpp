@@ -8,7 +8,9 @@
 //  * records: walking every CTA's segments the way the kernel does, each
 //    partial segment takes a slot no other segment of its CTA takes, and the
 //    combine's lookup (cf..cl with its slot rule) names exactly the records
-//    written for every split pair, and no pair it treats as whole was split.
+//    written for every split pair, and no pair it treats as whole was split;
+//  * the combine's boundary warps: every split pair is merged exactly once,
+//    by the boundary just after the CTA holding its first tile.
 #include <cstdio>
 #include <algorithm>
 #include <cstdlib>
@@ -139,6 +141,22 @@ static int check_weighted(const std::vector<int32_t>& n, int Hkv, int P, int alp
     }
     if (looked != written[r]) return fail("records", (long long)r, cf);
   }
+  // the combine's warps: each split pair is merged by exactly one CTA
+  // boundary (cf + 1), which names the pair and its CTAs; no other boundary
+  // merges anything
+  std::map<size_t, int> merged_by;
+  for (int bnd = 0; bnd <= P; ++bnd) {
+    int seq = -1, kvh = -1, bf = -1, bl = -1;
+    if (!tc_boundary_pair(bnd, prefix.data(), B, Hkv, alpha, P, &seq, &kvh, &bf, &bl)) continue;
+    const size_t r = static_cast<size_t>(seq) * Hkv + kvh;
+    const int cf = static_cast<int>(tc_owner(pair_u0[r], V, P));
+    const int cl = static_cast<int>(tc_owner(pair_u0[r] + pair_n[r] - 1, V, P));
+    if (cf == cl || bf != cf || bl != cl || bnd != cf + 1) return fail("boundary pair", bnd, cf);
+    if (merged_by.count(r)) return fail("pair merged twice", (long long)r, bnd);
+    merged_by[r] = bnd;
+  }
+  for (const auto& kv : written)
+    if (!merged_by.count(kv.first)) return fail("split pair not merged", (long long)kv.first, 0);
   return 0;
 }
 
