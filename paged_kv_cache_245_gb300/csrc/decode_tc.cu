@@ -82,10 +82,9 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
       return !(v != nullptr && v[0] == '0');
     }();
     const int64_t warps = static_cast<int64_t>(num_ctas - 1) * p.G;
-    const int early = pdl_enabled() ? 0 : 1;  // main kernel in plain stream order
     e = launch_pdl_if(combine_pdl || pdl_enabled(), decode_tc_combine_kernel<kContig>,
                       dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0, stream, p,
-                      num_ctas, early);
+                      num_ctas);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -112,11 +112,13 @@ __global__ void __launch_bounds__(W * 32, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
-  // Programmatic dependent launch: let the next kernel in the stream get
-  // scheduled now, and wait for the previous one to finish before reading
-  // any input (no-ops without the launch attribute).
-  grid_dependency_trigger();
+  // Programmatic dependent launch (no-ops without the launch attribute):
+  // wait for the previous kernel in the stream to finish before reading any
+  // input, then let the combine kernel get scheduled.  In this order every
+  // input is complete by the time the combine starts, which lets it read
+  // context_lens before waiting for this kernel.
   grid_dependency_wait();
+  grid_dependency_trigger();
 
   // ---- tile counts and their prefix over sequences (every CTA, once)
   for (int i = tid; i < B; i += W * 32) {
@@ -481,16 +483,15 @@ __global__ void __launch_bounds__(W * 32, 1)
 // first tile), the warp merges the records of the CTAs cf .. cl that share
 // the pair:  M = max m_c,  w_c = l_c 2^(m_c - M),  out = sum w_c o_c / sum w_c.
 // Every other pair was written whole by the main kernel.  The classification
-// reads only context_lens (and req_ids): with `early` set, the main kernel
-// was launched in plain stream order, so those inputs were complete before
-// it started and the warp classifies before waiting for the main kernel;
-// only the record loads and the merge follow the wait.
+// reads only context_lens (and req_ids), which were complete before this
+// kernel was launched (the main kernel lets it launch only after its own
+// dependency wait), so the warp classifies before waiting for the main
+// kernel; only the record loads and the merge follow the wait.
 template <bool kContig>
-__global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P, int early) {
+__global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P) {
   __shared__ int32_t prefix[kTcMaxSeqs + 1];
   __shared__ int32_t wsum[4];
   grid_dependency_trigger();
-  if (!early) grid_dependency_wait();
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
   const bool merge_it = tc_boundary_pair(bnd, prefix, B, p.Hkv, alpha, P, &seq, &kvh, &cf, &cl);
   // Every thread waits here, so that the combine never completes before the
   // main kernel (whose outputs later work in the stream may read).
-  if (early) grid_dependency_wait();
+  grid_dependency_wait();
   if (!merge_it) return;
   uint2* dst = reinterpret_cast<uint2*>(
       p.out + ((static_cast<int64_t>(seq) * p.Hq + kvh * p.G + gi) * kHeadDim) + lane * 4);
