@@ -251,21 +251,17 @@ class DeviceWorkload:
         if pairs is not None:
             self.pkv.block_copy(pairs, self.k_caches, self.v_caches)
 
-    def layer(self, l, events=None):
+    def layer(self, l):
+        """One layer's decode step: append + attention in one C-ABI call."""
         li = self.layers[l]
-        self.pkv.kv_append(self.slots, li.k_new, li.v_new, li.k_cache, li.v_cache)
-        if events is not None:
-            events[0].record()
-        self.pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, self.tables, self.ctx,
-                                        self.batch.max_context, self.scale, out=self.out[l],
-                                        workspace=self.workspace)
-        if events is not None:
-            events[1].record()
+        self.pkv.paged_decode_step(self.slots, li.k_new, li.v_new, li.q, li.k_cache, li.v_cache,
+                                   self.tables, self.ctx, self.batch.max_context, self.scale,
+                                   out=self.out[l], workspace=self.workspace)
 
-    def step(self, events=None):
+    def step(self):
         self.copy_on_write()
         for l in range(self.shape.num_layers):
-            self.layer(l, None if events is None else events[l])
+            self.layer(l)
 
     def attention_only(self):
         for l in range(self.shape.num_layers):
@@ -374,7 +370,8 @@ def run_gpu(args, world, rank, local):
                          "%.0f MB per layer" % (nl * alg / 1e9, alg / 1e6),
                    "step": ("block_copy of %d copy-on-write pairs (all layers), then "
                             % len(wl.cow) if wl.cow is not None else "")
-                           + "per layer: kv_append + paged_decode_attention (main + combine)"},
+                           + "per layer: paged_decode_step = kv_append + paged_decode_attention "
+                             "(main + combine) in one C-ABI call"},
         "hbm_tbs": round(achieved_gbs / 1e3, 4),
         "hbm_pct_of_8tbs": round(100 * achieved_gbs / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
@@ -541,9 +538,8 @@ def measure_e2e(wl, dev, args, world):
         for l in range(nl):
             q, kn, vn = views[3 * l:3 * l + 3]
             li = wl.layers[l]
-            pkv.kv_append(slots, kn, vn, li.k_cache, li.v_cache)
-            pkv.paged_decode_attention(q, li.k_cache, li.v_cache, tables, ctx, b.max_context,
-                                       wl.scale, out=out_all[l], workspace=wl.workspace)
+            pkv.paged_decode_step(slots, kn, vn, q, li.k_cache, li.v_cache, tables, ctx,
+                                  b.max_context, wl.scale, out=out_all[l], workspace=wl.workspace)
         host_out.copy_(out_all, non_blocking=True)
 
     iters = max(20, args.steps // 10)

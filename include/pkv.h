@@ -6,6 +6,8 @@
  *   pkv_paged_decode_attention    single-query attention through block tables
  *   pkv_contig_decode_attention   the same over per-request sub-tensors
  *   pkv_block_copy                copy whole blocks (copy on write)
+ * and pkv_paged_decode_step / pkv_contig_decode_step run append + attention
+ * of one layer as one call.
  *
  * Conventions for every call:
  *   - All tensor arguments are DEVICE pointers on the current CUDA device,
@@ -143,6 +145,41 @@ PKV_API pkv_status pkv_paged_decode_attention(
  */
 PKV_API pkv_status pkv_contig_decode_attention(
     const void *q, const void *k_buf, const void *v_buf,
+    const int32_t *req_ids, int32_t max_reqs,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int64_t S, float scale, pkv_heads heads, void *out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step of one layer in one call: the append of this step's token
+ * ("Insights into LLM Serving Systems: KV-Cache Memory Allocation Patterns",
+ * section 4, Observation-1: every request grows by one token per iteration)
+ * followed by the attention over the grown cache.  Same result, bit for bit,
+ * as
+ *   pkv_kv_append(slot_mapping, num_seqs, k_new, v_new, k_cache, v_cache,
+ *                 num_blocks * block_size, block_size, heads, stream);
+ *   pkv_paged_decode_attention(q, k_cache, v_cache, ..., stream);
+ * (contiguous: block_size = S, num_slots = max_reqs * S and
+ * pkv_contig_decode_attention), with one new token per sequence (k_new,
+ * v_new [num_seqs][Hkv][128]).  All arguments are checked before anything is
+ * launched.  The attention kernel starts while the append runs: it reads q,
+ * context_lens and block_tables (req_ids) at once and waits for the append
+ * only before it loads K/V, so none of those, nor out, may alias k_new, v_new
+ * or the caches (they never do in a decode step).  Errors as for the two
+ * calls.  The pages have no counterpart beyond the two operations it
+ * combines.
+ */
+PKV_API pkv_status pkv_paged_decode_step(
+    const int64_t *slot_mapping, const void *k_new, const void *v_new,
+    const void *q, void *k_cache, void *v_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_blocks,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int32_t block_size, float scale, pkv_heads heads, void *out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+PKV_API pkv_status pkv_contig_decode_step(
+    const int64_t *slot_mapping, const void *k_new, const void *v_new,
+    const void *q, void *k_buf, void *v_buf,
     const int32_t *req_ids, int32_t max_reqs,
     const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
     int64_t S, float scale, pkv_heads heads, void *out,

@@ -24,6 +24,7 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
             "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
+            "pkv_paged_decode_step", "pkv_contig_decode_step",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -61,6 +62,10 @@ def lib():
     L.pkv_contig_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i64,
                                               ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_block_copy.argtypes = [vp, i64, vp, vp, i32, i64, i64, vp]
+    L.pkv_paged_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
+                                        ctypes.c_float, Heads, vp, vp, sz, vp]
+    L.pkv_contig_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
+                                         ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_set_checked.argtypes = [ctypes.c_int]
     L.pkv_set_checked.restype = None
     L.pkv_get_checked.restype = ctypes.c_int
@@ -205,6 +210,79 @@ def contig_decode_attention(q, k_buf, v_buf, req_ids, context_lens, max_context,
     _check(lib().pkv_contig_decode_attention(
         _ptr(q), _ptr(k_buf), _ptr(v_buf), _ptr(req_ids), max_reqs, _ptr(context_lens), B,
         int(max_context), S, float(scale), h, _ptr(out), ws_ptr, ws_len, _stream(q)))
+    return out
+
+
+def _check_new_rows(slot_mapping, k_new, v_new, B, hkv, d):
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, n, 3)
+        if tuple(t.shape) != (B, hkv, d):
+            raise ValueError("%s must be [num_seqs, Hkv, D]" % n)
+    if slot_mapping.shape[0] != B:
+        raise ValueError("slot_mapping must have num_seqs entries")
+
+
+def paged_decode_step(slot_mapping, k_new, v_new, q, k_cache, v_cache, block_tables,
+                      context_lens, max_context, scale, out=None, workspace=None):
+    """One decode step of one layer in one call: kv_append(slot_mapping, k_new,
+    v_new, k_cache, v_cache) then paged_decode_attention(q, ...); the same
+    bytes as the two calls."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d != d2 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shapes disagree")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    _check_new_rows(slot_mapping, k_new, v_new, B, hkv, d)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    h = heads(hq, hkv, d)
+    nbytes = lib().pkv_decode_workspace_size(B, h, int(max_context)) if B > 0 else 0
+    workspace = _workspace(workspace, q, nbytes)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pkv_paged_decode_step(
+        _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], nb, _ptr(context_lens), B, int(max_context),
+        bs, float(scale), h, _ptr(out), ws_ptr, ws_len, _stream(q)))
+    return out
+
+
+def contig_decode_step(slot_mapping, k_new, v_new, q, k_buf, v_buf, req_ids, context_lens,
+                       max_context, scale, out=None, workspace=None):
+    """kv_append into the request rows (slot = reqId * S + position) then
+    contig_decode_attention, as one call."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_buf, "k_buf"), (v_buf, "v_buf")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(req_ids, torch.int32, "req_ids", 1)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, hq, d = q.shape
+    max_reqs, hkv, S, d2 = k_buf.shape
+    if d != d2 or tuple(v_buf.shape) != tuple(k_buf.shape):
+        raise ValueError("q / buffer shapes disagree")
+    if req_ids.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("req_ids / context_lens must have num_seqs rows")
+    _check_new_rows(slot_mapping, k_new, v_new, B, hkv, d)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    h = heads(hq, hkv, d)
+    nbytes = lib().pkv_decode_workspace_size(B, h, int(max_context)) if B > 0 else 0
+    workspace = _workspace(workspace, q, nbytes)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pkv_contig_decode_step(
+        _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(k_buf), _ptr(v_buf),
+        _ptr(req_ids), max_reqs, _ptr(context_lens), B, int(max_context), S, float(scale), h,
+        _ptr(out), ws_ptr, ws_len, _stream(q)))
     return out
 
 

@@ -72,7 +72,10 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     p.ctx_lens += s0;
     if (kContig) p.req_ids += s0;
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
-    e = launch_pdl(kernel, dim3(num_ctas), dim3(W * 32), L::kTotal, stream, tk, tv, p);
+    // the first chunk of a decode step starts while the append runs
+    p.early_inputs = s0 == 0 ? p0.early_inputs : 0;
+    e = launch_pdl_if(p.early_inputs != 0 || pdl_enabled(), kernel, dim3(num_ctas), dim3(W * 32),
+                      L::kTotal, stream, tk, tv, p);
     if (e != cudaSuccess) return e;
     if (num_ctas < 2) continue;  // one CTA: every pair was written whole
     // The combine may be scheduled while the main kernel drains (it waits

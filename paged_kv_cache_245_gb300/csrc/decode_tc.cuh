@@ -116,9 +116,15 @@ __global__ void __launch_bounds__(W * 32, 1)
   // wait for the previous kernel in the stream to finish before reading any
   // input, then let the combine kernel get scheduled.  In this order every
   // input is complete by the time the combine starts, which lets it read
-  // context_lens before waiting for this kernel.
-  grid_dependency_wait();
-  grid_dependency_trigger();
+  // context_lens before waiting for this kernel.  In a decode step whose
+  // previous kernel is the append (early_inputs), q, context_lens, req_ids
+  // and the block tables were complete before it started and only the
+  // caches are still being written: the prologue reads them at once and the
+  // wait comes just before the first K/V load.
+  if (!p.early_inputs) {
+    grid_dependency_wait();
+    grid_dependency_trigger();
+  }
 
   // ---- tile counts and their prefix over sequences (every CTA, once)
   for (int i = tid; i < B; i += W * 32) {
@@ -155,7 +161,10 @@ __global__ void __launch_bounds__(W * 32, 1)
   const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
   const int64_t lo = tc_unit_to_tile(tc_range_lo(c, V, P), prefix, B, p.Hkv, p.seg_cost);
   const int64_t hi = tc_unit_to_tile(tc_range_lo(c + 1, V, P), prefix, B, p.Hkv, p.seg_cost);
-  if (lo >= hi) return;  // uniform across the CTA
+  if (lo >= hi) {  // uniform across the CTA
+    if (p.early_inputs) grid_dependency_wait();  // never finish before the append
+    return;
+  }
 
   const uint64_t policy = l2_policy_evict_first();
   unsigned char* stage0 = smem + L::kStagesOff + warp * S * kTcStageBytes;
@@ -259,6 +268,10 @@ __global__ void __launch_bounds__(W * 32, 1)
         cx = cs.x0 + warp;
       }
     }
+  }
+  if (p.early_inputs) {
+    grid_dependency_wait();
+    grid_dependency_trigger();
   }
   for (int s = 0; s < S && ivalid; ++s) {
     issue(s, __shfl_sync(kFull, pre_entry, s));

@@ -34,11 +34,12 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   *reinterpret_cast<uint4*>(dst) = ld_global_nc_v4(src);
 }
 
-cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream, bool plain) {
   const int64_t rows = 2 * p.num_tokens * p.Hkv;
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + 15) / 16;
-  return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+  return launch_pdl_if(!plain && pdl_enabled(), kv_append_kernel,
+                       dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 // Block copy: blockIdx.x strides over the block's 16-byte chunks, blockIdx.y

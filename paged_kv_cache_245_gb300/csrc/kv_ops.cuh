@@ -34,7 +34,9 @@ struct CopyParams {
   int* err;
 };
 
-cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+// plain: launch in stream order even when PKV_PDL=1 (a decode step's append,
+// whose dependent attention kernel reads its inputs before waiting)
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream, bool plain = false);
 cudaError_t launch_block_copy(const CopyParams& p, int64_t num_pairs, cudaStream_t stream);
 
 }  // namespace pkv

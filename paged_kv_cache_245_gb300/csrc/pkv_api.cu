@@ -142,12 +142,15 @@ size_t decode_workspace_need(int32_t num_seqs, const pkv_heads& h, int32_t max_c
   return split > tc ? split : tc;
 }
 
+// Validates a decode call and, unless dry_run, launches it.  after_append: the
+// previous kernel in the stream is this step's append (plain launch), so the
+// tensor-core kernel may read its inputs before waiting for it.
 pkv_status decode_common(bool contig, const void* q, const void* k, const void* v,
                          const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
                          const int32_t* req_ids, int32_t max_reqs, const int32_t* context_lens,
                          int32_t num_seqs, int32_t max_context, int64_t bs_or_S, float scale,
                          pkv_heads h, void* out, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         void* stream, bool dry_run = false, bool after_append = false) {
   pkv_status st = check_heads(h);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_context < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
@@ -198,6 +201,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
       return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need,
                   workspace ? workspace_bytes : size_t{0});
     if (!aligned(workspace, 16)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (dry_run) return PKV_OK;
     pkv::TcParams t;
     std::memset(&t, 0, sizeof t);
     t.q = static_cast<const uint16_t*>(q);
@@ -217,6 +221,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     t.qscale = scale * 1.4426950408889634f;  // log2(e)
     t.checked = g_checked.load();
     t.stall_test = g_stall_test.exchange(0);
+    t.early_inputs = after_append ? 1 : 0;
     t.err = err;
     cudaError_t ce = cudaSuccess;
     const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total,
@@ -235,6 +240,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
                   workspace ? workspace_bytes : size_t{0});
     if (!aligned(workspace, 16)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
   }
+  if (dry_run) return PKV_OK;
 
   pkv::DecodeParams p;
   std::memset(&p, 0, sizeof p);
@@ -269,13 +275,11 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
   return PKV_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-pkv_status pkv_kv_append(const int64_t* slot_mapping, int64_t num_tokens, const void* k,
+// Validates and launches an append.  plain: launch in stream order whatever
+// PKV_PDL says (the append of a decode step).
+pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const void* k,
                          const void* v, void* k_cache, void* v_cache, int64_t num_slots,
-                         int64_t block_size, pkv_heads heads, void* stream) {
+                         int64_t block_size, pkv_heads heads, void* stream, bool plain) {
   if (heads.num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads must be positive");
   if (heads.head_dim != pkv::kHeadDim)
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (only 128 is built)", heads.head_dim);
@@ -304,9 +308,62 @@ pkv_status pkv_kv_append(const int64_t* slot_mapping, int64_t num_tokens, const 
   p.err = err;
   const int64_t rows = 2 * num_tokens * heads.num_kv_heads;
   if ((rows + 15) / 16 > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens");
-  const cudaError_t e = pkv::launch_kv_append(p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = pkv::launch_kv_append(p, static_cast<cudaStream_t>(stream), plain);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_kv_append(const int64_t* slot_mapping, int64_t num_tokens, const void* k,
+                         const void* v, void* k_cache, void* v_cache, int64_t num_slots,
+                         int64_t block_size, pkv_heads heads, void* stream) {
+  return append_common(slot_mapping, num_tokens, k, v, k_cache, v_cache, num_slots, block_size,
+                       heads, stream, false);
+}
+
+// A decode step: the attention call is checked first, so that a bad argument
+// launches nothing; then the append (plain launch) and the attention.
+pkv_status pkv_paged_decode_step(const int64_t* slot_mapping, const void* k_new,
+                                 const void* v_new, const void* q, void* k_cache, void* v_cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 int32_t num_blocks, const int32_t* context_lens,
+                                 int32_t num_seqs, int32_t max_context, int32_t block_size,
+                                 float scale, pkv_heads heads, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  pkv_status st = decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                num_blocks, nullptr, 0, context_lens, num_seqs, max_context,
+                                block_size, scale, heads, out, workspace, workspace_bytes, stream,
+                                true);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  st = append_common(slot_mapping, num_seqs, k_new, v_new, k_cache, v_cache,
+                     static_cast<int64_t>(num_blocks) * block_size, block_size, heads, stream,
+                     true);
+  if (st != PKV_OK) return st;
+  return decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq, num_blocks,
+                       nullptr, 0, context_lens, num_seqs, max_context, block_size, scale, heads,
+                       out, workspace, workspace_bytes, stream, false, true);
+}
+
+pkv_status pkv_contig_decode_step(const int64_t* slot_mapping, const void* k_new,
+                                  const void* v_new, const void* q, void* k_buf, void* v_buf,
+                                  const int32_t* req_ids, int32_t max_reqs,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t max_context, int64_t S, float scale, pkv_heads heads,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  pkv_status st = decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs,
+                                context_lens, num_seqs, max_context, S, scale, heads, out,
+                                workspace, workspace_bytes, stream, true);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  st = append_common(slot_mapping, num_seqs, k_new, v_new, k_buf, v_buf,
+                     static_cast<int64_t>(max_reqs) * S, S, heads, stream, true);
+  if (st != PKV_OK) return st;
+  return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
+                       num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
+                       stream, false, true);
 }
 
 int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads, int32_t max_context) {
