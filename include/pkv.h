@@ -250,6 +250,28 @@ PKV_API int pkv_get_decode_variant(void);
  */
 PKV_API void pkv_debug_stall_next_decode(void);
 
+/*
+ * Test-only gather: out[i][h][pos] (bf16 [num_seqs][Hkv][max_context][128])
+ * = the cache row that the decode kernels read for position pos of sequence
+ * i and KV head h, zeros for pos >= context_lens[i].  It locates rows with
+ * the same address function as the decode and append kernels, so a
+ * byte-for-byte comparison with a plain gather pins the block-table
+ * indexing ("Running Out of Cache": positions map to (block, offset) as
+ * virtual addresses map to frames) and the reqId x S rule of the contiguous
+ * layout ("Leveraging Low-Level CUDA APIs for vAttention's Dynamic Memory"
+ * 5.2.3).  Arguments as for the decode calls; checked mode reports and
+ * zero-fills rows with an out-of-range block id or request id.
+ */
+PKV_API pkv_status pkv_debug_gather_paged(
+    const void *cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+    int32_t num_blocks, const int32_t *context_lens, int32_t num_seqs,
+    int32_t max_context, int32_t block_size, int32_t num_kv_heads, void *out,
+    void *stream);
+PKV_API pkv_status pkv_debug_gather_contig(
+    const void *buf, const int32_t *req_ids, int32_t max_reqs,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int64_t S, int32_t num_kv_heads, void *out, void *stream);
+
 /* Checked mode on (1) or off (0, the default) for later calls. */
 PKV_API void pkv_set_checked(int enable);
 PKV_API int pkv_get_checked(void);

@@ -24,7 +24,8 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
             "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
-            "pkv_paged_decode_step", "pkv_contig_decode_step",
+            "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
+            "pkv_debug_gather_contig",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -66,6 +67,8 @@ def lib():
                                         ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_contig_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
                                          ctypes.c_float, Heads, vp, vp, sz, vp]
+    L.pkv_debug_gather_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp]
+    L.pkv_debug_gather_contig.argtypes = [vp, vp, i32, vp, i32, i32, i64, i32, vp, vp]
     L.pkv_set_checked.argtypes = [ctypes.c_int]
     L.pkv_set_checked.restype = None
     L.pkv_get_checked.restype = ctypes.c_int
@@ -283,6 +286,34 @@ def contig_decode_step(slot_mapping, k_new, v_new, q, k_buf, v_buf, req_ids, con
         _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(k_buf), _ptr(v_buf),
         _ptr(req_ids), max_reqs, _ptr(context_lens), B, int(max_context), S, float(scale), h,
         _ptr(out), ws_ptr, ws_len, _stream(q)))
+    return out
+
+
+def debug_gather_paged(cache, block_tables, context_lens, max_context):
+    """Test-only: the logical rows [B, Hkv, max_context, D] the decode kernels
+    read through block_tables (zeros past each context)."""
+    _need(cache, torch.bfloat16, "cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    nb, hkv, bs, d = cache.shape
+    B = context_lens.shape[0]
+    out = torch.empty((B, hkv, int(max_context), d), dtype=torch.bfloat16, device=cache.device)
+    _check(lib().pkv_debug_gather_paged(_ptr(cache), _ptr(block_tables), block_tables.shape[1],
+                                        nb, _ptr(context_lens), B, int(max_context), bs, hkv,
+                                        _ptr(out), _stream(cache)))
+    return out
+
+
+def debug_gather_contig(buf, req_ids, context_lens, max_context):
+    """Test-only: the logical rows of request rows req_ids (offset reqId x S)."""
+    _need(buf, torch.bfloat16, "buf", 4)
+    _need(req_ids, torch.int32, "req_ids", 1)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    max_reqs, hkv, S, d = buf.shape
+    B = context_lens.shape[0]
+    out = torch.empty((B, hkv, int(max_context), d), dtype=torch.bfloat16, device=buf.device)
+    _check(lib().pkv_debug_gather_contig(_ptr(buf), _ptr(req_ids), max_reqs, _ptr(context_lens),
+                                         B, int(max_context), S, hkv, _ptr(out), _stream(buf)))
     return out
 
 

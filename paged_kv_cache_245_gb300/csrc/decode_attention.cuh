@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const uint16_t* vbase = p.v;
   if (kContig) {
     const int64_t req = ctx > 0 ? p.req_ids[seq] : 0;
-    const int64_t off = (req * p.Hkv + kvh) * p.bs * kHeadDim;
+    const int64_t off = cache_row(req, kvh, p.Hkv, p.bs, 0) * kHeadDim;
     kbase += off;
     vbase += off;
   } else {
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
       if (lane == 0) mbar_arrive_expect_tx(&bars[s], total);
       __syncwarp();
       if (bytes != 0) {
-        const int64_t row = (static_cast<int64_t>(entry) * p.Hkv + kvh) * p.bs + off;
+        const int64_t row = cache_row(entry, kvh, p.Hkv, p.bs, off);
         bulk_copy_g2s(kdst + lane * kRowBytes, p.k + row * kHeadDim, bytes, &bars[s], policy);
         bulk_copy_g2s(vdst + lane * kRowBytes, p.v + row * kHeadDim, bytes, &bars[s], policy);
       }

@@ -223,13 +223,13 @@ __global__ void __launch_bounds__(W * 32, 1)
       bool kv_ok = true;
       int64_t row;
       if (kContig) {
-        row = (static_cast<int64_t>(req_s[iseg.seq]) * p.Hkv + iseg.kvh) * p.bs + pos;
+        row = cache_row(req_s[iseg.seq], iseg.kvh, p.Hkv, p.bs, pos);
       } else {
         if (p.checked && (entry < 0 || entry >= p.num_blocks)) {
           record_error(p.err, kErrBlockId);
           kv_ok = false;  // skip the copy: stale rows, undefined output, no fault
         }
-        row = (static_cast<int64_t>(entry) * p.Hkv + iseg.kvh) * p.bs + pos % p.bs;
+        row = cache_row(entry, iseg.kvh, p.Hkv, p.bs, pos % p.bs);
       }
       // (test hook: on its first tile, CTA 0's warp 0 announces 16 more bytes
       // than its copies bring, so that wait runs into its time limit)

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   const int64_t blk = slot / p.bs;
   const int64_t off = slot % p.bs;
   const uint16_t* src = (is_v ? p.v : p.k) + (t * p.Hkv + h) * kHeadDim + lane16 * 8;
-  uint16_t* dst = (is_v ? p.v_cache : p.k_cache) + ((blk * p.Hkv + h) * p.bs + off) * kHeadDim +
+  uint16_t* dst = (is_v ? p.v_cache : p.k_cache) + cache_row(blk, h, p.Hkv, p.bs, off) * kHeadDim +
                   lane16 * 8;
   *reinterpret_cast<uint4*>(dst) = ld_global_nc_v4(src);
 }
@@ -40,6 +40,47 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream, bool pl
   const int64_t blocks = (rows + 15) / 16;
   return launch_pdl_if(!plain && pdl_enabled(), kv_append_kernel,
                        dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+}
+
+// Gather: one 16-lane group per (sequence, KV head, position) row, as the
+// append moves rows; positions past the context are zero-filled.
+__global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
+  grid_dependency_trigger();
+  grid_dependency_wait();
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int lane16 = threadIdx.x & 15;
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hkv * p.max_context;
+  if (row >= rows) return;
+  const int64_t pos = row % p.max_context;
+  const int64_t h = (row / p.max_context) % p.Hkv;
+  const int64_t i = row / (static_cast<int64_t>(p.max_context) * p.Hkv);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + row * kHeadDim) + lane16;
+  const int ctx = p.ctx_lens[i];
+  if (pos >= ctx) {
+    *dst = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  int64_t block, off;
+  if (p.block_tables != nullptr) {
+    block = p.block_tables[i * p.max_blocks + pos / p.bs];
+    off = pos % p.bs;
+  } else {
+    block = p.req_ids[i];
+    off = pos;
+  }
+  if (p.checked && (block < 0 || block >= p.num_blocks)) {
+    if (lane16 == 0) record_error(p.err, p.block_tables != nullptr ? kErrBlockId : kErrReqId);
+    *dst = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  *dst = ld_global_nc_v4(p.cache + cache_row(block, h, p.Hkv, p.bs, off) * kHeadDim + lane16 * 8);
+}
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.Hkv * p.max_context;
+  if (rows == 0) return cudaSuccess;
+  return launch_pdl(gather_kernel, dim3(static_cast<unsigned>((rows + 15) / 16)), dim3(256), 0,
+                    stream, p);
 }
 
 // Block copy: blockIdx.x strides over the block's 16-byte chunks, blockIdx.y

@@ -34,6 +34,25 @@ struct CopyParams {
   int* err;
 };
 
+// Test-only gather of the logical rows: out[i][h][pos] = the cache row the
+// attention kernels read for position pos of sequence i, KV head h (zeros at
+// pos >= context_lens[i]).  Paged: block_tables; contiguous (block_tables
+// null): req_ids with bs = S.
+struct GatherParams {
+  const uint16_t* cache;
+  const int32_t* block_tables;  // [num_seqs][max_blocks] (paged)
+  const int32_t* req_ids;       // [num_seqs] (contiguous)
+  const int32_t* ctx_lens;      // [num_seqs]
+  uint16_t* out;                // [num_seqs][Hkv][max_context][128]
+  int64_t bs;
+  int64_t num_blocks;           // paged pool size / max_reqs (bounds in checked mode)
+  int32_t max_blocks, num_seqs, Hkv, max_context;
+  int32_t checked;
+  int* err;
+};
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+
 // plain: launch in stream order even when PKV_PDL=1 (a decode step's append,
 // whose dependent attention kernel reads its inputs before waiting)
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream, bool plain = false);

@@ -313,6 +313,50 @@ pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const 
   return PKV_OK;
 }
 
+pkv_status gather_common(const void* cache, const int32_t* block_tables, int32_t max_blocks,
+                         int32_t num_blocks, const int32_t* req_ids, int32_t max_reqs,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
+                         int64_t bs_or_S, int32_t num_kv_heads, void* out, void* stream) {
+  const bool contig = block_tables == nullptr;
+  if (num_seqs < 0 || max_context < 0 || num_kv_heads <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "negative size or no KV heads");
+  if (num_seqs == 0 || max_context == 0) return PKV_OK;
+  if (!cache || !context_lens || !out || (contig && !req_ids))
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(cache, 16) || !aligned(out, 16)) return fail(PKV_ERR_INVALID_ARG, "misaligned rows");
+  if (bs_or_S <= 0) return fail(PKV_ERR_INVALID_ARG, "block_size / S must be >= 1");
+  if (contig) {
+    if (max_reqs <= 0 || max_context > bs_or_S)
+      return fail(PKV_ERR_INVALID_ARG, "max_reqs < 1 or max_context > S");
+  } else if (max_blocks <= 0 || num_blocks <= 0 ||
+             static_cast<int64_t>(max_blocks) * bs_or_S < max_context) {
+    return fail(PKV_ERR_INVALID_ARG, "block table shorter than max_context");
+  }
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_kv_heads * max_context;
+  if ((rows + 15) / 16 > 0x7fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "gather too large");
+  int* err = nullptr;
+  pkv_status st = device_info(nullptr, &err, nullptr);
+  if (st != PKV_OK) return st;
+  pkv::GatherParams p;
+  std::memset(&p, 0, sizeof p);
+  p.cache = static_cast<const uint16_t*>(cache);
+  p.block_tables = block_tables;
+  p.req_ids = req_ids;
+  p.ctx_lens = context_lens;
+  p.out = static_cast<uint16_t*>(out);
+  p.bs = bs_or_S;
+  p.num_blocks = contig ? max_reqs : num_blocks;
+  p.max_blocks = max_blocks;
+  p.num_seqs = num_seqs;
+  p.Hkv = num_kv_heads;
+  p.max_context = max_context;
+  p.checked = g_checked.load();
+  p.err = err;
+  const cudaError_t e = pkv::launch_gather(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -400,6 +444,23 @@ pkv_status pkv_contig_decode_attention(const void* q, const void* k_buf, const v
   return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
                        num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
                        stream);
+}
+
+pkv_status pkv_debug_gather_paged(const void* cache, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, int32_t num_blocks,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t max_context, int32_t block_size, int32_t num_kv_heads,
+                                  void* out, void* stream) {
+  return gather_common(cache, block_tables, max_blocks_per_seq, num_blocks, nullptr, 0,
+                       context_lens, num_seqs, max_context, block_size, num_kv_heads, out, stream);
+}
+
+pkv_status pkv_debug_gather_contig(const void* buf, const int32_t* req_ids, int32_t max_reqs,
+                                   const int32_t* context_lens, int32_t num_seqs,
+                                   int32_t max_context, int64_t S, int32_t num_kv_heads,
+                                   void* out, void* stream) {
+  return gather_common(buf, nullptr, 0, 0, req_ids, max_reqs, context_lens, num_seqs,
+                       max_context, S, num_kv_heads, out, stream);
 }
 
 pkv_status pkv_block_copy(const int64_t* src_dst_pairs, int64_t n, void* const* k_caches,

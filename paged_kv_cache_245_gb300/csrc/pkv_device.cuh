@@ -89,6 +89,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// ---- cache addressing, shared by every kernel that reads or writes rows
+// Row (of 128 elements) that holds in-block offset `off` of KV head h in block
+// `block` of a [num_blocks][Hkv][bs][128] cache ("Running Out of Cache": a
+// block table maps a position to (block, offset) as a page table maps a
+// virtual address to a frame).  The contiguous layout is the same with
+// block = reqId and bs = S ("Leveraging Low-Level CUDA APIs for vAttention's
+// Dynamic Memory" 5.2.3: the request's sub-tensor at offset reqId x S).
+__host__ __device__ __forceinline__ int64_t cache_row(int64_t block, int64_t h, int64_t Hkv,
+                                                      int64_t bs, int64_t off) {
+  return (block * Hkv + h) * bs + off;
+}
+
 // ---- 1-D bulk copy global -> shared (TMA engine) ----------------------------
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
