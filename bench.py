@@ -103,6 +103,29 @@ def algorithmic_bytes(batch):
     return kv + qo + tables + 4 * batch.B
 
 
+def unique_kv_bytes(batch):
+    """K and V bytes of the distinct cache rows the call reads: sequences
+    that share prompt blocks read those rows once each, so this is below the
+    algorithmic count exactly when blocks are shared."""
+    s = batch.shape
+    bs = batch.block_size
+    rows = []
+    for i in range(batch.B):
+        c = int(batch.ctx[i])
+        if c <= 0:
+            continue
+        pos = np.arange(c, dtype=np.int64)
+        rows.append(batch.block_tables[i, pos // bs].astype(np.int64) * bs + pos % bs)
+    n = len(np.unique(np.concatenate(rows))) if rows else 0
+    return n * s.num_kv_heads * s.head_dim * 2 * 2
+
+
+def attention_flops(batch):
+    """q.K and p.V: 4 flops per (position, query head, dimension)."""
+    s = batch.shape
+    return 4 * int(batch.ctx.astype(np.int64).sum()) * s.num_q_heads * s.head_dim
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock, power and throttle reasons."""
 
@@ -382,6 +405,8 @@ def run_gpu(args, world, rank, local):
                                "paged_decode_attention call (decode_attention_kernel + "
                                "decode_combine_kernel)",
                      "algorithmic_bytes_per_launch": alg,
+                     "unique_kv_bytes_per_launch": unique_kv_bytes(wl.batch),
+                     "flops_per_launch": attention_flops(wl.batch),
                      "avg_launch_us": round(attn_avg_ms * 1e3, 3),
                      "timed_over": "%d replays of the step's %d attention calls" % (attn_reps, nl),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
@@ -597,11 +622,20 @@ def cpu_baseline(wl, args, budget_s=15.0):
         _oracle_step(oracle, b, h, scale, cores)
         t_total += time.perf_counter() - t
         done += 1
+    # the same on one core, over a shorter sample
+    one, t_one = 0, 0.0
+    while t_one < budget_s / 3 and one < 16:
+        t = time.perf_counter()
+        _oracle_step(oracle, b, h, scale, 1)
+        t_one += time.perf_counter() - t
+        one += 1
     return {"value": round(b.B * done / t_total, 2), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": "%d repetitions of one layer (%s, all %d sequences) of "
                       "the same workload, fp64 C oracle, %d threads"
-                      % (done, _oracle_step_text(h), b.B, cores)}
+                      % (done, _oracle_step_text(h), b.B, cores),
+            "single_core": {"value": round(b.B * one / t_one, 2), "unit": UNIT, "cores": 1,
+                            "sample": "%d repetitions of the same layer, 1 thread" % one}}
 
 
 def run_reference(args, world, rank):

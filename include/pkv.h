@@ -56,7 +56,8 @@ typedef enum pkv_status {
     PKV_ERR_UNSUPPORTED = 2,   /* head_dim != 128, group ratio > 8, ...     */
     PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than needed  */
     PKV_ERR_CUDA = 4,          /* a CUDA runtime call failed                */
-    PKV_ERR_DEVICE_BOUNDS = 5  /* pkv_get_device_error found a device error */
+    PKV_ERR_DEVICE_BOUNDS = 5, /* pkv_get_device_error found a device error */
+    PKV_ERR_OUT_OF_BLOCKS = 6  /* block manager: not enough free blocks     */
 } pkv_status;
 
 /* Codes stored in the device error word (checked mode, and wait limits). */

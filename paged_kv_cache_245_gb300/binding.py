@@ -15,8 +15,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_OUT_OF_BLOCKS = 6
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
-                3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_BOUNDS"}
+                3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_BOUNDS",
+                6: "PKV_ERR_OUT_OF_BLOCKS"}
 DEVERR_NAMES = {0: "none", 1: "block_id", 2: "slot", 3: "req_id", 4: "context",
                 5: "copy_pair", 6: "timeout"}
 
@@ -369,3 +372,133 @@ def get_device_error():
     if st not in (0, 5):
         _check(st)
     return DEVERR_NAMES.get(code.value, code.value)
+
+
+# ------------------------------------------------------------ block manager
+
+def _bm_lib():
+    L = lib()
+    if getattr(L, "_bm_ready", False):
+        return L
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.pkv_bm_create.argtypes = [i32, i32, vp]
+    L.pkv_bm_create.restype = vp
+    L.pkv_bm_destroy.argtypes = [vp]
+    L.pkv_bm_destroy.restype = None
+    L.pkv_bm_add_sequence.argtypes = [vp, i64]
+    L.pkv_bm_add_sequence.restype = i32
+    L.pkv_bm_fork.argtypes = [vp, i32]
+    L.pkv_bm_fork.restype = i32
+    L.pkv_bm_append.argtypes = [vp, vp, i32, vp, vp, vp]
+    L.pkv_bm_append.restype = ctypes.c_int
+    L.pkv_bm_free_sequence.argtypes = [vp, i32]
+    L.pkv_bm_free_sequence.restype = ctypes.c_int
+    L.pkv_bm_block_table.argtypes = [vp, i32, vp, i32]
+    L.pkv_bm_block_table.restype = i32
+    L.pkv_bm_export.argtypes = [vp, vp, i32, vp, i32, i32, vp]
+    L.pkv_bm_export.restype = ctypes.c_int
+    L.pkv_bm_length.argtypes = [vp, i32]
+    L.pkv_bm_length.restype = i64
+    L.pkv_bm_num_free_blocks.argtypes = [vp]
+    L.pkv_bm_num_free_blocks.restype = i32
+    L.pkv_bm_ref_count.argtypes = [vp, i32]
+    L.pkv_bm_ref_count.restype = i32
+    L._bm_ready = True
+    return L
+
+
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+class BlockManager:
+    """Host block pool of a paged KV cache (include/pkv_block_manager.h):
+    sequences, forks that share blocks, and the decode step's slot mapping
+    and copy-on-write pairs.  Arrays are numpy on the host."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        import numpy as np
+        self._np = np
+        L = _bm_lib()
+        self.block_size = int(block_size)
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(free_order, dtype=np.int32)
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must list every block once")
+        h = L.pkv_bm_create(int(num_blocks), int(block_size),
+                            _np_ptr(order) if order is not None else None)
+        if not h:
+            raise PkvError(PKV_ERR_INVALID_ARG, L.pkv_last_error().decode())
+        self._h = ctypes.c_void_p(h)
+
+    def close(self):
+        if self._h:
+            _bm_lib().pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _id(self, r):
+        if r < 0:
+            msg = _bm_lib().pkv_last_error().decode()
+            raise PkvError(PKV_ERR_OUT_OF_BLOCKS if "free blocks" in msg else PKV_ERR_INVALID_ARG,
+                           msg)
+        return int(r)
+
+    def add_sequence(self, num_tokens):
+        return self._id(_bm_lib().pkv_bm_add_sequence(self._h, int(num_tokens)))
+
+    def fork(self, parent):
+        return self._id(_bm_lib().pkv_bm_fork(self._h, int(parent)))
+
+    def append(self, seq_ids):
+        """One token for each listed sequence: (slot_mapping [n] int64,
+        cow_pairs [k, 2] int64)."""
+        np = self._np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        n = ids.shape[0]
+        slots = np.empty(n, dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int64)
+        k = ctypes.c_int32(0)
+        _check(_bm_lib().pkv_bm_append(self._h, _np_ptr(ids), n, _np_ptr(slots), _np_ptr(pairs),
+                                       ctypes.byref(k)))
+        return slots, pairs[:k.value].copy()
+
+    def free_sequence(self, seq):
+        _check(_bm_lib().pkv_bm_free_sequence(self._h, int(seq)))
+
+    def block_table(self, seq):
+        np = self._np
+        n = self.length(seq)
+        out = np.empty(max((n + self.block_size - 1) // self.block_size, 1), dtype=np.int32)
+        k = _bm_lib().pkv_bm_block_table(self._h, int(seq), _np_ptr(out), out.shape[0])
+        if k < 0:
+            raise PkvError(PKV_ERR_INVALID_ARG, "bad sequence id")
+        return out[:k].copy()
+
+    def export(self, seq_ids, max_blocks, filler=0):
+        """(block_tables [n, max_blocks] int32, context_lens [n] int32)."""
+        np = self._np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        tables = np.empty((ids.shape[0], max_blocks), dtype=np.int32)
+        ctx = np.empty(ids.shape[0], dtype=np.int32)
+        _check(_bm_lib().pkv_bm_export(self._h, _np_ptr(ids), ids.shape[0], _np_ptr(tables),
+                                       int(max_blocks), int(filler), _np_ptr(ctx)))
+        return tables, ctx
+
+    def length(self, seq):
+        n = _bm_lib().pkv_bm_length(self._h, int(seq))
+        if n < 0:
+            raise PkvError(PKV_ERR_INVALID_ARG, "bad sequence id")
+        return int(n)
+
+    def num_free_blocks(self):
+        return int(_bm_lib().pkv_bm_num_free_blocks(self._h))
+
+    def ref_count(self, block):
+        return int(_bm_lib().pkv_bm_ref_count(self._h, int(block)))

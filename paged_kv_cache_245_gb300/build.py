@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["pkv_api.cu", "kv_ops.cu", "decode_paged.cu", "decode_contig.cu", "decode_tc.cu",
-           "pkv_noalloc.cu"]
+           "pkv_noalloc.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
@@ -31,8 +31,9 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)
-             if f.endswith((".cu", ".cuh"))]
-    files.append(os.path.join(ROOT, "include", "pkv.h"))
+             if f.endswith((".cu", ".cuh", ".cpp", ".h"))]
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     return files
 
 
@@ -50,7 +51,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")

@@ -539,6 +539,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
     case PKV_ERR_CUDA: return "CUDA runtime error";
     case PKV_ERR_DEVICE_BOUNDS: return "device-side bounds error recorded";
+    case PKV_ERR_OUT_OF_BLOCKS: return "not enough free blocks";
   }
   return "unknown status";
 }

@@ -21,14 +21,18 @@ def L():
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    inc = os.path.join(ROOT, "include")
+    text = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                   if f.endswith(".h"))
     return set(re.findall(r"PKV_API[^;(]*?\b(pkv_\w+)\s*\(", text))
 
 
 def test_header_declares_the_calls(L):
     names = _declared()
     for call in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_contig_decode_attention",
-                 "pkv_block_copy", "pkv_decode_workspace_size", "pkv_get_device_error"):
+                 "pkv_block_copy", "pkv_decode_workspace_size", "pkv_get_device_error",
+                 "pkv_paged_decode_step", "pkv_debug_gather_paged", "pkv_bm_create",
+                 "pkv_bm_append"):
         assert call in names
 
 

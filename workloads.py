@@ -278,6 +278,7 @@ class SharingScenario:
     n: int
     tables_shared: np.ndarray        # [B, max_blocks] before any copy
     cow_pairs: np.ndarray            # [n_copies, 2] int64 (src, dst)
+    free_order: np.ndarray           # [num_blocks] int32: the order blocks are handed out
     tables: np.ndarray               # [B, max_blocks] after the copies
     steps: List[PagedBatch] = field(default_factory=list)  # one per decode step
 
@@ -357,7 +358,7 @@ def sharing_scenario(num_prompts: int = 32, n: int = 4, decode_steps: int = 64,
     pairs = np.array(cow_pairs, dtype=np.int64).reshape(-1, 2)
     return SharingScenario(shape=shape, block_size=bs, num_blocks=total,
                            prompt_lens=prompt_lens, n=n,
-                           tables_shared=tables_shared, cow_pairs=pairs,
+                           tables_shared=tables_shared, cow_pairs=pairs, free_order=perm,
                            tables=steps[0].block_tables if steps else tables,
                            steps=steps)
 
