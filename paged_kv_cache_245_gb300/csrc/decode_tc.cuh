@@ -55,7 +55,8 @@ struct TcSmem {
   static constexpr int kCtxOff = kMLOff + W * kTcHeads * 2 * 4;
   static constexpr int kReqOff = kCtxOff + kTcMaxSeqs * 4;
   static constexpr int kPrefixOff = kReqOff + kTcMaxSeqs * 4;
-  static constexpr int kEnd = kPrefixOff + (kTcMaxSeqs + 1) * 4;
+  static constexpr int kRangeOff = (kPrefixOff + (kTcMaxSeqs + 1) * 4 + 7) / 8 * 8;
+  static constexpr int kEnd = kRangeOff + 2 * 8;
   static constexpr int kTotal = kEnd + 1024;  // slack to align the base to 1 KiB
   static_assert(kTotal <= 232448, "shared memory per CTA exceeds 227 KiB");
 };
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   int32_t* ctx_s = reinterpret_cast<int32_t*>(smem + L::kCtxOff);
   int32_t* req_s = reinterpret_cast<int32_t*>(smem + L::kReqOff);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefixOff);
+  int64_t* range = reinterpret_cast<int64_t*>(smem + L::kRangeOff);  // this CTA's [lo, hi)
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -150,6 +152,12 @@ __global__ void __launch_bounds__(W * 32, 1)
       run += (ctx_s[i] + 15) >> 4;
     }
     if (lane == 31) prefix[B] = incl;
+    __syncwarp();
+    // this CTA's run of tiles, computed once: lane 0 its start, lane 1 its end
+    if (lane < 2) {
+      const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
+      range[lane] = tc_unit_to_tile(tc_range_lo(c + lane, V, P), prefix, B, p.Hkv, p.seg_cost);
+    }
   }
   __syncthreads();
   // outputs of empty contexts are zeros (sequences c, c + P, ... of this CTA)
@@ -158,9 +166,8 @@ __global__ void __launch_bounds__(W * 32, 1)
     uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(i) * p.Hq * kHeadDim);
     for (int k = tid; k < p.Hq * kHeadDim / 8; k += W * 32) o[k] = make_uint4(0u, 0u, 0u, 0u);
   }
-  const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
-  const int64_t lo = tc_unit_to_tile(tc_range_lo(c, V, P), prefix, B, p.Hkv, p.seg_cost);
-  const int64_t hi = tc_unit_to_tile(tc_range_lo(c + 1, V, P), prefix, B, p.Hkv, p.seg_cost);
+  const int64_t lo = range[0];
+  const int64_t hi = range[1];
   if (lo >= hi) {  // uniform across the CTA
     if (p.early_inputs) grid_dependency_wait();  // never finish before the append
     return;

@@ -33,13 +33,24 @@ struct TcParams {
 
 enum class TcStatus { kOk, kEncodeFailed, kCudaError };
 
+// The helpers below divide in 32 bits whenever every operand fits (the
+// same quotients as in 64 bits; a 64-bit division costs several times more).
+__host__ __device__ inline bool tc_small(int64_t V, int64_t P) {
+  return V < (int64_t{1} << 22) && P < (int64_t{1} << 10);  // (V + 1) * P < 2^32
+}
+
 // Even partition of [0, V) over P CTAs: CTA c owns [floor(c*V/P), floor((c+1)*V/P)).
 __host__ __device__ inline int64_t tc_range_lo(int64_t c, int64_t V, int64_t P) {
+  if (tc_small(V, P))
+    return static_cast<uint32_t>(c * V) / static_cast<uint32_t>(P);
   return c * V / P;
 }
 
 // The CTA whose range holds position u (the largest c with range_lo(c) <= u).
 __host__ __device__ inline int64_t tc_owner(int64_t u, int64_t V, int64_t P) {
+  if (tc_small(V, P))
+    return static_cast<int64_t>(static_cast<uint32_t>((u + 1) * P + V - 1) /
+                                static_cast<uint32_t>(V)) - 1;
   return ((u + 1) * P + V - 1) / V - 1;
 }
 
@@ -68,9 +79,16 @@ __host__ __device__ inline int64_t tc_unit_to_tile(int64_t u, const int32_t* pre
   }
   const int64_t n = prefix[a + 1] - prefix[a];
   if (n + alpha <= 0) return static_cast<int64_t>(Hkv) * prefix[a];  // (not reached: see above)
-  const int64_t r = u - tc_vseq(prefix, a, Hkv, alpha);
-  const int64_t h = r / (n + alpha);
-  const int64_t o = r % (n + alpha) - alpha;
+  const int64_t r = u - tc_vseq(prefix, a, Hkv, alpha);  // < Hkv * (n + alpha)
+  int64_t h, o;
+  if (r < (int64_t{1} << 31)) {
+    const uint32_t q = static_cast<uint32_t>(r) / static_cast<uint32_t>(n + alpha);
+    h = q;
+    o = r - static_cast<int64_t>(q) * (n + alpha) - alpha;
+  } else {
+    h = r / (n + alpha);
+    o = r % (n + alpha) - alpha;
+  }
   return static_cast<int64_t>(Hkv) * prefix[a] + h * n + (o > 0 ? o : 0);
 }
 
@@ -94,7 +112,9 @@ __host__ __device__ inline TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_
   const int n = prefix[a + 1] - prefix[a];  // > 0 because x < Hkv*prefix[a+1]
   TcSeg s;
   s.seq = a;
-  s.kvh = static_cast<int>((x - base) / n);
+  const int64_t dx = x - base;  // < Hkv * n
+  s.kvh = dx < (int64_t{1} << 31) ? static_cast<int>(static_cast<uint32_t>(dx) / static_cast<uint32_t>(n))
+                                  : static_cast<int>(dx / n);
   s.pstart = base + static_cast<int64_t>(s.kvh) * n;
   s.pend = s.pstart + n;
   s.x0 = x;
