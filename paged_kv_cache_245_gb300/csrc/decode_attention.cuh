@@ -175,7 +175,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
   auto load_entry = [&](int k) -> int32_t {
     if (kContig) return 0;
     const int pos = (first + k * kDecodeWarps) * kTileTokens + lane;
-    return (lane < kTileTokens && pos < ctx) ? __ldg(bt_row + pos / p.bs) : 0;
+    // positions are below 2^31: divide in 32 bits
+    return (lane < kTileTokens && pos < ctx)
+               ? __ldg(bt_row + static_cast<uint32_t>(pos) / static_cast<uint32_t>(p.bs))
+               : 0;
   };
 
   // Fill stage k % kStages with local tile k.  Whole warp.
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
       // Lane r < nvalid holds position row0 + r; a run of rows that share a
       // physical block starts where the in-block offset is 0 (or at r = 0).
       const int64_t pos = row0 + lane;
-      const int64_t off = pos % p.bs;
+      const int64_t off = static_cast<uint32_t>(pos) % static_cast<uint32_t>(p.bs);
       const bool start = lane < nvalid && (lane == 0 || off == 0);
       int len = 0;
       if (start) {
