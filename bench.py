@@ -482,6 +482,7 @@ def measure_legs(wl, dev, args):
     reps = max(10, args.steps // 20)
     t_contig = _time_graph(contig, reps, dev, calls=nl)
     t_paged = _time_graph(paged, reps, dev, calls=nl)
+    vmm = measure_vmm(wl, dev, bufs[0], S, req, reps)
     del bufs
     # the split (CUDA-core) kernel on the same calls, for comparison
     pkv.set_decode_variant(pkv.VARIANT_SPLIT)
@@ -522,7 +523,52 @@ def measure_legs(wl, dev, args):
         "block_copy_us": round(t_copy * 1e3, 3),
         "block_copy_gbs": round(copy_bytes / (t_copy / 1e3) / 1e9, 1),
         "block_copy_shape": "96 pairs x 60 layers x (K,V) of 32 KiB blocks (read + write)",
+        "on_demand_contig": vmm,
     }
+
+
+def measure_vmm(wl, dev, buf, S, req, reps):
+    """The contiguous layout on memory mapped on demand: back every request's
+    rows (timed on the host: the mapping rate), copy layer 0's rows in, and
+    time the same attention call there and on regular device memory."""
+    pkv = wl.pkv
+    b = wl.batch
+    vm = pkv.VmmBuffer(b.B, wl.shape.num_kv_heads, S)
+    try:
+        t0 = time.perf_counter()
+        for r in range(b.B):
+            vm.ensure(r, int(b.ctx[r]))
+        t_map = time.perf_counter() - t0
+        st = vm.stats()
+        for r in range(b.B):   # kernels below touch only backed rows
+            assert vm.backed_tokens(r) >= int(b.ctx[r])
+        for r in range(b.B):
+            c = int(b.ctx[r])
+            vm.k[r, :, :c].copy_(buf[0][r, :, :c])
+            vm.v[r, :, :c].copy_(buf[1][r, :, :c])
+        li = wl.layers[0]
+        out = torch.empty_like(li.q)
+
+        def on_vmm():
+            pkv.contig_decode_attention(li.q, vm.k, vm.v, req, wl.ctx, b.max_context, wl.scale,
+                                        out=out, workspace=wl.workspace)
+
+        def on_regular():
+            pkv.contig_decode_attention(li.q, buf[0], buf[1], req, wl.ctx, b.max_context,
+                                        wl.scale, out=out, workspace=wl.workspace)
+
+        t_vmm = _time_graph(on_vmm, reps, dev, calls=4)
+        t_reg = _time_graph(on_regular, reps, dev, calls=4)
+        mapped = 2 * st["mapped_pages"] * st["page_bytes"]
+        return {"page_bytes": st["page_bytes"], "mapped_bytes": mapped,
+                "map_ms": round(t_map * 1e3, 3),
+                "map_gbs": round(mapped / t_map / 1e9, 2),
+                "attention_us": round(t_vmm * 1e3, 3),
+                "regular_memory_attention_us": round(t_reg * 1e3, 3),
+                "how": "one layer's rows; the same call repeated 4x per graph on either memory"}
+    finally:
+        torch.cuda.synchronize(dev)
+        vm.close()
 
 
 def measure_e2e(wl, dev, args, world):

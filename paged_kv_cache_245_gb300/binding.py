@@ -502,3 +502,94 @@ class BlockManager:
 
     def ref_count(self, block):
         return int(_bm_lib().pkv_bm_ref_count(self._h, int(block)))
+
+
+# ------------------------------------------------------------ on-demand contiguous buffers
+
+def _vmm_lib():
+    L = lib()
+    if getattr(L, "_vmm_ready", False):
+        return L
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.pkv_vmm_create.argtypes = [i32, i32, i64, ctypes.POINTER(vp)]
+    L.pkv_vmm_create.restype = ctypes.c_int
+    L.pkv_vmm_destroy.argtypes = [vp]
+    L.pkv_vmm_destroy.restype = None
+    L.pkv_vmm_k.argtypes = [vp]
+    L.pkv_vmm_k.restype = vp
+    L.pkv_vmm_v.argtypes = [vp]
+    L.pkv_vmm_v.restype = vp
+    L.pkv_vmm_ensure.argtypes = [vp, i32, i64]
+    L.pkv_vmm_ensure.restype = ctypes.c_int
+    L.pkv_vmm_release.argtypes = [vp, i32]
+    L.pkv_vmm_release.restype = ctypes.c_int
+    L.pkv_vmm_backed_tokens.argtypes = [vp, i32]
+    L.pkv_vmm_backed_tokens.restype = i64
+    L.pkv_vmm_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(i64),
+                                ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                ctypes.POINTER(ctypes.c_double)]
+    L.pkv_vmm_stats.restype = ctypes.c_int
+    L._vmm_ready = True
+    return L
+
+
+class _DeviceArray:
+    """A view of device memory the library owns, for torch.as_tensor."""
+
+    def __init__(self, ptr, shape, owner):
+        self._owner = owner
+        self.__cuda_array_interface__ = {"version": 3, "shape": tuple(shape), "typestr": "<i2",
+                                         "data": (int(ptr), False), "strides": None}
+
+
+class VmmBuffer:
+    """K and V tensors [max_reqs, Hkv, S, 128] bf16 whose physical memory is
+    mapped on demand (include/pkv_vmm.h).  .k and .v are torch views of the
+    whole virtual range: touch only rows that ensure() has backed."""
+
+    def __init__(self, max_reqs, num_kv_heads, S):
+        L = _vmm_lib()
+        h = ctypes.c_void_p(0)
+        _check(L.pkv_vmm_create(int(max_reqs), int(num_kv_heads), int(S), ctypes.byref(h)))
+        self._h = h
+        shape = (max_reqs, num_kv_heads, S, 128)
+        self.shape = shape
+        # torch wraps the pointers without touching the memory (no copy); the
+        # explicit device index spares it a pointer query, which a reserved but
+        # not yet mapped range cannot answer
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.k = torch.as_tensor(_DeviceArray(L.pkv_vmm_k(h), shape, self),
+                                 device=dev).view(torch.bfloat16)
+        self.v = torch.as_tensor(_DeviceArray(L.pkv_vmm_v(h), shape, self),
+                                 device=dev).view(torch.bfloat16)
+        assert self.k.data_ptr() == L.pkv_vmm_k(h) and self.v.data_ptr() == L.pkv_vmm_v(h)
+
+    def ensure(self, req, tokens):
+        _check(_vmm_lib().pkv_vmm_ensure(self._h, int(req), int(tokens)))
+
+    def release(self, req):
+        _check(_vmm_lib().pkv_vmm_release(self._h, int(req)))
+
+    def backed_tokens(self, req):
+        return int(_vmm_lib().pkv_vmm_backed_tokens(self._h, int(req)))
+
+    def stats(self):
+        pb = ctypes.c_size_t(0)
+        mp, cp, mc = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        secs = ctypes.c_double(0.0)
+        _check(_vmm_lib().pkv_vmm_stats(self._h, ctypes.byref(pb), ctypes.byref(mp),
+                                        ctypes.byref(cp), ctypes.byref(mc), ctypes.byref(secs)))
+        return {"page_bytes": pb.value, "mapped_pages": mp.value, "created_pages": cp.value,
+                "map_calls": mc.value, "map_seconds": secs.value}
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            self.k = self.v = None
+            _vmm_lib().pkv_vmm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
