@@ -533,7 +533,7 @@ def measure_vmm(wl, dev, buf, S, req, reps):
     time the same attention call there and on regular device memory."""
     pkv = wl.pkv
     b = wl.batch
-    vm = pkv.VmmBuffer(b.B, wl.shape.num_kv_heads, S)
+    vm = pkv.VmmBuffer(b.B, wl.shape.num_kv_heads, (S + 15) // 16 * 16)
     try:
         t0 = time.perf_counter()
         for r in range(b.B):
