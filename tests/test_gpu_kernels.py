@@ -405,3 +405,24 @@ def test_cuda_graph_replay_matches_direct_calls():
     assert torch.equal(out, direct)
     L.oracle_append()
     assert_attention_close(out, L.oracle_attend(), "graph replay")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_long_contexts(variant):
+    """Contexts of 65K-131K positions next to tiny ones: a pair's tiles span
+    many CTA ranges (many split records per pair)."""
+    pkv.set_decode_variant(variant)
+    ctx = [1, 131072, 65536 + 7, 5]
+    L = DeviceLayer(_batch(32, 8, ctx, 16, seed=21), 0, DEV, fast_cache=True)
+    L.gpu_append()
+    L.oracle_append()
+    assert_attention_close(L.gpu_attend(), L.oracle_attend(), "long contexts")
+
+
+@pytest.mark.parametrize("variant", [pkv.VARIANT_AUTO, pkv.VARIANT_TC_12X2, pkv.VARIANT_TC_8X3])
+def test_one_pair_across_every_cta(variant):
+    """One sequence, one KV head, 200K positions: the only pair is cut by
+    every CTA boundary, so its combine merges far more than 32 records."""
+    pkv.set_decode_variant(variant)
+    L = DeviceLayer(_batch(8, 1, [200000], 16, seed=22), 0, DEV, fast_cache=True)
+    assert_attention_close(L.gpu_attend(), L.oracle_attend(), "one long pair")
