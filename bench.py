@@ -244,6 +244,15 @@ class DeviceWorkload:
             li = W.layer_inputs(b, l, device=dev, fast_cache=True)
             self.layers.append(li)
         self.cow = None if pairs is None else torch.as_tensor(pairs, device=dev)
+        # sequences forked from one prompt: attend their shared blocks once
+        # per group (the sharing workload: groups of `n` consecutive branches)
+        self.groups = None
+        if ctx == "sharing":
+            n = W.sharing_scenario(decode_steps=1).n
+            starts = np.arange(0, b.B + 1, n, dtype=np.int32)
+            shared = W.shared_prefix_blocks(b.block_tables, b.ctx, bs, starts)
+            self.groups = (torch.as_tensor(starts, device=dev), torch.as_tensor(shared, device=dev),
+                           n)
         self.k_caches = [li.k_cache for li in self.layers]
         self.v_caches = [li.v_cache for li in self.layers]
         self.tables = torch.as_tensor(b.block_tables, device=dev)
@@ -253,6 +262,10 @@ class DeviceWorkload:
         self.out = [torch.empty_like(li.q) for li in self.layers]
         nbytes = pkv.decode_workspace_size(b.B, shape.num_q_heads, shape.num_kv_heads,
                                            b.max_context)
+        if self.groups is not None:
+            nbytes = max(nbytes, pkv.lib().pkv_shared_decode_workspace_size(
+                b.B, len(self.groups[1]), self.groups[2], b.block_tables.shape[1],
+                pkv.binding.heads(shape.num_q_heads, shape.num_kv_heads, shape.head_dim)))
         self.workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
         self.nsplit = pkv.decode_num_splits(b.B, shape.num_q_heads, shape.num_kv_heads,
                                             b.max_context)
@@ -265,6 +278,9 @@ class DeviceWorkload:
         # kv_append, the attention kernel and its combine kernel per layer,
         # plus one block copy launch (all layers) when the step copies on write
         cow = 0 if self.cow is None else 1
+        if self.groups is not None:
+            # append; prep, prefix main + combine, own-part main + combine, merge
+            return self.shape.num_layers * 7 + cow
         if self.uses_tc:
             return self.shape.num_layers * 3 + cow
         return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0)) + cow
@@ -274,9 +290,28 @@ class DeviceWorkload:
         if pairs is not None:
             self.pkv.block_copy(pairs, self.k_caches, self.v_caches)
 
-    def layer(self, l):
-        """One layer's decode step: append + attention in one C-ABI call."""
+    def attend(self, l):
         li = self.layers[l]
+        if self.groups is not None:
+            gs, sb, n = self.groups
+            self.pkv.paged_decode_attention_shared(li.q, li.k_cache, li.v_cache, self.tables,
+                                                   self.ctx, self.batch.max_context, self.scale,
+                                                   gs, sb, n, out=self.out[l],
+                                                   workspace=self.workspace)
+        else:
+            self.pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, self.tables, self.ctx,
+                                            self.batch.max_context, self.scale, out=self.out[l],
+                                            workspace=self.workspace)
+
+    def layer(self, l):
+        """One layer's decode step: append + attention in one C-ABI call (the
+        sharing workload: append, then attention with its shared blocks read
+        once per group)."""
+        li = self.layers[l]
+        if self.groups is not None:
+            self.pkv.kv_append(self.slots, li.k_new, li.v_new, li.k_cache, li.v_cache)
+            self.attend(l)
+            return
         self.pkv.paged_decode_step(self.slots, li.k_new, li.v_new, li.q, li.k_cache, li.v_cache,
                                    self.tables, self.ctx, self.batch.max_context, self.scale,
                                    out=self.out[l], workspace=self.workspace)
@@ -288,10 +323,7 @@ class DeviceWorkload:
 
     def attention_only(self):
         for l in range(self.shape.num_layers):
-            li = self.layers[l]
-            self.pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, self.tables, self.ctx,
-                                            self.batch.max_context, self.scale, out=self.out[l],
-                                            workspace=self.workspace)
+            self.attend(l)
 
 
 def _barrier(world):
@@ -393,14 +425,18 @@ def run_gpu(args, world, rank, local):
                          "%.0f MB per layer" % (nl * alg / 1e9, alg / 1e6),
                    "step": ("block_copy of %d copy-on-write pairs (all layers), then "
                             % len(wl.cow) if wl.cow is not None else "")
-                           + "per layer: paged_decode_step = kv_append + paged_decode_attention "
-                             "(main + combine) in one C-ABI call"},
+                           + ("per layer: kv_append + paged_decode_attention_shared (shared "
+                              "prompt blocks read once per 2 branches)" if wl.groups is not None
+                              else "per layer: paged_decode_step = kv_append + "
+                              "paged_decode_attention (main + combine) in one C-ABI call")},
         "hbm_tbs": round(achieved_gbs / 1e3, 4),
         "hbm_pct_of_8tbs": round(100 * achieved_gbs / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                      "traffic": _profiled_traffic(args.workload),
-                     "kernel": "paged_decode_attention call (decode_tc_kernel + "
+                     "kernel": "paged_decode_attention_shared call (prep, decode_tc_kernel "
+                               "x2 with combines, merge)" if wl.groups is not None else
+                               "paged_decode_attention call (decode_tc_kernel + "
                                "decode_tc_combine_kernel)" if wl.uses_tc else
                                "paged_decode_attention call (decode_attention_kernel + "
                                "decode_combine_kernel)",
@@ -609,8 +645,16 @@ def measure_e2e(wl, dev, args, world):
         for l in range(nl):
             q, kn, vn = views[3 * l:3 * l + 3]
             li = wl.layers[l]
-            pkv.paged_decode_step(slots, kn, vn, q, li.k_cache, li.v_cache, tables, ctx,
-                                  b.max_context, wl.scale, out=out_all[l], workspace=wl.workspace)
+            if wl.groups is not None:
+                gs, sb, n = wl.groups
+                pkv.kv_append(slots, kn, vn, li.k_cache, li.v_cache)
+                pkv.paged_decode_attention_shared(q, li.k_cache, li.v_cache, tables, ctx,
+                                                  b.max_context, wl.scale, gs, sb, n,
+                                                  out=out_all[l], workspace=wl.workspace)
+            else:
+                pkv.paged_decode_step(slots, kn, vn, q, li.k_cache, li.v_cache, tables, ctx,
+                                      b.max_context, wl.scale, out=out_all[l],
+                                      workspace=wl.workspace)
         host_out.copy_(out_all, non_blocking=True)
 
     iters = max(20, args.steps // 10)

@@ -187,6 +187,39 @@ PKV_API pkv_status pkv_contig_decode_step(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Paged decode attention for batches whose sequences share prompt blocks
+ * ("Running Out of Cache", "Fragmentation is lost users", and the
+ * PagedAttention summary: sequences sampled from one prompt share its
+ * physical blocks until one of them writes into one).  The batch is split
+ * into num_groups groups of consecutive sequences: group g is sequences
+ * group_start[g] .. group_start[g+1]-1 (device int32 [num_groups + 1],
+ * group_start[0] = 0, group_start[num_groups] = num_seqs, at most
+ * max_group_size sequences per group), and its members' block tables begin
+ * with the same shared_blocks[g] entries (device int32 [num_groups]; every
+ * member's context covers them).  Singleton groups with shared_blocks 0 are
+ * plain sequences.  The shared positions are read once for every
+ * ceil(16 / G) members (their query heads stacked into one tensor-core tile)
+ * instead of once per member; each member's own later positions are read as
+ * usual, and the two softmax parts are merged.  Result: the same attention as
+ * pkv_paged_decode_attention within the attention tolerance (a different
+ * summation order).  Other arguments as there; block_size must be a multiple
+ * of 16.  workspace (256-byte aligned) must hold
+ * pkv_shared_decode_workspace_size(num_seqs, num_groups, max_group_size,
+ * max_blocks_per_seq, heads) bytes.  Checked mode also reports a member whose
+ * context does not cover its group's shared blocks (PKV_DEVERR_CONTEXT).
+ */
+PKV_API size_t pkv_shared_decode_workspace_size(int32_t num_seqs, int32_t num_groups,
+                                                int32_t max_group_size,
+                                                int32_t max_blocks_per_seq, pkv_heads heads);
+PKV_API pkv_status pkv_paged_decode_attention_shared(
+    const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_blocks,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
+    int32_t block_size, const int32_t *group_start, const int32_t *shared_blocks,
+    int32_t num_groups, int32_t max_group_size, float scale, pkv_heads heads,
+    void *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Copy-on-write block copy.  "Running Out of Cache" (section "Fragmentation
  * is lost users") and the PagedAttention summary: sequences share physical
  * blocks and copy a block only when one of them writes into it.

@@ -28,7 +28,8 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
             "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
             "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
-            "pkv_debug_gather_contig",
+            "pkv_debug_gather_contig", "pkv_paged_decode_attention_shared",
+            "pkv_shared_decode_workspace_size",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -70,6 +71,11 @@ def lib():
                                         ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_contig_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
                                          ctypes.c_float, Heads, vp, vp, sz, vp]
+    L.pkv_shared_decode_workspace_size.argtypes = [i32, i32, i32, i32, Heads]
+    L.pkv_shared_decode_workspace_size.restype = sz
+    L.pkv_paged_decode_attention_shared.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
+                                                    vp, vp, i32, i32, ctypes.c_float, Heads, vp,
+                                                    vp, sz, vp]
     L.pkv_debug_gather_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp]
     L.pkv_debug_gather_contig.argtypes = [vp, vp, i32, vp, i32, i32, i64, i32, vp, vp]
     L.pkv_set_checked.argtypes = [ctypes.c_int]
@@ -289,6 +295,41 @@ def contig_decode_step(slot_mapping, k_new, v_new, q, k_buf, v_buf, req_ids, con
         _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(k_buf), _ptr(v_buf),
         _ptr(req_ids), max_reqs, _ptr(context_lens), B, int(max_context), S, float(scale), h,
         _ptr(out), ws_ptr, ws_len, _stream(q)))
+    return out
+
+
+def paged_decode_attention_shared(q, k_cache, v_cache, block_tables, context_lens, max_context,
+                                  scale, group_start, shared_blocks, max_group_size, out=None,
+                                  workspace=None):
+    """Paged decode attention where groups of consecutive sequences share
+    their first shared_blocks[g] blocks (group_start [G+1], shared_blocks [G]:
+    int32 on the device; max_group_size a host bound): the shared positions
+    are read once for several sequences."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    _need(group_start, torch.int32, "group_start", 1)
+    _need(shared_blocks, torch.int32, "shared_blocks", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    G = shared_blocks.shape[0]
+    if group_start.shape[0] != G + 1:
+        raise ValueError("group_start must have num_groups + 1 entries")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    h = heads(hq, hkv, d)
+    nbytes = lib().pkv_shared_decode_workspace_size(B, G, int(max_group_size),
+                                                    block_tables.shape[1], h)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().pkv_paged_decode_attention_shared(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], nb,
+        _ptr(context_lens), B, int(max_context), bs, _ptr(group_start), _ptr(shared_blocks), G,
+        int(max_group_size), float(scale), h, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(q)))
     return out
 
 

@@ -1,0 +1,143 @@
+// cascade.cu -- decode attention for sequences that share prompt blocks
+// ("Running Out of Cache", "Fragmentation is lost users": sequences sampled
+// from one prompt share its blocks until one writes into them).  The shared
+// positions are attended once for several sequences at a time instead of
+// once per sequence: softmax over a concatenation splits into per-part
+// partial results (o, m, l) merged as
+//   M = max(m_a, m_b),  w_x = l_x 2^(m_x - M),  o = (w_a o_a + w_b o_b) / (w_a + w_b).
+//
+// Virtual batches built here (in the caller's workspace):
+//   prefix: entry v = g * SG + s holds the shared positions of group g with
+//           the query heads of the group's members s*m .. s*m+m-1 stacked
+//           (G_v = m * G heads per KV head, zero rows for absent members);
+//   suffix: entry i holds sequence i's own positions after the shared ones.
+// Both go through the tensor-core kernel in record mode; cascade_merge_kernel
+// merges the two records of every (sequence, head).
+#include "cascade.cuh"
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+namespace {
+
+// The group holding sequence i (group_start is ascending, group_start[0] = 0).
+__device__ __forceinline__ int group_of(const int32_t* group_start, int num_groups, int i) {
+  int a = 0, b = num_groups - 1;
+  while (a < b) {
+    const int mid = (a + b + 1) >> 1;
+    if (group_start[mid] <= i) a = mid; else b = mid - 1;
+  }
+  return a;
+}
+
+}  // namespace
+
+// Blocks [0, Vp): prefix entries; blocks [Vp, Vp + B): suffix entries.
+__global__ void __launch_bounds__(256) cascade_prep_kernel(const CascadeParams c) {
+  grid_dependency_wait();
+  grid_dependency_trigger();
+  const int tid = threadIdx.x;
+  const int Gv = c.m * c.G;
+  if (blockIdx.x < static_cast<unsigned>(c.Vp)) {
+    const int v = blockIdx.x;
+    const int g = v / c.SG;
+    const int s = v % c.SG;
+    const int first = c.group_start[g] + s * c.m;
+    const int end = c.group_start[g + 1];
+    const int count = end - first < c.m ? end - first : c.m;
+    const int sb_in = count > 0 ? c.shared_blocks[g] : 0;
+    const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);  // stay in the tables
+    if (tid == 0) c.ctx_p[v] = sb * c.bs;
+    for (int j = tid; j < sb; j += blockDim.x)
+      c.tables_p[static_cast<int64_t>(v) * c.max_blocks + j] =
+          c.block_tables[static_cast<int64_t>(first) * c.max_blocks + j];
+    // query rows: [Hkv][Gv][128], member k's head gi at row k * G + gi
+    const int rows = c.Hkv * Gv;
+    for (int idx = tid; idx < rows * 16; idx += blockDim.x) {
+      const int row = idx >> 4;
+      const int chunk = idx & 15;
+      const int kvh = row / Gv;
+      const int r = row % Gv;
+      const int k = r / c.G;
+      const int gi = r % c.G;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (k < count && sb > 0)
+        val = ld_global_nc_v4(c.q + (static_cast<int64_t>(first + k) * c.Hq + kvh * c.G + gi) *
+                                        kHeadDim + chunk * 8);
+      *reinterpret_cast<uint4*>(c.q_p + (static_cast<int64_t>(v) * rows + row) * kHeadDim +
+                                chunk * 8) = val;
+    }
+    if (c.checked && tid == 0 && count > 0) {
+      bool bad = sb != sb_in;
+      for (int i = first; i < first + count; ++i) bad |= c.ctx[i] < sb * c.bs;
+      if (bad) record_error(c.err, kErrContext);
+    }
+    return;
+  }
+  const int i = blockIdx.x - c.Vp;
+  if (i >= c.B) return;
+  const int g = group_of(c.group_start, c.num_groups, i);
+  const int sb_in = c.shared_blocks[g];
+  const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);
+  const int ctx = c.ctx[i];
+  const int rest = ctx - sb * c.bs;
+  if (tid == 0) c.ctx_s[i] = rest > 0 ? rest : 0;
+  const int n = rest > 0 ? (rest + c.bs - 1) / c.bs : 0;
+  for (int j = tid; j < n; j += blockDim.x)
+    c.tables_s[static_cast<int64_t>(i) * c.max_blocks + j] =
+        c.block_tables[static_cast<int64_t>(i) * c.max_blocks + sb + j];
+}
+
+// One warp per (sequence, query head): merge its prefix record (if the
+// sequence shares anything) with its suffix record into the bf16 output.
+__global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams c) {
+  grid_dependency_wait();
+  grid_dependency_trigger();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (idx >= static_cast<int64_t>(c.B) * c.Hq) return;
+  const int i = static_cast<int>(idx / c.Hq);
+  const int h = static_cast<int>(idx % c.Hq);
+  const int kvh = h / c.G;
+  const int gi = h % c.G;
+  const int g = group_of(c.group_start, c.num_groups, i);
+  const int kg = i - c.group_start[g];
+  // a member beyond the groups' size bound has no prefix entry (the caller
+  // broke the contract: its shared positions are missing, nothing is read)
+  const bool has_prefix = kg >= 0 && kg / c.m < c.SG;
+  const int v = g * c.SG + (has_prefix ? kg / c.m : 0);
+  const int k = has_prefix ? kg % c.m : 0;
+  const int Gv = c.m * c.G;
+  const float* rp = c.rec_p + (static_cast<int64_t>(v) * c.Hkv * Gv + kvh * Gv + k * c.G + gi) *
+                                  kRecStride;
+  const float* rs = c.rec_s + idx * kRecStride;
+  const float mp = has_prefix ? __ldcg(rp + 128) : -INFINITY;
+  const float lp = has_prefix ? __ldcg(rp + 129) : 0.f;
+  const float ms = __ldcg(rs + 128), ls = __ldcg(rs + 129);
+  const bool hp = lp > 0.f, hs = ls > 0.f;
+  const float M = fmaxf(hp ? mp : -INFINITY, hs ? ms : -INFINITY);
+  const float wp = hp ? lp * fast_exp2(mp - M) : 0.f;
+  const float ws = hs ? ls * fast_exp2(ms - M) : 0.f;
+  const float inv = wp + ws > 0.f ? 1.f / (wp + ws) : 0.f;
+  const float4 op = hp ? __ldcg(reinterpret_cast<const float4*>(rp) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 os = hs ? __ldcg(reinterpret_cast<const float4*>(rs) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float x = (wp * op.x + ws * os.x) * inv, y = (wp * op.y + ws * os.y) * inv;
+  const float z = (wp * op.z + ws * os.z) * inv, w = (wp * op.w + ws * os.w) * inv;
+  const uint32_t lo16 = f32_to_bf16_bits(x) | (uint32_t(f32_to_bf16_bits(y)) << 16);
+  const uint32_t hi16 = f32_to_bf16_bits(z) | (uint32_t(f32_to_bf16_bits(w)) << 16);
+  *reinterpret_cast<uint2*>(c.out + idx * kHeadDim + lane * 4) = make_uint2(lo16, hi16);
+}
+
+cudaError_t launch_cascade_prep(const CascadeParams& c, cudaStream_t stream) {
+  return launch_pdl(cascade_prep_kernel, dim3(static_cast<unsigned>(c.Vp + c.B)), dim3(256), 0,
+                    stream, c);
+}
+
+cudaError_t launch_cascade_merge(const CascadeParams& c, cudaStream_t stream) {
+  const int64_t warps = static_cast<int64_t>(c.B) * c.Hq;
+  return launch_pdl(cascade_merge_kernel, dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128),
+                    0, stream, c);
+}
+
+}  // namespace pkv

@@ -1,0 +1,41 @@
+// cascade.cuh -- parameters and launchers of the shared-prefix decode path
+// (cascade.cu): building the virtual prefix / suffix batches and merging
+// their (o, m, l) records.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "decode_tc_launch.h"
+
+namespace pkv {
+
+struct CascadeParams {
+  // the caller's batch
+  const uint16_t* q;             // [B][Hq][128]
+  const int32_t* ctx;            // [B]
+  const int32_t* block_tables;   // [B][max_blocks]
+  const int32_t* group_start;    // [num_groups + 1], 0 .. B ascending
+  const int32_t* shared_blocks;  // [num_groups]: leading table entries the group shares
+  uint16_t* out;                 // [B][Hq][128]
+  int32_t B, Hq, Hkv, G, max_blocks, num_groups;
+  int32_t bs;
+  int32_t m;   // sequences per prefix entry (their heads stacked: m * G <= 16)
+  int32_t SG;  // prefix entries per group: ceil(largest group / m)
+  int32_t Vp;  // num_groups * SG
+  int32_t checked;
+  int* err;
+  // workspace
+  uint16_t* q_p;      // [Vp][Hkv][m*G][128]
+  int32_t* tables_p;  // [Vp][max_blocks]
+  int32_t* ctx_p;     // [Vp]
+  int32_t* tables_s;  // [B][max_blocks]
+  int32_t* ctx_s;     // [B]
+  float* rec_p;       // [Vp][Hkv * m*G][kRecStride]
+  float* rec_s;       // [B][Hq][kRecStride]
+};
+
+cudaError_t launch_cascade_prep(const CascadeParams& c, cudaStream_t stream);
+cudaError_t launch_cascade_merge(const CascadeParams& c, cudaStream_t stream);
+
+}  // namespace pkv

@@ -42,16 +42,16 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
   return r == CUDA_SUCCESS;
 }
 
-template <bool kContig, int W, int S>
+template <bool kContig, int W, int S, int NT = 1>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,
                        int num_ctas, cudaStream_t stream) {
-  using L = TcSmem<W, S>;
+  using L = TcSmem<W, S, NT>;
   static unsigned long long done_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  auto kernel = decode_tc_kernel<kContig, W, S>;
+  auto kernel = decode_tc_kernel<kContig, W, S, NT>;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
     if (e != cudaSuccess) return e;
@@ -69,6 +69,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     p.num_seqs = (p0.num_seqs - s0) < chunk ? (p0.num_seqs - s0) : chunk;
     p.q += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
     p.out += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
+    if (p.rec_out != nullptr) p.rec_out += static_cast<int64_t>(s0) * p.Hq * kRecStride;
     p.ctx_lens += s0;
     if (kContig) p.req_ids += s0;
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
@@ -96,7 +97,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
 }  // namespace
 
 size_t tc_workspace_bytes(int num_ctas) {
-  return static_cast<size_t>(num_ctas) * 2 * kTcHeads * kRecStride * sizeof(float);
+  return static_cast<size_t>(num_ctas) * 2 * kTcRecHeads * kRecStride * sizeof(float);
 }
 
 TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, const void* v,
@@ -120,7 +121,9 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
   p.seg_cost = seg_cost;
   p.rec = static_cast<float*>(workspace);
   cudaError_t e;
-  if (contig) {
+  if (p.G > kTcHeads) {  // two n-tiles of query heads: paged, 8 warps x 3 stages
+    e = contig ? cudaErrorInvalidValue : launch_cfg<false, 8, 3, 2>(tk, tv, p, num_ctas, stream);
+  } else if (contig) {
     e = cfg == 1 ? launch_cfg<true, 12, 2>(tk, tv, p, num_ctas, stream)
                  : launch_cfg<true, 8, 3>(tk, tv, p, num_ctas, stream);
   } else {

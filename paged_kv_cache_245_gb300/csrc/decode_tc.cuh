@@ -40,19 +40,19 @@
 
 namespace pkv {
 
-constexpr int kTcHeads = 8;           // mma N: query heads of one KV head, padded
+constexpr int kTcHeads = 8;           // mma N of one n-tile: query heads of one KV head, padded
 constexpr int kTcMergeHeads = 4;      // heads merged per pass through shared memory
 constexpr int kTcStageBytes = 8192;   // K tile 4 KiB, V tile 4 KiB
 constexpr int kBoxBytes = 2048;       // 16 rows x 128 B: half a head_dim row
 
 
-template <int W, int S>
+template <int W, int S, int NT = 1>
 struct TcSmem {
   static constexpr int kStagesOff = 0;
   static constexpr int kBarsOff = W * S * kTcStageBytes;
   static constexpr int kMergeOff = kBarsOff + W * S * 8;
   static constexpr int kMLOff = kMergeOff + W * kTcMergeHeads * kRecStride * 4;
-  static constexpr int kCtxOff = kMLOff + W * kTcHeads * 2 * 4;
+  static constexpr int kCtxOff = kMLOff + W * kTcHeads * NT * 2 * 4;
   static constexpr int kReqOff = kCtxOff + kTcMaxSeqs * 4;
   static constexpr int kPrefixOff = kReqOff + kTcMaxSeqs * 4;
   static constexpr int kRangeOff = (kPrefixOff + (kTcMaxSeqs + 1) * 4 + 7) / 8 * 8;
@@ -83,11 +83,14 @@ __device__ __forceinline__ int tc_context(const TcParams& p, int i, bool contig,
   return ctx;
 }
 
-template <bool kContig, int W, int S>
+// NT n-tiles of 8 query heads per KV head (NT = 2: groups of up to 16 query
+// heads, e.g. the stacked heads of two sequences that share a prefix).
+template <bool kContig, int W, int S, int NT>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const TcParams p) {
-  using L = TcSmem<W, S>;
+  using L = TcSmem<W, S, NT>;
+  constexpr int H = kTcHeads * NT;  // padded query heads per KV head
   constexpr unsigned kFull = 0xffffffffu;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -163,8 +166,16 @@ __global__ void __launch_bounds__(W * 32, 1)
   // outputs of empty contexts are zeros (sequences c, c + P, ... of this CTA)
   for (int i = c; i < B; i += P) {
     if (ctx_s[i] != 0) continue;
-    uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(i) * p.Hq * kHeadDim);
-    for (int k = tid; k < p.Hq * kHeadDim / 8; k += W * 32) o[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (p.rec_out != nullptr) {  // empty records: o = 0, m = -inf, l = 0
+      float* r = p.rec_out + static_cast<int64_t>(i) * p.Hq * kRecStride;
+      for (int k = tid; k < p.Hq * kRecStride; k += W * 32) {
+        const int e = k % kRecStride;
+        r[k] = e == 128 ? -INFINITY : 0.f;
+      }
+    } else {
+      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(i) * p.Hq * kHeadDim);
+      for (int k = tid; k < p.Hq * kHeadDim / 8; k += W * 32) o[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   const int64_t lo = range[0];
   const int64_t hi = range[1];
@@ -178,15 +189,19 @@ __global__ void __launch_bounds__(W * 32, 1)
   const int g = lane >> 2;   // accumulator row group
   const int tq = lane & 3;   // accumulator column pair
 
-  // Q^T fragments of one segment straight from global memory:
-  // b0 = Q[g][16ks + 2tq, +1], b1 = Q[g][16ks + 2tq + 8, +9] (heads >= G are 0).
-  auto load_q = [&](uint32_t (&qf)[8][2], int seq, int kvh) {
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        p.q + (static_cast<int64_t>(seq) * p.Hq + kvh * G + (g < G ? g : 0)) * kHeadDim);
+  // Q^T fragments of one segment straight from global memory, n-tile t:
+  // b0 = Q[8t+g][16ks + 2tq, +1], b1 = Q[8t+g][16ks + 2tq + 8, +9] (heads >= G are 0).
+  auto load_q = [&](uint32_t (&qf)[NT][8][2], int seq, int kvh) {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qf[ks][0] = g < G ? __ldg(qrow + ks * 8 + tq) : 0u;
-      qf[ks][1] = g < G ? __ldg(qrow + ks * 8 + 4 + tq) : 0u;
+    for (int t = 0; t < NT; ++t) {
+      const int hq = 8 * t + g;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<int64_t>(seq) * p.Hq + kvh * G + (hq < G ? hq : 0)) * kHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qf[t][ks][0] = hq < G ? __ldg(qrow + ks * 8 + tq) : 0u;
+        qf[t][ks][1] = hq < G ? __ldg(qrow + ks * 8 + 4 + tq) : 0u;
+      }
     }
   };
 
@@ -208,7 +223,7 @@ __global__ void __launch_bounds__(W * 32, 1)
 
   // The next segment's Q fragments are fetched into qn when the stream first
   // reaches it (if qn is free), so the segment start does not wait on them.
-  uint32_t qn[8][2];
+  uint32_t qn[NT][8][2];
   int64_t qn_pair = -1;
 
   // block-table entry of the tile at the issue cursor (lane 0 only)
@@ -300,28 +315,33 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
   }
 
-  uint32_t qb[8][2];
-  float acc[8][4];
-  float m0, m1, l0, l1;
+  uint32_t qb[NT][8][2];
+  float acc[8][NT][4];
+  float m0[NT], m1[NT], l0[NT], l1[NT];
   int consumed = 0;
   bool dead = false;
 
   TcSeg seg = tc_find_seg(lo, hi, prefix, B, p.Hkv);
   while (true) {
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int t = 0; t < NT; ++t) {
+      m0[t] = m1[t] = -INFINITY;
+      l0[t] = l1[t] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i][t][0] = acc[i][t][1] = acc[i][t][2] = acc[i][t][3] = 0.f;
+    }
     const int ctx = ctx_s[seg.seq];
 
     for (int64_t x = seg.x0 + warp; x < seg.x1 && !dead; x += W) {
       if (x == seg.x0 + warp) {  // this warp's first tile of the segment
         if (qn_pair == seg.pstart) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            qb[ks][0] = qn[ks][0];
-            qb[ks][1] = qn[ks][1];
-          }
+          for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              qb[t][ks][0] = qn[t][ks][0];
+              qb[t][ks][1] = qn[t][ks][1];
+            }
           qn_pair = -1;
         } else {
           load_q(qb, seg.seq, seg.kvh);
@@ -350,56 +370,68 @@ __global__ void __launch_bounds__(W * 32, 1)
         __syncwarp();
       }
 
-      // ---- S^T = K . Q^T  (two accumulation chains)
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K . Q^T  (two accumulation chains per n-tile)
+      float sa[NT][4], sb[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[t][e] = sb[t][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t a[4];
         ldmatrix_x4(a, kaddr + (ks >> 2) * kBoxBytes + koff[ks & 3]);
-        if (ks & 1) mma_bf16_16816(sb, a, qb[ks][0], qb[ks][1]);
-        else mma_bf16_16816(sa, a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (ks & 1) mma_bf16_16816(sb[t], a, qb[t][ks][0], qb[t][ks][1]);
+          else mma_bf16_16816(sa[t], a, qb[t][ks][0], qb[t][ks][1]);
+        }
       }
       const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
-      const float s0 = v0 ? (sa[0] + sb[0]) * p.qscale : -INFINITY;  // token g,   head 2tq
-      const float s1 = v0 ? (sa[1] + sb[1]) * p.qscale : -INFINITY;  // token g,   head 2tq+1
-      const float s2 = v1 ? (sa[2] + sb[2]) * p.qscale : -INFINITY;  // token g+8, head 2tq
-      const float s3 = v1 ? (sa[3] + sb[3]) * p.qscale : -INFINITY;  // token g+8, head 2tq+1
+      uint32_t b0[NT], b1[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float s0 = v0 ? (sa[t][0] + sb[t][0]) * p.qscale : -INFINITY;  // token g,   head 2tq
+        const float s1 = v0 ? (sa[t][1] + sb[t][1]) * p.qscale : -INFINITY;  // token g,   head 2tq+1
+        const float s2 = v1 ? (sa[t][2] + sb[t][2]) * p.qscale : -INFINITY;  // token g+8, head 2tq
+        const float s3 = v1 ? (sa[t][3] + sb[t][3]) * p.qscale : -INFINITY;  // token g+8, head 2tq+1
 
-      // ---- online softmax, per head column
-      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        // ---- online softmax, per head column
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-      }
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      if (n0 > m0) {
-        const float a = fast_exp2(m0 - n0);
-        l0 *= a;
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+        }
+        const float n0 = fmaxf(m0[t], mx0), n1 = fmaxf(m1[t], mx1);
+        if (n0 > m0[t]) {
+          const float a = fast_exp2(m0[t] - n0);
+          l0[t] *= a;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { acc[i][0] *= a; acc[i][2] *= a; }
-        m0 = n0;
-      }
-      if (n1 > m1) {
-        const float a = fast_exp2(m1 - n1);
-        l1 *= a;
+          for (int i = 0; i < 8; ++i) { acc[i][t][0] *= a; acc[i][t][2] *= a; }
+          m0[t] = n0;
+        }
+        if (n1 > m1[t]) {
+          const float a = fast_exp2(m1[t] - n1);
+          l1[t] *= a;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { acc[i][1] *= a; acc[i][3] *= a; }
-        m1 = n1;
+          for (int i = 0; i < 8; ++i) { acc[i][t][1] *= a; acc[i][t][3] *= a; }
+          m1[t] = n1;
+        }
+        const float p0 = fast_exp2(s0 - m0[t]), p2 = fast_exp2(s2 - m0[t]);
+        const float p1 = fast_exp2(s1 - m1[t]), p3 = fast_exp2(s3 - m1[t]);
+        l0[t] += p0 + p2;
+        l1[t] += p1 + p3;
+        b0[t] = movmatrix_trans(pack_bf16x2(p0, p1));  // P^T rows: tokens 0..7
+        b1[t] = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8..15
       }
-      const float p0 = fast_exp2(s0 - m0), p2 = fast_exp2(s2 - m0);
-      const float p1 = fast_exp2(s1 - m1), p3 = fast_exp2(s3 - m1);
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));  // P^T rows: tokens 0..7
-      const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8..15
 
-      // ---- O^T += V^T . P^T
+      // ---- O^T += V^T . P^T  (each V^T fragment serves every n-tile)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         uint32_t a[4];
         ldmatrix_x4_trans(a, vaddr + (i >> 2) * kBoxBytes + voff[i & 3]);
-        mma_bf16_16816(acc[i], a, b0, b1);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) mma_bf16_16816(acc[i][t], a, b0[t], b1[t]);
       }
       __syncwarp();
 
@@ -416,30 +448,38 @@ __global__ void __launch_bounds__(W * 32, 1)
 
     // ---- merge the warps' partial results for this segment (4 heads a pass)
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(kFull, l0, o);
-      l1 += __shfl_xor_sync(kFull, l1, o);
-    }
-    if (g == 0) {
-      ml[(warp * kTcHeads + 2 * tq) * 2] = m0;
-      ml[(warp * kTcHeads + 2 * tq) * 2 + 1] = l0;
-      ml[(warp * kTcHeads + 2 * tq + 1) * 2] = m1;
-      ml[(warp * kTcHeads + 2 * tq + 1) * 2 + 1] = l1;
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0[t] += __shfl_xor_sync(kFull, l0[t], o);
+        l1[t] += __shfl_xor_sync(kFull, l1[t], o);
+      }
+      if (g == 0) {
+        const int h = 8 * t + 2 * tq;
+        ml[(warp * H + h) * 2] = m0[t];
+        ml[(warp * H + h) * 2 + 1] = l0[t];
+        ml[(warp * H + h + 1) * 2] = m1[t];
+        ml[(warp * H + h + 1) * 2 + 1] = l1[t];
+      }
     }
     const bool whole = seg.x0 == seg.pstart && seg.x1 == seg.pend;
     // record slot: 0 for a segment that began in an earlier CTA's range (it
     // starts this range), 1 for one that starts the pair (and ends this range)
     const int slot = seg.x0 > seg.pstart ? 0 : 1;
     for (int h0 = 0; h0 < G; h0 += kTcMergeHeads) {
-      // lanes whose head pair (2tq, 2tq+1) falls in [h0, h0 + 4) write it
-      if ((2 * tq) >= h0 && (2 * tq) < h0 + kTcMergeHeads) {
-        float* mb = merge + (warp * kTcMergeHeads + (2 * tq - h0)) * kRecStride;
+      // lanes whose head pair (8t + 2tq, + 1) falls in [h0, h0 + 4) write it
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          mb[16 * i + g] = acc[i][0];
-          mb[kRecStride + 16 * i + g] = acc[i][1];
-          mb[16 * i + g + 8] = acc[i][2];
-          mb[kRecStride + 16 * i + g + 8] = acc[i][3];
+      for (int t = 0; t < NT; ++t) {
+        const int h = 8 * t + 2 * tq;
+        if (h >= h0 && h < h0 + kTcMergeHeads) {
+          float* mb = merge + (warp * kTcMergeHeads + (h - h0)) * kRecStride;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            mb[16 * i + g] = acc[i][t][0];
+            mb[kRecStride + 16 * i + g] = acc[i][t][1];
+            mb[16 * i + g + 8] = acc[i][t][2];
+            mb[kRecStride + 16 * i + g + 8] = acc[i][t][3];
+          }
         }
       }
       __syncthreads();
@@ -449,8 +489,8 @@ __global__ void __launch_bounds__(W * 32, 1)
       const int nh = min(kTcMergeHeads, G - h0);
       if (warp < nh) {
         const int hh = h0 + warp;
-        const float mj = lane < W ? ml[(lane * kTcHeads + hh) * 2] : -INFINITY;
-        const float lj = lane < W ? ml[(lane * kTcHeads + hh) * 2 + 1] : 0.f;
+        const float mj = lane < W ? ml[(lane * H + hh) * 2] : -INFINITY;
+        const float lj = lane < W ? ml[(lane * H + hh) * 2 + 1] : 0.f;
         float M = mj;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
@@ -470,13 +510,20 @@ __global__ void __launch_bounds__(W * 32, 1)
           o4.z = fmaf(v.z, ww, o4.z);
           o4.w = fmaf(v.w, ww, o4.w);
         }
-        if (whole) {
+        if (whole && p.rec_out != nullptr) {  // an (o, m, l) record per head
+          float* r = p.rec_out + (static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) * kRecStride;
+          *reinterpret_cast<float4*>(r + lane * 4) = o4;
+          if (lane == 0) {
+            r[128] = Ls > 0.f ? M : -INFINITY;
+            r[129] = Ls;
+          }
+        } else if (whole) {
           const uint32_t lo16 = f32_to_bf16_bits(o4.x) | (uint32_t(f32_to_bf16_bits(o4.y)) << 16);
           const uint32_t hi16 = f32_to_bf16_bits(o4.z) | (uint32_t(f32_to_bf16_bits(o4.w)) << 16);
           *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) *
                                                 kHeadDim + lane * 4) = make_uint2(lo16, hi16);
         } else {
-          float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcHeads + hh) * kRecStride;
+          float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcRecHeads + hh) * kRecStride;
           *reinterpret_cast<float4*>(r + lane * 4) = o4;
           if (lane == 0) {
             r[128] = Ls > 0.f ? M : -INFINITY;
@@ -569,16 +616,17 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
     // the pair (its units lie inside the pair's run of tiles)
     if (tc_range_lo(cc, V, P) >= tc_range_lo(cc + 1, V, P)) return nullptr;
     const int slot = cc == cf ? 1 : 0;
-    return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcHeads + gi) * kRecStride;
+    return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcRecHeads + gi) * kRecStride;
   };
   const int K = cl - cf + 1;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float Wsum = 0.f;
+  float M = -INFINITY;
   if (K <= 32) {
     const float* rj = lane < K ? record(cf + lane) : nullptr;
     const float mj = rj != nullptr ? __ldcg(rj + 128) : -INFINITY;
     const float lj = rj != nullptr ? __ldcg(rj + 129) : 0.f;
-    float M = lj > 0.f ? mj : -INFINITY;
+    M = lj > 0.f ? mj : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     const float wj = (lj > 0.f && M != -INFINITY) ? lj * fast_exp2(mj - M) : 0.f;
@@ -606,7 +654,6 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
     }
   } else {
     // more than 32 CTAs share the pair (tiny batches): two passes
-    float M = -INFINITY;
     for (int cc = cf; cc <= cl; ++cc) {
       const float* r = record(cc);
       if (r != nullptr && r[129] > 0.f) M = fmaxf(M, r[128]);
@@ -626,6 +673,16 @@ __global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p
     }
   }
   const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
+  if (p.rec_out != nullptr) {  // the pair's (o, m, l) record
+    float* r = p.rec_out + (static_cast<int64_t>(seq) * p.Hq + kvh * p.G + gi) * kRecStride;
+    *reinterpret_cast<float4*>(r + lane * 4) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (lane == 0) {
+      r[128] = Wsum > 0.f ? M : -INFINITY;
+      r[129] = Wsum;
+    }
+    return;
+  }
   const uint32_t lo16 = f32_to_bf16_bits(acc.x * inv) | (uint32_t(f32_to_bf16_bits(acc.y * inv)) << 16);
   const uint32_t hi16 = f32_to_bf16_bits(acc.z * inv) | (uint32_t(f32_to_bf16_bits(acc.w * inv)) << 16);
   *dst = make_uint2(lo16, hi16);

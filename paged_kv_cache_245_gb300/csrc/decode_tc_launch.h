@@ -10,6 +10,7 @@ namespace pkv {
 
 constexpr int kTcMaxSeqs = 512;  // sequences per launch (larger batches run in chunks)
 constexpr int kRecStride = 132;  // floats per head record: o[128], m, l, pad
+constexpr int kTcRecHeads = 16;  // head slots per split record (up to two n-tiles)
 
 struct TcParams {
   const uint16_t* q;        // [B][Hq][128]
@@ -17,7 +18,8 @@ struct TcParams {
   const int32_t* ctx_lens;  // [B]
   const int32_t* block_tables;  // paged [B][max_blocks]
   const int32_t* req_ids;       // contig [B]
-  float* rec;               // [gridDim.x][2][8][kRecStride]
+  float* rec;               // [gridDim.x][2][kTcRecHeads][kRecStride]
+  float* rec_out;           // null: bf16 out; else [B][Hq][kRecStride] (o, m, l) records
   int32_t seg_cost;         // schedule weight of one segment, in tiles (alpha below)
   int64_t bs;               // paged block size (multiple of 16); contig S
   int64_t num_blocks;       // paged pool size (checked mode)
@@ -150,7 +152,9 @@ __host__ __device__ inline bool tc_boundary_pair(int bnd, const int32_t* prefix,
 // Workspace bytes for the per-CTA partial records.
 size_t tc_workspace_bytes(int num_ctas);
 
-// cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages.
+// cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages.  A group
+// of more than 8 query heads per KV head (p.G <= 16, paged only) runs with
+// two n-tiles of heads on 8 warps x 3 stages whatever cfg says.
 TcStatus launch_decode_tc(const TcParams& p, bool contig, const void* k, const void* v,
                           int64_t rows_total, int cfg, int num_ctas, void* workspace,
                           cudaStream_t stream, cudaError_t* cuda_err);

@@ -10,6 +10,7 @@
 
 #include "../../include/pkv.h"
 #include "decode_launch.cuh"
+#include "cascade.cuh"
 #include "decode_tc_launch.h"
 #include "kv_ops.cuh"
 
@@ -313,6 +314,41 @@ pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const 
   return PKV_OK;
 }
 
+// Shared-prefix plan: prefix entries stack the heads of m sequences (m * G
+// <= 16 query heads per KV head); workspace regions, 256-byte aligned.
+struct SharedPlan {
+  int32_t m = 0, SG = 0, Vp = 0, Gv = 0;
+  size_t q_p = 0, tables_p = 0, ctx_p = 0, tables_s = 0, ctx_s = 0, rec_p = 0, rec_s = 0, tc = 0;
+  size_t total = 0;
+};
+
+SharedPlan shared_plan(int32_t B, int32_t num_groups, int32_t max_group_size, int32_t max_blocks,
+                       const pkv_heads& h, int sms) {
+  SharedPlan s;
+  const int32_t G = h.num_q_heads / h.num_kv_heads;
+  s.m = pkv::kTcRecHeads / G;  // 16 query heads per KV head at most
+  s.Gv = s.m * G;
+  s.SG = (max_group_size + s.m - 1) / s.m;
+  s.Vp = num_groups * s.SG;
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t here = at;
+    at += (bytes + 255) / 256 * 256;
+    return here;
+  };
+  const size_t vp = static_cast<size_t>(s.Vp);
+  s.q_p = take(vp * h.num_kv_heads * s.Gv * pkv::kHeadDim * 2);
+  s.tables_p = take(vp * max_blocks * 4);
+  s.ctx_p = take(vp * 4);
+  s.tables_s = take(static_cast<size_t>(B) * max_blocks * 4);
+  s.ctx_s = take(static_cast<size_t>(B) * 4);
+  s.rec_p = take(vp * h.num_kv_heads * s.Gv * pkv::kRecStride * 4);
+  s.rec_s = take(static_cast<size_t>(B) * h.num_q_heads * pkv::kRecStride * 4);
+  s.tc = take(pkv::tc_workspace_bytes(tc_ctas(sms)));
+  s.total = at;
+  return s;
+}
+
 pkv_status gather_common(const void* cache, const int32_t* block_tables, int32_t max_blocks,
                          int32_t num_blocks, const int32_t* req_ids, int32_t max_reqs,
                          const int32_t* context_lens, int32_t num_seqs, int32_t max_context,
@@ -444,6 +480,123 @@ pkv_status pkv_contig_decode_attention(const void* q, const void* k_buf, const v
   return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
                        num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
                        stream);
+}
+
+size_t pkv_shared_decode_workspace_size(int32_t num_seqs, int32_t num_groups,
+                                        int32_t max_group_size, int32_t max_blocks_per_seq,
+                                        pkv_heads heads) {
+  int sms = 0;
+  if (device_info(nullptr, nullptr, &sms) != PKV_OK) return 0;
+  if (check_heads(heads) != PKV_OK || num_seqs <= 0 || num_groups <= 0 || max_group_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  return shared_plan(num_seqs, num_groups, max_group_size, max_blocks_per_seq, heads, sms).total;
+}
+
+pkv_status pkv_paged_decode_attention_shared(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t* context_lens, int32_t num_seqs,
+    int32_t max_context, int32_t block_size, const int32_t* group_start,
+    const int32_t* shared_blocks, int32_t num_groups, int32_t max_group_size, float scale,
+    pkv_heads heads, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  pkv_status st = check_heads(heads);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_context < 0 || num_groups < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_seqs > 65535");
+  if (num_groups < 1 || num_groups > num_seqs || max_group_size < 1 || max_group_size > num_seqs)
+    return fail(PKV_ERR_INVALID_ARG, "need 1 <= num_groups <= num_seqs and 1 <= max_group_size <= num_seqs");
+  if (!q || !k_cache || !v_cache || !out || !context_lens || !block_tables || !group_start ||
+      !shared_blocks)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(PKV_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  if (!aligned(context_lens, 4) || !aligned(block_tables, 4) || !aligned(group_start, 4) ||
+      !aligned(shared_blocks, 4))
+    return fail(PKV_ERR_INVALID_ARG, "int32 arrays misaligned");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (block_size <= 0 || block_size % 16 != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "the shared-prefix path needs block_size %% 16 == 0");
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+      static_cast<int64_t>(max_blocks_per_seq) * block_size < max_context)
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq * block_size < max_context");
+  const int64_t rows_total = static_cast<int64_t>(num_blocks) * heads.num_kv_heads * block_size;
+  if (rows_total > 0x7fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "cache of 2^31 rows or more");
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return fail(PKV_ERR_UNSUPPORTED, "block table longer than 2^31 positions");
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  st = device_info(&dev, &err, &sms);
+  if (st != PKV_OK) return st;
+  const SharedPlan sp = shared_plan(num_seqs, num_groups, max_group_size, max_blocks_per_seq,
+                                    heads, sms);
+  if (static_cast<int64_t>(num_groups) * sp.SG > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "too many prefix entries");
+  if (!workspace || workspace_bytes < sp.total)
+    return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", sp.total,
+                workspace ? workspace_bytes : size_t{0});
+  if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  pkv::CascadeParams c;
+  std::memset(&c, 0, sizeof c);
+  c.q = static_cast<const uint16_t*>(q);
+  c.ctx = context_lens;
+  c.block_tables = block_tables;
+  c.group_start = group_start;
+  c.shared_blocks = shared_blocks;
+  c.out = static_cast<uint16_t*>(out);
+  c.B = num_seqs;
+  c.Hq = heads.num_q_heads;
+  c.Hkv = heads.num_kv_heads;
+  c.G = heads.num_q_heads / heads.num_kv_heads;
+  c.max_blocks = max_blocks_per_seq;
+  c.num_groups = num_groups;
+  c.bs = block_size;
+  c.m = sp.m;
+  c.SG = sp.SG;
+  c.Vp = sp.Vp;
+  c.checked = g_checked.load();
+  c.err = err;
+  c.q_p = reinterpret_cast<uint16_t*>(ws + sp.q_p);
+  c.tables_p = reinterpret_cast<int32_t*>(ws + sp.tables_p);
+  c.ctx_p = reinterpret_cast<int32_t*>(ws + sp.ctx_p);
+  c.tables_s = reinterpret_cast<int32_t*>(ws + sp.tables_s);
+  c.ctx_s = reinterpret_cast<int32_t*>(ws + sp.ctx_s);
+  c.rec_p = reinterpret_cast<float*>(ws + sp.rec_p);
+  c.rec_s = reinterpret_cast<float*>(ws + sp.rec_s);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = pkv::launch_cascade_prep(c, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prep launch");
+  // the shared positions, once per m sequences, then every sequence's own
+  for (int part = 0; part < 2; ++part) {
+    pkv::TcParams t;
+    std::memset(&t, 0, sizeof t);
+    const bool prefix = part == 0;
+    t.q = prefix ? c.q_p : c.q;
+    t.out = c.out;  // unused: record mode
+    t.rec_out = prefix ? c.rec_p : c.rec_s;
+    t.ctx_lens = prefix ? c.ctx_p : c.ctx_s;
+    t.block_tables = prefix ? c.tables_p : c.tables_s;
+    t.bs = block_size;
+    t.num_blocks = num_blocks;
+    t.max_blocks = max_blocks_per_seq;
+    t.num_seqs = prefix ? c.Vp : num_seqs;
+    t.Hkv = heads.num_kv_heads;
+    t.G = prefix ? sp.Gv : c.G;
+    t.Hq = t.Hkv * t.G;
+    t.max_context = prefix ? max_blocks_per_seq * block_size : max_context;
+    t.qscale = scale * 1.4426950408889634f;  // log2(e)
+    t.checked = c.checked;
+    t.err = err;
+    const pkv::TcStatus ts = pkv::launch_decode_tc(t, false, k_cache, v_cache, rows_total, 1,
+                                                   tc_ctas(sms), ws + sp.tc, s, &ce);
+    if (ts == pkv::TcStatus::kEncodeFailed)
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
+    if (ts != pkv::TcStatus::kOk) return cuda_fail(ce, "prefix-sharing decode launch");
+  }
+  ce = pkv::launch_cascade_merge(c, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing merge launch");
+  return PKV_OK;
 }
 
 pkv_status pkv_debug_gather_paged(const void* cache, const int32_t* block_tables,

@@ -1,0 +1,108 @@
+"""Decode attention with shared prompt blocks read once per group of
+sequences (pkv_paged_decode_attention_shared) against the regular paged call
+and the oracle: the Yi-34B parallel-sampling scenario, synthetic groups over
+every group size (singletons, empty suffixes, ragged members), and checked
+mode's report for a member whose context does not cover the shared blocks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_245_gb300 as pkv
+import workloads as W
+from parity import DeviceLayer, assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _reset_modes():
+    pkv.set_checked(False)
+    pkv.set_decode_variant(pkv.VARIANT_AUTO)
+    yield
+    pkv.set_checked(False)
+    torch.cuda.synchronize()
+
+
+def shared_prefix_blocks(tables, ctx, bs, starts):
+    return W.shared_prefix_blocks(tables, ctx, bs, np.asarray(starts))
+
+
+def _run(b, starts, shared, L):
+    gs = torch.as_tensor(np.asarray(starts, np.int32), device=DEV)
+    sb = torch.as_tensor(shared, device=DEV)
+    maxg = int(np.max(np.diff(starts)))
+    return pkv.paged_decode_attention_shared(L.q, L.k_cache, L.v_cache, L.tables, L.ctx,
+                                             b.max_context, L.scale, gs, sb, maxg)
+
+
+@pytest.mark.parametrize("step", [0, 1, 63])
+def test_yi34b_sharing_scenario(step):
+    sc = W.sharing_scenario()
+    b = sc.steps[step]
+    L = DeviceLayer(b, 0, DEV, fast_cache=True)
+    starts = np.arange(0, b.B + 1, sc.n)
+    shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
+    assert shared.min() > 0
+    out = _run(b, starts, shared, L)
+    ref = L.gpu_attend()
+    torch.cuda.synchronize()
+    assert_attention_close(out, ref.float().cpu().numpy().astype(np.float64), "vs regular call")
+    if step != 1:
+        assert_attention_close(out, L.oracle_attend(), "vs oracle")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (28, 4), (32, 4)])
+def test_synthetic_groups(hq, hkv):
+    """Groups of 1..5 sequences over one prompt each: members have their own
+    tail blocks after the shared ones; some members stop exactly at the
+    shared positions (empty own part)."""
+    rng = np.random.default_rng(hq * 10 + hkv)
+    bs = 16
+    shape = W.ModelShape("s%d_%d" % (hq, hkv), 1, hq, hkv)
+    sizes = [1, 2, 3, 4, 5, 1, 3]
+    starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    B = int(starts[-1])
+    prompt = rng.integers(1, 40, size=len(sizes)) * bs   # whole shared blocks
+    own = [rng.integers(0, 70, size=s) for s in sizes]
+    own[1][0] = 0                                        # a member with no own positions
+    ctx = np.concatenate([p + o for p, o in zip(prompt, own)]).astype(np.int32)
+    ctx = np.maximum(ctx, 1)
+    max_blocks = int((ctx.max() + bs - 1) // bs)
+    nb = int(sum((c + bs - 1) // bs for c in ctx)) + 8
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.zeros((B, max_blocks), np.int32)
+    used = 0
+    for g, s in enumerate(sizes):
+        pb = int(prompt[g] // bs)
+        pblocks = perm[used:used + pb]
+        used += pb
+        for k in range(s):
+            i = int(starts[g]) + k
+            tables[i, :pb] = pblocks
+            rest = int((ctx[i] + bs - 1) // bs) - pb
+            tables[i, pb:pb + rest] = perm[used:used + rest]
+            used += rest
+    b = W.PagedBatch(shape=shape, seed=1, block_size=bs, num_blocks=nb, ctx_pre=ctx - 1, ctx=ctx,
+                     block_tables=tables, slot_mapping=np.full(B, -1, np.int64),
+                     req_ids=np.arange(B, dtype=np.int32), max_reqs=B)
+    L = DeviceLayer(b, 0, DEV)
+    shared = shared_prefix_blocks(tables, ctx, bs, starts)
+    out = _run(b, starts, shared, L)
+    assert_attention_close(out, L.oracle_attend(), "synthetic groups G=%d" % (hq // hkv))
+
+
+def test_checked_mode_reports_an_uncovered_member():
+    pkv.set_checked(True)
+    sc = W.sharing_scenario(num_prompts=4, decode_steps=1)
+    b = sc.steps[0]
+    L = DeviceLayer(b, 0, DEV, fast_cache=True)
+    starts = np.arange(0, b.B + 1, sc.n)
+    shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
+    shared[0] = int(b.ctx[:sc.n].max() // b.block_size) + 1   # beyond every member's context
+    assert pkv.get_device_error() == "none"
+    _run(b, starts, shared, L)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "context"

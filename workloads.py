@@ -363,6 +363,25 @@ def sharing_scenario(num_prompts: int = 32, n: int = 4, decode_steps: int = 64,
                            steps=steps)
 
 
+def shared_prefix_blocks(block_tables: np.ndarray, ctx: np.ndarray, block_size: int,
+                         group_start: np.ndarray) -> np.ndarray:
+    """For groups of consecutive sequences (group_start [G+1]), the number of
+    leading block-table entries all members have in common and whose
+    positions every member's context covers (0 for a singleton)."""
+    out = []
+    for g in range(len(group_start) - 1):
+        rows = block_tables[group_start[g]:group_start[g + 1]]
+        if len(rows) < 2:
+            out.append(0)
+            continue
+        n = int(ctx[group_start[g]:group_start[g + 1]].min() // block_size)
+        k = 0
+        while k < n and np.all(rows[:, k] == rows[0, k]):
+            k += 1
+        out.append(k)
+    return np.asarray(out, np.int32)
+
+
 def to_u16(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> its uint16 bit patterns as a host numpy array."""
     return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
