@@ -251,8 +251,9 @@ class DeviceWorkload:
             n = W.sharing_scenario(decode_steps=1).n
             starts = np.arange(0, b.B + 1, n, dtype=np.int32)
             shared = W.shared_prefix_blocks(b.block_tables, b.ctx, bs, starts)
+            own = int((b.ctx - np.repeat(shared, n) * bs).max())  # own positions per sequence
             self.groups = (torch.as_tensor(starts, device=dev), torch.as_tensor(shared, device=dev),
-                           n)
+                           n, own)
         self.k_caches = [li.k_cache for li in self.layers]
         self.v_caches = [li.v_cache for li in self.layers]
         self.tables = torch.as_tensor(b.block_tables, device=dev)
@@ -279,8 +280,8 @@ class DeviceWorkload:
         # plus one block copy launch (all layers) when the step copies on write
         cow = 0 if self.cow is None else 1
         if self.groups is not None:
-            # append; prep, prefix main + combine, own-part main + combine, merge
-            return self.shape.num_layers * 7 + cow
+            # append; prep, prefix main + combine, merge (own parts in the merge)
+            return self.shape.num_layers * 5 + cow
         if self.uses_tc:
             return self.shape.num_layers * 3 + cow
         return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0)) + cow
@@ -293,11 +294,11 @@ class DeviceWorkload:
     def attend(self, l):
         li = self.layers[l]
         if self.groups is not None:
-            gs, sb, n = self.groups
+            gs, sb, n, own = self.groups
             self.pkv.paged_decode_attention_shared(li.q, li.k_cache, li.v_cache, self.tables,
                                                    self.ctx, self.batch.max_context, self.scale,
-                                                   gs, sb, n, out=self.out[l],
-                                                   workspace=self.workspace)
+                                                   gs, sb, n, max_own_tokens=own,
+                                                   out=self.out[l], workspace=self.workspace)
         else:
             self.pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, self.tables, self.ctx,
                                             self.batch.max_context, self.scale, out=self.out[l],
@@ -435,7 +436,8 @@ def run_gpu(args, world, rank, local):
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                      "traffic": _profiled_traffic(args.workload),
                      "kernel": "paged_decode_attention_shared call (prep, decode_tc_kernel "
-                               "x2 with combines, merge)" if wl.groups is not None else
+                               "with combine, merge with the own positions)"
+                               if wl.groups is not None else
                                "paged_decode_attention call (decode_tc_kernel + "
                                "decode_tc_combine_kernel)" if wl.uses_tc else
                                "paged_decode_attention call (decode_attention_kernel + "
@@ -646,11 +648,12 @@ def measure_e2e(wl, dev, args, world):
             q, kn, vn = views[3 * l:3 * l + 3]
             li = wl.layers[l]
             if wl.groups is not None:
-                gs, sb, n = wl.groups
+                gs, sb, n, own = wl.groups
                 pkv.kv_append(slots, kn, vn, li.k_cache, li.v_cache)
                 pkv.paged_decode_attention_shared(q, li.k_cache, li.v_cache, tables, ctx,
                                                   b.max_context, wl.scale, gs, sb, n,
-                                                  out=out_all[l], workspace=wl.workspace)
+                                                  max_own_tokens=own, out=out_all[l],
+                                                  workspace=wl.workspace)
             else:
                 pkv.paged_decode_step(slots, kn, vn, q, li.k_cache, li.v_cache, tables, ctx,
                                       b.max_context, wl.scale, out=out_all[l],

@@ -200,7 +200,13 @@ PKV_API pkv_status pkv_contig_decode_step(
  * plain sequences.  The shared positions are read once for every
  * ceil(16 / G) members (their query heads stacked into one tensor-core tile)
  * instead of once per member; each member's own later positions are read as
- * usual, and the two softmax parts are merged.  Result: the same attention as
+ * usual, and the two softmax parts are merged.  max_own_tokens is a host
+ * bound on every sequence's own positions (context_lens[i] minus its group's
+ * shared positions), or -1 if unknown: with a bound of at most 256 the own
+ * positions are attended on CUDA cores inside the final merge instead of by
+ * a second tensor-core pass (checked mode reports a sequence beyond the
+ * bound, PKV_DEVERR_CONTEXT, and its later positions are left out).  Result:
+ * the same attention as
  * pkv_paged_decode_attention within the attention tolerance (a different
  * summation order).  Other arguments as there; block_size must be a multiple
  * of 16.  workspace (256-byte aligned) must hold
@@ -216,8 +222,8 @@ PKV_API pkv_status pkv_paged_decode_attention_shared(
     const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_blocks,
     const int32_t *context_lens, int32_t num_seqs, int32_t max_context,
     int32_t block_size, const int32_t *group_start, const int32_t *shared_blocks,
-    int32_t num_groups, int32_t max_group_size, float scale, pkv_heads heads,
-    void *out, void *workspace, size_t workspace_bytes, void *stream);
+    int32_t num_groups, int32_t max_group_size, int32_t max_own_tokens, float scale,
+    pkv_heads heads, void *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Copy-on-write block copy.  "Running Out of Cache" (section "Fragmentation

@@ -74,8 +74,8 @@ def lib():
     L.pkv_shared_decode_workspace_size.argtypes = [i32, i32, i32, i32, Heads]
     L.pkv_shared_decode_workspace_size.restype = sz
     L.pkv_paged_decode_attention_shared.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
-                                                    vp, vp, i32, i32, ctypes.c_float, Heads, vp,
-                                                    vp, sz, vp]
+                                                    vp, vp, i32, i32, i32, ctypes.c_float, Heads,
+                                                    vp, vp, sz, vp]
     L.pkv_debug_gather_paged.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, i32, vp, vp]
     L.pkv_debug_gather_contig.argtypes = [vp, vp, i32, vp, i32, i32, i64, i32, vp, vp]
     L.pkv_set_checked.argtypes = [ctypes.c_int]
@@ -299,8 +299,8 @@ def contig_decode_step(slot_mapping, k_new, v_new, q, k_buf, v_buf, req_ids, con
 
 
 def paged_decode_attention_shared(q, k_cache, v_cache, block_tables, context_lens, max_context,
-                                  scale, group_start, shared_blocks, max_group_size, out=None,
-                                  workspace=None):
+                                  scale, group_start, shared_blocks, max_group_size,
+                                  max_own_tokens=-1, out=None, workspace=None):
     """Paged decode attention where groups of consecutive sequences share
     their first shared_blocks[g] blocks (group_start [G+1], shared_blocks [G]:
     int32 on the device; max_group_size a host bound): the shared positions
@@ -328,7 +328,7 @@ def paged_decode_attention_shared(q, k_cache, v_cache, block_tables, context_len
     _check(lib().pkv_paged_decode_attention_shared(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], nb,
         _ptr(context_lens), B, int(max_context), bs, _ptr(group_start), _ptr(shared_blocks), G,
-        int(max_group_size), float(scale), h, _ptr(out), _ptr(workspace),
+        int(max_group_size), int(max_own_tokens), float(scale), h, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(q)))
     return out
 

@@ -88,8 +88,62 @@ __global__ void __launch_bounds__(256) cascade_prep_kernel(const CascadeParams c
         c.block_tables[static_cast<int64_t>(i) * c.max_blocks + sb + j];
 }
 
+// The own positions [s0, s0 + n) of sequence i for query head h, on CUDA
+// cores: lane j holds dimensions 4j .. 4j+3; the block-table entries are
+// loaded first (lane j: entry j), then 8 positions at a time with all their
+// K and V loads in flight.  Returns (o over this lane's dims, m, l) with o
+// not yet normalised (o / l is the attention over these positions).
+__device__ void own_attention(const CascadeParams& c, int i, int h, int sb, int n, float4& o,
+                              float& m, float& l) {
+  constexpr unsigned kFull = 0xffffffffu;
+  constexpr int U = 8;
+  const int lane = threadIdx.x & 31;
+  const int kvh = h / c.G;
+  const int nblk = (n + c.bs - 1) / c.bs;  // <= 32: own_cap <= 256 and bs >= 16
+  const int32_t ent =
+      lane < nblk ? c.block_tables[static_cast<int64_t>(i) * c.max_blocks + sb + lane] : 0;
+  const uint2 qraw = __ldg(reinterpret_cast<const uint2*>(c.q + (static_cast<int64_t>(i) * c.Hq + h) *
+                                                                  kHeadDim) + lane);
+  const float q0 = bf16_lo(qraw.x) * c.qscale, q1 = bf16_hi(qraw.x) * c.qscale;
+  const float q2 = bf16_lo(qraw.y) * c.qscale, q3 = bf16_hi(qraw.y) * c.qscale;
+  o = make_float4(0.f, 0.f, 0.f, 0.f);
+  m = -INFINITY;
+  l = 0.f;
+  for (int t0 = 0; t0 < n; t0 += U) {
+    uint2 kr[U], vr[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = t0 + u < n ? t0 + u : n - 1;
+      const int32_t blk = __shfl_sync(kFull, ent, t / c.bs);
+      const int64_t row = cache_row(blk, kvh, c.Hkv, c.bs, t % c.bs);
+      kr[u] = __ldg(reinterpret_cast<const uint2*>(c.k_cache + row * kHeadDim) + lane);
+      vr[u] = __ldg(reinterpret_cast<const uint2*>(c.v_cache + row * kHeadDim) + lane);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float d = q0 * bf16_lo(kr[u].x);
+      d = fmaf(q1, bf16_hi(kr[u].x), d);
+      d = fmaf(q2, bf16_lo(kr[u].y), d);
+      d = fmaf(q3, bf16_hi(kr[u].y), d);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(kFull, d, off);
+      if (t0 + u >= n) continue;
+      const float mn = fmaxf(m, d);
+      const float a = fast_exp2(m - mn);  // 0 while m is -inf
+      const float p = fast_exp2(d - mn);
+      l = fmaf(l, a, p);
+      o.x = fmaf(o.x, a, p * bf16_lo(vr[u].x));
+      o.y = fmaf(o.y, a, p * bf16_hi(vr[u].x));
+      o.z = fmaf(o.z, a, p * bf16_lo(vr[u].y));
+      o.w = fmaf(o.w, a, p * bf16_hi(vr[u].y));
+      m = mn;
+    }
+  }
+}
+
 // One warp per (sequence, query head): merge its prefix record (if the
-// sequence shares anything) with its suffix record into the bf16 output.
+// sequence shares anything) with its own part -- attended here, or a record
+// of the tensor-core pass -- into the bf16 output.
 __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams c) {
   grid_dependency_wait();
   grid_dependency_trigger();
@@ -114,14 +168,31 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   const float* rs = c.rec_s + idx * kRecStride;
   const float mp = has_prefix ? __ldcg(rp + 128) : -INFINITY;
   const float lp = has_prefix ? __ldcg(rp + 129) : 0.f;
-  const float ms = __ldcg(rs + 128), ls = __ldcg(rs + 129);
+  float ms, ls;
+  float4 own;
+  if (c.own_cap >= 0) {
+    const int sb_in = c.shared_blocks[g];
+    const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);
+    int n = c.ctx[i] - sb * c.bs;
+    if (n > c.own_cap) {
+      if (c.checked && (threadIdx.x & 31) == 0) record_error(c.err, kErrContext);
+      n = c.own_cap;  // the bound was wrong: the later positions are left out
+    }
+    own_attention(c, i, h, sb, n > 0 ? n : 0, own, ms, ls);
+    const float inv_own = ls > 0.f ? 1.f / ls : 0.f;
+    own = make_float4(own.x * inv_own, own.y * inv_own, own.z * inv_own, own.w * inv_own);
+  } else {
+    ms = __ldcg(rs + 128);
+    ls = __ldcg(rs + 129);
+  }
   const bool hp = lp > 0.f, hs = ls > 0.f;
   const float M = fmaxf(hp ? mp : -INFINITY, hs ? ms : -INFINITY);
   const float wp = hp ? lp * fast_exp2(mp - M) : 0.f;
   const float ws = hs ? ls * fast_exp2(ms - M) : 0.f;
   const float inv = wp + ws > 0.f ? 1.f / (wp + ws) : 0.f;
   const float4 op = hp ? __ldcg(reinterpret_cast<const float4*>(rp) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 os = hs ? __ldcg(reinterpret_cast<const float4*>(rs) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 os = !hs ? make_float4(0.f, 0.f, 0.f, 0.f)
+                  : (c.own_cap >= 0 ? own : __ldcg(reinterpret_cast<const float4*>(rs) + lane));
   const float x = (wp * op.x + ws * os.x) * inv, y = (wp * op.y + ws * os.y) * inv;
   const float z = (wp * op.z + ws * os.z) * inv, w = (wp * op.w + ws * os.w) * inv;
   const uint32_t lo16 = f32_to_bf16_bits(x) | (uint32_t(f32_to_bf16_bits(y)) << 16);

@@ -25,6 +25,12 @@ struct CascadeParams {
   int32_t Vp;  // num_groups * SG
   int32_t checked;
   int* err;
+  // own positions attended in the merge kernel (own_cap >= 0: at most own_cap
+  // of them per sequence), else (-1) by a tensor-core pass into rec_s
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  float qscale;                  // scale * log2(e)
+  int32_t own_cap;
   // workspace
   uint16_t* q_p;      // [Vp][Hkv][m*G][128]
   int32_t* tables_p;  // [Vp][max_blocks]

@@ -314,6 +314,9 @@ pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const 
   return PKV_OK;
 }
 
+// Own parts of at most this many positions are attended in the merge kernel.
+constexpr int32_t kInlineOwnMax = 256;
+
 // Shared-prefix plan: prefix entries stack the heads of m sequences (m * G
 // <= 16 query heads per KV head); workspace regions, 256-byte aligned.
 struct SharedPlan {
@@ -497,8 +500,9 @@ pkv_status pkv_paged_decode_attention_shared(
     const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
     int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t* context_lens, int32_t num_seqs,
     int32_t max_context, int32_t block_size, const int32_t* group_start,
-    const int32_t* shared_blocks, int32_t num_groups, int32_t max_group_size, float scale,
-    pkv_heads heads, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    const int32_t* shared_blocks, int32_t num_groups, int32_t max_group_size,
+    int32_t max_own_tokens, float scale, pkv_heads heads, void* out, void* workspace,
+    size_t workspace_bytes, void* stream) {
   pkv_status st = check_heads(heads);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_context < 0 || num_groups < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
@@ -557,6 +561,11 @@ pkv_status pkv_paged_decode_attention_shared(
   c.Vp = sp.Vp;
   c.checked = g_checked.load();
   c.err = err;
+  c.k_cache = static_cast<const uint16_t*>(k_cache);
+  c.v_cache = static_cast<const uint16_t*>(v_cache);
+  c.qscale = scale * 1.4426950408889634f;  // log2(e)
+  // short own parts are attended in the merge kernel (no second launch)
+  c.own_cap = max_own_tokens >= 0 && max_own_tokens <= kInlineOwnMax ? max_own_tokens : -1;
   c.q_p = reinterpret_cast<uint16_t*>(ws + sp.q_p);
   c.tables_p = reinterpret_cast<int32_t*>(ws + sp.tables_p);
   c.ctx_p = reinterpret_cast<int32_t*>(ws + sp.ctx_p);
@@ -567,8 +576,9 @@ pkv_status pkv_paged_decode_attention_shared(
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t ce = pkv::launch_cascade_prep(c, s);
   if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prep launch");
-  // the shared positions, once per m sequences, then every sequence's own
-  for (int part = 0; part < 2; ++part) {
+  // the shared positions, once per m sequences, then (unless the merge kernel
+  // takes them) every sequence's own
+  for (int part = 0; part < (c.own_cap >= 0 ? 1 : 2); ++part) {
     pkv::TcParams t;
     std::memset(&t, 0, sizeof t);
     const bool prefix = part == 0;

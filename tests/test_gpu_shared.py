@@ -30,23 +30,35 @@ def shared_prefix_blocks(tables, ctx, bs, starts):
     return W.shared_prefix_blocks(tables, ctx, bs, np.asarray(starts))
 
 
-def _run(b, starts, shared, L):
+def own_bound(b, starts, shared):
+    """The largest number of own (unshared) positions of any sequence."""
+    sizes = np.diff(np.asarray(starts))
+    per_seq = np.repeat(shared, sizes) * b.block_size
+    return int((b.ctx - per_seq).max())
+
+
+def _run(b, starts, shared, L, own=-1):
     gs = torch.as_tensor(np.asarray(starts, np.int32), device=DEV)
     sb = torch.as_tensor(shared, device=DEV)
     maxg = int(np.max(np.diff(starts)))
     return pkv.paged_decode_attention_shared(L.q, L.k_cache, L.v_cache, L.tables, L.ctx,
-                                             b.max_context, L.scale, gs, sb, maxg)
+                                             b.max_context, L.scale, gs, sb, maxg,
+                                             max_own_tokens=own)
 
 
+OWN = ["tensor_core_pass", "in_merge"]
+
+
+@pytest.mark.parametrize("own", OWN)
 @pytest.mark.parametrize("step", [0, 1, 63])
-def test_yi34b_sharing_scenario(step):
+def test_yi34b_sharing_scenario(step, own):
     sc = W.sharing_scenario()
     b = sc.steps[step]
     L = DeviceLayer(b, 0, DEV, fast_cache=True)
     starts = np.arange(0, b.B + 1, sc.n)
     shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
     assert shared.min() > 0
-    out = _run(b, starts, shared, L)
+    out = _run(b, starts, shared, L, -1 if own == OWN[0] else own_bound(b, starts, shared))
     ref = L.gpu_attend()
     torch.cuda.synchronize()
     assert_attention_close(out, ref.float().cpu().numpy().astype(np.float64), "vs regular call")
@@ -54,8 +66,9 @@ def test_yi34b_sharing_scenario(step):
         assert_attention_close(out, L.oracle_attend(), "vs oracle")
 
 
+@pytest.mark.parametrize("own", OWN)
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (28, 4), (32, 4)])
-def test_synthetic_groups(hq, hkv):
+def test_synthetic_groups(hq, hkv, own):
     """Groups of 1..5 sequences over one prompt each: members have their own
     tail blocks after the shared ones; some members stop exactly at the
     shared positions (empty own part)."""
@@ -66,6 +79,9 @@ def test_synthetic_groups(hq, hkv):
     starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     B = int(starts[-1])
     prompt = rng.integers(1, 40, size=len(sizes)) * bs   # whole shared blocks
+    # a singleton shares nothing: all its positions are its own (keep them
+    # within the in-merge bound)
+    prompt[np.asarray(sizes) == 1] = np.minimum(prompt[np.asarray(sizes) == 1], 10 * bs)
     own = [rng.integers(0, 70, size=s) for s in sizes]
     own[1][0] = 0                                        # a member with no own positions
     ctx = np.concatenate([p + o for p, o in zip(prompt, own)]).astype(np.int32)
@@ -90,7 +106,9 @@ def test_synthetic_groups(hq, hkv):
                      req_ids=np.arange(B, dtype=np.int32), max_reqs=B)
     L = DeviceLayer(b, 0, DEV)
     shared = shared_prefix_blocks(tables, ctx, bs, starts)
-    out = _run(b, starts, shared, L)
+    bound = own_bound(b, starts, shared)
+    assert bound <= 256   # singletons keep whole contexts: within the in-merge bound
+    out = _run(b, starts, shared, L, -1 if own == OWN[0] else bound)
     assert_attention_close(out, L.oracle_attend(), "synthetic groups G=%d" % (hq // hkv))
 
 
@@ -104,5 +122,22 @@ def test_checked_mode_reports_an_uncovered_member():
     shared[0] = int(b.ctx[:sc.n].max() // b.block_size) + 1   # beyond every member's context
     assert pkv.get_device_error() == "none"
     _run(b, starts, shared, L)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "context"
+
+
+def test_checked_mode_reports_an_own_part_beyond_the_bound():
+    pkv.set_checked(True)
+    sc = W.sharing_scenario(num_prompts=4, decode_steps=8)
+    b = sc.steps[7]
+    L = DeviceLayer(b, 0, DEV, fast_cache=True)
+    starts = np.arange(0, b.B + 1, sc.n)
+    shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
+    bound = own_bound(b, starts, shared)
+    assert pkv.get_device_error() == "none"
+    _run(b, starts, shared, L, bound)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "none"
+    _run(b, starts, shared, L, bound - 1)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == "context"
