@@ -38,12 +38,16 @@ def configure(L):
     L.pkv_oracle_contig_decode.argtypes = [_u16p, _u16p, _u16p, _i32p, i32,
                                            _i32p, i32, i32, i32, i32, i64,
                                            dbl, _f64p, ctypes.c_int]
+    L.pkv_oracle_paged_prefill.argtypes = [_u16p, _u16p, _u16p, i64, _i32p, i32, _i32p,
+                                           _i32p, i32, i32, i32, i32, i32, dbl, _f64p,
+                                           ctypes.c_int]
     L.pkv_oracle_kv_append.argtypes = [_i64p, i64, _u16p, _u16p, _u16p,
                                        _u16p, i64, i64, i32, i32]
     L.pkv_oracle_block_copy.argtypes = [_i64p, i64, ctypes.c_void_p,
                                         ctypes.c_void_p, i32, i64, i64]
     for name in ("pkv_oracle_gather_paged", "pkv_oracle_gather_contig",
                  "pkv_oracle_paged_decode", "pkv_oracle_contig_decode",
+                 "pkv_oracle_paged_prefill",
                  "pkv_oracle_kv_append", "pkv_oracle_block_copy"):
         getattr(L, name).restype = ctypes.c_int
     return L
@@ -115,6 +119,25 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
                                          bt.shape[1] if bt.ndim == 2 else 0,
                                          cl, B, hq, hkv, d, bs, float(scale),
                                          out, int(nthreads)), "paged_decode")
+    return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, cu_q, scale, nthreads=0):
+    """fp64 causal prefill, paged layout: q [T, Hq, D] holds every
+    sequence's chunk of new tokens (sequence i: rows cu_q[i] .. cu_q[i+1]-1,
+    the last positions of its context_lens[i]).  Returns out [T, Hq, D]."""
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    assert d == d2 and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_q, dtype=np.int32)
+    assert cu[-1] == T
+    out = np.zeros((T, hq, d), dtype=np.float64)
+    _check(lib().pkv_oracle_paged_prefill(q, k_cache, v_cache, nb, bt, bt.shape[1], cl, cu,
+                                          len(cl), hq, hkv, d, bs, float(scale), out,
+                                          int(nthreads)), "paged_prefill")
     return out
 
 

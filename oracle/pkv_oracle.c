@@ -340,6 +340,150 @@ int pkv_oracle_contig_decode(const uint16_t *q, const uint16_t *k_buf,
 }
 
 /* ---------------------------------------------------------------------- */
+/* Prefill over a paged cache: a chunk of new tokens per sequence, whose K  */
+/* and V rows are already in the cache, attends causally.  The pages name   */
+/* prefill only as a phase ([VA4], section headings); the reading here is   */
+/* the standard causal one: sequence i's chunk holds the last Lq_i of its   */
+/* ctx_i positions (Lq_i = cu_q[i+1] - cu_q[i]), and its j-th token, at      */
+/* position ctx_i - Lq_i + j, attends positions 0 .. ctx_i - Lq_i + j.  A    */
+/* chunk of one token is the decode step above.                             */
+/* Work is split over threads by (token, query head); each is computed       */
+/* start to finish by one thread: gather its positions, then attend.         */
+/* ---------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *q, *k, *v;   /* q [T][Hq][D] */
+    int64_t num_blocks;
+    const int32_t *block_tables;
+    int32_t max_blocks, bs;
+    const int32_t *context_lens, *cu_q;
+    int32_t B, T, Hq, Hkv, D;
+    double scale;
+    double *out;                 /* [T][Hq][D] */
+    int32_t max_ctx;
+    int nthreads, tid, status;
+} prefill_job;
+
+static void *prefill_worker(void *arg)
+{
+    prefill_job *job = (prefill_job *)arg;
+    int64_t rows = job->max_ctx > 0 ? job->max_ctx : 1;
+    uint16_t *K = malloc((size_t)(rows * job->D) * sizeof(uint16_t));
+    uint16_t *V = malloc((size_t)(rows * job->D) * sizeof(uint16_t));
+    double *scores = malloc((size_t)rows * sizeof(double));
+    if (!K || !V || !scores) {
+        job->status = -2;
+        goto done;
+    }
+    int32_t group = job->Hq / job->Hkv;
+    int64_t work = (int64_t)job->T * job->Hq;
+    for (int64_t w = job->tid; w < work; w += job->nthreads) {
+        int32_t t = (int32_t)(w / job->Hq);
+        int32_t hq = (int32_t)(w % job->Hq);
+        int32_t kv_head = hq / group;
+        int32_t i = 0; /* the sequence whose chunk holds token t */
+        while (i + 1 < job->B && job->cu_q[i + 1] <= t)
+            ++i;
+        int32_t Lq = job->cu_q[i + 1] - job->cu_q[i];
+        int32_t ctx = job->context_lens[i];
+        int32_t pos = ctx - Lq + (t - job->cu_q[i]);
+        int32_t n = pos + 1; /* positions 0 .. pos */
+        double *o = job->out + w * job->D;
+        if (n <= 0 || n > ctx || (int64_t)ctx > (int64_t)job->max_blocks * job->bs) {
+            job->status = -1;
+            goto done;
+        }
+        const int32_t *row = job->block_tables + (int64_t)i * job->max_blocks;
+        int rc = pkv_oracle_gather_paged(job->k, job->num_blocks, row, n, job->Hkv, job->bs,
+                                         job->D, kv_head, K);
+        rc |= pkv_oracle_gather_paged(job->v, job->num_blocks, row, n, job->Hkv, job->bs,
+                                      job->D, kv_head, V);
+        if (rc != 0) {
+            job->status = -1;
+            goto done;
+        }
+        pkv_oracle_attend(job->q + w * job->D, K, V, n, job->D, job->scale, scores, o);
+    }
+done:
+    free(K);
+    free(V);
+    free(scores);
+    return NULL;
+}
+
+/* Paged causal prefill.  out is fp64 [T][Hq][D], T = cu_q[B].  Returns 0;
+ * -1 on a chunk longer than its context, a bad block id or a context beyond
+ * the table; -2 on an allocation failure; -3 on bad sizes. */
+int pkv_oracle_paged_prefill(const uint16_t *q, const uint16_t *k_cache,
+                             const uint16_t *v_cache, int64_t num_blocks,
+                             const int32_t *block_tables, int32_t max_blocks,
+                             const int32_t *context_lens, const int32_t *cu_q,
+                             int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t bs,
+                             double scale, double *out, int nthreads)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || bs <= 0 || Hq % Hkv != 0 || cu_q[0] != 0)
+        return -3;
+    prefill_job proto;
+    memset(&proto, 0, sizeof proto);
+    proto.q = q;
+    proto.k = k_cache;
+    proto.v = v_cache;
+    proto.num_blocks = num_blocks;
+    proto.block_tables = block_tables;
+    proto.max_blocks = max_blocks;
+    proto.bs = bs;
+    proto.context_lens = context_lens;
+    proto.cu_q = cu_q;
+    proto.B = B;
+    proto.T = cu_q[B];
+    proto.Hq = Hq;
+    proto.Hkv = Hkv;
+    proto.D = D;
+    proto.scale = scale;
+    proto.out = out;
+    for (int32_t i = 0; i < B; ++i) {
+        if (cu_q[i + 1] < cu_q[i])
+            return -3;
+        if (context_lens[i] > proto.max_ctx)
+            proto.max_ctx = context_lens[i];
+    }
+    if (nthreads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = n > 0 ? (int)n : 1;
+    }
+    prefill_job *jobs = calloc((size_t)nthreads, sizeof *jobs);
+    pthread_t *th = calloc((size_t)nthreads, sizeof *th);
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -2;
+    }
+    int launched = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = proto;
+        jobs[t].nthreads = nthreads;
+        jobs[t].tid = t;
+        if (nthreads == 1) {
+            prefill_worker(&jobs[t]);
+        } else if (pthread_create(&th[t], NULL, prefill_worker, &jobs[t]) != 0) {
+            jobs[t].status = -2;
+            break;
+        }
+        launched = t + 1;
+    }
+    int status = 0;
+    for (int t = 0; t < launched; ++t)
+        if (nthreads > 1)
+            pthread_join(th[t], NULL);
+    for (int t = 0; t < nthreads; ++t)
+        if (jobs[t].status != 0)
+            status = jobs[t].status;
+    free(jobs);
+    free(th);
+    return status;
+}
+
+/* ---------------------------------------------------------------------- */
 /* KV append ([VA4] Observation-1; [RC]): the new token t's K and V rows   */
 /* for every KV head go to slot_mapping[t], where a slot names physical     */
 /* block slot / bs and offset slot % bs (paged), or, with bs := S, request  */

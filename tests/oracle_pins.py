@@ -17,7 +17,10 @@ raise AssertionError when the oracle is wrong.
     section 5.2.3; "Running Out of Cache", block tables);
   * GQA: repeating each KV head G times (plain MHA) gives the same result;
   * append then gather finds the new token at the last position; untouched
-    bytes stay untouched; copy on write makes dst equal src.
+    bytes stay untouched; copy on write makes dst equal src;
+  * causal prefill: torch fp64 attention with an explicit causal mask; a
+    chunk of one token is the decode step; the last token of a chunk equals
+    decode; a query ignores later positions and depends on its own.
 """
 import math
 
@@ -303,6 +306,98 @@ def pin_block_copy(orc):
         untouched = [b for b in range(nb) if b not in pairs[:, 1]]
         assert np.array_equal(ks[l][untouched], k0[l][untouched])
         assert np.array_equal(vs[l][untouched], v0[l][untouched])
+
+
+# --------------------------------------------------------------------- prefill
+
+def _prefill_case(rng, ctx, lq, hq=8, hkv=2, bs=16, nb=None):
+    """A paged batch whose sequence i's last lq[i] positions are new tokens."""
+    ctx = np.asarray(ctx, np.int32)
+    need = (ctx + bs - 1) // bs
+    nb = nb or int(need.sum()) + 3
+    table = np.zeros((len(ctx), need.max()), np.int32)
+    ids = rng.permutation(nb)
+    pos = 0
+    for i, n in enumerate(need):
+        table[i, :n] = ids[pos:pos + n]
+        pos += n
+    kc, vc = _pool(rng, nb, hkv, bs), _pool(rng, nb, hkv, bs)
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    q = _rand_bf16(rng, (int(cu[-1]), hq, D))
+    return ctx, cu, table, kc, vc, q
+
+
+def pin_prefill_library_causal(orc):
+    """torch fp64 causal attention (explicit mask) on one sequence laid out
+    with an identity table: new token j at position ctx - lq + j sees
+    positions 0 .. ctx - lq + j."""
+    rng = np.random.default_rng(21)
+    bs, hkv, hq = 16, 2, 4
+    for ctx, lq in ((1, 1), (5, 5), (40, 7), (70, 33)):
+        nb = (ctx + bs - 1) // bs
+        table = np.arange(nb, dtype=np.int32)[None, :]
+        kc, vc = _pool(rng, nb, hkv, bs), _pool(rng, nb, hkv, bs)
+        q = _rand_bf16(rng, (lq, hq, D))
+        scale = 1 / math.sqrt(D)
+        out = orc.paged_prefill(q, kc, vc, table, np.array([ctx], np.int32),
+                                np.array([0, lq], np.int32), scale)
+        K = torch.from_numpy(_val(kc)).permute(1, 0, 2, 3).reshape(hkv, nb * bs, D)[:, :ctx]
+        V = torch.from_numpy(_val(vc)).permute(1, 0, 2, 3).reshape(hkv, nb * bs, D)[:, :ctx]
+        Q = torch.from_numpy(_val(q))                     # [lq, hq, D]
+        posn = torch.arange(ctx - lq, ctx)[:, None]       # query positions
+        mask = torch.arange(ctx)[None, :] > posn          # [lq, ctx]
+        for h in range(hq):
+            s = (Q[:, h] @ K[h // (hq // hkv)].T) * scale
+            s = s.masked_fill(mask, float("-inf"))
+            ref = torch.softmax(s, dim=1) @ V[h // (hq // hkv)]
+            assert np.allclose(out[:, h], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_prefill_chunk_of_one_is_decode(orc):
+    """A chunk of one new token per sequence is the decode step."""
+    rng = np.random.default_rng(22)
+    ctx, cu, table, kc, vc, q = _prefill_case(rng, [1, 16, 17, 100, 33], [1] * 5)
+    scale = 1 / math.sqrt(D)
+    a = orc.paged_prefill(q, kc, vc, table, ctx, cu, scale)
+    b = orc.paged_decode(q, kc, vc, table, ctx, scale)
+    assert np.array_equal(a, b)
+
+
+def pin_prefill_last_token_is_decode(orc):
+    """The last new token of each chunk attends the whole context, exactly
+    as the decode step with that context does."""
+    rng = np.random.default_rng(23)
+    lq = [3, 16, 1, 40]
+    ctx, cu, table, kc, vc, q = _prefill_case(rng, [3, 50, 17, 120], lq)
+    scale = 1 / math.sqrt(D)
+    a = orc.paged_prefill(q, kc, vc, table, ctx, cu, scale)
+    last = cu[1:] - 1
+    b = orc.paged_decode(q[last], kc, vc, table, ctx, scale)
+    assert np.array_equal(a[last], b)
+
+
+def pin_prefill_is_causal(orc):
+    """A query's output ignores every later position and depends on its own."""
+    rng = np.random.default_rng(24)
+    ctx, cu, table, kc, vc, q = _prefill_case(rng, [48], [20], hq=2, hkv=1)
+    scale = 1 / math.sqrt(D)
+    base = orc.paged_prefill(q, kc, vc, table, ctx, cu, scale)
+    bs = kc.shape[2]
+    j = 9                                   # query at position 48 - 20 + 9 = 37
+    p = 48 - 20 + j
+    later_k, later_v = kc.copy(), vc.copy()
+    for pos in range(p + 1, 48):            # change every later position
+        blk, off = table[0, pos // bs], pos % bs
+        later_k[blk, :, off] = _rand_bf16(rng, (kc.shape[1], D))
+        later_v[blk, :, off] = _rand_bf16(rng, (kc.shape[1], D))
+    out = orc.paged_prefill(q, later_k, later_v, table, ctx, cu, scale)
+    assert np.array_equal(out[:j + 1], base[:j + 1])
+    assert not np.array_equal(out[-1], base[-1])
+    own_v = vc.copy()
+    own_v[table[0, p // bs], :, p % bs] = _rand_bf16(rng, (kc.shape[1], D))
+    out2 = orc.paged_prefill(q, kc, own_v, table, ctx, cu, scale)
+    assert not np.array_equal(out2[j], base[j])
+    assert np.array_equal(out2[:j], base[:j])
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -39,6 +39,14 @@ MUTANTS = {
                     "memmove(v_caches[l] + src * block_elems,\n                    v_caches[l] + src * block_elems,"),
     "copy_direction": ("memmove(k_caches[l] + dst * block_elems,\n                    k_caches[l] + src * block_elems,",
                        "memmove(k_caches[l] + src * block_elems,\n                    k_caches[l] + dst * block_elems,"),
+    "prefill_causal_off_by_one": ("int32_t n = pos + 1; /* positions 0 .. pos */",
+                                  "int32_t n = pos; /* positions 0 .. pos */"),
+    "prefill_positions_from_zero": ("int32_t pos = ctx - Lq + (t - job->cu_q[i]);",
+                                    "int32_t pos = (t - job->cu_q[i]);"),
+    "prefill_gqa_interleaved": ("int32_t kv_head = hq / group;",
+                                "int32_t kv_head = hq % job->Hkv;"),
+    "prefill_wrong_sequence": ("while (i + 1 < job->B && job->cu_q[i + 1] <= t)",
+                               "while (i + 1 < job->B && job->cu_q[i + 1] < t)"),
     "bf16_widen_wrong": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
 }
 
