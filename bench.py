@@ -562,7 +562,54 @@ def measure_legs(wl, dev, args):
         "block_copy_gbs": round(copy_bytes / (t_copy / 1e3) / 1e9, 1),
         "block_copy_shape": "96 pairs x 60 layers x (K,V) of 32 KiB blocks (read + write)",
         "on_demand_contig": vmm,
+        "prefill": measure_prefill(wl, dev, reps),
     }
+
+
+def _bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops)"
+    return 1900.0, "fallback"
+
+
+def measure_prefill(wl, dev, reps):
+    """Causal prefill over a paged cache with the workload's head shape:
+    8 fresh prompts of 2048 tokens, and 8 chunks of 512 tokens after 1536
+    cached positions (random blocks, block_size 16).  Flops: 4 * D per
+    (query token, head, attended position)."""
+    pkv = wl.pkv
+    shape = wl.shape
+    peak, peak_src = _bf16_peak()
+    res = {}
+    for name, cached, lq in (("fresh_8x2048", 0, 2048), ("chunk_8x512_after_1536", 1536, 512)):
+        ctx = np.full(8, cached + lq, np.int32)
+        b = W.make_paged_batch(shape, ctx, 16, 250)
+        li = W.layer_inputs(b, 0, device=dev, fast_cache=True)
+        cu = torch.as_tensor(np.arange(0, 8 * lq + 1, lq, dtype=np.int32), device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(251)
+        q = torch.randn((8 * lq, shape.num_q_heads, shape.head_dim), generator=g,
+                        device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        tables = torch.as_tensor(b.block_tables, device=dev)
+        ctx_d = torch.as_tensor(b.ctx, device=dev)
+
+        def call():
+            pkv.paged_prefill_attention(q, cu, li.k_cache, li.v_cache, tables, ctx_d, lq,
+                                        W.default_scale(shape), out=out)
+
+        t = _time_graph(call, max(5, reps // 4), dev, calls=2)
+        attended = 8 * sum(cached + j + 1 for j in range(lq))  # per head
+        flops = 4.0 * shape.head_dim * shape.num_q_heads * attended
+        res[name] = {"us": round(t * 1e3, 2), "tflops": round(flops / (t / 1e3) / 1e12, 1),
+                     "frac_of_bf16_peak": round(flops / (t / 1e3) / 1e12 / peak, 3)}
+        del li
+    res["peak_tflops"] = peak
+    res["peak_source"] = peak_src
+    res["kernel"] = "prefill_kernel (mma.sync m16n8k16, 4 warps, 64 query rows per CTA)"
+    return res
 
 
 def measure_vmm(wl, dev, buf, S, req, reps):

@@ -226,6 +226,31 @@ PKV_API pkv_status pkv_paged_decode_attention_shared(
     pkv_heads heads, void *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Causal prefill attention over a paged cache (chunked prefill).  The pages
+ * name prefill only as a serving phase ("Insights into LLM Serving Systems:
+ * KV-Cache Memory Allocation Patterns", section headings); the reading here
+ * is the standard one.  Sequence i's chunk of new tokens is rows
+ * cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 of q (device int32 [num_seqs + 1],
+ * cu_seqlens_q[0] = 0, cu_seqlens_q[num_seqs] = num_tokens) and holds the
+ * last Lq_i of its context_lens[i] positions; their K and V rows must already
+ * be in the cache (pkv_kv_append).  New token j of sequence i, at position
+ * ctx_i - Lq_i + j, gives
+ *   out[row][h] = sum_{p <= ctx_i - Lq_i + j} softmax_p(scale * q[row][h] . K_p) V_p
+ * with K_p, V_p found through block_tables[i] as in pkv_paged_decode_attention
+ * (a chunk of one token is exactly that call).  q, out: bf16 [num_tokens][Hq][128].
+ * max_q_tokens is a host bound on every chunk's length (it sizes the grid);
+ * block_size must be a multiple of 16.  Accumulation in fp32, output bf16.
+ * Checked mode reports a chunk longer than its context or than max_q_tokens,
+ * or a context beyond the block table (PKV_DEVERR_CONTEXT), and bad block ids.
+ */
+PKV_API pkv_status pkv_paged_prefill_attention(
+    const void *q, const int32_t *cu_seqlens_q, int32_t num_tokens,
+    const void *k_cache, const void *v_cache, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *context_lens,
+    int32_t num_seqs, int32_t max_q_tokens, int32_t block_size, float scale,
+    pkv_heads heads, void *out, void *stream);
+
+/*
  * Copy-on-write block copy.  "Running Out of Cache" (section "Fragmentation
  * is lost users") and the PagedAttention summary: sequences share physical
  * blocks and copy a block only when one of them writes into it.

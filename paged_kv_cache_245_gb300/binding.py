@@ -29,7 +29,7 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
             "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
             "pkv_debug_gather_contig", "pkv_paged_decode_attention_shared",
-            "pkv_shared_decode_workspace_size",
+            "pkv_shared_decode_workspace_size", "pkv_paged_prefill_attention",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -71,6 +71,8 @@ def lib():
                                         ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_contig_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
                                          ctypes.c_float, Heads, vp, vp, sz, vp]
+    L.pkv_paged_prefill_attention.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32,
+                                              i32, ctypes.c_float, Heads, vp, vp]
     L.pkv_shared_decode_workspace_size.argtypes = [i32, i32, i32, i32, Heads]
     L.pkv_shared_decode_workspace_size.restype = sz
     L.pkv_paged_decode_attention_shared.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
@@ -330,6 +332,32 @@ def paged_decode_attention_shared(q, k_cache, v_cache, block_tables, context_len
         _ptr(context_lens), B, int(max_context), bs, _ptr(group_start), _ptr(shared_blocks), G,
         int(max_group_size), int(max_own_tokens), float(scale), h, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(q)))
+    return out
+
+
+def paged_prefill_attention(q, cu_seqlens_q, k_cache, v_cache, block_tables, context_lens,
+                            max_q_tokens, scale, out=None):
+    """Causal prefill: q [T, Hq, D] packs every sequence's chunk of new tokens
+    (sequence i: rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1, the last
+    positions of its context_lens[i]; their K/V already appended)."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    B = context_lens.shape[0]
+    if cu_seqlens_q.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("cu_seqlens_q must have num_seqs + 1 entries, block_tables num_seqs rows")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    _check(lib().pkv_paged_prefill_attention(
+        _ptr(q), _ptr(cu_seqlens_q), T, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], nb, _ptr(context_lens), B, int(max_q_tokens), bs, float(scale),
+        heads(hq, hkv, d), _ptr(out), _stream(q)))
     return out
 
 

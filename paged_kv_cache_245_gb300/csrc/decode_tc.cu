@@ -26,6 +26,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+}  // namespace
+
 // [rows][128] bf16 viewed as a 2-D tensor; boxes of 16 rows x 64 columns
 // (128 bytes), 128-byte swizzle.
 bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
@@ -41,6 +43,8 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <bool kContig, int W, int S, int NT = 1>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,

@@ -2,6 +2,7 @@
 // path (decode_tc.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -148,6 +149,10 @@ __host__ __device__ inline bool tc_boundary_pair(int bnd, const int32_t* prefix,
   *cl = static_cast<int>(tc_owner(u0 + n - 1, V, P));
   return *cf + 1 == bnd;
 }
+
+// A TMA tensor map over a K or V cache viewed as [rows][128] bf16: boxes of
+// 16 rows x 64 columns, 128-byte swizzle.  False if the driver refuses it.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows);
 
 // Workspace bytes for the per-CTA partial records.
 size_t tc_workspace_bytes(int num_ctas);

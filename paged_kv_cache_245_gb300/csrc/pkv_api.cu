@@ -11,6 +11,7 @@
 #include "../../include/pkv.h"
 #include "decode_launch.cuh"
 #include "cascade.cuh"
+#include "prefill.cuh"
 #include "decode_tc_launch.h"
 #include "kv_ops.cuh"
 
@@ -606,6 +607,67 @@ pkv_status pkv_paged_decode_attention_shared(
   }
   ce = pkv::launch_cascade_merge(c, s);
   if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing merge launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_q,
+                                       int32_t num_tokens, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, int32_t num_blocks,
+                                       const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t max_q_tokens, int32_t block_size, float scale,
+                                       pkv_heads heads, void* out, void* stream) {
+  pkv_status st = check_heads(heads);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || max_q_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (num_seqs == 0 || num_tokens == 0 || max_q_tokens == 0) return PKV_OK;
+  if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_seqs > 65535");
+  if (!q || !cu_seqlens_q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PKV_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(PKV_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  if (!aligned(cu_seqlens_q, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return fail(PKV_ERR_INVALID_ARG, "int32 arrays misaligned");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (block_size <= 0 || block_size % 16 != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "prefill needs block_size %% 16 == 0");
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "empty block table or pool");
+  const int64_t rows_total = static_cast<int64_t>(num_blocks) * heads.num_kv_heads * block_size;
+  if (rows_total > 0x7fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "cache of 2^31 rows or more");
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return fail(PKV_ERR_UNSUPPORTED, "block table longer than 2^31 positions");
+  const int32_t G = heads.num_q_heads / heads.num_kv_heads;
+  if ((static_cast<int64_t>(max_q_tokens) * G + 63) / 64 > 0x7fffffffLL)
+    return fail(PKV_ERR_UNSUPPORTED, "chunk too long");
+  int dev = 0;
+  int* err = nullptr;
+  st = device_info(&dev, &err, nullptr);
+  if (st != PKV_OK) return st;
+  alignas(64) CUtensorMap tk;
+  alignas(64) CUtensorMap tv;
+  if (!pkv::encode_rows(&tk, k_cache, rows_total) || !pkv::encode_rows(&tv, v_cache, rows_total))
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
+  pkv::PrefillParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = static_cast<uint16_t*>(out);
+  p.cu_q = cu_seqlens_q;
+  p.ctx_lens = context_lens;
+  p.block_tables = block_tables;
+  p.bs = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.Hq = heads.num_q_heads;
+  p.Hkv = heads.num_kv_heads;
+  p.G = G;
+  p.max_q = max_q_tokens;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e)
+  p.checked = g_checked.load();
+  p.err = err;
+  const cudaError_t e = pkv::launch_prefill(tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PKV_OK;
 }
 

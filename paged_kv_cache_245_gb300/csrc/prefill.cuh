@@ -1,0 +1,30 @@
+// prefill.cuh -- parameters and launcher of causal prefill attention over a
+// paged KV cache (prefill.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct PrefillParams {
+  const uint16_t* q;             // [T][Hq][128] the chunks' new tokens, packed
+  uint16_t* out;                 // [T][Hq][128]
+  const int32_t* cu_q;           // [B + 1] chunk boundaries in q
+  const int32_t* ctx_lens;       // [B] positions after the chunk (cached + new)
+  const int32_t* block_tables;   // [B][max_blocks]
+  int64_t bs;                    // block size, a multiple of 16
+  int64_t num_blocks;
+  int32_t max_blocks, num_seqs, Hq, Hkv, G;
+  int32_t max_q;                 // host bound on any chunk's length
+  float qscale;                  // scale * log2(e)
+  int32_t checked;
+  int* err;
+};
+
+// One CTA per (64 query rows, KV head, sequence).
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           cudaStream_t stream);
+
+}  // namespace pkv

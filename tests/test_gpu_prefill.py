@@ -1,0 +1,89 @@
+"""Causal prefill over a paged cache (pkv_paged_prefill_attention) against
+the oracle: every group size, several block sizes, chunks from one token to
+several tiles over cached contexts of any length (and fresh prompts), a
+chunk of one token against the decode kernel, and checked mode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_245_gb300 as pkv
+import workloads as W
+from parity import assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _reset_modes():
+    pkv.set_checked(False)
+    yield
+    pkv.set_checked(False)
+    torch.cuda.synchronize()
+
+
+def _case(hq, hkv, cached, lq, bs, seed):
+    """Paged K/V holding every sequence's full context (cached + chunk), the
+    chunks' queries packed by cu_seqlens_q."""
+    shape = W.ModelShape("p%d_%d" % (hq, hkv), 1, hq, hkv)
+    ctx = np.asarray(cached, np.int32) + np.asarray(lq, np.int32)
+    b = W.make_paged_batch(shape, ctx, bs, seed, spare_blocks=3)
+    li = W.layer_inputs(b, 0, device="cpu")
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((int(cu[-1]), hq, 128), generator=g).to(torch.bfloat16)
+    return b, li, q, cu
+
+
+def _gpu(b, li, q, cu):
+    return pkv.paged_prefill_attention(
+        q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV), li.v_cache.to(DEV),
+        torch.as_tensor(b.block_tables, device=DEV), torch.as_tensor(b.ctx, device=DEV),
+        int(np.diff(cu).max()), W.default_scale(b.shape))
+
+
+def _oracle(b, li, q, cu):
+    return oracle.paged_prefill(W.to_u16(q), W.to_u16(li.k_cache), W.to_u16(li.v_cache),
+                                b.block_tables, b.ctx, cu, W.default_scale(b.shape))
+
+
+@pytest.mark.parametrize("bs", [16, 32, 128])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (32, 8), (16, 2)])
+def test_chunks_against_oracle(hq, hkv, bs):
+    cached = [0, 3, 100, 64, 17, 0]
+    lq = [1, 5, 64, 65, 130, 33]
+    b, li, q, cu = _case(hq, hkv, cached, lq, bs, seed=hq * 7 + hkv + bs)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu),
+                           "prefill G=%d bs=%d" % (hq // hkv, bs))
+
+
+def test_llama_shaped_chunked_prefill():
+    b, li, q, cu = _case(32, 8, [256, 44], [256, 256], 16, seed=91)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "llama chunks")
+
+
+def test_chunk_of_one_token_is_the_decode_call():
+    b, li, q, cu = _case(32, 8, [0, 16, 99, 700], [1, 1, 1, 1], 16, seed=92)
+    out = _gpu(b, li, q, cu)
+    dec = pkv.paged_decode_attention(q.to(DEV), li.k_cache.to(DEV), li.v_cache.to(DEV),
+                                     torch.as_tensor(b.block_tables, device=DEV),
+                                     torch.as_tensor(b.ctx, device=DEV), b.max_context,
+                                     W.default_scale(b.shape))
+    ref = _oracle(b, li, q, cu)
+    assert_attention_close(out, ref, "prefill, chunks of one")
+    assert_attention_close(dec, ref, "decode")
+
+
+def test_checked_mode_reports_a_chunk_longer_than_its_context():
+    pkv.set_checked(True)
+    b, li, q, cu = _case(8, 2, [10, 10], [4, 4], 16, seed=93)
+    bad_ctx = b.ctx.copy()
+    bad_ctx[1] = 2                       # shorter than its 4-token chunk
+    assert pkv.get_device_error() == "none"
+    pkv.paged_prefill_attention(q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV),
+                                li.v_cache.to(DEV), torch.as_tensor(b.block_tables, device=DEV),
+                                torch.as_tensor(bad_ctx, device=DEV), 4, W.default_scale(b.shape))
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "context"
