@@ -188,13 +188,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# The sources the attention call's kernels (decode_tc_kernel and its
+# combine) are built from; the DRAM counters of a profile summary stand for
+# the kernel only while these are unchanged.
+DECODE_SOURCES = ("decode_tc.cu", "decode_tc.cuh", "decode_tc_launch.h", "pkv_device.cuh")
+
+
 def _source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_245_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in DECODE_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
