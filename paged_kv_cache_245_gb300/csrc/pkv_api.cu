@@ -638,7 +638,7 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
     return fail(PKV_ERR_UNSUPPORTED, "block table longer than 2^31 positions");
   const int32_t G = heads.num_q_heads / heads.num_kv_heads;
-  if ((static_cast<int64_t>(max_q_tokens) * G + 63) / 64 > 0x7fffffffLL)
+  if ((static_cast<int64_t>(max_q_tokens) * G + 255) / 256 > 0x7fffffffLL)
     return fail(PKV_ERR_UNSUPPORTED, "chunk too long");
   int dev = 0;
   int* err = nullptr;

@@ -1,4 +1,6 @@
-// prefill.cu -- causal prefill attention over a paged KV cache (sm_103a).
+// prefill.cu -- causal prefill attention over a paged KV cache on the
+// fifth-generation tensor cores (tcgen05: operands in shared or tensor
+// memory, fp32 accumulators in tensor memory).
 //
 // Sequence i's chunk of Lq new tokens (rows cu_q[i] .. cu_q[i+1]-1 of q, whose
 // K and V rows are already in the cache) holds the last Lq of its ctx
@@ -6,20 +8,31 @@
 // 0 .. ctx - Lq + j ("Running Out of Cache": a block table maps positions to
 // blocks; a chunk of one token is the decode step).
 //
-// Work: one CTA of 4 warps per (64 query rows, KV head, sequence).  The rows
-// are the chunk's (token, query head) pairs of the KV head's group, token
-// major (row r: token r / G, head r % G), so every K/V tile serves the whole
-// group; warp w owns rows 16w .. 16w+15.  Keys come in tiles of 64 positions
-// (four 16-position runs, each inside one block) through the TMA engine --
-// 2-D tensor maps over the cache rows, 128-byte swizzled boxes of 16 rows x
-// 64 columns -- into a 3-stage ring shared by the CTA.
+// Work: one CTA per (256 query rows, KV head, sequence).  The rows are the
+// chunk's (token, query head) pairs of the KV head's group, token major (row
+// r: token r / G, head r % G), so every K/V tile serves the whole group.  The
+// CTA's rows form two tiles of 128 (the M of one tcgen05.mma), each with its
+// own softmax warpgroup; one warp streams K/V, one warp issues the MMAs:
 //
-// Math per warp and key tile, on tensor cores (mma.m16n8k16, bf16 in, fp32
-// accumulate): S = Q K^T (16 x 64: 8 n-tiles x 8 k-steps; K from ldmatrix),
-// causal mask, online softmax in base 2, then O += P V with P taken straight
-// from the S accumulators as the A operand and V^T from ldmatrix.trans.  V
-// rows at or past the context are zeroed in shared memory first, so stale
-// bytes never reach P V.
+//   warps 0-3  softmax of row tile 0      warps 4-7  softmax of row tile 1
+//   warp 8     K/V tiles of 128 keys by TMA (2-D maps over the cache rows,
+//              128-byte swizzled boxes of 16 rows x 64 columns, one 16-key
+//              run per block-table entry) into a 2-stage ring
+//   warp 9     tensor-memory owner and MMA issuer (one thread)
+//
+// Tensor memory (512 columns, lane = query row of the tile): S_t = Q_t K^T in
+// columns 128t .. 128t+127, O_t in columns 256 + 128t ..  For key tile j the
+// MMA thread issues PV_0(j) S_0(j+1) | PV_1(j) S_1(j+1), so the tensor cores
+// run one row tile's products while the other tile's softmax runs.  The
+// softmax thread of row r reads its row of S, masks keys past its position
+// and writes P = 2^(S * scale * log2 e - m) as packed bf16 pairs over the
+// first 64 columns of S in place; PV_t(j) takes P straight from tensor memory
+// (A operand) and V from shared memory (MN-major B operand).  The running
+// maximum m is updated lazily: O and l are rescaled only when a row's
+// maximum grows by more than 8 (a factor 2^8), so P stays below 256 and most
+// tiles skip the rescale.  The MMAs of one thread complete in issue order, so
+// the barrier that reports S_t(j+1) also reports PV_t(j): from then on the
+// softmax warps own O_t until they hand P_t(j+1) over.
 #include "pkv_device.cuh"
 #include "prefill.cuh"
 
@@ -27,47 +40,181 @@ namespace pkv {
 
 namespace {
 
-constexpr int kPfWarps = 4;
-constexpr int kPfRows = 16 * kPfWarps;     // query rows per CTA
-constexpr int kPfKeys = 64;                // keys per tile
-constexpr int kPfStages = 3;
-constexpr int kPfStageBytes = 2 * kPfKeys * kRowBytes;  // K then V: 32 KiB
-constexpr int kPfBox = 2048;               // 16 rows x 128 B
-constexpr int kPfSmem = kPfStages * kPfStageBytes + kPfStages * 8 + 1024;
+constexpr int kRowTile = 128;                         // query rows per tile (MMA M)
+constexpr int kKeys = 128;                            // keys per K/V tile
+constexpr int kStages = 2;
+constexpr int kOpBytes = 128 * kRowBytes;             // 32 KiB: a Q, K or V tile
+constexpr int kHalfBytes = kOpBytes / 2;              // one 64-column half
+constexpr int kRunBytes = 16 * 128;                   // one TMA box: 16 rows x 128 B
+constexpr int kOffK = 2 * kOpBytes;                   // after Q_0, Q_1
+constexpr int kStageBytes = 2 * kOpBytes;             // K then V
+constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 192 KiB
+constexpr int kSmemBytes = kTilesBytes + 256 + 1024;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kRescaleLog2 = 8.f;
+
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
+// 4-5), bf16 A and B (7-9, 10-12), N / 8 (17-22), M / 16 (24-28); A K-major;
+// B K-major for S = Q K^T, MN-major (bit 16) for O = P V, whose V rows hold
+// the N (head) dimension contiguously.
+constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                             ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
+
+// Shared-memory matrix descriptor with 128-byte swizzling: start address,
+// leading and stride byte offsets (all / 16), the fixed 0b001 at bits 46-48
+// and the swizzle mode at 61-63.  K-major operands: 1024 bytes between
+// 8-row groups, leading offset unused.  The MN-major V: leading offset = the
+// step between the two 64-column halves, stride = 1024 bytes per 8 keys.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+#define PKV_R32(F, r)                                                                          \
+  F(r[0]), F(r[1]), F(r[2]), F(r[3]), F(r[4]), F(r[5]), F(r[6]), F(r[7]), F(r[8]), F(r[9]),    \
+      F(r[10]), F(r[11]), F(r[12]), F(r[13]), F(r[14]), F(r[15]), F(r[16]), F(r[17]),          \
+      F(r[18]), F(r[19]), F(r[20]), F(r[21]), F(r[22]), F(r[23]), F(r[24]), F(r[25]),          \
+      F(r[26]), F(r[27]), F(r[28]), F(r[29]), F(r[30]), F(r[31])
+#define PKV_OUT(x) "=r"(x)
+#define PKV_IN(x) "r"(x)
+#define PKV_INOUT(x) "+r"(x)
+#define PKV_LIST32                                                                             \
+  "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24," \
+  "%25,%26,%27,%28,%29,%30,%31"
+
+// 32 consecutive 32-bit columns of this warp's 32 lanes (lane = thread).  The
+// registers are valid only after tmem_wait_ld / tmem_ready on them.
+__device__ __forceinline__ void tmem_ld32(uint32_t (&r)[32], uint32_t taddr) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {" PKV_LIST32 "}, [%32];"
+               : PKV_R32(PKV_OUT, r)
+               : "r"(taddr));
+}
+
+// Wait for this thread's tensor-memory loads; the registers named here (and
+// through tmem_ready, any others loaded before the wait) are then valid.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PKV_R32(PKV_INOUT, r) : : "memory");
+}
+__device__ __forceinline__ void tmem_ready(uint32_t (&r)[32]) {
+  asm volatile("" : PKV_R32(PKV_INOUT, r) : : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+               "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,"
+               "%31,%32};" ::"r"(taddr),
+               PKV_R32(PKV_IN, r)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Wait for phase `parity` of `bar`; give up when another role has given up
+// (*abort) or after kWaitLimitNs (then set *abort and record the timeout).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_error(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Byte offset of 16-byte chunk c (0..15) of row r in a 128-row operand tile
+// stored as two 64-column halves of 128-byte rows, 128-byte swizzled (the
+// layout the TMA engine writes for the 16 x 64 boxes).
+__device__ __forceinline__ int tile_chunk_offset(int r, int c) {
+  return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
 
 }  // namespace
 
-__global__ void __launch_bounds__(kPfWarps * 32, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
-  constexpr unsigned kFull = 0xffffffffu;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPfStages * kPfStageBytes);
-  __shared__ int32_t s_entry[kPfStages][kPfKeys / 16];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTilesBytes);
+  uint64_t* kfull = bars;        // [2] K of a stage landed
+  uint64_t* vfull = bars + 2;    // [2] V of a stage landed
+  uint64_t* kvempty = bars + 4;  // [2] every MMA reading a stage completed
+  uint64_t* sfull = bars + 6;    // [2] S_t of the current key tile (and PV_t before it) done
+  uint64_t* pfull = bars + 8;    // [2] P_t written (one arrival per row)
+  uint64_t* ofull = bars + 10;   // [2] the last PV_t completed
+  uint64_t* qfull = bars + 12;   // Q_0, Q_1 in shared memory (one arrival per row)
+  uint64_t* drain = bars + 13;   // wind-down after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 15);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int g = lane >> 2;
-  const int tq = lane & 3;
   const int i = blockIdx.z;
   const int kvh = blockIdx.y;
   const int rt = gridDim.x - 1 - blockIdx.x;  // latest (heaviest) rows first
   const int G = p.G;
 
-  if (tid == 0) {
-    for (int s = 0; s < kPfStages; ++s) mbar_init(&bars[s], 1);
-    fence_barrier_init();
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-  }
   grid_dependency_wait();
   grid_dependency_trigger();
 
   const int q0 = p.cu_q[i];
   const int Lq = p.cu_q[i + 1] - q0;
-  int ctx = p.ctx_lens[i];
+  const int ctx = p.ctx_lens[i];
   if (p.checked) {
     const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.bs;
     if (Lq < 0 || Lq > p.max_q || ctx < Lq || ctx > cap) {
@@ -76,223 +223,305 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2)
     }
   }
   const int rows = Lq * G;
-  const int row0 = rt * kPfRows;
+  const int row0 = rt * 2 * kRowTile;
   if (row0 >= rows) return;  // this CTA's rows lie past the chunk (uniform)
   const int base = ctx - Lq;  // position of the chunk's first token
-  // keys this CTA needs: up to the position of its last valid row
-  const int last_row = min(row0 + kPfRows, rows) - 1;
-  const int kend = base + last_row / G + 1;
-  const int ntiles = (kend + kPfKeys - 1) / kPfKeys;
+  const int last_row = min(row0 + 2 * kRowTile, rows) - 1;
+  const int kend = base + last_row / G + 1;  // keys this CTA needs
+  if (kend <= 0) return;  // only when ctx < Lq (caught in checked mode)
+  const int ntiles = (kend + kKeys - 1) / kKeys;
 
-  const uint64_t policy = l2_policy_evict_first();
+  if (tid == 0) {
+    for (int b = 0; b < 12; ++b) mbar_init(&bars[b], (b == 8 || b == 9) ? kRowTile : 1);
+    mbar_init(qfull, 2 * kRowTile);
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t smem_base = smem_addr(smem);
 
-  // ---- producer (thread 0): tile t into stage t % kPfStages
-  auto issue = [&](int t) {
-    const int stage = t % kPfStages;
-    unsigned char* st = smem + stage * kPfStageBytes;
-    if (lane < kPfKeys / 16) {  // warp 0: block-table entries of the 4 runs
-      const int pos = t * kPfKeys + lane * 16;
-      int32_t e = 0;
-      if (pos < ctx) {
+  if (warp < 8) {
+    // ================= softmax warpgroups =================
+    const int t = warp >> 2;                        // row tile
+    const int lr = tid & (kRowTile - 1);            // row in the tile = tensor-memory lane
+    const int r = row0 + t * kRowTile + lr;         // row of the chunk
+    const bool valid = r < rows;
+    const int rr = valid ? r : rows - 1;            // padding rows mirror the last row
+    const int tok = rr / G;
+    const int head = kvh * G + rr % G;
+    const int pos = base + tok;
+    const int64_t qrow = (static_cast<int64_t>(q0) + tok) * p.Hq + head;
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim);
+      unsigned char* dst = smem + t * kOpBytes;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = valid ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(dst + tile_chunk_offset(lr, c)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(qfull);
+    }
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + t * 128;
+    const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
+    const float sc = p.qscale;
+    float m_used = -INFINITY;  // the maximum P is taken against (scaled logits)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      ok = __all_sync(kFull, wait_or_abort(&sfull[t], j & 1, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = j * kKeys;
+      const bool diag = k0 + kKeys - 1 > pos;  // some key of the tile lies past the row
+      // pass 1: the row maximum of the scaled, masked logits
+      float mx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[32], b[32];
+        tmem_ld32(a, s_tm + 64 * h);
+        tmem_ld32(b, s_tm + 64 * h + 32);
+        tmem_wait_ld(a);
+        tmem_ready(b);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float x = __uint_as_float(c < 32 ? a[c] : b[c - 32]) * sc;
+          mx[c & 7] = fmaxf(mx[c & 7], !diag || k0 + 64 * h + c <= pos ? x : -INFINITY);
+        }
+      }
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m_used, tmax);
+      if (j == 0) {
+        m_used = m_new;  // finite: position 0 is visible to every row
+      } else {
+        const bool grow = m_new > m_used + kRescaleLog2;
+        if (__any_sync(kFull, grow)) {
+          const float alpha = grow ? fast_exp2(m_used - m_new) : 1.f;
+          if (grow) {
+            l *= alpha;
+            m_used = m_new;
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+            uint32_t w[32];
+            tmem_ld32(w, o_tm + c0);
+            tmem_wait_ld(w);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * alpha);
+            tmem_st32(o_tm + c0, w);
+          }
+        }
+      }
+      // pass 2: P = 2^(s * scale - m) as bf16 pairs over the columns already read
+      const float neg_m = -m_used;
+      float ls[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[32], b[32];
+        tmem_ld32(a, s_tm + 64 * h);
+        tmem_ld32(b, s_tm + 64 * h + 32);
+        tmem_wait_ld(a);
+        tmem_ready(b);
+        // keys of this half the row sees: bit c of (lo, hi) for key 64h + c
+        const int seen = diag ? min(max(pos - k0 - 64 * h + 1, 0), 64) : 64;
+        const uint32_t lo = seen >= 32 ? 0xffffffffu : (1u << seen) - 1u;
+        const uint32_t hi = seen >= 64 ? 0xffffffffu : (seen <= 32 ? 0u : (1u << (seen - 32)) - 1u);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
+          const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
+          float e0 = fast_exp2(fmaf(__uint_as_float(u0), sc, neg_m));
+          float e1 = fast_exp2(fmaf(__uint_as_float(u1), sc, neg_m));
+          const uint32_t bits = c < 16 ? lo : hi;
+          e0 = (bits >> ((2 * c) & 31)) & 1u ? e0 : 0.f;
+          e1 = (bits >> ((2 * c + 1) & 31)) & 1u ? e1 : 0.f;
+          ls[c & 7] += e0 + e1;
+          pk[c] = pack_bf16x2(e0, e1);
+        }
+        tmem_st32(s_tm + 32 * h, pk);
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&pfull[t]);
+    }
+    if (ok) ok = __all_sync(kFull, wait_or_abort(&ofull[t], 0, abort, p.err));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * kHeadDim);
+#pragma unroll
+      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(w, o_tm + c0);
+        tmem_wait_ld(w);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]) * inv, __uint_as_float(w[8 * q + 1]) * inv);
+            o.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]) * inv, __uint_as_float(w[8 * q + 3]) * inv);
+            o.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]) * inv, __uint_as_float(w[8 * q + 5]) * inv);
+            o.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]) * inv, __uint_as_float(w[8 * q + 7]) * inv);
+            dst[c0 / 8 + q] = o;
+          }
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // ================= K/V producer =================
+    // Every row tile of the sequence and KV head reads the same K/V tiles:
+    // keep them in L2 for the CTAs that follow.
+    const uint64_t policy = l2_policy_evict_last();
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j & 1;
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&kvempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
+        break;
+      const int pos = j * kKeys + lane * 16;  // run `lane` (lanes 0-7)
+      int32_t e = -1;
+      if (lane < kKeys / 16 && pos < ctx) {
         e = p.block_tables[static_cast<int64_t>(i) * p.max_blocks + pos / p.bs];
         if (p.checked && (e < 0 || e >= p.num_blocks)) {
           record_error(p.err, kErrBlockId);
           e = -1;  // skip the copy: stale rows, undefined output, no fault
         }
-      } else {
-        e = -1;
       }
-      s_entry[stage][lane] = e;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      uint32_t bytes = 0;
-      for (int r = 0; r < kPfKeys / 16; ++r)
-        if (s_entry[stage][r] >= 0) bytes += 4 * kPfBox;
-      mbar_arrive_expect_tx(&bars[stage], bytes);
-      for (int r = 0; r < kPfKeys / 16; ++r) {
-        const int32_t e = s_entry[stage][r];
-        if (e < 0) continue;
-        const int pos = t * kPfKeys + r * 16;
+      const uint32_t runs = __popc(__ballot_sync(kFull, e >= 0));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&kfull[s], runs * 2 * kRunBytes);
+        mbar_arrive_expect_tx(&vfull[s], runs * 2 * kRunBytes);
+      }
+      __syncwarp();
+      if (e >= 0) {
         const int32_t y = static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, pos % p.bs));
-        unsigned char* kd = st + r * 2 * kPfBox;
-        unsigned char* vd = st + kPfKeys * kRowBytes + r * 2 * kPfBox;
-        tma_load_2d(kd, &tmk, 0, y, &bars[stage], policy);
-        tma_load_2d(kd + kPfBox, &tmk, 64, y, &bars[stage], policy);
-        tma_load_2d(vd, &tmv, 0, y, &bars[stage], policy);
-        tma_load_2d(vd + kPfBox, &tmv, 64, y, &bars[stage], policy);
+        unsigned char* kd = smem + kOffK + s * kStageBytes + lane * kRunBytes;
+        unsigned char* vd = kd + kOpBytes;
+        tma_load_2d(kd, &tmk, 0, y, &kfull[s], policy);
+        tma_load_2d(kd + kHalfBytes, &tmk, 64, y, &kfull[s], policy);
+        tma_load_2d(vd, &tmv, 0, y, &vfull[s], policy);
+        tma_load_2d(vd + kHalfBytes, &tmv, 64, y, &vfull[s], policy);
+      }
+      issued = j + 1;
+    }
+    if (*abort && lane == 0) {
+      // let the copies in flight land before the CTA's shared memory is released
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        mbar_wait_bounded(&kfull[j & 1], (j >> 1) & 1);
+        mbar_wait_bounded(&vfull[j & 1], (j >> 1) & 1);
       }
     }
-  };
-  int issued = 0;  // tiles issued so far (tracked by warp 0)
-  if (warp == 0)
-    for (; issued < kPfStages && issued < ntiles; ++issued) issue(issued);
-
-  // ---- this warp's 16 query rows: A fragments of Q for the 8 k-steps
-  const int ra = row0 + warp * 16 + g;  // rows g and g + 8 of the warp
-  const int rb = ra + 8;
-  const bool va = ra < rows, vb = rb < rows;
-  const int pa = va ? base + ra / G : -1;  // query positions (-1: padding row)
-  const int pb = vb ? base + rb / G : -1;
-  uint32_t qa[8][4];
-  {
-    const uint32_t* qra = reinterpret_cast<const uint32_t*>(
-        p.q + (static_cast<int64_t>(q0 + (va ? ra / G : 0)) * p.Hq + kvh * G + (va ? ra % G : 0)) *
-                  kHeadDim);
-    const uint32_t* qrb = reinterpret_cast<const uint32_t*>(
-        p.q + (static_cast<int64_t>(q0 + (vb ? rb / G : 0)) * p.Hq + kvh * G + (vb ? rb % G : 0)) *
-                  kHeadDim);
+  } else {
+    // ================= MMA issuer (warp 9, lane 0 issues) =================
+    auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+      const uint32_t q_addr = smem_base + t * kOpBytes;
+      const uint32_t k_addr = smem_base + kOffK + (j & 1) * kStageBytes;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = va ? __ldg(qra + ks * 8 + tq) : 0u;
-      qa[ks][1] = vb ? __ldg(qrb + ks * 8 + tq) : 0u;
-      qa[ks][2] = va ? __ldg(qra + ks * 8 + 4 + tq) : 0u;
-      qa[ks][3] = vb ? __ldg(qrb + ks * 8 + 4 + tq) : 0u;
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        umma_ss(tmem + t * 128, smem_desc(q_addr + off, 16, 1024),
+                smem_desc(k_addr + off, 16, 1024), kIdescS, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int t, int j) {  // O_t (+)= P_t V_j
+      const uint32_t v_addr = smem_base + kOffK + (j & 1) * kStageBytes + kOpBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                smem_desc(v_addr + kk * 16 * 128, kHalfBytes, 1024), kIdescPV, (j > 0 || kk > 0));
+    };
+    bool ok = __all_sync(kFull, wait_or_abort(qfull, 0, abort, p.err));
+    if (ok) ok = __all_sync(kFull, wait_or_abort(&kfull[0], 0, abort, p.err));
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, 0);
+        umma_commit(&sfull[0]);
+        issue_s(1, 0);
+        umma_commit(&sfull[1]);
+      }
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int s = j & 1;
+      ok = __all_sync(kFull, wait_or_abort(&vfull[s], (j >> 1) & 1, abort, p.err));
+      if (!ok) break;
+      const int k0 = j * kKeys;
+      if (k0 + kKeys > ctx) {  // zero V rows at or past the context (0 x stale bytes)
+        unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
+        const int first = ctx - k0;
+        for (int idx = lane; idx < (kKeys - first) * 16; idx += 32)
+          *reinterpret_cast<uint4*>(vt + tile_chunk_offset(first + (idx >> 4), idx & 15)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      const bool more = j + 1 < ntiles;
+      ok = __all_sync(kFull, wait_or_abort(&pfull[0], j & 1, abort, p.err));
+      if (ok && more)
+        ok = __all_sync(kFull, wait_or_abort(&kfull[s ^ 1], ((j + 1) >> 1) & 1, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(0, j);
+        if (more) {
+          issue_s(0, j + 1);
+          umma_commit(&sfull[0]);
+        } else {
+          umma_commit(&ofull[0]);
+        }
+      }
+      __syncwarp();
+      ok = __all_sync(kFull, wait_or_abort(&pfull[1], j & 1, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(1, j);
+        if (j + kStages < ntiles) umma_commit(&kvempty[s]);  // the producer reuses the stage
+        if (more) {
+          issue_s(1, j + 1);
+          umma_commit(&sfull[1]);
+        } else {
+          umma_commit(&ofull[1]);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // let the MMAs in flight finish before tensor memory is released
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0);
     }
   }
 
-  // per-lane ldmatrix offsets in a 128-byte-swizzled 16 x 128 B box
-  // K (B operand, non-transposed): matrices (keys 0-7 | 8-15) x (dims lo | hi)
-  const int krow = (lane >> 4) * 8 + (lane & 7);
-  const int kchunk = (lane >> 3) & 1;
-  // V (B operand via .trans): matrices (keys 0-7 | 8-15) x (dims d | d + 8)
-  const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int vchunk = lane >> 4;
-
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
-  bool dead = false;
-  int consumed = 0;
-
-  for (int t = 0; t < ntiles; ++t) {
-    consumed = t;
-    const int stage = t % kPfStages;
-    if (!__all_sync(kFull, mbar_wait_bounded(&bars[stage], static_cast<uint32_t>(t / kPfStages) & 1u))) {
-      dead = true;
-      if (lane == 0) record_error(p.err, kErrTimeout);
-    }
-    dead = __syncthreads_or(dead);
-    if (dead) break;
-    unsigned char* st = smem + stage * kPfStageBytes;
-    const int k0 = t * kPfKeys;
-    if (k0 + kPfKeys > ctx) {  // zero V rows at or past the context
-      unsigned char* vt = st + kPfKeys * kRowBytes;
-      for (int idx = tid; idx < kPfKeys * 16; idx += kPfWarps * 32) {
-        const int r = idx >> 4;
-        if (k0 + r < ctx) continue;
-        const int ch = idx & 15;
-        *reinterpret_cast<uint4*>(vt + (r >> 4) * 2 * kPfBox + (ch >> 3) * kPfBox + (r & 15) * 128 +
-                                  (ch & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      __syncthreads();
-    }
-    const uint32_t kbase = smem_addr(st);
-    const uint32_t vbase = kbase + kPfKeys * kRowBytes;
-
-    // ---- S = Q K^T: 16 rows x 64 keys
-    float s[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {      // 16-key run r: n-tiles 2r, 2r + 1
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t b[4];
-        const int c = (ks & 3) * 2 + kchunk;
-        ldmatrix_x4(b, kbase + (r * 2 + (ks >> 2)) * kPfBox + krow * 128 + ((c ^ (krow & 7)) << 4));
-        mma_bf16_16816(s[2 * r], qa[ks], b[0], b[1]);
-        mma_bf16_16816(s[2 * r + 1], qa[ks], b[2], b[3]);
-      }
-    }
-    // ---- causal mask and online softmax (rows g and g + 8)
-    float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int key = k0 + 8 * n + 2 * tq;
-      s[n][0] = key <= pa ? s[n][0] * p.qscale : -INFINITY;
-      s[n][1] = key + 1 <= pa ? s[n][1] * p.qscale : -INFINITY;
-      s[n][2] = key <= pb ? s[n][2] * p.qscale : -INFINITY;
-      s[n][3] = key + 1 <= pb ? s[n][3] * p.qscale : -INFINITY;
-      mxa = fmaxf(mxa, fmaxf(s[n][0], s[n][1]));
-      mxb = fmaxf(mxb, fmaxf(s[n][2], s[n][3]));
-    }
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      mxa = fmaxf(mxa, __shfl_xor_sync(kFull, mxa, off));
-      mxb = fmaxf(mxb, __shfl_xor_sync(kFull, mxb, off));
-    }
-    const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
-    const float fa = na == -INFINITY ? 1.f : fast_exp2(ma - na);
-    const float fb = nb == -INFINITY ? 1.f : fast_exp2(mb - nb);
-    la *= fa;
-    lb *= fb;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= fa;
-      o[n][1] *= fa;
-      o[n][2] *= fb;
-      o[n][3] *= fb;
-    }
-    ma = na;
-    mb = nb;
-    uint32_t pa_[8], pb_[8];  // P packed to bf16: row g / row g + 8, per n-tile
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const float e0 = na == -INFINITY ? 0.f : fast_exp2(s[n][0] - na);
-      const float e1 = na == -INFINITY ? 0.f : fast_exp2(s[n][1] - na);
-      const float e2 = nb == -INFINITY ? 0.f : fast_exp2(s[n][2] - nb);
-      const float e3 = nb == -INFINITY ? 0.f : fast_exp2(s[n][3] - nb);
-      la += e0 + e1;
-      lb += e2 + e3;
-      pa_[n] = pack_bf16x2(e0, e1);
-      pb_[n] = pack_bf16x2(e2, e3);
-    }
-    // ---- O += P V: k-step r covers keys 16r .. 16r + 15 (n-tiles 2r, 2r + 1)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint32_t a[4] = {pa_[2 * r], pb_[2 * r], pa_[2 * r + 1], pb_[2 * r + 1]};
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {  // dims 16dp .. 16dp + 15: n-tiles 2dp, 2dp + 1
-        uint32_t b[4];
-        const int c = (dp & 3) * 2 + vchunk;
-        ldmatrix_x4_trans(b, vbase + (r * 2 + (dp >> 2)) * kPfBox + vrow * 128 + ((c ^ (vrow & 7)) << 4));
-        mma_bf16_16816(o[2 * dp], a, b[0], b[1]);
-        mma_bf16_16816(o[2 * dp + 1], a, b[2], b[3]);
-      }
-    }
-    __syncthreads();  // every warp is done with this stage
-    if (warp == 0 && t + kPfStages < ntiles) {
-      fence_proxy_async_smem();
-      issue(t + kPfStages);
-      ++issued;
-    }
-  }
-
-  if (dead) {
-    // give the copies still in flight a bounded chance to land before exit
-    if (tid == 0)
-      for (int k = consumed; k < issued; ++k)
-        mbar_wait_bounded(&bars[k % kPfStages], static_cast<uint32_t>(k / kPfStages) & 1u);
-    return;
-  }
-  // ---- normalise and store rows g and g + 8
-#pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    la += __shfl_xor_sync(kFull, la, off);
-    lb += __shfl_xor_sync(kFull, lb, off);
-  }
-  const float ia = la > 0.f ? 1.f / la : 0.f;
-  const float ib = lb > 0.f ? 1.f / lb : 0.f;
-  uint16_t* oa = p.out + (static_cast<int64_t>(q0 + (va ? ra / G : 0)) * p.Hq + kvh * G + (va ? ra % G : 0)) * kHeadDim;
-  uint16_t* ob = p.out + (static_cast<int64_t>(q0 + (vb ? rb / G : 0)) * p.Hq + kvh * G + (vb ? rb % G : 0)) * kHeadDim;
-#pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const int d = 8 * n + 2 * tq;
-    if (va) *reinterpret_cast<uint32_t*>(oa + d) = pack_bf16x2(o[n][0] * ia, o[n][1] * ia);
-    if (vb) *reinterpret_cast<uint32_t*>(ob + d) = pack_bf16x2(o[n][2] * ib, o[n][3] * ib);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
   }
 }
 
@@ -300,14 +529,14 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const P
                            cudaStream_t stream) {
   static bool attr_done = false;  // one device per process in practice; repeated calls are harmless
   if (!attr_done) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    const cudaError_t e = cudaFuncSetAttribute(
+        prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int row_tiles = (p.max_q * p.G + kPfRows - 1) / kPfRows;
-  return launch_pdl(prefill_kernel, dim3(row_tiles, p.Hkv, p.num_seqs), dim3(kPfWarps * 32),
-                    kPfSmem, stream, tk, tv, p);
+  const int row_tiles = (p.max_q * p.G + 2 * kRowTile - 1) / (2 * kRowTile);
+  return launch_pdl(prefill_kernel, dim3(row_tiles, p.Hkv, p.num_seqs), dim3(kThreads),
+                    kSmemBytes, stream, tk, tv, p);
 }
 
 }  // namespace pkv

@@ -87,3 +87,29 @@ def test_checked_mode_reports_a_chunk_longer_than_its_context():
                                 torch.as_tensor(bad_ctx, device=DEV), 4, W.default_scale(b.shape))
     torch.cuda.synchronize()
     assert pkv.get_device_error() == "context"
+
+
+def test_long_chunks_span_many_row_and_key_tiles():
+    # 2800 / 2052 / 516 rows: several CTAs of 256 rows each; up to 9 key tiles
+    b, li, q, cu = _case(32, 8, [0, 300, 1000], [700, 513, 129], 16, seed=94)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "long chunks")
+
+
+def test_group_of_seven_splits_tokens_across_row_tiles():
+    # G = 7 (Yi-34B heads): 128-row tiles and 256-row CTAs cut through tokens
+    b, li, q, cu = _case(56, 8, [5, 0, 130], [100, 300, 37], 16, seed=95)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "G=7")
+
+
+@pytest.mark.parametrize("scale", [0.5, 2.0, 0.0])
+def test_growing_maxima_and_degenerate_scale(scale):
+    # large scales make the running maximum jump between key tiles (the
+    # rescale of O in tensor memory); scale 0 gives the mean of the visible V
+    b, li, q, cu = _case(16, 4, [0, 200, 513], [400, 129, 300], 16, seed=96)
+    out = pkv.paged_prefill_attention(
+        q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV), li.v_cache.to(DEV),
+        torch.as_tensor(b.block_tables, device=DEV), torch.as_tensor(b.ctx, device=DEV),
+        int(np.diff(cu).max()), scale)
+    ref = oracle.paged_prefill(W.to_u16(q), W.to_u16(li.k_cache), W.to_u16(li.v_cache),
+                               b.block_tables, b.ctx, cu, scale)
+    assert_attention_close(out, ref, "scale %g" % scale)
