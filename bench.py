@@ -835,6 +835,31 @@ def profile_case(args):
     torch.cuda.synchronize(dev)
 
 
+def profile_prefill_case(args):
+    """A small case for ncu: a few prefill calls over 8 fresh 2048-token
+    prompts with the workload's head shape (block_size 16)."""
+    import paged_kv_cache_245_gb300 as pkv
+    from __graft_entry__ import build
+    build()
+    dev = torch.device("cuda", 0)
+    shape = rank_batch(args.workload, 0).shape
+    ctx = np.full(8, 2048, np.int32)
+    b = W.make_paged_batch(shape, ctx, 16, 250)
+    li = W.layer_inputs(b, 0, device=dev, fast_cache=True)
+    cu = torch.as_tensor(np.arange(0, 8 * 2048 + 1, 2048, dtype=np.int32), device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(251)
+    q = torch.randn((8 * 2048, shape.num_q_heads, shape.head_dim), generator=g,
+                    device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    for _ in range(args.profile_prefill_calls):
+        pkv.paged_prefill_attention(q, cu, li.k_cache, li.v_cache,
+                                    torch.as_tensor(b.block_tables, device=dev),
+                                    torch.as_tensor(b.ctx, device=dev), 2048,
+                                    W.default_scale(shape), out=out)
+    torch.cuda.synchronize(dev)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -848,10 +873,16 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="profiling case: run this many paged attention calls over 4 layers "
                          "of the workload and exit (no timing, no JSON)")
+    ap.add_argument("--profile-prefill-calls", type=int, default=0,
+                    help="profiling case: run this many prefill calls over 8 fresh 2048-token "
+                         "prompts and exit (no timing, no JSON)")
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.profile_calls > 0:
         profile_case(args)
+        return
+    if args.profile_prefill_calls > 0:
+        profile_prefill_case(args)
         return
     if args.impl == "reference":
         # CPU-only arm: rank 0 runs it; other ranks exit without work.

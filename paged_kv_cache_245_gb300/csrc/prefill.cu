@@ -158,6 +158,32 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Packed pairs of fp32 (one register pair, lo in the low word) for the
+// two-wide fp32 instructions of sm_100 and later.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Wait for phase `parity` of `bar`; give up when another role has given up
 // (*abort) or after kWaitLimitNs (then set *abort and record the timeout).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
@@ -288,25 +314,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int k0 = j * kKeys;
       const bool diag = k0 + kKeys - 1 > pos;  // some key of the tile lies past the row
+      // general: a masked tile in this warp, or a negative scale (the maximum
+      // of the scaled logits is then not the scaled maximum)
+      const bool general = __any_sync(kFull, diag) || !(sc >= 0.f);
       // pass 1: the row maximum of the scaled, masked logits
-      float mx[8];
+      float tmax;
+      if (!general) {
+        float mx[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+        for (int u = 0; u < 4; ++u) mx[u] = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t a[32], b[32];
-        tmem_ld32(a, s_tm + 64 * h);
-        tmem_ld32(b, s_tm + 64 * h + 32);
-        tmem_wait_ld(a);
-        tmem_ready(b);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float x = __uint_as_float(c < 32 ? a[c] : b[c - 32]) * sc;
-          mx[c & 7] = fmaxf(mx[c & 7], !diag || k0 + 64 * h + c <= pos ? x : -INFINITY);
+          for (int c = 0; c < 16; ++c) {
+            mx[c & 3] = fmax3(mx[c & 3], __uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1]));
+            mx[(c + 2) & 3] =
+                fmax3(mx[(c + 2) & 3], __uint_as_float(b[2 * c]), __uint_as_float(b[2 * c + 1]));
+          }
         }
+        tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+      } else {
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float x = __uint_as_float(c < 32 ? a[c] : b[c - 32]) * sc;
+            mx[c & 7] = fmaxf(mx[c & 7], !diag || k0 + 64 * h + c <= pos ? x : -INFINITY);
+          }
+        }
+        tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       }
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_used, tmax);
       if (j == 0) {
         m_used = m_new;  // finite: position 0 is visible to every row
@@ -331,36 +382,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // pass 2: P = 2^(s * scale - m) as bf16 pairs over the columns already read
       const float neg_m = -m_used;
-      float ls[8];
+      if (!general) {
+        const uint64_t sc2 = f2_pack(__float_as_uint(sc), __float_as_uint(sc));
+        const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
+        uint64_t ls2[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+        for (int u = 0; u < 4; ++u) ls2[u] = 0ull;  // (+0, +0)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t a[32], b[32];
-        tmem_ld32(a, s_tm + 64 * h);
-        tmem_ld32(b, s_tm + 64 * h + 32);
-        tmem_wait_ld(a);
-        tmem_ready(b);
-        // keys of this half the row sees: bit c of (lo, hi) for key 64h + c
-        const int seen = diag ? min(max(pos - k0 - 64 * h + 1, 0), 64) : 64;
-        const uint32_t lo = seen >= 32 ? 0xffffffffu : (1u << seen) - 1u;
-        const uint32_t hi = seen >= 64 ? 0xffffffffu : (seen <= 32 ? 0u : (1u << (seen - 32)) - 1u);
-        uint32_t pk[32];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
-          const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
-          float e0 = fast_exp2(fmaf(__uint_as_float(u0), sc, neg_m));
-          float e1 = fast_exp2(fmaf(__uint_as_float(u1), sc, neg_m));
-          const uint32_t bits = c < 16 ? lo : hi;
-          e0 = (bits >> ((2 * c) & 31)) & 1u ? e0 : 0.f;
-          e1 = (bits >> ((2 * c + 1) & 31)) & 1u ? e1 : 0.f;
-          ls[c & 7] += e0 + e1;
-          pk[c] = pack_bf16x2(e0, e1);
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
+            const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(u0, u1), sc2, nm2), x0, x1);
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+            const uint64_t e2 = f2_pack(__float_as_uint(e0), __float_as_uint(e1));
+            ls2[c & 3] = f2_add(ls2[c & 3], e2);
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          tmem_st32(s_tm + 32 * h, pk);
         }
-        tmem_st32(s_tm + 32 * h, pk);
+        float l0, l1, l2, l3;
+        f2_unpack(f2_add(ls2[0], ls2[1]), l0, l1);
+        f2_unpack(f2_add(ls2[2], ls2[3]), l2, l3);
+        l += (l0 + l2) + (l1 + l3);
+      } else {
+        float ls[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+          // keys of this half the row sees: bit c of (lo, hi) for key 64h + c
+          const int seen = diag ? min(max(pos - k0 - 64 * h + 1, 0), 64) : 64;
+          const uint32_t lo = seen >= 32 ? 0xffffffffu : (1u << seen) - 1u;
+          const uint32_t hi =
+              seen >= 64 ? 0xffffffffu : (seen <= 32 ? 0u : (1u << (seen - 32)) - 1u);
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
+            const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
+            float e0 = fast_exp2(fmaf(__uint_as_float(u0), sc, neg_m));
+            float e1 = fast_exp2(fmaf(__uint_as_float(u1), sc, neg_m));
+            const uint32_t bits = c < 16 ? lo : hi;
+            e0 = (bits >> ((2 * c) & 31)) & 1u ? e0 : 0.f;
+            e1 = (bits >> ((2 * c + 1) & 31)) & 1u ? e1 : 0.f;
+            ls[c & 7] += e0 + e1;
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          tmem_st32(s_tm + 32 * h, pk);
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&pfull[t]);
