@@ -646,7 +646,10 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
   if (st != PKV_OK) return st;
   alignas(64) CUtensorMap tk;
   alignas(64) CUtensorMap tv;
-  if (!pkv::encode_rows(&tk, k_cache, rows_total) || !pkv::encode_rows(&tv, v_cache, rows_total))
+  int run_rows = 128;  // gcd(block_size, 128): a run of rows inside one block
+  while (block_size % run_rows != 0) run_rows >>= 1;
+  if (!pkv::encode_prefill_runs(&tk, k_cache, rows_total, run_rows) ||
+      !pkv::encode_prefill_runs(&tv, v_cache, rows_total, run_rows))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
   pkv::PrefillParams p;
   std::memset(&p, 0, sizeof p);
@@ -663,6 +666,7 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
   p.Hkv = heads.num_kv_heads;
   p.G = G;
   p.max_q = max_q_tokens;
+  p.run_rows = run_rows;
   p.qscale = scale * 1.4426950408889634f;  // log2(e)
   p.checked = g_checked.load();
   p.err = err;

@@ -15,9 +15,9 @@
 // own softmax warpgroup; one warp streams K/V, one warp issues the MMAs:
 //
 //   warps 0-3  softmax of row tile 0      warps 4-7  softmax of row tile 1
-//   warp 8     K/V tiles of 128 keys by TMA (2-D maps over the cache rows,
-//              128-byte swizzled boxes of 16 rows x 64 columns, one 16-key
-//              run per block-table entry) into a 2-stage ring
+//   warp 8     K/V tiles of 128 keys by TMA into a 2-stage ring: one box per
+//              run of a block's rows (gcd(bs, 128) rows), landing as 8-row x
+//              128-byte swizzled atoms ordered (row group, column half)
 //   warp 9     tensor-memory owner and MMA issuer (one thread)
 //
 // Tensor memory (512 columns, lane = query row of the tile): S_t = Q_t K^T in
@@ -33,6 +33,10 @@
 // tiles skip the rescale.  The MMAs of one thread complete in issue order, so
 // the barrier that reports S_t(j+1) also reports PV_t(j): from then on the
 // softmax warps own O_t until they hand P_t(j+1) over.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "pkv_device.cuh"
 #include "prefill.cuh"
 
@@ -45,7 +49,6 @@ constexpr int kKeys = 128;                            // keys per K/V tile
 constexpr int kStages = 2;
 constexpr int kOpBytes = 128 * kRowBytes;             // 32 KiB: a Q, K or V tile
 constexpr int kHalfBytes = kOpBytes / 2;              // one 64-column half
-constexpr int kRunBytes = 16 * 128;                   // one TMA box: 16 rows x 128 B
 constexpr int kOffK = 2 * kOpBytes;                   // after Q_0, Q_1
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 192 KiB
@@ -65,9 +68,13 @@ constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
 
 // Shared-memory matrix descriptor with 128-byte swizzling: start address,
 // leading and stride byte offsets (all / 16), the fixed 0b001 at bits 46-48
-// and the swizzle mode at 61-63.  K-major operands: 1024 bytes between
-// 8-row groups, leading offset unused.  The MN-major V: leading offset = the
-// step between the two 64-column halves, stride = 1024 bytes per 8 keys.
+// and the swizzle mode at 61-63.  Operand tiles hold 8-row x 128-byte atoms.
+// Q (written by the softmax threads): column half h at h * 16 KiB, 8-row
+// groups 1024 bytes apart.  K and V (TMA): atom (row group g, half h) at
+// g * 2048 + h * 1024.  K-major operands (Q, K): stride = the 8-row group
+// step, leading offset unused, the k-step's half and 32-byte column offset
+// in the start address.  The MN-major V: leading offset = the step between
+// the two 64-column halves (1024), stride = 2048 bytes per 8 keys.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
@@ -201,11 +208,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// Byte offset of 16-byte chunk c (0..15) of row r in a 128-row operand tile
-// stored as two 64-column halves of 128-byte rows, 128-byte swizzled (the
-// layout the TMA engine writes for the 16 x 64 boxes).
-__device__ __forceinline__ int tile_chunk_offset(int r, int c) {
+// Byte offset of 16-byte chunk c (0..15) of row r in the Q tile: two
+// 64-column halves of 128 rows x 128 bytes, 128-byte swizzled.
+__device__ __forceinline__ int q_chunk_offset(int r, int c) {
   return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// The same for a K or V tile as the 4-D boxes land: atom (r / 8, c / 8).
+__device__ __forceinline__ int kv_chunk_offset(int r, int c) {
+  return (r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, int32_t group,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst_smem)),
+      "l"(tmap), "r"(0), "r"(0), "r"(0), "r"(group), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
 }
 
 }  // namespace
@@ -296,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const uint4 v = valid ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(dst + tile_chunk_offset(lr, c)) = v;
+        *reinterpret_cast<uint4*>(dst + q_chunk_offset(lr, c)) = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(qfull);
@@ -478,37 +498,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every row tile of the sequence and KV head reads the same K/V tiles:
     // keep them in L2 for the CTAs that follow.
     const uint64_t policy = l2_policy_evict_last();
-    int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      if (j >= kStages &&
-          !__all_sync(kFull, wait_or_abort(&kvempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
-        break;
-      const int pos = j * kKeys + lane * 16;  // run `lane` (lanes 0-7)
+    const int run = p.run_rows;        // rows per box (16 .. 128, divides 128 and bs)
+    const int runs = kKeys / run;      // boxes per tile and tensor (<= 8)
+    const int r = lane & 15;           // lanes 0-7: K of run r, lanes 16-23: V of run r
+    // block-table entry of run r of tile j (-1: past the context or rejected)
+    auto entry = [&](int j) -> int32_t {
+      const int pos = j * kKeys + r * run;
       int32_t e = -1;
-      if (lane < kKeys / 16 && pos < ctx) {
+      if (j < ntiles && r < runs && pos < ctx) {
         e = p.block_tables[static_cast<int64_t>(i) * p.max_blocks + pos / p.bs];
         if (p.checked && (e < 0 || e >= p.num_blocks)) {
           record_error(p.err, kErrBlockId);
           e = -1;  // skip the copy: stale rows, undefined output, no fault
         }
       }
-      const uint32_t runs = __popc(__ballot_sync(kFull, e >= 0));
+      return e;
+    };
+    int32_t e = entry(0);
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j & 1;
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&kvempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
+        break;
+      const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
       if (lane == 0) {
-        mbar_arrive_expect_tx(&kfull[s], runs * 2 * kRunBytes);
-        mbar_arrive_expect_tx(&vfull[s], runs * 2 * kRunBytes);
+        mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
+        mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
       }
       __syncwarp();
       if (e >= 0) {
-        const int32_t y = static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, pos % p.bs));
-        unsigned char* kd = smem + kOffK + s * kStageBytes + lane * kRunBytes;
-        unsigned char* vd = kd + kOpBytes;
-        tma_load_2d(kd, &tmk, 0, y, &kfull[s], policy);
-        tma_load_2d(kd + kHalfBytes, &tmk, 64, y, &kfull[s], policy);
-        tma_load_2d(vd, &tmv, 0, y, &vfull[s], policy);
-        tma_load_2d(vd + kHalfBytes, &tmv, 64, y, &vfull[s], policy);
+        const int off = (j * kKeys + r * run) % p.bs;
+        const int32_t y = static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off));
+        unsigned char* dst = smem + kOffK + s * kStageBytes + (lane >= 16 ? kOpBytes : 0) +
+                             r * run * kRowBytes;
+        tma_load_4d(dst, lane >= 16 ? &tmv : &tmk, y >> 3, lane >= 16 ? &vfull[s] : &kfull[s],
+                    policy);
       }
       issued = j + 1;
+      e = entry(j + 1);  // the next tile's entries load while this one lands
     }
     if (*abort && lane == 0) {
       // let the copies in flight land before the CTA's shared memory is released
@@ -524,9 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_addr = smem_base + kOffK + (j & 1) * kStageBytes;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-        umma_ss(tmem + t * 128, smem_desc(q_addr + off, 16, 1024),
-                smem_desc(k_addr + off, 16, 1024), kIdescS, kk > 0);
+        const uint32_t koff = (kk & 3) * 32;
+        umma_ss(tmem + t * 128, smem_desc(q_addr + (kk >> 2) * kHalfBytes + koff, 16, 1024),
+                smem_desc(k_addr + (kk >> 2) * 1024 + koff, 16, 2048), kIdescS, kk > 0);
       }
     };
     auto issue_pv = [&](int t, int j) {  // O_t (+)= P_t V_j
@@ -534,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                smem_desc(v_addr + kk * 16 * 128, kHalfBytes, 1024), kIdescPV, (j > 0 || kk > 0));
+                smem_desc(v_addr + kk * 4096, 1024, 2048), kIdescPV, (j > 0 || kk > 0));
     };
     bool ok = __all_sync(kFull, wait_or_abort(qfull, 0, abort, p.err));
     if (ok) ok = __all_sync(kFull, wait_or_abort(&kfull[0], 0, abort, p.err));
@@ -557,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
         const int first = ctx - k0;
         for (int idx = lane; idx < (kKeys - first) * 16; idx += 32)
-          *reinterpret_cast<uint4*>(vt + tile_chunk_offset(first + (idx >> 4), idx & 15)) =
+          *reinterpret_cast<uint4*>(vt + kv_chunk_offset(first + (idx >> 4), idx & 15)) =
               make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         __syncwarp();
@@ -608,6 +636,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   }
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 prefill_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int run_rows) {
+  auto enc = prefill_map_encoder();
+  if (enc == nullptr || rows % 8 != 0 || run_rows % 8 != 0 || run_rows > 128) return false;
+  // dims (innermost first): 64 columns, 8 rows of a group, 2 column halves, groups
+  const cuuint64_t dims[4] = {64u, 8u, 2u, static_cast<cuuint64_t>(rows / 8)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kRowBytes), 128u,
+                                 static_cast<cuuint64_t>(8 * kRowBytes)};
+  const cuuint32_t box[4] = {64u, 8u, 2u, static_cast<cuuint32_t>(run_rows / 8)};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,

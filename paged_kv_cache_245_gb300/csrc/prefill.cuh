@@ -18,12 +18,20 @@ struct PrefillParams {
   int64_t num_blocks;
   int32_t max_blocks, num_seqs, Hq, Hkv, G;
   int32_t max_q;                 // host bound on any chunk's length
+  int32_t run_rows;              // rows per TMA box: gcd(bs, 128), one box per block run
   float qscale;                  // scale * log2(e)
   int32_t checked;
   int* err;
 };
 
-// One CTA per (64 query rows, KV head, sequence).
+// The K or V cache ([rows][128] bf16) as a 4-D tensor (64 columns, 8 rows,
+// 2 column halves, row groups of 8) whose boxes of run_rows rows land in
+// shared memory as 8-row x 128-byte atoms, 128-byte swizzled, ordered
+// (row group, half): the layout the prefill MMAs read.  False when the
+// driver rejects the map.
+bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int run_rows);
+
+// One CTA per (256 query rows, KV head, sequence).
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                            cudaStream_t stream);
 
