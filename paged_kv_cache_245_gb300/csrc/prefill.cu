@@ -238,14 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTilesBytes);
   uint64_t* kfull = bars;        // [2] K of a stage landed
   uint64_t* vfull = bars + 2;    // [2] V of a stage landed
-  uint64_t* kvempty = bars + 4;  // [2] every MMA reading a stage completed
+  uint64_t* vempty = bars + 4;   // [2] both P V products reading a stage's V completed
   uint64_t* sfull = bars + 6;    // [2] S_t of the current key tile (and PV_t before it) done
   uint64_t* pfull = bars + 8;    // [2] P_t written (one arrival per row)
   uint64_t* ofull = bars + 10;   // [2] the last PV_t completed
   uint64_t* qfull = bars + 12;   // Q_0, Q_1 in shared memory (one arrival per row)
   uint64_t* drain = bars + 13;   // wind-down after an abort
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 15);
+  uint64_t* kempty = bars + 14;  // [2] both S products reading a stage's K completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 17);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -281,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 12; ++b) mbar_init(&bars[b], (b == 8 || b == 9) ? kRowTile : 1);
     mbar_init(qfull, 2 * kRowTile);
     mbar_init(drain, 1);
+    mbar_init(&kempty[0], 1);
+    mbar_init(&kempty[1], 1);
     *abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmk);
@@ -515,26 +518,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       return e;
     };
     int32_t e = entry(0);
-    int issued = 0;
+    int issued = 0;       // tiles whose K and V were both issued
+    bool kv_half = false;  // tile `issued` has its K issued, not its V
     for (int j = 0; j < ntiles; ++j) {
       const int s = j & 1;
-      if (j >= kStages &&
-          !__all_sync(kFull, wait_or_abort(&kvempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
-        break;
       const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
-        mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
-      }
+      const int off = (j * kKeys + r * run) % p.bs;
+      const int32_t grp = e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
+      unsigned char* dst = smem + kOffK + s * kStageBytes + r * run * kRowBytes;
+      // K first: its stage frees once both S products of tile j - 2 are done
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&kempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
       __syncwarp();
-      if (e >= 0) {
-        const int off = (j * kKeys + r * run) % p.bs;
-        const int32_t y = static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off));
-        unsigned char* dst = smem + kOffK + s * kStageBytes + (lane >= 16 ? kOpBytes : 0) +
-                             r * run * kRowBytes;
-        tma_load_4d(dst, lane >= 16 ? &tmv : &tmk, y >> 3, lane >= 16 ? &vfull[s] : &kfull[s],
-                    policy);
+      if (lane < 16 && e >= 0) tma_load_4d(dst, &tmk, grp, &kfull[s], policy);
+      // then V, whose stage frees after both P V products of tile j - 2
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&vempty[s], ((j >> 1) - 1) & 1, abort, p.err))) {
+        issued = j;  // K of tile j is in flight: wait for it below
+        kv_half = true;
+        break;
       }
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
+      __syncwarp();
+      if (lane >= 16 && e >= 0) tma_load_4d(dst + kOpBytes, &tmv, grp, &vfull[s], policy);
       issued = j + 1;
       e = entry(j + 1);  // the next tile's entries load while this one lands
     }
@@ -544,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&kfull[j & 1], (j >> 1) & 1);
         mbar_wait_bounded(&vfull[j & 1], (j >> 1) & 1);
       }
+      if (kv_half) mbar_wait_bounded(&kfull[issued & 1], (issued >> 1) & 1);
     }
   } else {
     // ================= MMA issuer (warp 9, lane 0 issues) =================
@@ -573,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&sfull[0]);
         issue_s(1, 0);
         umma_commit(&sfull[1]);
+        if (kStages < ntiles) umma_commit(&kempty[0]);
       }
       __syncwarp();
     }
@@ -611,10 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         issue_pv(1, j);
-        if (j + kStages < ntiles) umma_commit(&kvempty[s]);  // the producer reuses the stage
+        if (j + kStages < ntiles) umma_commit(&vempty[s]);  // the producer reuses the stage
         if (more) {
           issue_s(1, j + 1);
           umma_commit(&sfull[1]);
+          if (j + 1 + kStages < ntiles) umma_commit(&kempty[s ^ 1]);
         } else {
           umma_commit(&ofull[1]);
         }
