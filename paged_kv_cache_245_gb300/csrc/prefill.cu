@@ -278,23 +278,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (kend <= 0) return;  // only when ctx < Lq (caught in checked mode)
   const int ntiles = (kend + kKeys - 1) / kKeys;
 
-  if (tid == 0) {
-    for (int b = 0; b < 12; ++b) mbar_init(&bars[b], (b == 8 || b == 9) ? kRowTile : 1);
-    mbar_init(qfull, 2 * kRowTile);
-    mbar_init(drain, 1);
-    mbar_init(&kempty[0], 1);
-    mbar_init(&kempty[1], 1);
-    *abort = 0;
-    fence_barrier_init();
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-  }
-  if (warp == 9) {
+  // Producer state (warp 8): lanes 0-7 copy K of run r of a tile, lanes
+  // 16-23 V of the same run; every row tile of the sequence and KV head
+  // reads the same K/V tiles, so they are kept in L2 for the CTAs after.
+  const uint64_t policy = l2_policy_evict_last();
+  const int run = p.run_rows;    // rows per box (16 .. 128, divides 128 and bs)
+  const int runs = kKeys / run;  // boxes per tile and tensor (<= 8)
+  const int prun = lane & 15;
+  // block-table entry of run prun of tile j (-1: past the context or rejected)
+  auto entry = [&](int j) -> int32_t {
+    const int kpos = j * kKeys + prun * run;
+    int32_t e = -1;
+    if (j < ntiles && prun < runs && kpos < ctx) {
+      e = p.block_tables[static_cast<int64_t>(i) * p.max_blocks + kpos / p.bs];
+      if (p.checked && (e < 0 || e >= p.num_blocks)) {
+        record_error(p.err, kErrBlockId);
+        e = -1;  // skip the copy: stale rows, undefined output, no fault
+      }
+    }
+    return e;
+  };
+  int32_t e = -1;        // entries of the next tile to issue
+  int issued = 0;        // tiles whose K and V were both issued
+  bool kv_half = false;  // tile `issued` has its K issued, not its V
+  // Issue tiles [j0, j1); false when a wait gave up.
+  auto produce = [&](int j0, int j1) -> bool {
+    for (int j = j0; j < j1; ++j) {
+      const int s = j & 1;
+      const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
+      const int off = (j * kKeys + prun * run) % p.bs;
+      const int32_t grp =
+          e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
+      unsigned char* dst = smem + kOffK + s * kStageBytes + prun * run * kRowBytes;
+      // K first: its stage frees once both S products of tile j - 2 are done
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&kempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
+        return false;
+      if (lane == 0) mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
+      __syncwarp();
+      if (lane < 16 && e >= 0) tma_load_4d(dst, &tmk, grp, &kfull[s], policy);
+      // then V, whose stage frees after both P V products of tile j - 2
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&vempty[s], ((j >> 1) - 1) & 1, abort, p.err))) {
+        kv_half = true;  // K of tile `issued` is in flight
+        return false;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
+      __syncwarp();
+      if (lane >= 16 && e >= 0) tma_load_4d(dst + kOpBytes, &tmv, grp, &vfull[s], policy);
+      issued = j + 1;
+      e = entry(j + 1);  // the next tile's entries load while this one lands
+    }
+    return true;
+  };
+
+  // Softmax row of this thread (warps 0-7).
+  const int t = (warp >> 2) & 1;                // row tile
+  const int lr = tid & (kRowTile - 1);          // row in the tile = tensor-memory lane
+  const int r = row0 + t * kRowTile + lr;       // row of the chunk
+  const bool valid = r < rows;
+  const int rr = valid ? r : rows - 1;          // padding rows mirror the last row
+  const int tok = rr / G;
+  const int head = kvh * G + rr % G;
+  const int pos = base + tok;
+  const int64_t qrow = (static_cast<int64_t>(q0) + tok) * p.Hq + head;
+
+  // Prologue: every role starts its global reads before the CTA-wide barrier.
+  if (warp == 8) {
+    if (lane == 0) {
+      for (int b = 0; b < 12; ++b) mbar_init(&bars[b], (b == 8 || b == 9) ? kRowTile : 1);
+      mbar_init(qfull, 2 * kRowTile);
+      mbar_init(drain, 1);
+      mbar_init(&kempty[0], 1);
+      mbar_init(&kempty[1], 1);
+      *abort = 0;
+      fence_barrier_init();
+      prefetch_tensormap(&tmk);
+      prefetch_tensormap(&tmv);
+    }
+    __syncwarp();
+    e = entry(0);
+    produce(0, min(kStages, ntiles));  // no waits: the stages are fresh
+  } else if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim);
+    unsigned char* dst = smem + t * kOpBytes;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = valid ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(dst + q_chunk_offset(lr, c)) = v;
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -304,26 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ================= softmax warpgroups =================
-    const int t = warp >> 2;                        // row tile
-    const int lr = tid & (kRowTile - 1);            // row in the tile = tensor-memory lane
-    const int r = row0 + t * kRowTile + lr;         // row of the chunk
-    const bool valid = r < rows;
-    const int rr = valid ? r : rows - 1;            // padding rows mirror the last row
-    const int tok = rr / G;
-    const int head = kvh * G + rr % G;
-    const int pos = base + tok;
-    const int64_t qrow = (static_cast<int64_t>(q0) + tok) * p.Hq + head;
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim);
-      unsigned char* dst = smem + t * kOpBytes;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = valid ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(dst + q_chunk_offset(lr, c)) = v;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(qfull);
-    }
+    mbar_arrive(qfull);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + t * 128;
     const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
@@ -497,55 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 8) {
-    // ================= K/V producer =================
-    // Every row tile of the sequence and KV head reads the same K/V tiles:
-    // keep them in L2 for the CTAs that follow.
-    const uint64_t policy = l2_policy_evict_last();
-    const int run = p.run_rows;        // rows per box (16 .. 128, divides 128 and bs)
-    const int runs = kKeys / run;      // boxes per tile and tensor (<= 8)
-    const int r = lane & 15;           // lanes 0-7: K of run r, lanes 16-23: V of run r
-    // block-table entry of run r of tile j (-1: past the context or rejected)
-    auto entry = [&](int j) -> int32_t {
-      const int pos = j * kKeys + r * run;
-      int32_t e = -1;
-      if (j < ntiles && r < runs && pos < ctx) {
-        e = p.block_tables[static_cast<int64_t>(i) * p.max_blocks + pos / p.bs];
-        if (p.checked && (e < 0 || e >= p.num_blocks)) {
-          record_error(p.err, kErrBlockId);
-          e = -1;  // skip the copy: stale rows, undefined output, no fault
-        }
-      }
-      return e;
-    };
-    int32_t e = entry(0);
-    int issued = 0;       // tiles whose K and V were both issued
-    bool kv_half = false;  // tile `issued` has its K issued, not its V
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
-      const int off = (j * kKeys + r * run) % p.bs;
-      const int32_t grp = e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
-      unsigned char* dst = smem + kOffK + s * kStageBytes + r * run * kRowBytes;
-      // K first: its stage frees once both S products of tile j - 2 are done
-      if (j >= kStages &&
-          !__all_sync(kFull, wait_or_abort(&kempty[s], ((j >> 1) - 1) & 1, abort, p.err)))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
-      __syncwarp();
-      if (lane < 16 && e >= 0) tma_load_4d(dst, &tmk, grp, &kfull[s], policy);
-      // then V, whose stage frees after both P V products of tile j - 2
-      if (j >= kStages &&
-          !__all_sync(kFull, wait_or_abort(&vempty[s], ((j >> 1) - 1) & 1, abort, p.err))) {
-        issued = j;  // K of tile j is in flight: wait for it below
-        kv_half = true;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
-      __syncwarp();
-      if (lane >= 16 && e >= 0) tma_load_4d(dst + kOpBytes, &tmv, grp, &vfull[s], policy);
-      issued = j + 1;
-      e = entry(j + 1);  // the next tile's entries load while this one lands
-    }
+    // ================= K/V producer: the remaining tiles =================
+    produce(kStages, ntiles);
     if (*abort && lane == 0) {
       // let the copies in flight land before the CTA's shared memory is released
       for (int j = max(0, issued - kStages); j < issued; ++j) {
