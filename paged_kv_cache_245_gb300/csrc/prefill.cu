@@ -240,9 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* vfull = bars + 2;    // [2] V of a stage landed
   uint64_t* vempty = bars + 4;   // [2] both P V products reading a stage's V completed
   uint64_t* sfull = bars + 6;    // [2] S_t of the current key tile (and PV_t before it) done
-  uint64_t* pfull = bars + 8;    // [2] P_t written (one arrival per row)
+  uint64_t* pfull = bars + 8;    // [2] P_t written (one arrival per warp)
   uint64_t* ofull = bars + 10;   // [2] the last PV_t completed
-  uint64_t* qfull = bars + 12;   // Q_0, Q_1 in shared memory (one arrival per row)
   uint64_t* drain = bars + 13;   // wind-down after an abort
   uint64_t* kempty = bars + 14;  // [2] both S products reading a stage's K completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
@@ -346,8 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Prologue: every role starts its global reads before the CTA-wide barrier.
   if (warp == 8) {
     if (lane == 0) {
-      for (int b = 0; b < 12; ++b) mbar_init(&bars[b], (b == 8 || b == 9) ? kRowTile : 1);
-      mbar_init(qfull, 2 * kRowTile);
+      for (int b = 0; b < 12; ++b) mbar_init(&bars[b], (b == 8 || b == 9) ? 4 : 1);
       mbar_init(drain, 1);
       mbar_init(&kempty[0], 1);
       mbar_init(&kempty[1], 1);
@@ -383,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ================= softmax warpgroups =================
-    mbar_arrive(qfull);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + t * 128;
     const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
@@ -531,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&pfull[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[t]);
     }
     if (ok) ok = __all_sync(kFull, wait_or_abort(&ofull[t], 0, abort, p.err));
     if (ok) {
@@ -586,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
                 smem_desc(v_addr + kk * 4096, 1024, 2048), kIdescPV, (j > 0 || kk > 0));
     };
-    bool ok = __all_sync(kFull, wait_or_abort(qfull, 0, abort, p.err));
-    if (ok) ok = __all_sync(kFull, wait_or_abort(&kfull[0], 0, abort, p.err));
+    // Q is in shared memory: written and fenced before the CTA-wide barrier
+    bool ok = __all_sync(kFull, wait_or_abort(&kfull[0], 0, abort, p.err));
     if (ok) {
       tc_fence_after();
       if (lane == 0) {
