@@ -49,7 +49,7 @@ def _oracle(b, li, q, cu):
                                 b.block_tables, b.ctx, cu, W.default_scale(b.shape))
 
 
-@pytest.mark.parametrize("bs", [16, 32, 128])
+@pytest.mark.parametrize("bs", [16, 32, 48, 64, 128, 256])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (32, 8), (16, 2)])
 def test_chunks_against_oracle(hq, hkv, bs):
     cached = [0, 3, 100, 64, 17, 0]
@@ -101,10 +101,11 @@ def test_group_of_seven_splits_tokens_across_row_tiles():
     assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "G=7")
 
 
-@pytest.mark.parametrize("scale", [0.5, 2.0, 0.0])
+@pytest.mark.parametrize("scale", [0.5, 2.0, 0.0, -0.3])
 def test_growing_maxima_and_degenerate_scale(scale):
     # large scales make the running maximum jump between key tiles (the
-    # rescale of O in tensor memory); scale 0 gives the mean of the visible V
+    # rescale of O in tensor memory); scale 0 gives the mean of the visible V;
+    # a negative scale takes the general (masked) softmax path on every tile
     b, li, q, cu = _case(16, 4, [0, 200, 513], [400, 129, 300], 16, seed=96)
     out = pkv.paged_prefill_attention(
         q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV), li.v_cache.to(DEV),
@@ -113,3 +114,9 @@ def test_growing_maxima_and_degenerate_scale(scale):
     ref = oracle.paged_prefill(W.to_u16(q), W.to_u16(li.k_cache), W.to_u16(li.v_cache),
                                b.block_tables, b.ctx, cu, scale)
     assert_attention_close(out, ref, "scale %g" % scale)
+
+
+def test_short_chunk_after_a_long_context():
+    # 157 key tiles of 128 behind a 64-token chunk, block_size 32
+    b, li, q, cu = _case(8, 2, [20000, 7], [64, 40], 32, seed=97)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "long context")
