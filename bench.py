@@ -454,8 +454,8 @@ def run_gpu(args, world, rank, local):
                      "timed_over": "%d replays of the step's %d attention calls" % (attn_reps, nl),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
         "gpu_launches": wl.launches_per_step() * args.steps,
-        "timing": "CUDA-graph replay of the step; roofline from a replay of the 32 "
-                  "attention calls alone",
+        "timing": "CUDA-graph replay of the step; roofline from a replay of the %d "
+                  "attention calls alone" % nl,
         "clocks": clock_info,
     }
     if e2e is not None:
