@@ -120,3 +120,33 @@ def test_short_chunk_after_a_long_context():
     # 157 key tiles of 128 behind a 64-token chunk, block_size 32
     b, li, q, cu = _case(8, 2, [20000, 7], [64, 40], 32, seed=97)
     assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "long context")
+
+
+def test_sequences_without_new_tokens_are_skipped():
+    # chunks of 0 tokens (repeated cu_seqlens_q entries) next to real ones
+    b, li, q, cu = _case(32, 8, [50, 20, 300, 9], [0, 70, 0, 3], 16, seed=98)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "empty chunks")
+
+
+def test_checked_mode_reports_a_chunk_longer_than_the_host_bound():
+    pkv.set_checked(True)
+    b, li, q, cu = _case(8, 2, [10, 10], [4, 6], 16, seed=99)
+    assert pkv.get_device_error() == "none"
+    pkv.paged_prefill_attention(q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV),
+                                li.v_cache.to(DEV), torch.as_tensor(b.block_tables, device=DEV),
+                                torch.as_tensor(b.ctx, device=DEV), 4, W.default_scale(b.shape))
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "context"
+
+
+def test_checked_mode_reports_a_block_id_outside_the_pool():
+    pkv.set_checked(True)
+    b, li, q, cu = _case(8, 2, [40, 10], [8, 8], 16, seed=100)
+    tables = b.block_tables.copy()
+    tables[0, 1] = li.k_cache.shape[0]  # one past the last block
+    assert pkv.get_device_error() == "none"
+    pkv.paged_prefill_attention(q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV),
+                                li.v_cache.to(DEV), torch.as_tensor(tables, device=DEV),
+                                torch.as_tensor(b.ctx, device=DEV), 8, W.default_scale(b.shape))
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "block_id"
