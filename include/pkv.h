@@ -7,7 +7,8 @@
  *   pkv_contig_decode_attention   the same over per-request sub-tensors
  *   pkv_block_copy                copy whole blocks (copy on write)
  * and pkv_paged_decode_step / pkv_contig_decode_step run append + attention
- * of one layer as one call.
+ * of one layer as one call.  pkv_paged_prefill_attention /
+ * pkv_contig_prefill_attention attend chunks of new tokens causally (prefill).
  *
  * Conventions for every call:
  *   - All tensor arguments are DEVICE pointers on the current CUDA device,
@@ -249,6 +250,24 @@ PKV_API pkv_status pkv_paged_prefill_attention(
     int32_t max_blocks_per_seq, int32_t num_blocks, const int32_t *context_lens,
     int32_t num_seqs, int32_t max_q_tokens, int32_t block_size, float scale,
     pkv_heads heads, void *out, void *stream);
+
+/*
+ * The same causal prefill over per-request sub-tensors ("Leveraging Low-Level
+ * CUDA APIs for vAttention's Dynamic Memory", 5.2.3: request reqId's K rows
+ * at offset reqId x S of a per-layer buffer).  k_buf, v_buf: bf16
+ * [max_reqs][Hkv][S][128]; sequence i reads request req_ids[i] (device int32
+ * [num_seqs]); q, cu_seqlens_q, context_lens (<= S), out as in
+ * pkv_paged_prefill_attention.  S must be a multiple of 16.  No row at or
+ * past round_up(context_lens[i], 16) of a request is read, so buffers whose
+ * pages are mapped on demand (pkv_vmm_ensure) need only that many rows
+ * backed.  Checked mode also reports req_ids outside [0, max_reqs) as
+ * PKV_DEVERR_BLOCK_ID.
+ */
+PKV_API pkv_status pkv_contig_prefill_attention(
+    const void *q, const int32_t *cu_seqlens_q, int32_t num_tokens,
+    const void *k_buf, const void *v_buf, const int32_t *req_ids, int32_t max_reqs,
+    const int32_t *context_lens, int32_t num_seqs, int32_t max_q_tokens, int64_t S,
+    float scale, pkv_heads heads, void *out, void *stream);
 
 /*
  * Copy-on-write block copy.  "Running Out of Cache" (section "Fragmentation

@@ -1,10 +1,10 @@
-"""Decode attention over a paged (block-table) or contiguous (reqId x S) KV
-cache, with KV append and copy-on-write block copy, as hand-written sm_103a
-CUDA kernels behind a C ABI (include/pkv.h).  This package is the thin
+"""Decode and prefill attention over a paged (block-table) or contiguous
+(reqId x S) KV cache, with KV append and copy-on-write block copy, as
+hand-written sm_103a CUDA kernels behind a C ABI (include/pkv.h).  This package is the thin
 Python binding; build the library with ``build.build()``."""
 from .binding import (BlockManager, PkvError, VmmBuffer, block_copy, contig_decode_attention, contig_decode_step,
                       decode_num_splits, paged_decode_step, paged_decode_attention_shared,
-                      paged_prefill_attention,
+                      paged_prefill_attention, contig_prefill_attention,
                       decode_workspace_size, get_checked, get_device_error, kv_append, lib,
                       paged_decode_attention, set_checked, set_decode_variant, get_decode_variant,
                       set_split_tiles, VARIANT_AUTO, VARIANT_SPLIT, VARIANT_TC_8X3,
@@ -12,6 +12,7 @@ from .binding import (BlockManager, PkvError, VmmBuffer, block_copy, contig_deco
 
 __all__ = ["BlockManager", "PkvError", "VmmBuffer", "block_copy", "contig_decode_attention", "contig_decode_step",
            "paged_decode_step", "paged_decode_attention_shared", "paged_prefill_attention",
+           "contig_prefill_attention",
            "decode_num_splits",
            "decode_workspace_size", "get_checked", "get_device_error", "kv_append", "lib",
            "paged_decode_attention", "set_checked", "set_split_tiles", "set_decode_variant",

@@ -30,6 +30,7 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
             "pkv_debug_gather_contig", "pkv_paged_decode_attention_shared",
             "pkv_shared_decode_workspace_size", "pkv_paged_prefill_attention",
+            "pkv_contig_prefill_attention",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -73,6 +74,8 @@ def lib():
                                          ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_paged_prefill_attention.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32,
                                               i32, ctypes.c_float, Heads, vp, vp]
+    L.pkv_contig_prefill_attention.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i64,
+                                               ctypes.c_float, Heads, vp, vp]
     L.pkv_shared_decode_workspace_size.argtypes = [i32, i32, i32, i32, Heads]
     L.pkv_shared_decode_workspace_size.restype = sz
     L.pkv_paged_decode_attention_shared.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
@@ -358,6 +361,34 @@ def paged_prefill_attention(q, cu_seqlens_q, k_cache, v_cache, block_tables, con
         _ptr(q), _ptr(cu_seqlens_q), T, _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], nb, _ptr(context_lens), B, int(max_q_tokens), bs, float(scale),
         heads(hq, hkv, d), _ptr(out), _stream(q)))
+    return out
+
+
+def contig_prefill_attention(q, cu_seqlens_q, k_buf, v_buf, req_ids, context_lens,
+                             max_q_tokens, scale, out=None):
+    """Causal prefill over per-request sub-tensors: sequence i's rows are
+    k_buf[req_ids[i], h, :context_lens[i]] (offset reqId x S); q,
+    cu_seqlens_q and out as in paged_prefill_attention."""
+    _need(q, torch.bfloat16, "q", 3)
+    for t, n in ((k_buf, "k_buf"), (v_buf, "v_buf")):
+        _need(t, torch.bfloat16, n, 4)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _need(req_ids, torch.int32, "req_ids", 1)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    T, hq, d = q.shape
+    max_reqs, hkv, S, d2 = k_buf.shape
+    B = context_lens.shape[0]
+    if d != d2 or tuple(v_buf.shape) != tuple(k_buf.shape):
+        raise ValueError("q / buffer shapes disagree")
+    if cu_seqlens_q.shape[0] != B + 1 or req_ids.shape[0] != B:
+        raise ValueError("cu_seqlens_q must have num_seqs + 1 entries, req_ids num_seqs")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    _check(lib().pkv_contig_prefill_attention(
+        _ptr(q), _ptr(cu_seqlens_q), T, _ptr(k_buf), _ptr(v_buf), _ptr(req_ids), max_reqs,
+        _ptr(context_lens), B, int(max_q_tokens), S, float(scale), heads(hq, hkv, d), _ptr(out),
+        _stream(q)))
     return out
 
 

@@ -610,13 +610,18 @@ pkv_status pkv_paged_decode_attention_shared(
   return PKV_OK;
 }
 
-pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_q,
-                                       int32_t num_tokens, const void* k_cache,
-                                       const void* v_cache, const int32_t* block_tables,
-                                       int32_t max_blocks_per_seq, int32_t num_blocks,
-                                       const int32_t* context_lens, int32_t num_seqs,
-                                       int32_t max_q_tokens, int32_t block_size, float scale,
-                                       pkv_heads heads, void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Causal prefill over rows addressed as block (or request) x block_size; a
+// TMA box covers run_rows rows of one block.
+pkv_status prefill_common(const void* q, const int32_t* cu_seqlens_q, int32_t num_tokens,
+                          const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, int32_t num_blocks,
+                          const int32_t* context_lens, int32_t num_seqs, int32_t max_q_tokens,
+                          int32_t block_size, int run_rows, float scale, pkv_heads heads,
+                          void* out, void* stream) {
   pkv_status st = check_heads(heads);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_tokens < 0 || max_q_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
@@ -646,8 +651,6 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
   if (st != PKV_OK) return st;
   alignas(64) CUtensorMap tk;
   alignas(64) CUtensorMap tv;
-  int run_rows = 128;  // gcd(block_size, 128): a run of rows inside one block
-  while (block_size % run_rows != 0) run_rows >>= 1;
   if (!pkv::encode_prefill_runs(&tk, k_cache, rows_total, run_rows) ||
       !pkv::encode_prefill_runs(&tv, v_cache, rows_total, run_rows))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
@@ -673,6 +676,39 @@ pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_
   const cudaError_t e = pkv::launch_prefill(tk, tv, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_prefill_attention(const void* q, const int32_t* cu_seqlens_q,
+                                       int32_t num_tokens, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, int32_t num_blocks,
+                                       const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t max_q_tokens, int32_t block_size, float scale,
+                                       pkv_heads heads, void* out, void* stream) {
+  int run_rows = 128;  // gcd(block_size, 128): a run of rows inside one block
+  while (block_size > 0 && block_size % run_rows != 0) run_rows >>= 1;
+  return prefill_common(q, cu_seqlens_q, num_tokens, k_cache, v_cache, block_tables,
+                        max_blocks_per_seq, num_blocks, context_lens, num_seqs, max_q_tokens,
+                        block_size, run_rows, scale, heads, out, stream);
+}
+
+pkv_status pkv_contig_prefill_attention(const void* q, const int32_t* cu_seqlens_q,
+                                        int32_t num_tokens, const void* k_buf, const void* v_buf,
+                                        const int32_t* req_ids, int32_t max_reqs,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t max_q_tokens, int64_t S, float scale,
+                                        pkv_heads heads, void* out, void* stream) {
+  if (S <= 0 || S > 0x7fffffffLL) return fail(PKV_ERR_UNSUPPORTED, "S out of range");
+  // The contiguous layout is the paged one with block_size S and a one-entry
+  // table [reqId].  Boxes of 16 rows never read past round_up(ctx, 16) rows,
+  // so buffers whose pages are mapped on demand stay within their backing.
+  return prefill_common(q, cu_seqlens_q, num_tokens, k_buf, v_buf, req_ids, 1, max_reqs,
+                        context_lens, num_seqs, max_q_tokens, static_cast<int32_t>(S), 16, scale,
+                        heads, out, stream);
 }
 
 pkv_status pkv_debug_gather_paged(const void* cache, const int32_t* block_tables,

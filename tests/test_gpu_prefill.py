@@ -150,3 +150,53 @@ def test_checked_mode_reports_a_block_id_outside_the_pool():
                                 torch.as_tensor(b.ctx, device=DEV), 8, W.default_scale(b.shape))
     torch.cuda.synchronize()
     assert pkv.get_device_error() == "block_id"
+
+
+def _contig_case(hq, hkv, S, max_reqs, req_ids, cached, lq, seed):
+    g = torch.Generator().manual_seed(seed)
+    kb = torch.randn((max_reqs, hkv, S, 128), generator=g).to(torch.bfloat16)
+    vb = torch.randn((max_reqs, hkv, S, 128), generator=g).to(torch.bfloat16)
+    ctx = (np.asarray(cached) + np.asarray(lq)).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    q = torch.randn((int(cu[-1]), hq, 128), generator=g).to(torch.bfloat16)
+    return kb, vb, np.asarray(req_ids, np.int32), ctx, cu, q
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (56, 8)])
+def test_contiguous_layout_against_oracle(hq, hkv):
+    # request rows at reqId x S; the oracle reads the buffer as a paged cache
+    # of max_reqs blocks of S rows and one-entry tables [reqId]
+    kb, vb, req, ctx, cu, q = _contig_case(hq, hkv, 1024, 6, [4, 0, 5, 2], [0, 300, 17, 900],
+                                           [200, 129, 40, 100], seed=101)
+    out = pkv.contig_prefill_attention(q.to(DEV), torch.as_tensor(cu, device=DEV), kb.to(DEV),
+                                       vb.to(DEV), torch.as_tensor(req, device=DEV),
+                                       torch.as_tensor(ctx, device=DEV), int(np.diff(cu).max()),
+                                       128 ** -0.5)
+    ref = oracle.paged_prefill(W.to_u16(q), W.to_u16(kb), W.to_u16(vb), req[:, None], ctx, cu,
+                               128 ** -0.5)
+    assert_attention_close(out, ref, "contiguous prefill")
+
+
+def test_contiguous_prefill_on_memory_mapped_on_demand():
+    # only the rows each request needs are backed; the output is the same
+    # bytes as on regular memory
+    S = 16384
+    kb, vb, req, ctx, cu, q = _contig_case(32, 8, S, 3, [0, 1, 2], [8000, 0, 12000],
+                                           [192, 70, 300], seed=102)
+    vm = pkv.VmmBuffer(3, 8, S)
+    try:
+        for r in range(3):
+            vm.ensure(int(req[r]), int(ctx[r]))
+            assert vm.backed_tokens(int(req[r])) >= ctx[r]
+            vm.k[int(req[r]), :, :ctx[r]].copy_(kb[int(req[r]), :, :ctx[r]])
+            vm.v[int(req[r]), :, :ctx[r]].copy_(vb[int(req[r]), :, :ctx[r]])
+        args = (torch.as_tensor(req, device=DEV), torch.as_tensor(ctx, device=DEV),
+                int(np.diff(cu).max()), 128 ** -0.5)
+        qd, cud = q.to(DEV), torch.as_tensor(cu, device=DEV)
+        ref = pkv.contig_prefill_attention(qd, cud, kb.to(DEV), vb.to(DEV), *args)
+        out = pkv.contig_prefill_attention(qd, cud, vm.k, vm.v, *args)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    finally:
+        torch.cuda.synchronize()
+        vm.close()
