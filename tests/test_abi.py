@@ -114,3 +114,30 @@ def test_checked_flag_and_split_override_round_trip(L):
     pkv.set_checked(False)
     assert not pkv.get_checked()
     pkv.set_split_tiles(0)
+
+
+def test_prefill_validation(L):
+    # paged: (q, cu, T, k, v, tables, max_blocks, num_blocks, ctx, B, max_q, bs, scale, heads, out, stream)
+    args = lambda **kw: dict(dict(q=FAKE, cu=FAKE, T=8, k=FAKE, v=FAKE, tab=FAKE, mb=4, nb=10,
+                                  ctx=FAKE, B=2, mq=4, bs=16, sc=0.1, h=_h(), out=FAKE), **kw)
+
+    def paged(**kw):
+        a = args(**kw)
+        return L.pkv_paged_prefill_attention(a["q"], a["cu"], a["T"], a["k"], a["v"], a["tab"],
+                                             a["mb"], a["nb"], a["ctx"], a["B"], a["mq"], a["bs"],
+                                             a["sc"], a["h"], a["out"], None)
+
+    assert paged(h=_h(d=64)) == 2
+    assert paged(q=None) == 1
+    assert paged(out=MISALIGNED) == 1 and b"aligned" in L.pkv_last_error()
+    assert paged(bs=8) == 2 and b"block_size" in L.pkv_last_error()
+    assert paged(sc=float("inf")) == 1
+    assert paged(mb=0) == 1
+    assert paged(T=0) == 0 and paged(B=0) == 0  # nothing to attend
+    # contiguous: (q, cu, T, k_buf, v_buf, req_ids, max_reqs, ctx, B, max_q, S, scale, heads, out, stream)
+    assert L.pkv_contig_prefill_attention(FAKE, FAKE, 8, FAKE, FAKE, FAKE, 4, FAKE, 2, 4, 1000,
+                                          0.1, _h(), FAKE, None) == 2  # S % 16 != 0
+    assert L.pkv_contig_prefill_attention(FAKE, FAKE, 8, FAKE, FAKE, FAKE, 4, FAKE, 2, 4, 0,
+                                          0.1, _h(), FAKE, None) == 2
+    assert L.pkv_contig_prefill_attention(FAKE, FAKE, 8, MISALIGNED, FAKE, FAKE, 4, FAKE, 2, 4,
+                                          1024, 0.1, _h(), FAKE, None) == 1
