@@ -1,18 +1,18 @@
 // cascade.cu -- decode attention for sequences that share prompt blocks
 // ("Running Out of Cache", "Fragmentation is lost users": sequences sampled
 // from one prompt share its blocks until one writes into them).  The shared
-// positions are attended once for several sequences at a time instead of
-// once per sequence: softmax over a concatenation splits into per-part
-// partial results (o, m, l) merged as
+// positions are attended once for all members of a group instead of once
+// per sequence: softmax over a concatenation splits into per-part partial
+// results (o, m, l) merged as
 //   M = max(m_a, m_b),  w_x = l_x 2^(m_x - M),  o = (w_a o_a + w_b o_b) / (w_a + w_b).
 //
-// Virtual batches built here (in the caller's workspace):
-//   prefix: entry v = g * SG + s holds the shared positions of group g with
-//           the query heads of the group's members s*m .. s*m+m-1 stacked
-//           (G_v = m * G heads per KV head, zero rows for absent members);
-//   suffix: entry i holds sequence i's own positions after the shared ones.
-// Both go through the tensor-core kernel in record mode; cascade_merge_kernel
-// merges the two records of every (sequence, head).
+// The shared part of every group is one item of the tcgen05 prefill kernel
+// in prefix mode (prefill.cu): the group's (member, query head) rows against
+// its shared blocks, fp32 records out.  The own part after the shared blocks
+// is attended here, inside the merge (a host bound of at most 256 own
+// positions), or by the tensor-core decode kernel in record mode over a
+// virtual batch the prep kernel builds (entry i: sequence i's own positions).
+// cascade_merge_kernel merges the two records of every (sequence, head).
 #include "cascade.cuh"
 #include "pkv_device.cuh"
 
@@ -157,13 +157,15 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   const int gi = h % c.G;
   const int g = group_of(c.group_start, c.num_groups, i);
   const int kg = i - c.group_start[g];
-  // a member beyond the groups' size bound has no prefix entry (the caller
-  // broke the contract: its shared positions are missing, nothing is read)
-  const bool has_prefix = kg >= 0 && kg / c.m < c.SG;
-  const int v = g * c.SG + (has_prefix ? kg / c.m : 0);
-  const int k = has_prefix ? kg % c.m : 0;
-  const int Gv = c.m * c.G;
-  const float* rp = c.rec_p + (static_cast<int64_t>(v) * c.Hkv * Gv + kvh * Gv + k * c.G + gi) *
+  const int sb_in = c.shared_blocks[g];
+  const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);
+  if (c.checked && lane == 0 && (sb != sb_in || c.ctx[i] < sb * c.bs))
+    record_error(c.err, kErrContext);  // the group's shared blocks are not all this member's
+  // the prefix record of this (member, head); a member beyond the group size
+  // bound has none (the caller broke the contract: nothing is read)
+  const bool has_prefix = sb > 0 && kg >= 0 && kg * c.G < c.prefix_rows;
+  const float* rp = c.rec_p + ((static_cast<int64_t>(g) * c.Hkv + kvh) * c.prefix_rows +
+                               (has_prefix ? kg * c.G + gi : 0)) *
                                   kRecStride;
   const float* rs = c.rec_s + idx * kRecStride;
   const float mp = has_prefix ? __ldcg(rp + 128) : -INFINITY;
@@ -171,8 +173,6 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   float ms, ls;
   float4 own;
   if (c.own_cap >= 0) {
-    const int sb_in = c.shared_blocks[g];
-    const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);
     int n = c.ctx[i] - sb * c.bs;
     if (n > c.own_cap) {
       if (c.checked && (threadIdx.x & 31) == 0) record_error(c.err, kErrContext);

@@ -20,9 +20,9 @@ struct CascadeParams {
   uint16_t* out;                 // [B][Hq][128]
   int32_t B, Hq, Hkv, G, max_blocks, num_groups;
   int32_t bs;
-  int32_t m;   // sequences per prefix entry (their heads stacked: m * G <= 16)
-  int32_t SG;  // prefix entries per group: ceil(largest group / m)
-  int32_t Vp;  // num_groups * SG
+  int32_t m;   // (unused: 0)
+  int32_t SG;  // (unused: 0)
+  int32_t Vp;  // prefix entries built by the prep kernel (0: it builds the own-part tables only)
   int32_t checked;
   int* err;
   // own positions attended in the merge kernel (own_cap >= 0: at most own_cap
@@ -37,8 +37,9 @@ struct CascadeParams {
   int32_t* ctx_p;     // [Vp]
   int32_t* tables_s;  // [B][max_blocks]
   int32_t* ctx_s;     // [B]
-  float* rec_p;       // [Vp][Hkv * m*G][kRecStride]
+  float* rec_p;       // [num_groups][Hkv][prefix_rows][kRecStride] (tensor-core prefill kernel)
   float* rec_s;       // [B][Hq][kRecStride]
+  int32_t prefix_rows;  // largest group x G: record rows per (group, KV head)
 };
 
 cudaError_t launch_cascade_prep(const CascadeParams& c, cudaStream_t stream);

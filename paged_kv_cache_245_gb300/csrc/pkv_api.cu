@@ -320,9 +320,14 @@ constexpr int32_t kInlineOwnMax = 256;
 
 // Shared-prefix plan: prefix entries stack the heads of m sequences (m * G
 // <= 16 query heads per KV head); workspace regions, 256-byte aligned.
+static_assert(pkv::kPrefillRecStride == pkv::kRecStride, "one record layout for every kernel");
+
+// Workspace of the shared-prefix call: the prefix records (one per group,
+// KV head and (member, query head) row), and for own parts attended by the
+// tensor-core decode pass, their tables, lengths and records.
 struct SharedPlan {
-  int32_t m = 0, SG = 0, Vp = 0, Gv = 0;
-  size_t q_p = 0, tables_p = 0, ctx_p = 0, tables_s = 0, ctx_s = 0, rec_p = 0, rec_s = 0, tc = 0;
+  int32_t rows = 0;  // largest group x G
+  size_t tables_s = 0, ctx_s = 0, rec_p = 0, rec_s = 0, tc = 0;
   size_t total = 0;
 };
 
@@ -330,23 +335,16 @@ SharedPlan shared_plan(int32_t B, int32_t num_groups, int32_t max_group_size, in
                        const pkv_heads& h, int sms) {
   SharedPlan s;
   const int32_t G = h.num_q_heads / h.num_kv_heads;
-  s.m = pkv::kTcRecHeads / G;  // 16 query heads per KV head at most
-  s.Gv = s.m * G;
-  s.SG = (max_group_size + s.m - 1) / s.m;
-  s.Vp = num_groups * s.SG;
+  s.rows = max_group_size * G;
   size_t at = 0;
   auto take = [&](size_t bytes) {
     const size_t here = at;
     at += (bytes + 255) / 256 * 256;
     return here;
   };
-  const size_t vp = static_cast<size_t>(s.Vp);
-  s.q_p = take(vp * h.num_kv_heads * s.Gv * pkv::kHeadDim * 2);
-  s.tables_p = take(vp * max_blocks * 4);
-  s.ctx_p = take(vp * 4);
+  s.rec_p = take(static_cast<size_t>(num_groups) * h.num_kv_heads * s.rows * pkv::kRecStride * 4);
   s.tables_s = take(static_cast<size_t>(B) * max_blocks * 4);
   s.ctx_s = take(static_cast<size_t>(B) * 4);
-  s.rec_p = take(vp * h.num_kv_heads * s.Gv * pkv::kRecStride * 4);
   s.rec_s = take(static_cast<size_t>(B) * h.num_q_heads * pkv::kRecStride * 4);
   s.tc = take(pkv::tc_workspace_bytes(tc_ctas(sms)));
   s.total = at;
@@ -535,8 +533,6 @@ pkv_status pkv_paged_decode_attention_shared(
   if (st != PKV_OK) return st;
   const SharedPlan sp = shared_plan(num_seqs, num_groups, max_group_size, max_blocks_per_seq,
                                     heads, sms);
-  if (static_cast<int64_t>(num_groups) * sp.SG > 65535)
-    return fail(PKV_ERR_UNSUPPORTED, "too many prefix entries");
   if (!workspace || workspace_bytes < sp.total)
     return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", sp.total,
                 workspace ? workspace_bytes : size_t{0});
@@ -557,9 +553,8 @@ pkv_status pkv_paged_decode_attention_shared(
   c.max_blocks = max_blocks_per_seq;
   c.num_groups = num_groups;
   c.bs = block_size;
-  c.m = sp.m;
-  c.SG = sp.SG;
-  c.Vp = sp.Vp;
+  c.Vp = 0;  // the prep kernel builds own-part tables only
+  c.prefix_rows = sp.rows;
   c.checked = g_checked.load();
   c.err = err;
   c.k_cache = static_cast<const uint16_t*>(k_cache);
@@ -567,36 +562,68 @@ pkv_status pkv_paged_decode_attention_shared(
   c.qscale = scale * 1.4426950408889634f;  // log2(e)
   // short own parts are attended in the merge kernel (no second launch)
   c.own_cap = max_own_tokens >= 0 && max_own_tokens <= kInlineOwnMax ? max_own_tokens : -1;
-  c.q_p = reinterpret_cast<uint16_t*>(ws + sp.q_p);
-  c.tables_p = reinterpret_cast<int32_t*>(ws + sp.tables_p);
-  c.ctx_p = reinterpret_cast<int32_t*>(ws + sp.ctx_p);
   c.tables_s = reinterpret_cast<int32_t*>(ws + sp.tables_s);
   c.ctx_s = reinterpret_cast<int32_t*>(ws + sp.ctx_s);
   c.rec_p = reinterpret_cast<float*>(ws + sp.rec_p);
   c.rec_s = reinterpret_cast<float*>(ws + sp.rec_s);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t ce = pkv::launch_cascade_prep(c, s);
-  if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prep launch");
-  // the shared positions, once per m sequences, then (unless the merge kernel
-  // takes them) every sequence's own
-  for (int part = 0; part < (c.own_cap >= 0 ? 1 : 2); ++part) {
+  cudaError_t ce = cudaSuccess;
+  if (c.own_cap < 0) {  // own parts by the tensor-core decode pass: their tables
+    ce = pkv::launch_cascade_prep(c, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prep launch");
+  }
+  // The shared positions, once per group: every (member, query head) row of
+  // a group against its shared blocks on the tcgen05 prefill kernel (no
+  // causal mask), records out.
+  {
+    int run_rows = 128;  // gcd(block_size, 128)
+    while (block_size % run_rows != 0) run_rows >>= 1;
+    alignas(64) CUtensorMap tk;
+    alignas(64) CUtensorMap tv;
+    if (!pkv::encode_prefill_runs(&tk, k_cache, rows_total, run_rows) ||
+        !pkv::encode_prefill_runs(&tv, v_cache, rows_total, run_rows))
+      return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
+    pkv::PrefillParams pp;
+    std::memset(&pp, 0, sizeof pp);
+    pp.q = c.q;
+    pp.block_tables = block_tables;
+    pp.bs = block_size;
+    pp.num_blocks = num_blocks;
+    pp.max_blocks = max_blocks_per_seq;
+    pp.num_seqs = num_groups;
+    pp.Hq = heads.num_q_heads;
+    pp.Hkv = heads.num_kv_heads;
+    pp.G = c.G;
+    pp.max_q = max_group_size;
+    pp.run_rows = run_rows;
+    pp.qscale = c.qscale;
+    pp.checked = c.checked;
+    pp.err = err;
+    pp.prefix = 1;
+    pp.group_start = group_start;
+    pp.shared_blocks = shared_blocks;
+    pp.rec_out = c.rec_p;
+    pp.prefix_rows = sp.rows;
+    ce = pkv::launch_prefill(tk, tv, pp, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prefix launch");
+  }
+  if (c.own_cap < 0) {  // every sequence's own positions: tensor-core decode, records
     pkv::TcParams t;
     std::memset(&t, 0, sizeof t);
-    const bool prefix = part == 0;
-    t.q = prefix ? c.q_p : c.q;
+    t.q = c.q;
     t.out = c.out;  // unused: record mode
-    t.rec_out = prefix ? c.rec_p : c.rec_s;
-    t.ctx_lens = prefix ? c.ctx_p : c.ctx_s;
-    t.block_tables = prefix ? c.tables_p : c.tables_s;
+    t.rec_out = c.rec_s;
+    t.ctx_lens = c.ctx_s;
+    t.block_tables = c.tables_s;
     t.bs = block_size;
     t.num_blocks = num_blocks;
     t.max_blocks = max_blocks_per_seq;
-    t.num_seqs = prefix ? c.Vp : num_seqs;
+    t.num_seqs = num_seqs;
     t.Hkv = heads.num_kv_heads;
-    t.G = prefix ? sp.Gv : c.G;
+    t.G = c.G;
     t.Hq = t.Hkv * t.G;
-    t.max_context = prefix ? max_blocks_per_seq * block_size : max_context;
-    t.qscale = scale * 1.4426950408889634f;  // log2(e)
+    t.max_context = max_context;
+    t.qscale = c.qscale;
     t.checked = c.checked;
     t.err = err;
     const pkv::TcStatus ts = pkv::launch_decode_tc(t, false, k_cache, v_cache, rows_total, 1,

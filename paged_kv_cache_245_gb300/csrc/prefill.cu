@@ -258,24 +258,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   grid_dependency_trigger();
 
-  const int q0 = p.cu_q[i];
-  const int Lq = p.cu_q[i + 1] - q0;
-  const int ctx = p.ctx_lens[i];
-  if (p.checked) {
-    const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.bs;
-    if (Lq < 0 || Lq > p.max_q || ctx < Lq || ctx > cap) {
-      if (tid == 0 && blockIdx.x == 0 && kvh == 0) record_error(p.err, kErrContext);
-      return;
+  // Chunk of sequence i (prefill), or group z's members (shared prefix):
+  // rows r -> (token or member r / G, query head r % G), q rows q0 + r / G.
+  const bool prefix = p.prefix != 0;
+  const int seq = prefix ? p.group_start[i] : i;  // whose block table
+  const int q0 = prefix ? seq : p.cu_q[i];
+  const int Lq = prefix ? p.group_start[i + 1] - seq : p.cu_q[i + 1] - q0;
+  int ctx;
+  if (prefix) {
+    const int sb = min(max(p.shared_blocks[i], 0), p.max_blocks);
+    ctx = sb * static_cast<int>(p.bs);  // the shared positions
+  } else {
+    ctx = p.ctx_lens[i];
+    if (p.checked) {
+      const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.bs;
+      if (Lq < 0 || Lq > p.max_q || ctx < Lq || ctx > cap) {
+        if (tid == 0 && blockIdx.x == 0 && kvh == 0) record_error(p.err, kErrContext);
+        return;
+      }
     }
   }
   const int rows = Lq * G;
   const int row0 = rt * 2 * kRowTile;
   if (row0 >= rows) return;  // this CTA's rows lie past the chunk (uniform)
-  const int base = ctx - Lq;  // position of the chunk's first token
+  // key positions: causal (token j of a chunk at ctx - Lq + j) or, for a
+  // prefix, every shared position for every row
+  const int base = prefix ? ctx - 1 : ctx - Lq;
   const int last_row = min(row0 + 2 * kRowTile, rows) - 1;
-  const int kend = base + last_row / G + 1;  // keys this CTA needs
-  if (kend <= 0) return;  // only when ctx < Lq (caught in checked mode)
+  const int kend = prefix ? ctx : base + last_row / G + 1;  // keys this CTA needs
+  if (kend <= 0) return;  // ctx < Lq (caught in checked mode), or nothing shared
   const int ntiles = (kend + kKeys - 1) / kKeys;
+  const bool two = rows > row0 + kRowTile;  // row tile 1 holds rows (else it idles)
 
   // Producer state (warp 8): lanes 0-7 copy K of run r of a tile, lanes
   // 16-23 V of the same run; every row tile of the sequence and KV head
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kpos = j * kKeys + prun * run;
     int32_t e = -1;
     if (j < ntiles && prun < runs && kpos < ctx) {
-      e = p.block_tables[static_cast<int64_t>(i) * p.max_blocks + kpos / p.bs];
+      e = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs];
       if (p.checked && (e < 0 || e >= p.num_blocks)) {
         record_error(p.err, kErrBlockId);
         e = -1;  // skip the copy: stale rows, undefined output, no fault
@@ -339,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rr = valid ? r : rows - 1;          // padding rows mirror the last row
   const int tok = rr / G;
   const int head = kvh * G + rr % G;
-  const int pos = base + tok;
+  const int pos = prefix ? base : base + tok;
   const int64_t qrow = (static_cast<int64_t>(q0) + tok) * p.Hq + head;
 
   // Prologue: every role starts its global reads before the CTA-wide barrier.
@@ -379,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_addr(smem);
 
-  if (warp < 8) {
+  if (warp < 8 && t == 1 && !two) {
+    // row tile 1 holds no rows: its softmax warpgroup has nothing to do
+  } else if (warp < 8) {
     // ================= softmax warpgroups =================
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + t * 128;
@@ -532,7 +547,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&pfull[t]);
     }
     if (ok) ok = __all_sync(kFull, wait_or_abort(&ofull[t], 0, abort, p.err));
-    if (ok) {
+    if (ok && prefix) {
+      // fp32 record of this (member, head): o / l, m, l
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* rec = p.rec_out + ((static_cast<int64_t>(blockIdx.z) * p.Hkv + kvh) * p.prefix_rows +
+                                row0 + t * kRowTile + lr) *
+                                   kPrefillRecStride;
+#pragma unroll
+      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(w, o_tm + c0);
+        tmem_wait_ld(w);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(rec + c0)[q] =
+                make_float4(__uint_as_float(w[4 * q]) * inv, __uint_as_float(w[4 * q + 1]) * inv,
+                            __uint_as_float(w[4 * q + 2]) * inv, __uint_as_float(w[4 * q + 3]) * inv);
+        }
+      }
+      if (valid) {
+        rec[128] = m_used;
+        rec[129] = l;
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * kHeadDim);
@@ -565,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kv_half) mbar_wait_bounded(&kfull[issued & 1], (issued >> 1) & 1);
     }
-  } else {
+  } else if (warp == 9) {
     // ================= MMA issuer (warp 9, lane 0 issues) =================
     auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
       const uint32_t q_addr = smem_base + t * kOpBytes;
@@ -591,8 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         issue_s(0, 0);
         umma_commit(&sfull[0]);
-        issue_s(1, 0);
-        umma_commit(&sfull[1]);
+        if (two) {
+          issue_s(1, 0);
+          umma_commit(&sfull[1]);
+        }
         if (kStages < ntiles) umma_commit(&kempty[0]);
       }
       __syncwarp();
@@ -619,14 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         issue_pv(0, j);
+        if (!two && j + kStages < ntiles) umma_commit(&vempty[s]);
         if (more) {
           issue_s(0, j + 1);
           umma_commit(&sfull[0]);
+          if (!two && j + 1 + kStages < ntiles) umma_commit(&kempty[s ^ 1]);
         } else {
           umma_commit(&ofull[0]);
         }
       }
       __syncwarp();
+      if (!two) continue;  // a single row tile
       ok = __all_sync(kFull, wait_or_abort(&pfull[1], j & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
