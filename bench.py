@@ -285,8 +285,8 @@ class DeviceWorkload:
         # plus one block copy launch (all layers) when the step copies on write
         cow = 0 if self.cow is None else 1
         if self.groups is not None:
-            # append; prep, prefix main + combine, merge (own parts in the merge)
-            return self.shape.num_layers * 5 + cow
+            # append; the prefix on the prefill kernel; the merge (own parts in the merge)
+            return self.shape.num_layers * 3 + cow
         if self.uses_tc:
             return self.shape.num_layers * 3 + cow
         return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0)) + cow
@@ -431,8 +431,9 @@ def run_gpu(args, world, rank, local):
                          "%.0f MB per layer" % (nl * alg / 1e9, alg / 1e6),
                    "step": ("block_copy of %d copy-on-write pairs (all layers), then "
                             % len(wl.cow) if wl.cow is not None else "")
-                           + ("per layer: kv_append + paged_decode_attention_shared (shared "
-                              "prompt blocks read once per 2 branches)" if wl.groups is not None
+                           + ("per layer: kv_append + paged_decode_attention_shared (each "
+                              "group's shared prompt blocks read once for all its branches)"
+                              if wl.groups is not None
                               else "per layer: paged_decode_step = kv_append + "
                               "paged_decode_attention (main + combine) in one C-ABI call")},
         "hbm_tbs": round(achieved_gbs / 1e3, 4),
@@ -440,8 +441,8 @@ def run_gpu(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                      "traffic": _profiled_traffic(args.workload),
-                     "kernel": "paged_decode_attention_shared call (prep, decode_tc_kernel "
-                               "with combine, merge with the own positions)"
+                     "kernel": "paged_decode_attention_shared call (prefill_kernel in "
+                               "prefix mode, then cascade_merge_kernel with the own positions)"
                                if wl.groups is not None else
                                "paged_decode_attention call (decode_tc_kernel + "
                                "decode_tc_combine_kernel)" if wl.uses_tc else

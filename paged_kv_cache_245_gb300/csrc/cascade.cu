@@ -32,49 +32,13 @@ __device__ __forceinline__ int group_of(const int32_t* group_start, int num_grou
 
 }  // namespace
 
-// Blocks [0, Vp): prefix entries; blocks [Vp, Vp + B): suffix entries.
+// One block per sequence: the table and length of its own positions (after
+// the group's shared blocks), for the tensor-core decode pass.
 __global__ void __launch_bounds__(256) cascade_prep_kernel(const CascadeParams c) {
   grid_dependency_wait();
   grid_dependency_trigger();
   const int tid = threadIdx.x;
-  const int Gv = c.m * c.G;
-  if (blockIdx.x < static_cast<unsigned>(c.Vp)) {
-    const int v = blockIdx.x;
-    const int g = v / c.SG;
-    const int s = v % c.SG;
-    const int first = c.group_start[g] + s * c.m;
-    const int end = c.group_start[g + 1];
-    const int count = end - first < c.m ? end - first : c.m;
-    const int sb_in = count > 0 ? c.shared_blocks[g] : 0;
-    const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);  // stay in the tables
-    if (tid == 0) c.ctx_p[v] = sb * c.bs;
-    for (int j = tid; j < sb; j += blockDim.x)
-      c.tables_p[static_cast<int64_t>(v) * c.max_blocks + j] =
-          c.block_tables[static_cast<int64_t>(first) * c.max_blocks + j];
-    // query rows: [Hkv][Gv][128], member k's head gi at row k * G + gi
-    const int rows = c.Hkv * Gv;
-    for (int idx = tid; idx < rows * 16; idx += blockDim.x) {
-      const int row = idx >> 4;
-      const int chunk = idx & 15;
-      const int kvh = row / Gv;
-      const int r = row % Gv;
-      const int k = r / c.G;
-      const int gi = r % c.G;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (k < count && sb > 0)
-        val = ld_global_nc_v4(c.q + (static_cast<int64_t>(first + k) * c.Hq + kvh * c.G + gi) *
-                                        kHeadDim + chunk * 8);
-      *reinterpret_cast<uint4*>(c.q_p + (static_cast<int64_t>(v) * rows + row) * kHeadDim +
-                                chunk * 8) = val;
-    }
-    if (c.checked && tid == 0 && count > 0) {
-      bool bad = sb != sb_in;
-      for (int i = first; i < first + count; ++i) bad |= c.ctx[i] < sb * c.bs;
-      if (bad) record_error(c.err, kErrContext);
-    }
-    return;
-  }
-  const int i = blockIdx.x - c.Vp;
+  const int i = blockIdx.x;
   if (i >= c.B) return;
   const int g = group_of(c.group_start, c.num_groups, i);
   const int sb_in = c.shared_blocks[g];
@@ -201,8 +165,8 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
 }
 
 cudaError_t launch_cascade_prep(const CascadeParams& c, cudaStream_t stream) {
-  return launch_pdl(cascade_prep_kernel, dim3(static_cast<unsigned>(c.Vp + c.B)), dim3(256), 0,
-                    stream, c);
+  return launch_pdl(cascade_prep_kernel, dim3(static_cast<unsigned>(c.B)), dim3(256), 0, stream,
+                    c);
 }
 
 cudaError_t launch_cascade_merge(const CascadeParams& c, cudaStream_t stream) {

@@ -1,6 +1,6 @@
 // cascade.cuh -- parameters and launchers of the shared-prefix decode path
-// (cascade.cu): building the virtual prefix / suffix batches and merging
-// their (o, m, l) records.
+// (cascade.cu): the own-position tables for the tensor-core pass, and the
+// merge of the prefix and own (o, m, l) parts.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -20,9 +20,6 @@ struct CascadeParams {
   uint16_t* out;                 // [B][Hq][128]
   int32_t B, Hq, Hkv, G, max_blocks, num_groups;
   int32_t bs;
-  int32_t m;   // (unused: 0)
-  int32_t SG;  // (unused: 0)
-  int32_t Vp;  // prefix entries built by the prep kernel (0: it builds the own-part tables only)
   int32_t checked;
   int* err;
   // own positions attended in the merge kernel (own_cap >= 0: at most own_cap
@@ -32,9 +29,6 @@ struct CascadeParams {
   float qscale;                  // scale * log2(e)
   int32_t own_cap;
   // workspace
-  uint16_t* q_p;      // [Vp][Hkv][m*G][128]
-  int32_t* tables_p;  // [Vp][max_blocks]
-  int32_t* ctx_p;     // [Vp]
   int32_t* tables_s;  // [B][max_blocks]
   int32_t* ctx_s;     // [B]
   float* rec_p;       // [num_groups][Hkv][prefix_rows][kRecStride] (tensor-core prefill kernel)

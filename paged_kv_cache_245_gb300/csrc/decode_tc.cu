@@ -125,8 +125,8 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
   p.seg_cost = seg_cost;
   p.rec = static_cast<float*>(workspace);
   cudaError_t e;
-  if (p.G > kTcHeads) {  // two n-tiles of query heads: paged, 8 warps x 3 stages
-    e = contig ? cudaErrorInvalidValue : launch_cfg<false, 8, 3, 2>(tk, tv, p, num_ctas, stream);
+  if (p.G > kTcHeads) {  // one n-tile of 8 query heads per KV head (the API allows G <= 8)
+    e = cudaErrorInvalidValue;
   } else if (contig) {
     e = cfg == 1 ? launch_cfg<true, 12, 2>(tk, tv, p, num_ctas, stream)
                  : launch_cfg<true, 8, 3>(tk, tv, p, num_ctas, stream);

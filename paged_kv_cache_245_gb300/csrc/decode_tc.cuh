@@ -83,8 +83,8 @@ __device__ __forceinline__ int tc_context(const TcParams& p, int i, bool contig,
   return ctx;
 }
 
-// NT n-tiles of 8 query heads per KV head (NT = 2: groups of up to 16 query
-// heads, e.g. the stacked heads of two sequences that share a prefix).
+// NT n-tiles of 8 query heads per KV head (instantiated with NT = 1: GQA
+// groups of up to 8 query heads).
 template <bool kContig, int W, int S, int NT>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,

@@ -553,7 +553,6 @@ pkv_status pkv_paged_decode_attention_shared(
   c.max_blocks = max_blocks_per_seq;
   c.num_groups = num_groups;
   c.bs = block_size;
-  c.Vp = 0;  // the prep kernel builds own-part tables only
   c.prefix_rows = sp.rows;
   c.checked = g_checked.load();
   c.err = err;
