@@ -125,40 +125,54 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   const int sb = sb_in < 0 ? 0 : (sb_in > c.max_blocks ? c.max_blocks : sb_in);
   if (c.checked && lane == 0 && (sb != sb_in || c.ctx[i] < sb * c.bs))
     record_error(c.err, kErrContext);  // the group's shared blocks are not all this member's
-  // the prefix record of this (member, head); a member beyond the group size
-  // bound has none (the caller broke the contract: nothing is read)
-  const bool has_prefix = sb > 0 && kg >= 0 && kg * c.G < c.prefix_rows;
-  const float* rp = c.rec_p + ((static_cast<int64_t>(g) * c.Hkv + kvh) * c.prefix_rows +
-                               (has_prefix ? kg * c.G + gi : 0)) *
-                                  kRecStride;
+  // The own part: attended here, or the tensor-core pass's record.
   const float* rs = c.rec_s + idx * kRecStride;
-  const float mp = has_prefix ? __ldcg(rp + 128) : -INFINITY;
-  const float lp = has_prefix ? __ldcg(rp + 129) : 0.f;
   float ms, ls;
-  float4 own;
+  float4 os;
   if (c.own_cap >= 0) {
     int n = c.ctx[i] - sb * c.bs;
     if (n > c.own_cap) {
       if (c.checked && (threadIdx.x & 31) == 0) record_error(c.err, kErrContext);
       n = c.own_cap;  // the bound was wrong: the later positions are left out
     }
-    own_attention(c, i, h, sb, n > 0 ? n : 0, own, ms, ls);
+    own_attention(c, i, h, sb, n > 0 ? n : 0, os, ms, ls);
     const float inv_own = ls > 0.f ? 1.f / ls : 0.f;
-    own = make_float4(own.x * inv_own, own.y * inv_own, own.z * inv_own, own.w * inv_own);
+    os = make_float4(os.x * inv_own, os.y * inv_own, os.z * inv_own, os.w * inv_own);
   } else {
     ms = __ldcg(rs + 128);
     ls = __ldcg(rs + 129);
+    os = ls > 0.f ? __ldcg(reinterpret_cast<const float4*>(rs) + lane)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  const bool hp = lp > 0.f, hs = ls > 0.f;
-  const float M = fmaxf(hp ? mp : -INFINITY, hs ? ms : -INFINITY);
-  const float wp = hp ? lp * fast_exp2(mp - M) : 0.f;
-  const float ws = hs ? ls * fast_exp2(ms - M) : 0.f;
-  const float inv = wp + ws > 0.f ? 1.f / (wp + ws) : 0.f;
-  const float4 op = hp ? __ldcg(reinterpret_cast<const float4*>(rp) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 os = !hs ? make_float4(0.f, 0.f, 0.f, 0.f)
-                  : (c.own_cap >= 0 ? own : __ldcg(reinterpret_cast<const float4*>(rs) + lane));
-  const float x = (wp * op.x + ws * os.x) * inv, y = (wp * op.y + ws * os.y) * inv;
-  const float z = (wp * op.z + ws * os.z) * inv, w = (wp * op.w + ws * os.w) * inv;
+  // Fold in the prefix records, one per chunk of the shared positions (a
+  // member beyond the group size bound has none: the caller broke the
+  // contract, nothing is read):  M' = max(M, m),  acc' = acc 2^(M - M') +
+  // l 2^(m - M') o,  W' = W 2^(M - M') + l 2^(m - M').
+  float M = ls > 0.f ? ms : -INFINITY;
+  float W = ls > 0.f ? ls : 0.f;
+  float4 acc = ls > 0.f ? make_float4(os.x * ls, os.y * ls, os.z * ls, os.w * ls)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool member = kg >= 0 && kg * c.G < c.prefix_rows;
+  const int chunks = member ? (sb * c.bs + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys : 0;
+  for (int k = 0; k < chunks; ++k) {
+    const float* rp = c.rec_p + (((static_cast<int64_t>(g) * c.prefix_chunks + k) * c.Hkv + kvh) *
+                                     c.prefix_rows +
+                                 kg * c.G + gi) *
+                                    kRecStride;
+    const float mp = __ldcg(rp + 128);
+    const float lp = __ldcg(rp + 129);
+    if (!(lp > 0.f)) continue;
+    const float Mn = fmaxf(M, mp);
+    const float a = W > 0.f ? fast_exp2(M - Mn) : 0.f;
+    const float wgt = lp * fast_exp2(mp - Mn);
+    const float4 op = __ldcg(reinterpret_cast<const float4*>(rp) + lane);
+    acc = make_float4(acc.x * a + wgt * op.x, acc.y * a + wgt * op.y, acc.z * a + wgt * op.z,
+                      acc.w * a + wgt * op.w);
+    W = W * a + wgt;
+    M = Mn;
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  const float x = acc.x * inv, y = acc.y * inv, z = acc.z * inv, w = acc.w * inv;
   const uint32_t lo16 = f32_to_bf16_bits(x) | (uint32_t(f32_to_bf16_bits(y)) << 16);
   const uint32_t hi16 = f32_to_bf16_bits(z) | (uint32_t(f32_to_bf16_bits(w)) << 16);
   *reinterpret_cast<uint2*>(c.out + idx * kHeadDim + lane * 4) = make_uint2(lo16, hi16);

@@ -325,6 +325,18 @@ static_assert(pkv::kPrefillRecStride == pkv::kRecStride, "one record layout for 
 // Workspace of the shared-prefix call: the prefix records (one per group,
 // KV head and (member, query head) row), and for own parts attended by the
 // tensor-core decode pass, their tables, lengths and records.
+constexpr int kMaxPrefixChunks = 8;  // chunks of a group's shared positions (bound)
+
+// Chunk of the shared positions for the prefix kernel: whole blocks, a
+// multiple of 128 positions, at least 2048 positions, and at most
+// kMaxPrefixChunks chunks per group.
+int32_t prefix_chunk_blocks(int32_t max_blocks, int32_t block_size) {
+  auto up8 = [](int64_t x) { return static_cast<int32_t>((x + 7) / 8 * 8); };
+  const int32_t a = up8((max_blocks + kMaxPrefixChunks - 1) / kMaxPrefixChunks);
+  const int32_t b = up8((2048 + block_size - 1) / block_size);
+  return a > b ? a : b;
+}
+
 struct SharedPlan {
   int32_t rows = 0;  // largest group x G
   size_t tables_s = 0, ctx_s = 0, rec_p = 0, rec_s = 0, tc = 0;
@@ -342,7 +354,8 @@ SharedPlan shared_plan(int32_t B, int32_t num_groups, int32_t max_group_size, in
     at += (bytes + 255) / 256 * 256;
     return here;
   };
-  s.rec_p = take(static_cast<size_t>(num_groups) * h.num_kv_heads * s.rows * pkv::kRecStride * 4);
+  s.rec_p = take(static_cast<size_t>(num_groups) * kMaxPrefixChunks * h.num_kv_heads * s.rows *
+                 pkv::kRecStride * 4);
   s.tables_s = take(static_cast<size_t>(B) * max_blocks * 4);
   s.ctx_s = take(static_cast<size_t>(B) * 4);
   s.rec_s = take(static_cast<size_t>(B) * h.num_q_heads * pkv::kRecStride * 4);
@@ -554,6 +567,11 @@ pkv_status pkv_paged_decode_attention_shared(
   c.num_groups = num_groups;
   c.bs = block_size;
   c.prefix_rows = sp.rows;
+  const int32_t chunk_blocks = prefix_chunk_blocks(max_blocks_per_seq, block_size);
+  c.prefix_chunks = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
+  c.prefix_chunk_keys = chunk_blocks * block_size;
+  if (static_cast<int64_t>(num_groups) * c.prefix_chunks > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "too many groups");
   c.checked = g_checked.load();
   c.err = err;
   c.k_cache = static_cast<const uint16_t*>(k_cache);
@@ -589,7 +607,7 @@ pkv_status pkv_paged_decode_attention_shared(
     pp.bs = block_size;
     pp.num_blocks = num_blocks;
     pp.max_blocks = max_blocks_per_seq;
-    pp.num_seqs = num_groups;
+    pp.num_seqs = num_groups * c.prefix_chunks;  // items: (group, chunk)
     pp.Hq = heads.num_q_heads;
     pp.Hkv = heads.num_kv_heads;
     pp.G = c.G;
@@ -603,6 +621,8 @@ pkv_status pkv_paged_decode_attention_shared(
     pp.shared_blocks = shared_blocks;
     pp.rec_out = c.rec_p;
     pp.prefix_rows = sp.rows;
+    pp.prefix_chunks = c.prefix_chunks;
+    pp.prefix_chunk_keys = c.prefix_chunk_keys;
     ce = pkv::launch_prefill(tk, tv, pp, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prefix launch");
   }

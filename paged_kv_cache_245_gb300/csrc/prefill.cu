@@ -261,13 +261,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Chunk of sequence i (prefill), or group z's members (shared prefix):
   // rows r -> (token or member r / G, query head r % G), q rows q0 + r / G.
   const bool prefix = p.prefix != 0;
-  const int seq = prefix ? p.group_start[i] : i;  // whose block table
+  const int grp = prefix ? i / p.prefix_chunks : i;     // group (prefix) or sequence
+  const int seq = prefix ? p.group_start[grp] : i;      // whose block table
   const int q0 = prefix ? seq : p.cu_q[i];
-  const int Lq = prefix ? p.group_start[i + 1] - seq : p.cu_q[i + 1] - q0;
+  const int Lq = prefix ? p.group_start[grp + 1] - seq : p.cu_q[i + 1] - q0;
+  // keys from kbase (a chunk of a group's shared positions; 0 for prefill)
+  const int kbase = prefix ? (i % p.prefix_chunks) * p.prefix_chunk_keys : 0;
   int ctx;
   if (prefix) {
-    const int sb = min(max(p.shared_blocks[i], 0), p.max_blocks);
+    const int sb = min(max(p.shared_blocks[grp], 0), p.max_blocks);
     ctx = sb * static_cast<int>(p.bs);  // the shared positions
+    if (kbase >= ctx) return;          // a chunk past them (uniform)
   } else {
     ctx = p.ctx_lens[i];
     if (p.checked) {
@@ -285,9 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // prefix, every shared position for every row
   const int base = prefix ? ctx - 1 : ctx - Lq;
   const int last_row = min(row0 + 2 * kRowTile, rows) - 1;
-  const int kend = prefix ? ctx : base + last_row / G + 1;  // keys this CTA needs
-  if (kend <= 0) return;  // ctx < Lq (caught in checked mode), or nothing shared
-  const int ntiles = (kend + kKeys - 1) / kKeys;
+  const int kend = prefix ? min(ctx, kbase + p.prefix_chunk_keys)  // keys this CTA needs
+                          : base + last_row / G + 1;
+  if (kend <= 0) return;  // only when ctx < Lq (caught in checked mode)
+  const int ntiles = (kend - kbase + kKeys - 1) / kKeys;
   const bool two = rows > row0 + kRowTile;  // row tile 1 holds rows (else it idles)
 
   // Producer state (warp 8): lanes 0-7 copy K of run r of a tile, lanes
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int prun = lane & 15;
   // block-table entry of run prun of tile j (-1: past the context or rejected)
   auto entry = [&](int j) -> int32_t {
-    const int kpos = j * kKeys + prun * run;
+    const int kpos = kbase + j * kKeys + prun * run;
     int32_t e = -1;
     if (j < ntiles && prun < runs && kpos < ctx) {
       e = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs];
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = j0; j < j1; ++j) {
       const int s = j & 1;
       const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
-      const int off = (j * kKeys + prun * run) % p.bs;
+      const int off = (kbase + j * kKeys + prun * run) % p.bs;
       const int32_t grp =
           e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
       unsigned char* dst = smem + kOffK + s * kStageBytes + prun * run * kRowBytes;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(kFull, wait_or_abort(&sfull[t], j & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      const int k0 = j * kKeys;
+      const int k0 = kbase + j * kKeys;
       const bool diag = k0 + kKeys - 1 > pos;  // some key of the tile lies past the row
       // general: a masked tile in this warp, or a negative scale (the maximum
       // of the scaled logits is then not the scaled maximum)
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_new = fmaxf(m_used, tmax);
       if (j == 0) {
-        m_used = m_new;  // finite: position 0 is visible to every row
+        m_used = m_new;  // finite: the first key of the item is visible to every row
       } else {
         const bool grow = m_new > m_used + kRescaleLog2;
         if (__any_sync(kFull, grow)) {
@@ -642,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = j & 1;
       ok = __all_sync(kFull, wait_or_abort(&vfull[s], (j >> 1) & 1, abort, p.err));
       if (!ok) break;
-      const int k0 = j * kKeys;
+      const int k0 = kbase + j * kKeys;
       if (k0 + kKeys > ctx) {  // zero V rows at or past the context (0 x stale bytes)
         unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
         const int first = ctx - k0;

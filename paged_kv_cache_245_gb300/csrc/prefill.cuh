@@ -27,13 +27,18 @@ struct PrefillParams {
   // per sequence, [B][Hq][128]); its rows are (member, query head) pairs and
   // they all attend the group's first shared_blocks[z] blocks (the first
   // member's table), with no causal mask.  Results go to rec_out as fp32
-  // records [num_groups][Hkv][prefix_rows][kPrefillRecStride]: o / l, m, l
-  // (log2 units of scale * log2 e); groups without shared blocks write none.
+  // records of kPrefillRecStride floats: o / l, m, l (log2 units of
+  // scale * log2 e); chunks past a group's shared positions write none.
   int32_t prefix;
   const int32_t* group_start;    // [num_groups + 1]
   const int32_t* shared_blocks;  // [num_groups]
   float* rec_out;
   int32_t prefix_rows;           // max group size x G
+  // A group's shared positions split into chunks of prefix_chunk_keys (a
+  // multiple of 128): item z is chunk z % prefix_chunks of group
+  // z / prefix_chunks; records [num_groups][prefix_chunks][Hkv][prefix_rows].
+  int32_t prefix_chunks;
+  int32_t prefix_chunk_keys;
 };
 
 constexpr int kPrefillRecStride = 132;  // floats per record: o[128], m, l, pad
