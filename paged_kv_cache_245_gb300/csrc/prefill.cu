@@ -230,6 +230,9 @@ __device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, in
 
 }  // namespace
 
+// kPrefix: the shared-prefix mode of PrefillParams (records out, no causal
+// mask); a separate instantiation keeps the prefill path free of its branches.
+template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Chunk of sequence i (prefill), or group z's members (shared prefix):
   // rows r -> (token or member r / G, query head r % G), q rows q0 + r / G.
-  const bool prefix = p.prefix != 0;
+  constexpr bool prefix = kPrefix;
   const int grp = prefix ? i / p.prefix_chunks : i;     // group (prefix) or sequence
   const int seq = prefix ? p.group_start[grp] : i;      // whose block table
   const int q0 = prefix ? seq : p.cu_q[i];
@@ -743,18 +746,29 @@ bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int r
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                           cudaStream_t stream) {
+namespace {
+
+template <bool kPrefix>
+cudaError_t launch_prefill_cfg(const CUtensorMap& tk, const CUtensorMap& tv,
+                               const PrefillParams& p, cudaStream_t stream) {
   static bool attr_done = false;  // one device per process in practice; repeated calls are harmless
   if (!attr_done) {
     const cudaError_t e = cudaFuncSetAttribute(
-        prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        prefill_kernel<kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int row_tiles = (p.max_q * p.G + 2 * kRowTile - 1) / (2 * kRowTile);
-  return launch_pdl(prefill_kernel, dim3(row_tiles, p.Hkv, p.num_seqs), dim3(kThreads),
+  return launch_pdl(prefill_kernel<kPrefix>, dim3(row_tiles, p.Hkv, p.num_seqs), dim3(kThreads),
                     kSmemBytes, stream, tk, tv, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           cudaStream_t stream) {
+  return p.prefix ? launch_prefill_cfg<true>(tk, tv, p, stream)
+                  : launch_prefill_cfg<false>(tk, tv, p, stream);
 }
 
 }  // namespace pkv
