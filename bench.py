@@ -670,9 +670,10 @@ def measure_e2e(wl, dev, args, world, chunks=4):
     per layer), and reads every layer's output back to pinned host memory.
     The copies are pipelined as a serving loop would, in `chunks` groups of
     layers: a group's inputs go up on one copy stream and its outputs come
-    back on another while other groups compute; inputs and outputs are
-    double-buffered across steps.  Every copy of every step is inside the
-    timed region."""
+    back on another while other groups compute.  The whole step -- copies
+    and C-ABI calls -- is captured once as a CUDA graph and replayed every
+    step, as a serving loop would; every replay moves the step's inputs and
+    outputs across the host link, inside the timed region."""
     nl = wl.shape.num_layers
     b = wl.batch
     shared = [torch.as_tensor(b.slot_mapping), torch.as_tensor(b.block_tables),
@@ -714,12 +715,10 @@ def measure_e2e(wl, dev, args, world, chunks=4):
     step_done = [ev() for _ in range(2)]
     out_read = [ev() for _ in range(2)]
     used = [False, False]
-    state = {"s": 0}
 
-    def step():
-        bi = state["s"] & 1
-        state["s"] += 1
+    def step(bi=0):
         with torch.cuda.stream(up):
+            up.wait_stream(comp)  # fork from the capturing stream
             if used[bi]:
                 up.wait_event(step_done[bi])  # kernels of two steps ago done with the buffers
             sh[1][bi].copy_(sh[0], non_blocking=True)
@@ -758,17 +757,28 @@ def measure_e2e(wl, dev, args, world, chunks=4):
                 host_out[l0:l1].copy_(out_all[l0:l1], non_blocking=True)
         step_done[bi].record(comp)
         out_read[bi].record(down)
+        comp.wait_event(out_read[bi])  # join: the step ends when its outputs are on the host
 
-    iters = max(20, args.steps // 10)
-    for _ in range(3):
+    # Graph of one step (buffers 0); replays run in stream order, one whole
+    # step after another.
+    for _ in range(2):
         step()
     torch.cuda.synchronize(dev)
+    used[0] = used[1] = False  # the graph waits on no event from outside it
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        comp = torch.cuda.current_stream(dev)
+        step()
+    iters = max(20, args.steps // 10)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(dev)
     _barrier(world)
+    comp = torch.cuda.current_stream(dev)
     a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(comp)
     for _ in range(iters):
-        step()
-    comp.wait_event(out_read[(state["s"] - 1) & 1])  # the last step's outputs are on the host
+        graph.replay()
     c.record(comp)
     torch.cuda.synchronize(dev)
     _barrier(world)
@@ -776,9 +786,10 @@ def measure_e2e(wl, dev, args, world, chunks=4):
     return {"value": round(world * b.B / (ms / 1e3 / nl), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 4), "steps": iters,
-            "how": "direct C-ABI calls (no graph); pinned H2D of the step's inputs and D2H of "
-                   "its outputs in %d groups of layers on two copy streams, pipelined with "
-                   "the kernels, all inside the timed region" % len(groups)}
+            "how": "the step's C-ABI calls and its pinned H2D inputs / D2H outputs (in %d "
+                   "groups of layers on two copy streams, pipelined with the kernels) "
+                   "captured as one CUDA graph and replayed every step; every copy inside "
+                   "the timed region" % len(groups)}
 
 
 # ------------------------------------------------------------------ CPU oracle
