@@ -877,20 +877,36 @@ def run_reference(args, world, rank):
 
 
 def profile_case(args):
-    """A small case for ncu: 4 layers of the workload (about 1 GB), a few
-    paged attention calls through the C ABI."""
+    """A small case for ncu: a few layers of the workload (about 1 GB at the
+    Llama shape; 2 layers of the sharing workload), a few attention calls
+    through the C ABI -- the shared-prefix call on the sharing workload."""
     import paged_kv_cache_245_gb300 as pkv
     from __graft_entry__ import build
     build()
     dev = torch.device("cuda", 0)
     b = rank_batch(args.workload, 0)
-    layers = [W.layer_inputs(b, l, device=dev, fast_cache=True) for l in range(4)]
+    shape, _, kind, bs, _ = WORKLOADS[args.workload]
+    nl = 2 if kind == "sharing" else 4
+    layers = [W.layer_inputs(b, l, device=dev, fast_cache=True) for l in range(nl)]
     tables = torch.as_tensor(b.block_tables, device=dev)
     ctx = torch.as_tensor(b.ctx, device=dev)
+    scale = W.default_scale(b.shape)
+    if kind == "sharing":
+        n = W.sharing_scenario(decode_steps=1).n
+        starts = np.arange(0, b.B + 1, n, dtype=np.int32)
+        shared = W.shared_prefix_blocks(b.block_tables, b.ctx, bs, starts)
+        own = int((b.ctx - np.repeat(shared, n) * bs).max())
+        gs = torch.as_tensor(starts, device=dev)
+        sb = torch.as_tensor(shared, device=dev)
     for i in range(args.profile_calls):
-        li = layers[i % 4]
-        pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, tables, ctx, b.max_context,
-                                   W.default_scale(b.shape))
+        li = layers[i % nl]
+        if kind == "sharing":
+            pkv.paged_decode_attention_shared(li.q, li.k_cache, li.v_cache, tables, ctx,
+                                              b.max_context, scale, gs, sb, n,
+                                              max_own_tokens=own)
+        else:
+            pkv.paged_decode_attention(li.q, li.k_cache, li.v_cache, tables, ctx, b.max_context,
+                                       scale)
     torch.cuda.synchronize(dev)
 
 
