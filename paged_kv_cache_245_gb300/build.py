@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["pkv_api.cu", "kv_ops.cu", "decode_paged.cu", "decode_contig.cu", "decode_tc.cu",
-           "pkv_noalloc.cu", "block_manager.cpp", "vmm.cpp", "cascade.cu", "prefill.cu"]
+           "pkv_noalloc.cu", "block_manager.cpp", "vmm.cpp", "cascade.cu", "prefill.cu", "prefix.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

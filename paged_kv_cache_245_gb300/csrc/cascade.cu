@@ -6,9 +6,9 @@
 // results (o, m, l) merged as
 //   M = max(m_a, m_b),  w_x = l_x 2^(m_x - M),  o = (w_a o_a + w_b o_b) / (w_a + w_b).
 //
-// The shared part of every group is one item of the tcgen05 prefill kernel
-// in prefix mode (prefill.cu): the group's (member, query head) rows against
-// its shared blocks, fp32 records out.  The own part after the shared blocks
+// The shared part of every group goes through the tcgen05 prefix kernel
+// (prefix.cu): the group's (member, query head) rows against its shared
+// blocks, fp32 records out (per chunk of the shared positions, two halves).  The own part after the shared blocks
 // is attended here, inside the merge (a host bound of at most 256 own
 // positions), or by the tensor-core decode kernel in record mode over a
 // virtual batch the prep kernel builds (entry i: sequence i's own positions).
@@ -153,12 +153,18 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   float4 acc = ls > 0.f ? make_float4(os.x * ls, os.y * ls, os.z * ls, os.w * ls)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
   const bool member = kg >= 0 && kg * c.G < c.prefix_rows;
-  const int chunks = member ? (sb * c.bs + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys : 0;
-  for (int k = 0; k < chunks; ++k) {
-    const float* rp = c.rec_p + (((static_cast<int64_t>(g) * c.prefix_chunks + k) * c.Hkv + kvh) *
-                                     c.prefix_rows +
-                                 kg * c.G + gi) *
-                                    kRecStride;
+  const int shared = sb * c.bs;
+  const int chunks = member ? (shared + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys : 0;
+  // per chunk two records: even and odd key tiles (the second only if the
+  // chunk has more than one tile)
+  for (int kh = 0; kh < 2 * chunks; ++kh) {
+    const int k = kh >> 1, half = kh & 1;
+    if (half == 1 && min(c.prefix_chunk_keys, shared - k * c.prefix_chunk_keys) <= 128) continue;
+    const float* rp =
+        c.rec_p + ((((static_cast<int64_t>(g) * c.prefix_chunks + k) * 2 + half) * c.Hkv + kvh) *
+                       c.prefix_rows +
+                   kg * c.G + gi) *
+                      kRecStride;
     const float mp = __ldcg(rp + 128);
     const float lp = __ldcg(rp + 129);
     if (!(lp > 0.f)) continue;

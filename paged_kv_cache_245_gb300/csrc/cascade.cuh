@@ -31,7 +31,7 @@ struct CascadeParams {
   // workspace
   int32_t* tables_s;  // [B][max_blocks]
   int32_t* ctx_s;     // [B]
-  float* rec_p;       // [num_groups][prefix_chunks][Hkv][prefix_rows][kRecStride] (prefill kernel)
+  float* rec_p;       // [num_groups][prefix_chunks][2][Hkv][prefix_rows][kRecStride] (prefix kernel)
   float* rec_s;       // [B][Hq][kRecStride]
   int32_t prefix_rows;        // largest group x G: record rows per (group, chunk, KV head)
   int32_t prefix_chunks;      // chunks of the shared positions per group (bound)

@@ -12,6 +12,7 @@
 #include "decode_launch.cuh"
 #include "cascade.cuh"
 #include "prefill.cuh"
+#include "prefix.cuh"
 #include "decode_tc_launch.h"
 #include "kv_ops.cuh"
 
@@ -320,7 +321,7 @@ constexpr int32_t kInlineOwnMax = 256;
 
 // Shared-prefix plan: prefix entries stack the heads of m sequences (m * G
 // <= 16 query heads per KV head); workspace regions, 256-byte aligned.
-static_assert(pkv::kPrefillRecStride == pkv::kRecStride, "one record layout for every kernel");
+static_assert(pkv::kPrefixRecStride == pkv::kRecStride, "one record layout for every kernel");
 
 // Workspace of the shared-prefix call: the prefix records (one per group,
 // KV head and (member, query head) row), and for own parts attended by the
@@ -354,8 +355,8 @@ SharedPlan shared_plan(int32_t B, int32_t num_groups, int32_t max_group_size, in
     at += (bytes + 255) / 256 * 256;
     return here;
   };
-  s.rec_p = take(static_cast<size_t>(num_groups) * kMaxPrefixChunks * h.num_kv_heads * s.rows *
-                 pkv::kRecStride * 4);
+  s.rec_p = take(static_cast<size_t>(num_groups) * kMaxPrefixChunks * 2 * h.num_kv_heads *
+                 s.rows * pkv::kRecStride * 4);
   s.tables_s = take(static_cast<size_t>(B) * max_blocks * 4);
   s.ctx_s = take(static_cast<size_t>(B) * 4);
   s.rec_s = take(static_cast<size_t>(B) * h.num_q_heads * pkv::kRecStride * 4);
@@ -600,30 +601,28 @@ pkv_status pkv_paged_decode_attention_shared(
     if (!pkv::encode_prefill_runs(&tk, k_cache, rows_total, run_rows) ||
         !pkv::encode_prefill_runs(&tv, v_cache, rows_total, run_rows))
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
-    pkv::PrefillParams pp;
-    std::memset(&pp, 0, sizeof pp);
-    pp.q = c.q;
-    pp.block_tables = block_tables;
-    pp.bs = block_size;
-    pp.num_blocks = num_blocks;
-    pp.max_blocks = max_blocks_per_seq;
-    pp.num_seqs = num_groups * c.prefix_chunks;  // items: (group, chunk)
-    pp.Hq = heads.num_q_heads;
-    pp.Hkv = heads.num_kv_heads;
-    pp.G = c.G;
-    pp.max_q = max_group_size;
-    pp.run_rows = run_rows;
-    pp.qscale = c.qscale;
-    pp.checked = c.checked;
-    pp.err = err;
-    pp.prefix = 1;
-    pp.group_start = group_start;
-    pp.shared_blocks = shared_blocks;
-    pp.rec_out = c.rec_p;
-    pp.prefix_rows = sp.rows;
-    pp.prefix_chunks = c.prefix_chunks;
-    pp.prefix_chunk_keys = c.prefix_chunk_keys;
-    ce = pkv::launch_prefill(tk, tv, pp, s);
+    pkv::PrefixParams pf;
+    std::memset(&pf, 0, sizeof pf);
+    pf.q = c.q;
+    pf.group_start = group_start;
+    pf.shared_blocks = shared_blocks;
+    pf.block_tables = block_tables;
+    pf.rec_out = c.rec_p;
+    pf.bs = block_size;
+    pf.num_blocks = num_blocks;
+    pf.max_blocks = max_blocks_per_seq;
+    pf.num_groups = num_groups;
+    pf.Hq = heads.num_q_heads;
+    pf.Hkv = heads.num_kv_heads;
+    pf.G = c.G;
+    pf.rows = sp.rows;
+    pf.chunks = c.prefix_chunks;
+    pf.chunk_keys = c.prefix_chunk_keys;
+    pf.run_rows = run_rows;
+    pf.qscale = c.qscale;
+    pf.checked = c.checked;
+    pf.err = err;
+    ce = pkv::launch_prefix(tk, tv, pf, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing prefix launch");
   }
   if (c.own_cap < 0) {  // every sequence's own positions: tensor-core decode, records

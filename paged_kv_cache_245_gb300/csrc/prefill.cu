@@ -39,200 +39,23 @@
 
 #include "pkv_device.cuh"
 #include "prefill.cuh"
+#include "umma.cuh"
 
 namespace pkv {
 
+using namespace umma;
+
 namespace {
 
-constexpr int kRowTile = 128;                         // query rows per tile (MMA M)
-constexpr int kKeys = 128;                            // keys per K/V tile
 constexpr int kStages = 2;
-constexpr int kOpBytes = 128 * kRowBytes;             // 32 KiB: a Q, K or V tile
-constexpr int kHalfBytes = kOpBytes / 2;              // one 64-column half
 constexpr int kOffK = 2 * kOpBytes;                   // after Q_0, Q_1
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 192 KiB
 constexpr int kSmemBytes = kTilesBytes + 256 + 1024;
 constexpr int kThreads = 320;
-constexpr uint32_t kTmemCols = 512;
-constexpr unsigned kFull = 0xffffffffu;
-constexpr float kRescaleLog2 = 8.f;
-
-// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
-// 4-5), bf16 A and B (7-9, 10-12), N / 8 (17-22), M / 16 (24-28); A K-major;
-// B K-major for S = Q K^T, MN-major (bit 16) for O = P V, whose V rows hold
-// the N (head) dimension contiguously.
-constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
-                             ((128u >> 4) << 24);
-constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
-
-// Shared-memory matrix descriptor with 128-byte swizzling: start address,
-// leading and stride byte offsets (all / 16), the fixed 0b001 at bits 46-48
-// and the swizzle mode at 61-63.  Operand tiles hold 8-row x 128-byte atoms.
-// Q (written by the softmax threads): column half h at h * 16 KiB, 8-row
-// groups 1024 bytes apart.  K and V (TMA): atom (row group g, half h) at
-// g * 2048 + h * 1024.  K-major operands (Q, K): stride = the 8-row group
-// step, leading offset unused, the k-step's half and 32-byte column offset
-// in the start address.  The MN-major V: leading offset = the step between
-// the two 64-column halves (1024), stride = 2048 bytes per 8 keys.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t policy;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
-  return policy;
-}
-
-#define PKV_R32(F, r)                                                                          \
-  F(r[0]), F(r[1]), F(r[2]), F(r[3]), F(r[4]), F(r[5]), F(r[6]), F(r[7]), F(r[8]), F(r[9]),    \
-      F(r[10]), F(r[11]), F(r[12]), F(r[13]), F(r[14]), F(r[15]), F(r[16]), F(r[17]),          \
-      F(r[18]), F(r[19]), F(r[20]), F(r[21]), F(r[22]), F(r[23]), F(r[24]), F(r[25]),          \
-      F(r[26]), F(r[27]), F(r[28]), F(r[29]), F(r[30]), F(r[31])
-#define PKV_OUT(x) "=r"(x)
-#define PKV_IN(x) "r"(x)
-#define PKV_INOUT(x) "+r"(x)
-#define PKV_LIST32                                                                             \
-  "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24," \
-  "%25,%26,%27,%28,%29,%30,%31"
-
-// 32 consecutive 32-bit columns of this warp's 32 lanes (lane = thread).  The
-// registers are valid only after tmem_wait_ld / tmem_ready on them.
-__device__ __forceinline__ void tmem_ld32(uint32_t (&r)[32], uint32_t taddr) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {" PKV_LIST32 "}, [%32];"
-               : PKV_R32(PKV_OUT, r)
-               : "r"(taddr));
-}
-
-// Wait for this thread's tensor-memory loads; the registers named here (and
-// through tmem_ready, any others loaded before the wait) are then valid.
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : PKV_R32(PKV_INOUT, r) : : "memory");
-}
-__device__ __forceinline__ void tmem_ready(uint32_t (&r)[32]) {
-  asm volatile("" : PKV_R32(PKV_INOUT, r) : : "memory");
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
-               "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,"
-               "%31,%32};" ::"r"(taddr),
-               PKV_R32(PKV_IN, r)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Packed pairs of fp32 (one register pair, lo in the low word) for the
-// two-wide fp32 instructions of sm_100 and later.
-__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Wait for phase `parity` of `bar`; give up when another role has given up
-// (*abort) or after kWaitLimitNs (then set *abort and record the timeout).
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      record_error(err, kErrTimeout);
-      return false;
-    }
-  }
-  return true;
-}
-
-// Byte offset of 16-byte chunk c (0..15) of row r in the Q tile: two
-// 64-column halves of 128 rows x 128 bytes, 128-byte swizzled.
-__device__ __forceinline__ int q_chunk_offset(int r, int c) {
-  return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
-
-// The same for a K or V tile as the 4-D boxes land: atom (r / 8, c / 8).
-__device__ __forceinline__ int kv_chunk_offset(int r, int c) {
-  return (r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
-
-__device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, int32_t group,
-                                            uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst_smem)),
-      "l"(tmap), "r"(0), "r"(0), "r"(0), "r"(group), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
 
 }  // namespace
 
-// kPrefix: the shared-prefix mode of PrefillParams (records out, no causal
-// mask); a separate instantiation keeps the prefill path free of its branches.
-template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
@@ -261,41 +84,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   grid_dependency_trigger();
 
-  // Chunk of sequence i (prefill), or group z's members (shared prefix):
-  // rows r -> (token or member r / G, query head r % G), q rows q0 + r / G.
-  constexpr bool prefix = kPrefix;
-  const int grp = prefix ? i / p.prefix_chunks : i;     // group (prefix) or sequence
-  const int seq = prefix ? p.group_start[grp] : i;      // whose block table
-  const int q0 = prefix ? seq : p.cu_q[i];
-  const int Lq = prefix ? p.group_start[grp + 1] - seq : p.cu_q[i + 1] - q0;
-  // keys from kbase (a chunk of a group's shared positions; 0 for prefill)
-  const int kbase = prefix ? (i % p.prefix_chunks) * p.prefix_chunk_keys : 0;
-  int ctx;
-  if (prefix) {
-    const int sb = min(max(p.shared_blocks[grp], 0), p.max_blocks);
-    ctx = sb * static_cast<int>(p.bs);  // the shared positions
-    if (kbase >= ctx) return;          // a chunk past them (uniform)
-  } else {
-    ctx = p.ctx_lens[i];
-    if (p.checked) {
-      const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.bs;
-      if (Lq < 0 || Lq > p.max_q || ctx < Lq || ctx > cap) {
-        if (tid == 0 && blockIdx.x == 0 && kvh == 0) record_error(p.err, kErrContext);
-        return;
-      }
+  const int q0 = p.cu_q[i];
+  const int Lq = p.cu_q[i + 1] - q0;
+  const int ctx = p.ctx_lens[i];
+  if (p.checked) {
+    const int64_t cap = static_cast<int64_t>(p.max_blocks) * p.bs;
+    if (Lq < 0 || Lq > p.max_q || ctx < Lq || ctx > cap) {
+      if (tid == 0 && blockIdx.x == 0 && kvh == 0) record_error(p.err, kErrContext);
+      return;
     }
   }
   const int rows = Lq * G;
   const int row0 = rt * 2 * kRowTile;
   if (row0 >= rows) return;  // this CTA's rows lie past the chunk (uniform)
-  // key positions: causal (token j of a chunk at ctx - Lq + j) or, for a
-  // prefix, every shared position for every row
-  const int base = prefix ? ctx - 1 : ctx - Lq;
+  const int base = ctx - Lq;  // position of the chunk's first token
   const int last_row = min(row0 + 2 * kRowTile, rows) - 1;
-  const int kend = prefix ? min(ctx, kbase + p.prefix_chunk_keys)  // keys this CTA needs
-                          : base + last_row / G + 1;
+  const int kend = base + last_row / G + 1;  // keys this CTA needs
   if (kend <= 0) return;  // only when ctx < Lq (caught in checked mode)
-  const int ntiles = (kend - kbase + kKeys - 1) / kKeys;
+  const int ntiles = (kend + kKeys - 1) / kKeys;
   const bool two = rows > row0 + kRowTile;  // row tile 1 holds rows (else it idles)
 
   // Producer state (warp 8): lanes 0-7 copy K of run r of a tile, lanes
@@ -307,10 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int prun = lane & 15;
   // block-table entry of run prun of tile j (-1: past the context or rejected)
   auto entry = [&](int j) -> int32_t {
-    const int kpos = kbase + j * kKeys + prun * run;
+    const int kpos = j * kKeys + prun * run;
     int32_t e = -1;
     if (j < ntiles && prun < runs && kpos < ctx) {
-      e = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs];
+      e = p.block_tables[static_cast<int64_t>(i) * p.max_blocks + kpos / p.bs];
       if (p.checked && (e < 0 || e >= p.num_blocks)) {
         record_error(p.err, kErrBlockId);
         e = -1;  // skip the copy: stale rows, undefined output, no fault
@@ -326,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = j0; j < j1; ++j) {
       const int s = j & 1;
       const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
-      const int off = (kbase + j * kKeys + prun * run) % p.bs;
+      const int off = (j * kKeys + prun * run) % p.bs;
       const int32_t grp =
           e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
       unsigned char* dst = smem + kOffK + s * kStageBytes + prun * run * kRowBytes;
@@ -360,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rr = valid ? r : rows - 1;          // padding rows mirror the last row
   const int tok = rr / G;
   const int head = kvh * G + rr % G;
-  const int pos = prefix ? base : base + tok;
+  const int pos = base + tok;
   const int64_t qrow = (static_cast<int64_t>(q0) + tok) * p.Hq + head;
 
   // Prologue: every role starts its global reads before the CTA-wide barrier.
@@ -415,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(kFull, wait_or_abort(&sfull[t], j & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      const int k0 = kbase + j * kKeys;
+      const int k0 = j * kKeys;
       const bool diag = k0 + kKeys - 1 > pos;  // some key of the tile lies past the row
       // general: a masked tile in this warp, or a negative scale (the maximum
       // of the scaled logits is then not the scaled maximum)
@@ -463,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_new = fmaxf(m_used, tmax);
       if (j == 0) {
-        m_used = m_new;  // finite: the first key of the item is visible to every row
+        m_used = m_new;  // finite: position 0 is visible to every row
       } else {
         const bool grow = m_new > m_used + kRescaleLog2;
         if (__any_sync(kFull, grow)) {
@@ -555,31 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&pfull[t]);
     }
     if (ok) ok = __all_sync(kFull, wait_or_abort(&ofull[t], 0, abort, p.err));
-    if (ok && prefix) {
-      // fp32 record of this (member, head): o / l, m, l
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* rec = p.rec_out + ((static_cast<int64_t>(blockIdx.z) * p.Hkv + kvh) * p.prefix_rows +
-                                row0 + t * kRowTile + lr) *
-                                   kPrefillRecStride;
-#pragma unroll
-      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-        uint32_t w[32];
-        tmem_ld32(w, o_tm + c0);
-        tmem_wait_ld(w);
-        if (valid) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(rec + c0)[q] =
-                make_float4(__uint_as_float(w[4 * q]) * inv, __uint_as_float(w[4 * q + 1]) * inv,
-                            __uint_as_float(w[4 * q + 2]) * inv, __uint_as_float(w[4 * q + 3]) * inv);
-        }
-      }
-      if (valid) {
-        rec[128] = m_used;
-        rec[129] = l;
-      }
-    } else if (ok) {
+    if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * kHeadDim);
@@ -650,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = j & 1;
       ok = __all_sync(kFull, wait_or_abort(&vfull[s], (j >> 1) & 1, abort, p.err));
       if (!ok) break;
-      const int k0 = kbase + j * kKeys;
+      const int k0 = j * kKeys;
       if (k0 + kKeys > ctx) {  // zero V rows at or past the context (0 x stale bytes)
         unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
         const int first = ctx - k0;
@@ -746,29 +528,18 @@ bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int r
   return r == CUDA_SUCCESS;
 }
 
-namespace {
-
-template <bool kPrefix>
-cudaError_t launch_prefill_cfg(const CUtensorMap& tk, const CUtensorMap& tv,
-                               const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           cudaStream_t stream) {
   static bool attr_done = false;  // one device per process in practice; repeated calls are harmless
   if (!attr_done) {
     const cudaError_t e = cudaFuncSetAttribute(
-        prefill_kernel<kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int row_tiles = (p.max_q * p.G + 2 * kRowTile - 1) / (2 * kRowTile);
-  return launch_pdl(prefill_kernel<kPrefix>, dim3(row_tiles, p.Hkv, p.num_seqs), dim3(kThreads),
+  return launch_pdl(prefill_kernel, dim3(row_tiles, p.Hkv, p.num_seqs), dim3(kThreads),
                     kSmemBytes, stream, tk, tv, p);
-}
-
-}  // namespace
-
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                           cudaStream_t stream) {
-  return p.prefix ? launch_prefill_cfg<true>(tk, tv, p, stream)
-                  : launch_prefill_cfg<false>(tk, tv, p, stream);
 }
 
 }  // namespace pkv

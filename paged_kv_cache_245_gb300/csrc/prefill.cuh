@@ -22,26 +22,7 @@ struct PrefillParams {
   float qscale;                  // scale * log2(e)
   int32_t checked;
   int* err;
-  // Shared-prefix mode (prefix != 0): item z is group z of consecutive
-  // sequences group_start[z] .. group_start[z+1]-1 (q holds one decode query
-  // per sequence, [B][Hq][128]); its rows are (member, query head) pairs and
-  // they all attend the group's first shared_blocks[z] blocks (the first
-  // member's table), with no causal mask.  Results go to rec_out as fp32
-  // records of kPrefillRecStride floats: o / l, m, l (log2 units of
-  // scale * log2 e); chunks past a group's shared positions write none.
-  int32_t prefix;
-  const int32_t* group_start;    // [num_groups + 1]
-  const int32_t* shared_blocks;  // [num_groups]
-  float* rec_out;
-  int32_t prefix_rows;           // max group size x G
-  // A group's shared positions split into chunks of prefix_chunk_keys (a
-  // multiple of 128): item z is chunk z % prefix_chunks of group
-  // z / prefix_chunks; records [num_groups][prefix_chunks][Hkv][prefix_rows].
-  int32_t prefix_chunks;
-  int32_t prefix_chunk_keys;
 };
-
-constexpr int kPrefillRecStride = 132;  // floats per record: o[128], m, l, pad
 
 // The K or V cache ([rows][128] bf16) as a 4-D tensor (64 columns, 8 rows,
 // 2 column halves, row groups of 8) whose boxes of run_rows rows land in

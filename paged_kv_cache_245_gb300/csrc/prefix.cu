@@ -1,0 +1,466 @@
+// prefix.cu -- shared-prefix attention for decode on the fifth-generation
+// tensor cores (tcgen05): sequences sampled from one prompt share its blocks
+// ("Running Out of Cache", "Fragmentation is lost users"), and a group's
+// shared positions are attended here once for all its members.  Softmax over
+// a context splits into per-part partial results (o, m, l); the merge kernel
+// (cascade.cu) folds this kernel's records with each member's own positions.
+//
+// Work: one CTA per (128 rows, KV head, group, chunk of the shared
+// positions).  The rows are the group's (member, query head) pairs of the KV
+// head; every row attends every shared position (no causal mask).  A group
+// has few rows (28 for 4 branches at G = 7), so both row tiles of the CTA
+// hold the same rows (one Q tile in shared memory) and take alternate key
+// tiles: tile j goes to row tile j % 2, whose S, softmax and P V run while
+// the other row tile's run -- each writes its own record (half j % 2).  K/V
+// come by TMA (the 4-D boxes of prefill.cu) through a 3-stage ring: with
+// each tile used by one row tile, a third stage keeps the next loads ahead
+// of the chain S -> softmax -> P V.  Tensor memory as in prefill.cu: S_t in
+// columns 128t .., O_t in 256 + 128t ..; P over S in place; lazy rescale.
+#include "pkv_device.cuh"
+#include "prefix.cuh"
+#include "umma.cuh"
+
+namespace pkv {
+
+using namespace umma;
+
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kOffK = kOpBytes;                       // after the one Q tile
+constexpr int kStageBytes = 2 * kOpBytes;             // K then V
+constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 224 KiB
+constexpr int kSmemBytes = kTilesBytes + 256 + 1024;
+constexpr int kThreads = 320;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefix_kernel(const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const PrefixParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTilesBytes);
+  uint64_t* kfull = bars;        // [3] K of a stage landed
+  uint64_t* vfull = bars + 3;    // [3] V of a stage landed
+  uint64_t* kempty = bars + 6;   // [3] the S product reading a stage's K completed
+  uint64_t* vempty = bars + 9;   // [3] the P V product reading a stage's V completed
+  uint64_t* sfull = bars + 12;   // [2] S_t of its current tile (and PV_t before it) done
+  uint64_t* pfull = bars + 14;   // [2] P_t written (one arrival per warp)
+  uint64_t* ofull = bars + 16;   // [2] the last PV_t completed
+  uint64_t* drain = bars + 18;   // wind-down after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 20);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int kvh = blockIdx.y;
+  const int g = blockIdx.z / p.chunks;
+  const int kc = blockIdx.z % p.chunks;
+  const int G = p.G;
+
+  grid_dependency_wait();
+  grid_dependency_trigger();
+
+  const int seq = p.group_start[g];  // the group's first member: its block table
+  const int rows = (p.group_start[g + 1] - seq) * G;
+  const int row0 = blockIdx.x * kRowTile;
+  if (row0 >= rows) return;  // past the group's rows (uniform)
+  const int sb = min(max(p.shared_blocks[g], 0), p.max_blocks);
+  const int ctx = sb * static_cast<int>(p.bs);  // the shared positions
+  const int kbase = kc * p.chunk_keys;
+  if (kbase >= ctx) return;  // a chunk past them (uniform)
+  const int kend = min(ctx, kbase + p.chunk_keys);
+  const int ntiles = (kend - kbase + kKeys - 1) / kKeys;
+  const bool two = ntiles > 1;  // row tile 1 has odd tiles to take
+
+  // Producer state (warp 8): lanes 0-7 copy K of run r of a tile, lanes
+  // 16-23 V of the same run.
+  const uint64_t policy = l2_policy_evict_first();  // read once
+  const int run = p.run_rows;    // rows per box (16 .. 128, divides 128 and bs)
+  const int runs = kKeys / run;  // boxes per tile and tensor (<= 8)
+  const int prun = lane & 15;
+  auto entry = [&](int j) -> int32_t {
+    const int kpos = kbase + j * kKeys + prun * run;
+    int32_t e = -1;
+    if (j < ntiles && prun < runs && kpos < ctx) {
+      e = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs];
+      if (p.checked && (e < 0 || e >= p.num_blocks)) {
+        record_error(p.err, kErrBlockId);
+        e = -1;  // skip the copy: stale rows, undefined output, no fault
+      }
+    }
+    return e;
+  };
+  int32_t e = -1;        // entries of the next tile to issue
+  int issued = 0;        // tiles whose K and V were both issued
+  bool kv_half = false;  // tile `issued` has its K issued, not its V
+  auto produce = [&](int j0, int j1) -> bool {
+    for (int j = j0; j < j1; ++j) {
+      const int s = j % kStages;
+      const uint32_t u = static_cast<uint32_t>(j / kStages);  // use of the stage
+      const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
+      const int off = (kbase + j * kKeys + prun * run) % p.bs;
+      const int32_t grp =
+          e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
+      unsigned char* dst = smem + kOffK + s * kStageBytes + prun * run * kRowBytes;
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&kempty[s], (u - 1) & 1, abort, p.err)))
+        return false;
+      if (lane == 0) mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
+      __syncwarp();
+      if (lane < 16 && e >= 0) tma_load_4d(dst, &tmk, grp, &kfull[s], policy);
+      if (j >= kStages &&
+          !__all_sync(kFull, wait_or_abort(&vempty[s], (u - 1) & 1, abort, p.err))) {
+        kv_half = true;  // K of tile `issued` is in flight
+        return false;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
+      __syncwarp();
+      if (lane >= 16 && e >= 0) tma_load_4d(dst + kOpBytes, &tmv, grp, &vfull[s], policy);
+      issued = j + 1;
+      e = entry(j + 1);  // the next tile's entries load while this one lands
+    }
+    return true;
+  };
+
+  // Rows of both row tiles (the same rows): row r -> (member r / G, head r % G).
+  const int t = (warp >> 2) & 1;
+  const int lr = tid & (kRowTile - 1);
+  const int r = row0 + lr;
+  const bool valid = r < rows;
+  const int rr = valid ? r : rows - 1;  // padding rows mirror the last row
+  const int64_t qrow = (static_cast<int64_t>(seq) + rr / G) * p.Hq + kvh * G + rr % G;
+  const int pos = ctx - 1;              // every shared position is visible
+
+  if (warp == 8) {
+    if (lane == 0) {
+      for (int b = 0; b < 18; ++b) mbar_init(&bars[b], (b == 14 || b == 15) ? 4 : 1);
+      mbar_init(drain, 1);
+      *abort = 0;
+      fence_barrier_init();
+      prefetch_tensormap(&tmk);
+      prefetch_tensormap(&tmv);
+    }
+    __syncwarp();
+    e = entry(0);
+    produce(0, min(kStages, ntiles));  // no waits: the stages are fresh
+  } else if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else if (warp < 4) {
+    // the Q tile; the MMA warp reads it after the barrier
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = valid ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + q_chunk_offset(lr, c)) = v;
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t smem_base = smem_addr(smem);
+
+  if (warp < 8 && t == 1 && !two) {
+    // one key tile: row tile 1 has nothing to do
+  } else if (warp < 8) {
+    // ================= softmax: row tile t takes key tiles t, t + 2, ... =================
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + t * 128;
+    const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
+    const float sc = p.qscale;
+    float m_used = -INFINITY;  // the maximum P is taken against (scaled logits)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = t, n = 0; j < ntiles; j += 2, ++n) {
+      ok = __all_sync(kFull, wait_or_abort(&sfull[t], n & 1, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = kbase + j * kKeys;
+      const bool diag = k0 + kKeys - 1 > pos;  // some key of the tile lies past the row
+      // general: a masked tile in this warp, or a negative scale (the maximum
+      // of the scaled logits is then not the scaled maximum)
+      const bool general = __any_sync(kFull, diag) || !(sc >= 0.f);
+      // pass 1: the row maximum of the scaled, masked logits
+      float tmax;
+      if (!general) {
+        float mx[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx[u] = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            mx[c & 3] = fmax3(mx[c & 3], __uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1]));
+            mx[(c + 2) & 3] =
+                fmax3(mx[(c + 2) & 3], __uint_as_float(b[2 * c]), __uint_as_float(b[2 * c + 1]));
+          }
+        }
+        tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+      } else {
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float x = __uint_as_float(c < 32 ? a[c] : b[c - 32]) * sc;
+            mx[c & 7] = fmaxf(mx[c & 7], !diag || k0 + 64 * h + c <= pos ? x : -INFINITY);
+          }
+        }
+        tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      }
+      const float m_new = fmaxf(m_used, tmax);
+      if (n == 0) {
+        m_used = m_new;  // finite: the tile's first key is visible to every row
+      } else {
+        const bool grow = m_new > m_used + kRescaleLog2;
+        if (__any_sync(kFull, grow)) {
+          const float alpha = grow ? fast_exp2(m_used - m_new) : 1.f;
+          if (grow) {
+            l *= alpha;
+            m_used = m_new;
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+            uint32_t w[32];
+            tmem_ld32(w, o_tm + c0);
+            tmem_wait_ld(w);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * alpha);
+            tmem_st32(o_tm + c0, w);
+          }
+        }
+      }
+      // pass 2: P = 2^(s * scale - m) as bf16 pairs over the columns already read
+      const float neg_m = -m_used;
+      if (!general) {
+        const uint64_t sc2 = f2_pack(__float_as_uint(sc), __float_as_uint(sc));
+        const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
+        uint64_t ls2[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ls2[u] = 0ull;  // (+0, +0)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
+            const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(u0, u1), sc2, nm2), x0, x1);
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+            const uint64_t e2 = f2_pack(__float_as_uint(e0), __float_as_uint(e1));
+            ls2[c & 3] = f2_add(ls2[c & 3], e2);
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          tmem_st32(s_tm + 32 * h, pk);
+        }
+        float l0, l1, l2, l3;
+        f2_unpack(f2_add(ls2[0], ls2[1]), l0, l1);
+        f2_unpack(f2_add(ls2[2], ls2[3]), l2, l3);
+        l += (l0 + l2) + (l1 + l3);
+      } else {
+        float ls[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32], b[32];
+          tmem_ld32(a, s_tm + 64 * h);
+          tmem_ld32(b, s_tm + 64 * h + 32);
+          tmem_wait_ld(a);
+          tmem_ready(b);
+          // keys of this half the row sees: bit c of (lo, hi) for key 64h + c
+          const int seen = diag ? min(max(pos - k0 - 64 * h + 1, 0), 64) : 64;
+          const uint32_t lo = seen >= 32 ? 0xffffffffu : (1u << seen) - 1u;
+          const uint32_t hi =
+              seen >= 64 ? 0xffffffffu : (seen <= 32 ? 0u : (1u << (seen - 32)) - 1u);
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
+            const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
+            float e0 = fast_exp2(fmaf(__uint_as_float(u0), sc, neg_m));
+            float e1 = fast_exp2(fmaf(__uint_as_float(u1), sc, neg_m));
+            const uint32_t bits = c < 16 ? lo : hi;
+            e0 = (bits >> ((2 * c) & 31)) & 1u ? e0 : 0.f;
+            e1 = (bits >> ((2 * c + 1) & 31)) & 1u ? e1 : 0.f;
+            ls[c & 7] += e0 + e1;
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          tmem_st32(s_tm + 32 * h, pk);
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[t]);
+    }
+    if (ok) ok = __all_sync(kFull, wait_or_abort(&ofull[t], 0, abort, p.err));
+    if (ok) {
+      // fp32 record of this (member, head) and half: o / l, m, l
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* rec = p.rec_out +
+                   ((((static_cast<int64_t>(g) * p.chunks + kc) * 2 + t) * p.Hkv + kvh) * p.rows +
+                    r) *
+                       kPrefixRecStride;
+#pragma unroll
+      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(w, o_tm + c0);
+        tmem_wait_ld(w);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(rec + c0)[q] =
+                make_float4(__uint_as_float(w[4 * q]) * inv, __uint_as_float(w[4 * q + 1]) * inv,
+                            __uint_as_float(w[4 * q + 2]) * inv,
+                            __uint_as_float(w[4 * q + 3]) * inv);
+        }
+      }
+      if (valid) {
+        rec[128] = m_used;
+        rec[129] = l;
+      }
+    }
+  } else if (warp == 8) {
+    // ================= K/V producer: the remaining tiles =================
+    produce(kStages, ntiles);
+    if (*abort && lane == 0) {
+      // let the copies in flight land before the CTA's shared memory is released
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        mbar_wait_bounded(&kfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1);
+        mbar_wait_bounded(&vfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1);
+      }
+      if (kv_half)
+        mbar_wait_bounded(&kfull[issued % kStages], static_cast<uint32_t>(issued / kStages) & 1);
+    }
+  } else if (warp == 9) {
+    // ================= MMA issuer (lane 0 issues) =================
+    // order S_0(0) S_1(1) | PV_0(0) S_0(2) | PV_1(1) S_1(3) | PV_0(2) S_0(4) | ...
+    auto issue_s = [&](int rt, int j) {  // S_rt = Q K_j^T
+      const uint32_t k_addr = smem_base + kOffK + (j % kStages) * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t koff = (kk & 3) * 32;
+        umma_ss(tmem + rt * 128, smem_desc(smem_base + (kk >> 2) * kHalfBytes + koff, 16, 1024),
+                smem_desc(k_addr + (kk >> 2) * 1024 + koff, 16, 2048), kIdescS, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int rt, int j, bool acc) {  // O_rt (+)= P_rt V_j
+      const uint32_t v_addr = smem_base + kOffK + (j % kStages) * kStageBytes + kOpBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_ts(tmem + 256 + rt * 128, tmem + rt * 128 + kk * 8,
+                smem_desc(v_addr + kk * 4096, 1024, 2048), kIdescPV, (acc || kk > 0));
+    };
+    bool ok = true;
+    for (int j = 0; ok && j < min(2, ntiles); ++j) {  // the first S of each row tile
+      ok = __all_sync(kFull, wait_or_abort(&kfull[j], 0, abort, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(j, j);
+        umma_commit(&sfull[j]);
+        if (j + kStages < ntiles) umma_commit(&kempty[j]);
+      }
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int tj = j & 1;                                // row tile
+      const int s = j % kStages;                           // stage
+      const uint32_t u = static_cast<uint32_t>(j / kStages);
+      const uint32_t c = static_cast<uint32_t>(j >> 1);    // the row tile's tile count
+      ok = __all_sync(kFull, wait_or_abort(&vfull[s], u & 1, abort, p.err));
+      if (!ok) break;
+      const int k0 = kbase + j * kKeys;
+      if (k0 + kKeys > ctx) {  // zero V rows at or past the shared positions
+        unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
+        const int first = ctx - k0;
+        for (int idx = lane; idx < (kKeys - first) * 16; idx += 32)
+          *reinterpret_cast<uint4*>(vt + kv_chunk_offset(first + (idx >> 4), idx & 15)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      const bool more = j + 2 < ntiles;  // this row tile has another tile
+      ok = __all_sync(kFull, wait_or_abort(&pfull[tj], c & 1, abort, p.err));
+      if (ok && more)
+        ok = __all_sync(kFull, wait_or_abort(&kfull[(j + 2) % kStages],
+                                             static_cast<uint32_t>((j + 2) / kStages) & 1, abort,
+                                             p.err));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(tj, j, c > 0);
+        if (j + kStages < ntiles) umma_commit(&vempty[s]);  // the producer reuses the stage
+        if (more) {
+          issue_s(tj, j + 2);
+          umma_commit(&sfull[tj]);
+          if (j + 2 + kStages < ntiles) umma_commit(&kempty[(j + 2) % kStages]);
+        } else {
+          umma_commit(&ofull[tj]);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // let the MMAs in flight finish before tensor memory is released
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+cudaError_t launch_prefix(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p,
+                          cudaStream_t stream) {
+  static bool attr_done = false;  // one device per process in practice; repeated calls are harmless
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int row_blocks = (p.rows + kRowTile - 1) / kRowTile;
+  return launch_pdl(prefix_kernel, dim3(row_blocks, p.Hkv, p.num_groups * p.chunks),
+                    dim3(kThreads), kSmemBytes, stream, tk, tv, p);
+}
+
+}  // namespace pkv
