@@ -329,12 +329,13 @@ static_assert(pkv::kPrefixRecStride == pkv::kRecStride, "one record layout for e
 constexpr int kMaxPrefixChunks = 8;  // chunks of a group's shared positions (bound)
 
 // Chunk of the shared positions for the prefix kernel: whole blocks, a
-// multiple of 128 positions, at least 2048 positions, and at most
+// multiple of 128 positions, at least 4096 positions (a sweep of 1024 .. 8192
+// on the Yi-34B sharing workload: 154, 138, 129, 147 us), and at most
 // kMaxPrefixChunks chunks per group.
 int32_t prefix_chunk_blocks(int32_t max_blocks, int32_t block_size) {
   auto up8 = [](int64_t x) { return static_cast<int32_t>((x + 7) / 8 * 8); };
   const int32_t a = up8((max_blocks + kMaxPrefixChunks - 1) / kMaxPrefixChunks);
-  const int32_t b = up8((2048 + block_size - 1) / block_size);
+  const int32_t b = up8((4096 + block_size - 1) / block_size);
   return a > b ? a : b;
 }
 
