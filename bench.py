@@ -285,7 +285,7 @@ class DeviceWorkload:
         # plus one block copy launch (all layers) when the step copies on write
         cow = 0 if self.cow is None else 1
         if self.groups is not None:
-            # append; the prefix on the prefill kernel; the merge (own parts in the merge)
+            # append; the prefix kernel; the merge (own parts in the merge)
             return self.shape.num_layers * 3 + cow
         if self.uses_tc:
             return self.shape.num_layers * 3 + cow
@@ -441,8 +441,8 @@ def run_gpu(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                      "traffic": _profiled_traffic(args.workload),
-                     "kernel": "paged_decode_attention_shared call (prefill_kernel in "
-                               "prefix mode, then cascade_merge_kernel with the own positions)"
+                     "kernel": "paged_decode_attention_shared call (prefix_kernel, then "
+                               "cascade_merge_kernel with the own positions)"
                                if wl.groups is not None else
                                "paged_decode_attention call (decode_tc_kernel + "
                                "decode_tc_combine_kernel)" if wl.uses_tc else
