@@ -109,8 +109,10 @@ __device__ void own_attention(const CascadeParams& c, int i, int h, int sb, int 
 // sequence shares anything) with its own part -- attended here, or a record
 // of the tensor-core pass -- into the bf16 output.
 __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams c) {
-  grid_dependency_wait();
-  grid_dependency_trigger();
+  // Launched as a programmatic dependent of the prefix kernel when it attends
+  // the own positions itself: those need only this call's inputs, so they
+  // run before the wait, overlapping the prefix kernel's tail.
+  if (c.own_cap < 0) grid_dependency_wait();  // the own parts' records come from the previous kernel
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
     os = ls > 0.f ? __ldcg(reinterpret_cast<const float4*>(rs) + lane)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if (c.own_cap >= 0) grid_dependency_wait();  // the prefix records are complete
+  grid_dependency_trigger();
   // Fold in the prefix records, one per chunk of the shared positions (a
   // member beyond the group size bound has none: the caller broke the
   // contract, nothing is read):  M' = max(M, m),  acc' = acc 2^(M - M') +
@@ -191,8 +195,8 @@ cudaError_t launch_cascade_prep(const CascadeParams& c, cudaStream_t stream) {
 
 cudaError_t launch_cascade_merge(const CascadeParams& c, cudaStream_t stream) {
   const int64_t warps = static_cast<int64_t>(c.B) * c.Hq;
-  return launch_pdl(cascade_merge_kernel, dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128),
-                    0, stream, c);
+  return launch_pdl_if(c.own_cap >= 0 || pdl_enabled(), cascade_merge_kernel,
+                       dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0, stream, c);
 }
 
 }  // namespace pkv
