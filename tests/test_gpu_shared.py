@@ -66,25 +66,19 @@ def test_yi34b_sharing_scenario(step, own):
         assert_attention_close(out, L.oracle_attend(), "vs oracle")
 
 
-@pytest.mark.parametrize("own", OWN)
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (28, 4), (32, 4)])
-def test_synthetic_groups(hq, hkv, own):
-    """Groups of 1..5 sequences over one prompt each: members have their own
-    tail blocks after the shared ones; some members stop exactly at the
-    shared positions (empty own part)."""
-    rng = np.random.default_rng(hq * 10 + hkv)
+def _synthetic(hq, hkv, own, sizes, max_prompt_blocks, seed):
+    rng = np.random.default_rng(seed)
     bs = 16
     shape = W.ModelShape("s%d_%d" % (hq, hkv), 1, hq, hkv)
-    sizes = [1, 2, 3, 4, 5, 1, 3]
     starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     B = int(starts[-1])
-    prompt = rng.integers(1, 40, size=len(sizes)) * bs   # whole shared blocks
+    prompt = rng.integers(1, max_prompt_blocks, size=len(sizes)) * bs   # whole shared blocks
     # a singleton shares nothing: all its positions are its own (keep them
     # within the in-merge bound)
     prompt[np.asarray(sizes) == 1] = np.minimum(prompt[np.asarray(sizes) == 1], 10 * bs)
-    own = [rng.integers(0, 70, size=s) for s in sizes]
-    own[1][0] = 0                                        # a member with no own positions
-    ctx = np.concatenate([p + o for p, o in zip(prompt, own)]).astype(np.int32)
+    own_pos = [rng.integers(0, 70, size=s) for s in sizes]
+    own_pos[int(np.argmax(np.asarray(sizes) > 1))][0] = 0  # a member with no own positions
+    ctx = np.concatenate([p + o for p, o in zip(prompt, own_pos)]).astype(np.int32)
     ctx = np.maximum(ctx, 1)
     max_blocks = int((ctx.max() + bs - 1) // bs)
     nb = int(sum((c + bs - 1) // bs for c in ctx)) + 8
@@ -109,7 +103,25 @@ def test_synthetic_groups(hq, hkv, own):
     bound = own_bound(b, starts, shared)
     assert bound <= 256   # singletons keep whole contexts: within the in-merge bound
     out = _run(b, starts, shared, L, -1 if own == OWN[0] else bound)
-    assert_attention_close(out, L.oracle_attend(), "synthetic groups G=%d" % (hq // hkv))
+    assert_attention_close(out, L.oracle_attend(), "synthetic groups G=%d sizes %s"
+                           % (hq // hkv, sizes))
+
+
+@pytest.mark.parametrize("own", OWN)
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (28, 4), (32, 4)])
+def test_synthetic_groups(hq, hkv, own):
+    """Groups of 1..5 sequences over one prompt each: members have their own
+    tail blocks after the shared ones; some members stop exactly at the
+    shared blocks."""
+    _synthetic(hq, hkv, own, [1, 2, 3, 4, 5, 1, 3], 40, hq * 10 + hkv)
+
+
+@pytest.mark.parametrize("own", OWN)
+def test_large_groups_and_long_shared_prompts(own):
+    """A group of 24 members at G = 8 (192 rows: two row blocks of the prefix
+    kernel) and shared prompts of up to 600 blocks (several chunks of the
+    shared positions)."""
+    _synthetic(32, 4, own, [24, 2, 1, 5], 600, 77)
 
 
 def test_checked_mode_reports_an_uncovered_member():
