@@ -569,7 +569,54 @@ def measure_legs(wl, dev, args):
         "block_copy_shape": "96 pairs x 60 layers x (K,V) of 32 KiB blocks (read + write)",
         "on_demand_contig": vmm,
         "prefill": measure_prefill(wl, dev, reps),
+        "swap": measure_swap(pkv, dev),
     }
+
+
+def measure_swap(pkv, dev, reps=8):
+    """Pre-emption by swapping, Llama-3-8B-shaped: four sequences of 1024
+    tokens (256 blocks scattered over the pool) x 32 layers x (K, V) of
+    32 KiB blocks, out to a page-locked host pool and back, one block_swap
+    launch each way.  Beside it, one contiguous copy of the same bytes by
+    the copy engine (cudaMemcpyAsync), the link's plain transfer rate."""
+    L, nb, n = 32, 512, 256
+    shape = (nb, 8, 16, 128)
+    dk = [torch.zeros(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    dv = [torch.zeros(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    hk = [torch.zeros((n,) + shape[1:], dtype=torch.bfloat16, pin_memory=True) for _ in range(L)]
+    hv = [torch.zeros((n,) + shape[1:], dtype=torch.bfloat16, pin_memory=True) for _ in range(L)]
+    g = torch.Generator().manual_seed(W.SEED_LLAMA)
+    blocks = torch.randperm(nb, generator=g)[:n]
+    out = torch.stack([blocks, torch.arange(n)], 1).to(dev)
+    back = torch.stack([torch.arange(n), blocks], 1).to(dev)
+    moved = 2 * L * n * 8 * 16 * 128 * 2
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps / 1e3
+
+    try:
+        t_out = timed(lambda: pkv.block_swap(out, dk, dv, hk, hv))
+        t_in = timed(lambda: pkv.block_swap(back, hk, hv, dk, dv))
+        flat_d = torch.empty(moved // 2, dtype=torch.bfloat16, device=dev)
+        flat_h = torch.empty(moved // 2, dtype=torch.bfloat16, pin_memory=True)
+        t_d2h = timed(lambda: flat_h.copy_(flat_d, non_blocking=True))
+        t_h2d = timed(lambda: flat_d.copy_(flat_h, non_blocking=True))
+    finally:
+        torch.cuda.synchronize(dev)
+    gbs = lambda t: round(moved / t / 1e9, 1)
+    return {"bytes": moved, "swap_out_us": round(t_out * 1e6, 1), "swap_out_gbs": gbs(t_out),
+            "swap_in_us": round(t_in * 1e6, 1), "swap_in_gbs": gbs(t_in),
+            "copy_engine_d2h_gbs": gbs(t_d2h), "copy_engine_h2d_gbs": gbs(t_h2d),
+            "shape": "256 scattered blocks x 32 layers x (K,V) of 32 KiB, device <-> "
+                     "page-locked host, one launch each way"}
 
 
 def _bf16_peak():

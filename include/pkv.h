@@ -9,6 +9,8 @@
  * and pkv_paged_decode_step / pkv_contig_decode_step run append + attention
  * of one layer as one call.  pkv_paged_prefill_attention /
  * pkv_contig_prefill_attention attend chunks of new tokens causally (prefill).
+ * pkv_block_swap moves whole blocks between the device cache and a pool in
+ * page-locked host memory (pre-emption by swapping).
  *
  * Conventions for every call:
  *   - All tensor arguments are DEVICE pointers on the current CUDA device,
@@ -285,6 +287,30 @@ PKV_API pkv_status pkv_block_copy(const int64_t *src_dst_pairs, int64_t n,
                           void *const *k_caches, void *const *v_caches,
                           int32_t num_layers, int64_t num_blocks,
                           int64_t block_bytes, void *stream);
+
+/*
+ * Block swap between two pools, for pre-emption.  "Running Out of Cache"
+ * (closing paragraph, and the glossary entry "Pre-emption"): when even a
+ * paged cache runs out, a server evicts a request's cache and swaps it back
+ * in later.  pkv_bm_preempt / pkv_bm_resume (pkv_block_manager.h) give the
+ * pairs.
+ *
+ * For each pair c < n of pairs (int64 [n][2] = (src, dst)) and each layer
+ * l < num_layers, copies block_bytes bytes from block src of src_k[l] to
+ * block dst of dst_k[l], and from src_v[l] to dst_v[l].  src_k, src_v,
+ * dst_k and dst_v are HOST arrays of num_layers pointers.  Each of those
+ * pointers, and pairs, must be device memory, managed memory, or page-locked
+ * host memory (cudaHostAlloc, cudaHostRegister; the kernel reads and writes
+ * it across the CPU-GPU link); ordinary pageable memory, a null or a
+ * misaligned pointer (16 bytes; 8 for pairs) gives PKV_ERR_INVALID_ARG.
+ * block_bytes must be a multiple of 16.  src_num_blocks / dst_num_blocks
+ * bound the ids in checked mode (PKV_DEVERR_COPY_PAIR).  The two sides must
+ * not overlap.  Bit-exact.
+ */
+PKV_API pkv_status pkv_block_swap(const int64_t *pairs, int64_t n,
+                          void *const *src_k, void *const *src_v, int64_t src_num_blocks,
+                          void *const *dst_k, void *const *dst_v, int64_t dst_num_blocks,
+                          int32_t num_layers, int64_t block_bytes, void *stream);
 
 /*
  * Paged decode attention without a caller workspace.  The pages have no

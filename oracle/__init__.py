@@ -187,3 +187,19 @@ def block_copy(pairs, k_caches, v_caches):
     vp = (ctypes.c_void_p * L)(*[c.ctypes.data for c in v_caches])
     _check(lib().pkv_oracle_block_copy(pairs, pairs.shape[0], kp, vp, L, nb,
                                        block_elems), "block_copy")
+
+
+def block_swap(pairs, src_k, src_v, dst_k, dst_v):
+    """Swap of whole blocks between two pools ("Running Out of Cache",
+    closing paragraph, and the glossary entry "Pre-emption": an evicted
+    request's cache is swapped out and brought back later).  For every
+    (src, dst) pair and every layer, block src of the source pool's K and V
+    becomes block dst of the destination pool's.  Plain numpy indexing, one
+    block at a time, in pair order."""
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    L = len(src_k)
+    assert len(src_v) == len(dst_k) == len(dst_v) == L and L > 0
+    for src, dst in pairs:
+        for layer in range(L):
+            dst_k[layer][dst] = src_k[layer][src]
+            dst_v[layer][dst] = src_v[layer][src]

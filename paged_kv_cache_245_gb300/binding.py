@@ -30,7 +30,7 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
             "pkv_debug_gather_contig", "pkv_paged_decode_attention_shared",
             "pkv_shared_decode_workspace_size", "pkv_paged_prefill_attention",
-            "pkv_contig_prefill_attention",
+            "pkv_contig_prefill_attention", "pkv_block_swap",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
 
@@ -68,6 +68,7 @@ def lib():
     L.pkv_contig_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i64,
                                               ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_block_copy.argtypes = [vp, i64, vp, vp, i32, i64, i64, vp]
+    L.pkv_block_swap.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, i32, i64, vp]
     L.pkv_paged_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
                                         ctypes.c_float, Heads, vp, vp, sz, vp]
     L.pkv_contig_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
@@ -97,7 +98,7 @@ def lib():
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_last_error.restype = ctypes.c_char_p
     for name in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_contig_decode_attention",
-                 "pkv_block_copy", "pkv_get_device_error"):
+                 "pkv_block_copy", "pkv_block_swap", "pkv_get_device_error"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -440,6 +441,37 @@ def block_copy(src_dst_pairs, k_caches, v_caches):
                                 block_bytes, _stream(k_caches[0])))
 
 
+def block_swap(pairs, src_k, src_v, dst_k, dst_v):
+    """Copy whole blocks from one pool to another, pairs [n, 2] int64 of
+    (src block, dst block), in every layer's K and V (lists of [blocks, ...]
+    bf16 tensors, one shape per side).  Either side may be page-locked host
+    memory (``tensor.pin_memory()``): that is the swap of pre-empted
+    sequences out of, and back into, the device cache.  pairs may be a
+    device tensor or a pinned host tensor."""
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2 \
+            or not pairs.is_contiguous():
+        raise ValueError("pairs must be a contiguous [n, 2] int64 tensor")
+    L = len(src_k)
+    if not (L == len(src_v) == len(dst_k) == len(dst_v)) or L == 0:
+        raise ValueError("need one K and one V pool per layer on each side")
+    blocks = []
+    for side in ((src_k, src_v), (dst_k, dst_v)):
+        shape = tuple(side[0][0].shape)
+        for t in list(side[0]) + list(side[1]):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError("pools must be contiguous bf16 tensors of one shape per side")
+        blocks.append(shape)
+    if blocks[0][1:] != blocks[1][1:]:
+        raise ValueError("the two sides must have the same block shape")
+    block_bytes = src_k[0][0].numel() * 2
+    arr = [(ctypes.c_void_p * L)(*[t.data_ptr() for t in x]) for x in (src_k, src_v, dst_k, dst_v)]
+    dev = next((t for t in (src_k[0], dst_k[0], pairs) if t.is_cuda), None)
+    if dev is None:
+        raise ValueError("one side (or pairs) must be on the GPU")
+    _check(lib().pkv_block_swap(_ptr(pairs), pairs.shape[0], arr[0], arr[1], blocks[0][0],
+                                arr[2], arr[3], blocks[1][0], L, block_bytes, _stream(dev)))
+
+
 def set_checked(enable):
     lib().pkv_set_checked(1 if enable else 0)
 
@@ -501,6 +533,24 @@ def _bm_lib():
     L.pkv_bm_length.restype = i64
     L.pkv_bm_num_free_blocks.argtypes = [vp]
     L.pkv_bm_num_free_blocks.restype = i32
+    L.pkv_bm_set_swap_space.argtypes = [vp, i32]
+    L.pkv_bm_set_swap_space.restype = ctypes.c_int
+    L.pkv_bm_step_blocks.argtypes = [vp, vp, i32]
+    L.pkv_bm_step_blocks.restype = i64
+    L.pkv_bm_plan_preemption.argtypes = [vp, vp, i32, vp]
+    L.pkv_bm_plan_preemption.restype = ctypes.c_int
+    L.pkv_bm_preempt.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.pkv_bm_preempt.restype = ctypes.c_int
+    L.pkv_bm_resume.argtypes = [vp, vp, i32, vp, vp]
+    L.pkv_bm_resume.restype = ctypes.c_int
+    L.pkv_bm_state.argtypes = [vp, i32]
+    L.pkv_bm_state.restype = i32
+    L.pkv_bm_num_free_host_blocks.argtypes = [vp]
+    L.pkv_bm_num_free_host_blocks.restype = i32
+    L.pkv_bm_host_ref_count.argtypes = [vp, i32]
+    L.pkv_bm_host_ref_count.restype = i32
+    L.pkv_bm_get_counters.argtypes = [vp, ctypes.POINTER(BmCounters)]
+    L.pkv_bm_get_counters.restype = ctypes.c_int
     L.pkv_bm_ref_count.argtypes = [vp, i32]
     L.pkv_bm_ref_count.restype = i32
     L._bm_ready = True
@@ -509,6 +559,17 @@ def _bm_lib():
 
 def _np_ptr(a):
     return ctypes.c_void_p(a.ctypes.data)
+
+
+class BmCounters(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "cow_copies", "preempted_recompute", "preempted_swap", "resumed",
+        "blocks_swapped_out", "blocks_swapped_in", "tokens_recomputed")]
+
+
+# sequence states and pre-emption modes of include/pkv_block_manager.h
+BM_RETIRED, BM_RUNNING, BM_SWAPPED, BM_RECOMPUTE = 0, 1, 2, 3
+PREEMPT_RECOMPUTE, PREEMPT_SWAP = 0, 1
 
 
 class BlockManager:
@@ -602,6 +663,70 @@ class BlockManager:
 
     def ref_count(self, block):
         return int(_bm_lib().pkv_bm_ref_count(self._h, int(block)))
+
+    # ---- pre-emption
+    def set_swap_space(self, num_host_blocks):
+        _check(_bm_lib().pkv_bm_set_swap_space(self._h, int(num_host_blocks)))
+
+    def _ids(self, seq_ids):
+        return self._np.ascontiguousarray(seq_ids, dtype=self._np.int32)
+
+    def step_blocks(self, seq_ids):
+        """Free blocks an append of these running sequences needs."""
+        ids = self._ids(seq_ids)
+        n = _bm_lib().pkv_bm_step_blocks(self._h, _np_ptr(ids), ids.shape[0])
+        if n < 0:
+            raise PkvError(PKV_ERR_INVALID_ARG, _bm_lib().pkv_last_error().decode())
+        return int(n)
+
+    def plan_preemption(self, seq_ids):
+        """How many of the listed running sequences, taken from the back,
+        must be evicted for the rest to append one token each."""
+        ids = self._ids(seq_ids)
+        k = ctypes.c_int32(0)
+        _check(_bm_lib().pkv_bm_plan_preemption(self._h, _np_ptr(ids), ids.shape[0],
+                                                ctypes.byref(k)))
+        return int(k.value)
+
+    def _held(self, ids):
+        return sum(len(self.block_table(int(s))) for s in ids)
+
+    def preempt(self, seq_ids, mode=PREEMPT_RECOMPUTE):
+        """Evict running sequences; returns the (device block, host slot)
+        swap-out pairs [k, 2] int64 (empty for recompute)."""
+        np = self._np
+        ids = self._ids(seq_ids)
+        pairs = np.empty((max(self._held(ids), 1), 2), dtype=np.int64)
+        k = ctypes.c_int32(0)
+        _check(_bm_lib().pkv_bm_preempt(self._h, _np_ptr(ids), ids.shape[0], int(mode),
+                                        _np_ptr(pairs), ctypes.byref(k)))
+        return pairs[:k.value].copy()
+
+    def resume(self, seq_ids):
+        """Bring evicted sequences back; returns the (host slot, device
+        block) swap-in pairs [k, 2] int64."""
+        np = self._np
+        ids = self._ids(seq_ids)
+        held = sum(len(self.block_table(int(s))) for s in ids if self.state(int(s)) == BM_SWAPPED)
+        pairs = np.empty((max(held, 1), 2), dtype=np.int64)
+        k = ctypes.c_int32(0)
+        _check(_bm_lib().pkv_bm_resume(self._h, _np_ptr(ids), ids.shape[0], _np_ptr(pairs),
+                                       ctypes.byref(k)))
+        return pairs[:k.value].copy()
+
+    def state(self, seq):
+        return int(_bm_lib().pkv_bm_state(self._h, int(seq)))
+
+    def num_free_host_blocks(self):
+        return int(_bm_lib().pkv_bm_num_free_host_blocks(self._h))
+
+    def host_ref_count(self, slot):
+        return int(_bm_lib().pkv_bm_host_ref_count(self._h, int(slot)))
+
+    def counters(self):
+        c = BmCounters()
+        _check(_bm_lib().pkv_bm_get_counters(self._h, ctypes.byref(c)))
+        return {n: int(getattr(c, n)) for n, _ in BmCounters._fields_}
 
 
 # ------------------------------------------------------------ on-demand contiguous buffers

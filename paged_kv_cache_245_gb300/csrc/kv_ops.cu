@@ -83,8 +83,9 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
                     stream, p);
 }
 
-// Block copy: blockIdx.x strides over the block's 16-byte chunks, blockIdx.y
-// is the pair, blockIdx.z = 2 * layer + (0 for K, 1 for V).
+// Block copy (within one pool) and block swap (between two): blockIdx.x
+// strides over the block's 16-byte chunks, blockIdx.y is the pair,
+// blockIdx.z = 2 * layer + (0 for K, 1 for V).
 __global__ void __launch_bounds__(256) block_copy_kernel(const CopyParams p) {
   grid_dependency_trigger();
   grid_dependency_wait();
@@ -93,13 +94,14 @@ __global__ void __launch_bounds__(256) block_copy_kernel(const CopyParams p) {
   const bool is_v = blockIdx.z & 1;
   const int64_t src = p.pairs[2 * pair];
   const int64_t dst = p.pairs[2 * pair + 1];
-  if (p.checked && (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks)) {
+  if (p.checked && (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.dst_num_blocks)) {
     if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrCopyPair);
     return;
   }
-  unsigned char* base = static_cast<unsigned char*>(is_v ? p.v[layer] : p.k[layer]);
-  const uint4* s = reinterpret_cast<const uint4*>(base + src * p.block_bytes);
-  uint4* d = reinterpret_cast<uint4*>(base + dst * p.block_bytes);
+  const unsigned char* sbase = static_cast<const unsigned char*>(is_v ? p.v[layer] : p.k[layer]);
+  unsigned char* dbase = static_cast<unsigned char*>(is_v ? p.dv[layer] : p.dk[layer]);
+  const uint4* s = reinterpret_cast<const uint4*>(sbase + src * p.block_bytes);
+  uint4* d = reinterpret_cast<uint4*>(dbase + dst * p.block_bytes);
   const int64_t n16 = p.block_bytes / 16;
   constexpr int kUnroll = 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;

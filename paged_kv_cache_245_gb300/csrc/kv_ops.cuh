@@ -25,10 +25,13 @@ constexpr int kMaxCopyLayers = 64;  // layers per launch (pointers passed by val
 
 struct CopyParams {
   const int64_t* pairs;  // [n][2] (src, dst)
-  void* k[kMaxCopyLayers];
+  void* k[kMaxCopyLayers];   // source pools
   void* v[kMaxCopyLayers];
+  void* dk[kMaxCopyLayers];  // destination pools (the sources for a copy on write)
+  void* dv[kMaxCopyLayers];
   int32_t num_layers;    // <= kMaxCopyLayers for this launch
-  int64_t num_blocks;
+  int64_t num_blocks;     // source ids in checked mode
+  int64_t dst_num_blocks; // destination ids in checked mode
   int64_t block_bytes;
   int32_t checked;
   int* err;

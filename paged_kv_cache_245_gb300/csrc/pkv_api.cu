@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "../../include/pkv.h"
 #include "decode_launch.cuh"
@@ -774,6 +775,70 @@ pkv_status pkv_debug_gather_contig(const void* buf, const int32_t* req_ids, int3
                        max_context, S, num_kv_heads, out, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Launches the block copy kernel over n pairs and num_layers layers in
+// slices of at most 65535 pairs (grid y) and kMaxCopyLayers layers.
+pkv_status copy_blocks(const int64_t* pairs, int64_t n, void* const* sk, void* const* sv,
+                       int64_t src_blocks, void* const* dk, void* const* dv, int64_t dst_blocks,
+                       int32_t num_layers, int64_t block_bytes, void* stream) {
+  int* err = nullptr;
+  pkv_status st = device_info(nullptr, &err, nullptr);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int64_t p0 = 0; p0 < n; p0 += 65535) {
+    const int64_t np = (n - p0) < 65535 ? (n - p0) : 65535;
+    for (int32_t l0 = 0; l0 < num_layers; l0 += pkv::kMaxCopyLayers) {
+      pkv::CopyParams p;
+      std::memset(&p, 0, sizeof p);
+      p.pairs = pairs + 2 * p0;
+      p.num_layers = (num_layers - l0) < pkv::kMaxCopyLayers ? (num_layers - l0) : pkv::kMaxCopyLayers;
+      for (int32_t l = 0; l < p.num_layers; ++l) {
+        p.k[l] = sk[l0 + l];
+        p.v[l] = sv[l0 + l];
+        p.dk[l] = dk[l0 + l];
+        p.dv[l] = dv[l0 + l];
+      }
+      p.num_blocks = src_blocks;
+      p.dst_num_blocks = dst_blocks;
+      p.block_bytes = block_bytes;
+      p.checked = g_checked.load();
+      p.err = err;
+      const cudaError_t e = pkv::launch_block_copy(p, np, s);
+      if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+    }
+  }
+  return PKV_OK;
+}
+
+// The address the kernels on `dev` use for p: p itself for device memory of
+// `dev` or managed memory, the device alias of page-locked host memory;
+// null for pageable host memory, another device's memory or an unknown
+// pointer.
+void* device_view(void* p, int dev) {
+  if (p == nullptr) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      return a.device == dev ? a.devicePointer : nullptr;
+    case cudaMemoryTypeManaged:
+    case cudaMemoryTypeHost:
+      return a.devicePointer;
+    default:
+      return nullptr;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
 pkv_status pkv_block_copy(const int64_t* src_dst_pairs, int64_t n, void* const* k_caches,
                           void* const* v_caches, int32_t num_layers, int64_t num_blocks,
                           int64_t block_bytes, void* stream) {
@@ -789,30 +854,46 @@ pkv_status pkv_block_copy(const int64_t* src_dst_pairs, int64_t n, void* const* 
     if (!k_caches[l] || !v_caches[l] || !aligned(k_caches[l], 16) || !aligned(v_caches[l], 16))
       return fail(PKV_ERR_INVALID_ARG, "cache pointer of layer %d null or misaligned", l);
   }
-  int* err = nullptr;
-  pkv_status st = device_info(nullptr, &err, nullptr);
+  return copy_blocks(src_dst_pairs, n, k_caches, v_caches, num_blocks, k_caches, v_caches,
+                     num_blocks, num_layers, block_bytes, stream);
+}
+
+pkv_status pkv_block_swap(const int64_t* pairs, int64_t n, void* const* src_k,
+                          void* const* src_v, int64_t src_num_blocks, void* const* dst_k,
+                          void* const* dst_v, int64_t dst_num_blocks, int32_t num_layers,
+                          int64_t block_bytes, void* stream) {
+  if (n < 0 || num_layers < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (n == 0 || num_layers == 0) return PKV_OK;
+  if (!src_k || !src_v || !dst_k || !dst_v)
+    return fail(PKV_ERR_INVALID_ARG, "null pool pointer array");
+  if (block_bytes <= 0 || block_bytes % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "block_bytes must be a positive multiple of 16");
+  if (src_num_blocks <= 0 || dst_num_blocks <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "pool sizes must be >= 1");
+  if (num_layers > 4096) return fail(PKV_ERR_INVALID_ARG, "more than 4096 layers");
+  int dev = 0;
+  pkv_status st = device_info(&dev, nullptr, nullptr);
   if (st != PKV_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (int64_t p0 = 0; p0 < n; p0 += 65535) {
-    const int64_t np = (n - p0) < 65535 ? (n - p0) : 65535;
-    for (int32_t l0 = 0; l0 < num_layers; l0 += pkv::kMaxCopyLayers) {
-      pkv::CopyParams p;
-      std::memset(&p, 0, sizeof p);
-      p.pairs = src_dst_pairs + 2 * p0;
-      p.num_layers = (num_layers - l0) < pkv::kMaxCopyLayers ? (num_layers - l0) : pkv::kMaxCopyLayers;
-      for (int32_t l = 0; l < p.num_layers; ++l) {
-        p.k[l] = k_caches[l0 + l];
-        p.v[l] = v_caches[l0 + l];
-      }
-      p.num_blocks = num_blocks;
-      p.block_bytes = block_bytes;
-      p.checked = g_checked.load();
-      p.err = err;
-      const cudaError_t e = pkv::launch_block_copy(p, np, s);
-      if (e != cudaSuccess) return cuda_fail(e, "block_copy launch");
+  const int64_t* pv =
+      static_cast<const int64_t*>(device_view(const_cast<int64_t*>(pairs), dev));
+  if (pv == nullptr || !aligned(pv, 8))
+    return fail(PKV_ERR_INVALID_ARG,
+                "pairs must be device, managed or page-locked host memory, 8-byte aligned");
+  std::vector<void*> view(4 * static_cast<size_t>(num_layers));
+  void* const* in[4] = {src_k, src_v, dst_k, dst_v};
+  static const char* const kName[4] = {"src_k", "src_v", "dst_k", "dst_v"};
+  for (int a = 0; a < 4; ++a)
+    for (int32_t l = 0; l < num_layers; ++l) {
+      void* d = device_view(in[a][l], dev);
+      if (d == nullptr || !aligned(d, 16))
+        return fail(PKV_ERR_INVALID_ARG,
+                    "%s[%d] must be device, managed or page-locked host memory, 16-byte aligned",
+                    kName[a], l);
+      view[a * num_layers + l] = d;
     }
-  }
-  return PKV_OK;
+  return copy_blocks(pv, n, view.data(), view.data() + num_layers, src_num_blocks,
+                     view.data() + 2 * num_layers, view.data() + 3 * num_layers, dst_num_blocks,
+                     num_layers, block_bytes, stream);
 }
 
 void pkv_set_checked(int enable) { g_checked.store(enable ? 1 : 0); }

@@ -17,7 +17,8 @@ raise AssertionError when the oracle is wrong.
     section 5.2.3; "Running Out of Cache", block tables);
   * GQA: repeating each KV head G times (plain MHA) gives the same result;
   * append then gather finds the new token at the last position; untouched
-    bytes stay untouched; copy on write makes dst equal src;
+    bytes stay untouched; copy on write makes dst equal src; a swap out to
+    another pool and back into new blocks gives the same logical rows;
   * causal prefill: torch fp64 attention with an explicit causal mask; a
     chunk of one token is the decode step; the last token of a chunk equals
     decode; a query ignores later positions and depends on its own.
@@ -306,6 +307,43 @@ def pin_block_copy(orc):
         untouched = [b for b in range(nb) if b not in pairs[:, 1]]
         assert np.array_equal(ks[l][untouched], k0[l][untouched])
         assert np.array_equal(vs[l][untouched], v0[l][untouched])
+
+
+def pin_block_swap(orc):
+    # out of a device-like pool into a host-like pool of another size, then
+    # back into new blocks: the sequence read through its new table is the
+    # one it was; blocks no pair names are untouched
+    rng = np.random.default_rng(19)
+    L, nb, nh, hkv, bs = 2, 9, 5, 2, 4
+    dk = [_pool(rng, nb, hkv, bs) for _ in range(L)]
+    dv = [_pool(rng, nb, hkv, bs) for _ in range(L)]
+    hk = [_pool(rng, nh, hkv, bs) for _ in range(L)]
+    hv = [_pool(rng, nh, hkv, bs) for _ in range(L)]
+    table = np.array([6, 1, 4], np.int32)
+    before = [orc.gather_paged(dk[l], table, 11, bs, h) for l in range(L) for h in range(hkv)]
+    h0 = [a.copy() for a in hk]
+    out = np.array([[6, 3], [1, 0], [4, 4]], np.int64)
+    orc.block_swap(out, dk, dv, hk, hv)
+    for l in range(L):
+        assert np.array_equal(hk[l][[1, 2]], h0[l][[1, 2]])
+        assert np.array_equal(hk[l][3], dk[l][6]) and np.array_equal(hv[l][0], dv[l][1])
+    for l in range(L):                                  # the device blocks are reused
+        dk[l][[6, 1, 4]] = 0
+        dv[l][[6, 1, 4]] = 0
+    new_table = np.array([2, 8, 0], np.int32)
+    orc.block_swap(np.array([[3, 2], [0, 8], [4, 0]], np.int64), hk, hv, dk, dv)
+    after = [orc.gather_paged(dk[l], new_table, 11, bs, h) for l in range(L) for h in range(hkv)]
+    for a, b in zip(before, after):
+        assert np.array_equal(a, b)
+    # within one pool it is the copy on write
+    ks = [_pool(rng, nb, hkv, bs) for _ in range(L)]
+    vs = [_pool(rng, nb, hkv, bs) for _ in range(L)]
+    ks2, vs2 = [a.copy() for a in ks], [a.copy() for a in vs]
+    pairs = np.array([[3, 7], [0, 5]], np.int64)
+    orc.block_swap(pairs, ks, vs, ks, vs)
+    orc.block_copy(pairs, ks2, vs2)
+    for l in range(L):
+        assert np.array_equal(ks[l], ks2[l]) and np.array_equal(vs[l], vs2[l])
 
 
 # --------------------------------------------------------------------- prefill

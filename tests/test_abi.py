@@ -141,3 +141,15 @@ def test_prefill_validation(L):
                                           0.1, _h(), FAKE, None) == 2
     assert L.pkv_contig_prefill_attention(FAKE, FAKE, 8, MISALIGNED, FAKE, FAKE, 4, FAKE, 2, 4,
                                           1024, 0.1, _h(), FAKE, None) == 1
+
+
+def test_block_swap_validation(L):
+    one = (ctypes.c_void_p * 1)(FAKE)
+    # (pairs, n, src_k, src_v, src_blocks, dst_k, dst_v, dst_blocks, layers, block_bytes, stream)
+    assert L.pkv_block_swap(FAKE, -1, one, one, 4, one, one, 4, 1, 64, None) == 1
+    assert L.pkv_block_swap(FAKE, 0, one, one, 4, one, one, 4, 1, 64, None) == 0  # no pairs
+    assert L.pkv_block_swap(FAKE, 2, None, one, 4, one, one, 4, 1, 64, None) == 1
+    assert L.pkv_block_swap(FAKE, 2, one, one, 4, one, one, 4, 1, 24, None) == 1
+    assert b"multiple of 16" in L.pkv_last_error()
+    assert L.pkv_block_swap(FAKE, 2, one, one, 0, one, one, 4, 1, 64, None) == 1
+    assert L.pkv_block_swap(FAKE, 2, one, one, 4, one, one, 0, 1, 64, None) == 1
