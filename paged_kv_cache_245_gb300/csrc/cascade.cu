@@ -148,38 +148,54 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   }
   if (c.own_cap >= 0) grid_dependency_wait();  // the prefix records are complete
   grid_dependency_trigger();
-  // Fold in the prefix records, one per chunk of the shared positions (a
-  // member beyond the group size bound has none: the caller broke the
-  // contract, nothing is read):  M' = max(M, m),  acc' = acc 2^(M - M') +
-  // l 2^(m - M') o,  W' = W 2^(M - M') + l 2^(m - M').
-  float M = ls > 0.f ? ms : -INFINITY;
-  float W = ls > 0.f ? ls : 0.f;
-  float4 acc = ls > 0.f ? make_float4(os.x * ls, os.y * ls, os.z * ls, os.w * ls)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  // Fold in the prefix records, two per chunk of the shared positions (even
+  // and odd key tiles; the second only if the chunk has more than one tile).
+  // A member beyond the group size bound has none: the caller broke the
+  // contract, nothing is read.  Lane k loads record k's (m, l), all at once;
+  // every lane loads its four o values of four records at a time; then
+  //   M' = max(M, m_k),  acc' = acc 2^(M - M') + sum_k l_k 2^(m_k - M') o_k,
+  //   W' = W 2^(M - M') + sum_k l_k 2^(m_k - M').
+  constexpr int kMaxRec = 16;  // 2 records per chunk, at most 8 chunks
   const bool member = kg >= 0 && kg * c.G < c.prefix_rows;
   const int shared = sb * c.bs;
-  const int chunks = member ? (shared + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys : 0;
-  // per chunk two records: even and odd key tiles (the second only if the
-  // chunk has more than one tile)
-  for (int kh = 0; kh < 2 * chunks; ++kh) {
-    const int k = kh >> 1, half = kh & 1;
-    if (half == 1 && min(c.prefix_chunk_keys, shared - k * c.prefix_chunk_keys) <= 128) continue;
-    const float* rp =
-        c.rec_p + ((((static_cast<int64_t>(g) * c.prefix_chunks + k) * 2 + half) * c.Hkv + kvh) *
-                       c.prefix_rows +
-                   kg * c.G + gi) *
-                      kRecStride;
-    const float mp = __ldcg(rp + 128);
-    const float lp = __ldcg(rp + 129);
-    if (!(lp > 0.f)) continue;
-    const float Mn = fmaxf(M, mp);
-    const float a = W > 0.f ? fast_exp2(M - Mn) : 0.f;
-    const float wgt = lp * fast_exp2(mp - Mn);
-    const float4 op = __ldcg(reinterpret_cast<const float4*>(rp) + lane);
-    acc = make_float4(acc.x * a + wgt * op.x, acc.y * a + wgt * op.y, acc.z * a + wgt * op.z,
-                      acc.w * a + wgt * op.w);
-    W = W * a + wgt;
-    M = Mn;
+  const int chunks = member ? min((shared + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys,
+                                  min(c.prefix_chunks, kMaxRec / 2))
+                            : 0;
+  auto used = [&](int kh) {
+    return kh < 2 * chunks &&
+           ((kh & 1) == 0 || min(c.prefix_chunk_keys, shared - (kh >> 1) * c.prefix_chunk_keys) > 128);
+  };
+  auto rec = [&](int kh) {
+    return c.rec_p + ((((static_cast<int64_t>(g) * c.prefix_chunks + (kh >> 1)) * 2 + (kh & 1)) *
+                           c.Hkv + kvh) * c.prefix_rows + kg * c.G + gi) * kRecStride;
+  };
+  float mk = -INFINITY, lk = 0.f;
+  if (lane < kMaxRec && used(lane)) {
+    mk = __ldcg(rec(lane) + 128);
+    lk = __ldcg(rec(lane) + 129);
+  }
+  float M = ls > 0.f ? ms : -INFINITY;
+  float mx = lk > 0.f ? mk : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float Mn = fmaxf(M, mx);
+  const float wk = lk > 0.f ? lk * fast_exp2(mk - Mn) : 0.f;  // lane k: record k's weight
+  const float a = ls > 0.f ? ls * fast_exp2(M - Mn) : 0.f;     // the own part's weight
+  float W = a;
+  float4 acc = make_float4(os.x * a, os.y * a, os.z * a, os.w * a);
+  for (int k0 = 0; k0 < 2 * chunks; k0 += 4) {  // o of four records at a time
+    float4 op[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      op[u] = used(k0 + u) ? __ldcg(reinterpret_cast<const float4*>(rec(k0 + u)) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wk, k0 + u);
+      W += w;
+      acc = make_float4(fmaf(w, op[u].x, acc.x), fmaf(w, op[u].y, acc.y), fmaf(w, op[u].z, acc.z),
+                        fmaf(w, op[u].w, acc.w));
+    }
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   const float x = acc.x * inv, y = acc.y * inv, z = acc.z * inv, w = acc.w * inv;

@@ -6,7 +6,7 @@
 // (cascade.cu) folds this kernel's records with each member's own positions.
 //
 // Work: one CTA per (128 rows, KV head, group, chunk of the shared
-// positions).  The rows are the group's (member, query head) pairs of the KV
+// positions), chunks with the most key tiles first.  The rows are the group's (member, query head) pairs of the KV
 // head; every row attends every shared position (no causal mask).  A group
 // has few rows (28 for 4 branches at G = 7), so both row tiles of the CTA
 // hold the same rows (one Q tile in shared memory) and take alternate key
@@ -53,16 +53,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort = reinterpret_cast<volatile int*>(bars + 20);
 
+  int* pick = reinterpret_cast<int*>(bars + 22);  // [2] the chosen key-tile count, chunk
+
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int kvh = blockIdx.y;
-  const int g = blockIdx.z / p.chunks;
-  const int kc = blockIdx.z % p.chunks;
   const int G = p.G;
 
   grid_dependency_wait();
   grid_dependency_trigger();
+
+  // ---- longest chunks first.  CTAs start in index order as SMs free up, so
+  // CTA z takes the chunk of rank z in the order (key tiles descending, chunk
+  // index ascending): the long chunks start first and the short ones fill
+  // the tail.  A counting sort over key-tile counts, its scratch in the K/V
+  // stages (nothing is loaded there yet).
+  int item = blockIdx.z;
+  {
+    const int N = p.num_groups * p.chunks;
+    const int nb = p.chunk_keys / kKeys + 1;  // key-tile counts 0 .. chunk_keys / 128
+    int* shared_pos = reinterpret_cast<int*>(smem + kOffK);  // [num_groups]
+    int* hist = shared_pos + p.num_groups;                   // [nb]
+    int* start = hist + nb;                                  // [nb] rank of a count's first chunk
+    if (p.num_groups + 2 * nb <= kStages * kStageBytes / 4) {
+      for (int i = tid; i < p.num_groups; i += kThreads)
+        shared_pos[i] = min(max(p.shared_blocks[i], 0), p.max_blocks) * static_cast<int>(p.bs);
+      for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+      if (tid == 0) {  // identity, should no count match (it always does: z < N)
+        pick[0] = -1;
+        pick[1] = blockIdx.z;
+      }
+      __syncthreads();
+      auto tiles_of = [&](int i) -> int {
+        const int kb = (i % p.chunks) * p.chunk_keys;
+        const int len = min(shared_pos[i / p.chunks] - kb, p.chunk_keys);
+        return len > 0 ? (len + kKeys - 1) / kKeys : 0;
+      };
+      for (int i = tid; i < N; i += kThreads) atomicAdd(&hist[tiles_of(i)], 1);
+      __syncthreads();
+      if (warp == 0) {  // start[b] = chunks with more key tiles than b
+        int carry = 0;
+        for (int top = nb - 1; top >= 0; top -= 32) {
+          const int b = top - lane;
+          const int v = b >= 0 ? hist[b] : 0;
+          int incl = v;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+          }
+          if (b >= 0) start[b] = carry + incl - v;
+          carry += __shfl_sync(kFull, incl, 31);
+        }
+      }
+      __syncthreads();
+      const int z = blockIdx.z;
+      for (int b = tid; b < nb; b += kThreads)
+        if (start[b] <= z && z < start[b] + hist[b]) pick[0] = b;
+      __syncthreads();
+      const int b = pick[0];
+      if (warp == 0 && b >= 0 && b < nb) {  // the (z - start[b])-th chunk, in index order, with b key tiles
+        int want = z - start[b];
+        for (int base = 0; base < N; base += 32) {
+          const int i = base + lane;
+          const unsigned m = __ballot_sync(kFull, i < N && tiles_of(i) == b);
+          const int c = __popc(m);
+          if (want < c) {
+            unsigned x = m;
+            for (int k = 0; k < want; ++k) x &= x - 1;
+            if (lane == 0) pick[1] = base + __ffs(x) - 1;
+            break;
+          }
+          want -= c;
+        }
+      }
+      fence_proxy_async_smem();  // the stages are TMA destinations from here on
+      __syncthreads();
+      item = min(max(pick[1], 0), N - 1);
+    }
+  }
+  const int g = item / p.chunks;
+  const int kc = item % p.chunks;
 
   const int seq = p.group_start[g];  // the group's first member: its block table
   const int rows = (p.group_start[g + 1] - seq) * G;
