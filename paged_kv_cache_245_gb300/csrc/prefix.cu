@@ -14,7 +14,7 @@
 // the other row tile's run -- each writes its own record (half j % 2).  K/V
 // come by TMA (the 4-D boxes of prefill.cu) through a 3-stage ring: with
 // each tile used by one row tile, a third stage keeps the next loads ahead
-// of the chain S -> softmax -> P V.  Tensor memory as in prefill.cu: S_t in
+// of the chain S -> softmax -> P V.  K and V have a producer warp each.  Tensor memory as in prefill.cu: S_t in
 // columns 128t .., O_t in 256 + 128t ..; P over S in place; lazy rescale.
 #include "pkv_device.cuh"
 #include "prefix.cuh"
@@ -31,7 +31,7 @@ constexpr int kOffK = kOpBytes;                       // after the one Q tile
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 224 KiB
 constexpr int kSmemBytes = kTilesBytes + 256 + 1024;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;  // 8 softmax warps, K producer, MMA issuer, V producer
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 }  // namespace
@@ -148,16 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (kend - kbase + kKeys - 1) / kKeys;
   const bool two = ntiles > 1;  // row tile 1 has odd tiles to take
 
-  // Producer state (warp 8): lanes 0-7 copy K of run r of a tile, lanes
-  // 16-23 V of the same run.
+  // Producers: warp 8 copies K, warp 10 copies V, each on its own stage
+  // schedule -- K of tile j waits only for the S product of tile j - 3, not
+  // for its P V, so the K loads run a tile further ahead of the S chain.
+  // Lane r < runs copies run r of a tile.
   const uint64_t policy = l2_policy_evict_first();  // read once
   const int run = p.run_rows;    // rows per box (16 .. 128, divides 128 and bs)
   const int runs = kKeys / run;  // boxes per tile and tensor (<= 8)
-  const int prun = lane & 15;
   auto entry = [&](int j) -> int32_t {
-    const int kpos = kbase + j * kKeys + prun * run;
+    const int kpos = kbase + j * kKeys + lane * run;
     int32_t e = -1;
-    if (j < ntiles && prun < runs && kpos < ctx) {
+    if (j < ntiles && lane < runs && kpos < ctx) {
       e = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs];
       if (p.checked && (e < 0 || e >= p.num_blocks)) {
         record_error(p.err, kErrBlockId);
@@ -166,36 +167,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return e;
   };
-  int32_t e = -1;        // entries of the next tile to issue
-  int issued = 0;        // tiles whose K and V were both issued
-  bool kv_half = false;  // tile `issued` has its K issued, not its V
+  const bool is_v = warp == 10;
+  const CUtensorMap* tm = is_v ? &tmv : &tmk;
+  uint64_t* full = is_v ? vfull : kfull;
+  uint64_t* empty = is_v ? vempty : kempty;
+  int32_t e = -1;   // entries of the next tile to issue
+  int issued = 0;   // tiles this producer issued
   auto produce = [&](int j0, int j1) -> bool {
     for (int j = j0; j < j1; ++j) {
       const int s = j % kStages;
       const uint32_t u = static_cast<uint32_t>(j / kStages);  // use of the stage
-      const uint32_t loaded = __popc(__ballot_sync(kFull, lane < 16 && e >= 0));
-      const int off = (kbase + j * kKeys + prun * run) % p.bs;
+      const uint32_t loaded = __popc(__ballot_sync(kFull, e >= 0));
+      const int off = (kbase + j * kKeys + lane * run) % p.bs;
       const int32_t grp =
           e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
-      unsigned char* dst = smem + kOffK + s * kStageBytes + prun * run * kRowBytes;
+      unsigned char* dst =
+          smem + kOffK + s * kStageBytes + (is_v ? kOpBytes : 0) + lane * run * kRowBytes;
       if (j >= kStages &&
-          !__all_sync(kFull, wait_or_abort(&kempty[s], (u - 1) & 1, abort, p.err)))
+          !__all_sync(kFull, wait_or_abort(&empty[s], (u - 1) & 1, abort, p.err)))
         return false;
-      if (lane == 0) mbar_arrive_expect_tx(&kfull[s], loaded * run * kRowBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], loaded * run * kRowBytes);
       __syncwarp();
-      if (lane < 16 && e >= 0) tma_load_4d(dst, &tmk, grp, &kfull[s], policy);
-      if (j >= kStages &&
-          !__all_sync(kFull, wait_or_abort(&vempty[s], (u - 1) & 1, abort, p.err))) {
-        kv_half = true;  // K of tile `issued` is in flight
-        return false;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&vfull[s], loaded * run * kRowBytes);
-      __syncwarp();
-      if (lane >= 16 && e >= 0) tma_load_4d(dst + kOpBytes, &tmv, grp, &vfull[s], policy);
+      if (e >= 0) tma_load_4d(dst, tm, grp, &full[s], policy);
       issued = j + 1;
       e = entry(j + 1);  // the next tile's entries load while this one lands
     }
     return true;
+  };
+  // after an abort: let this producer's copies in flight land before the
+  // CTA's shared memory is released
+  auto drain_copies = [&]() {
+    if (*abort && lane == 0)
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        mbar_wait_bounded(&full[j % kStages], static_cast<uint32_t>(j / kStages) & 1);
   };
 
   // Rows of both row tiles (the same rows): row r -> (member r / G, head r % G).
@@ -424,17 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 8) {
-    // ================= K/V producer: the remaining tiles =================
+    // ================= K producer: the remaining tiles =================
     produce(kStages, ntiles);
-    if (*abort && lane == 0) {
-      // let the copies in flight land before the CTA's shared memory is released
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
-        mbar_wait_bounded(&kfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1);
-        mbar_wait_bounded(&vfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1);
-      }
-      if (kv_half)
-        mbar_wait_bounded(&kfull[issued % kStages], static_cast<uint32_t>(issued / kStages) & 1);
-    }
+    drain_copies();
+  } else if (warp == 10) {
+    // ================= V producer: every tile (the barriers exist now) =================
+    e = entry(0);
+    produce(0, ntiles);
+    drain_copies();
   } else if (warp == 9) {
     // ================= MMA issuer (lane 0 issues) =================
     // order S_0(0) S_1(1) | PV_0(0) S_0(2) | PV_1(1) S_1(3) | PV_0(2) S_0(4) | ...
