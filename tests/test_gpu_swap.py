@@ -92,3 +92,43 @@ def test_checked_mode_reports_an_id_outside_the_host_pool():
     torch.cuda.synchronize()
     assert pkv.get_device_error() == "copy_pair"
     assert all(torch.equal(a, b) for a, b in zip(hk, before))
+
+
+def test_many_pairs_and_layers_cross_the_launch_slices():
+    # more pairs than one launch's grid takes (65535) and more layers than
+    # one launch's parameters hold (64): 16-byte blocks keep the pools small
+    rng = np.random.default_rng(11)
+    nb, n = 140000, 70000
+    perm = rng.permutation(nb)
+    pairs = np.stack([perm[:n], perm[n:]], 1).astype(np.int64)
+    g = torch.Generator().manual_seed(12)
+    k = torch.randn((nb, 8), generator=g).to(torch.bfloat16)
+    v = torch.randn((nb, 8), generator=g).to(torch.bfloat16)
+    # copy on write within one pool
+    dk, dv = k.to(DEV), v.to(DEV)
+    pkv.block_copy(torch.as_tensor(pairs, device=DEV), [dk], [dv])
+    mk, mv = W.to_u16(k).copy(), W.to_u16(v).copy()
+    oracle.block_copy(pairs, [mk], [mv])
+    torch.cuda.synchronize()
+    assert np.array_equal(W.to_u16(dk), mk) and np.array_equal(W.to_u16(dv), mv)
+    # swap out to a page-locked pool, slots in order
+    out = np.stack([perm[:n], np.arange(n)], 1).astype(np.int64)
+    hk = torch.zeros((n, 8), dtype=torch.bfloat16).pin_memory()
+    hv = torch.zeros((n, 8), dtype=torch.bfloat16).pin_memory()
+    pkv.block_swap(torch.as_tensor(out, device=DEV), [dk], [dv], [hk], [hv])
+    torch.cuda.synchronize()
+    assert np.array_equal(W.to_u16(hk), mk[perm[:n]]) and np.array_equal(W.to_u16(hv), mv[perm[:n]])
+    # 70 layers back in, one launch per 64 layers
+    L = 70
+    src_k = [torch.randn((6, 8), generator=g).to(torch.bfloat16).pin_memory() for _ in range(L)]
+    src_v = [torch.randn((6, 8), generator=g).to(torch.bfloat16).pin_memory() for _ in range(L)]
+    dst_k = [torch.zeros((10, 8), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    dst_v = [torch.zeros((10, 8), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    back = np.array([[5, 0], [0, 9], [3, 4]], np.int64)
+    pkv.block_swap(torch.as_tensor(back, device=DEV), src_k, src_v, dst_k, dst_v)
+    mdk = [np.zeros((10, 8), np.uint16) for _ in range(L)]
+    mdv = [np.zeros((10, 8), np.uint16) for _ in range(L)]
+    oracle.block_swap(back, _u16(src_k), _u16(src_v), mdk, mdv)
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert np.array_equal(W.to_u16(dst_k[l]), mdk[l]) and np.array_equal(W.to_u16(dst_v[l]), mdv[l])
