@@ -6,16 +6,18 @@
 // (cascade.cu) folds this kernel's records with each member's own positions.
 //
 // Work: one CTA per (128 rows, KV head, group, chunk of the shared
-// positions), chunks with the most key tiles first.  The rows are the group's (member, query head) pairs of the KV
-// head; every row attends every shared position (no causal mask).  A group
-// has few rows (28 for 4 branches at G = 7), so both row tiles of the CTA
-// hold the same rows (one Q tile in shared memory) and take alternate key
-// tiles: tile j goes to row tile j % 2, whose S, softmax and P V run while
-// the other row tile's run -- each writes its own record (half j % 2).  K/V
-// come by TMA (the 4-D boxes of prefill.cu) through a 3-stage ring: with
-// each tile used by one row tile, a third stage keeps the next loads ahead
-// of the chain S -> softmax -> P V.  K and V have a producer warp each.  Tensor memory as in prefill.cu: S_t in
-// columns 128t .., O_t in 256 + 128t ..; P over S in place; lazy rescale.
+// positions), chunks with the most key tiles first.  The rows are the
+// group's (member, query head) pairs of the KV head; every row attends every
+// shared position (no causal mask).  A group has few rows (28 for 4 branches
+// at G = 7), so both row tiles of the CTA hold the same rows (one Q tile in
+// shared memory, row tile 1's copy further down when the rows fit twice) and
+// take alternate key tiles: tile j goes to row tile j % 2, whose S, softmax
+// and P V run while the other row tile's run -- each writes its own record
+// (half j % 2).  K/V come by TMA (the 4-D boxes of prefill.cu) through a
+// 3-stage ring: with each tile used by one row tile, a third stage keeps the
+// next loads ahead of the chain S -> softmax -> P V.  K and V have a producer
+// warp each.  Tensor memory as in prefill.cu: S_t in columns 128t .., O_t in
+// 256 + 128t ..; P over S in place; lazy rescale.
 #include "pkv_device.cuh"
 #include "prefix.cuh"
 #include "umma.cuh"
@@ -202,18 +204,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&full[j % kStages], static_cast<uint32_t>(j / kStages) & 1);
   };
 
-  // Rows of both row tiles (the same rows): row r -> (member r / G, head r % G).
+  // Rows: row r -> (member r / G, head r % G).  Both row tiles hold the same
+  // rows; a TMEM lane quadrant can only be read by the warps of one SM
+  // sub-partition, so when the rows fit twice (at most 64), row tile 1 reads
+  // them from a copy `shift` rows further down the Q tile: its softmax then
+  // runs in other quadrants, on other sub-partitions, than row tile 0's.
+  // Softmax warps whose quadrant holds none of their row tile's rows idle.
   const int t = (warp >> 2) & 1;
-  const int lr = tid & (kRowTile - 1);
-  const int r = row0 + lr;
-  const bool valid = r < rows;
-  const int rr = valid ? r : rows - 1;  // padding rows mirror the last row
+  const int lr = tid & (kRowTile - 1);  // Q row / TMEM lane
+  const int rows_here = min(rows - row0, kRowTile);
+  const int nq = (rows_here + 31) / 32;                  // quadrants of a row tile at work
+  const int shift = two && nq <= 2 ? 32 * nq : 0;
+  const int qr = shift > 0 && lr >= shift && lr < 2 * shift ? lr - shift : lr;  // row of Q lane lr
+  const int rr = qr < rows_here ? row0 + qr : rows - 1;  // padding rows mirror the last row
   const int64_t qrow = (static_cast<int64_t>(seq) + rr / G) * p.Hq + kvh * G + rr % G;
-  const int pos = ctx - 1;              // every shared position is visible
+  // row tile t's row at lane lr, and whether row tile t owns that lane
+  auto row_of = [&]() { return t == 1 ? lr - shift : lr; };
+  auto owns = [&]() {
+    const int rt = row_of();
+    return rt >= 0 && rt < rows_here && (t == 1 || shift == 0 || lr < shift);
+  };
+  const int pos = ctx - 1;                               // every shared position is visible
 
   if (warp == 8) {
     if (lane == 0) {
-      for (int b = 0; b < 18; ++b) mbar_init(&bars[b], (b == 14 || b == 15) ? 4 : 1);
+      for (int b = 0; b < 18; ++b) mbar_init(&bars[b], (b == 14 || b == 15) ? nq : 1);
       mbar_init(drain, 1);
       *abort = 0;
       fence_barrier_init();
@@ -234,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint4 v = valid ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 v = qr < rows_here ? ld_global_nc_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(smem + q_chunk_offset(lr, c)) = v;
     }
     fence_proxy_async_smem();
@@ -245,14 +260,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_addr(smem);
 
-  if (warp < 8 && t == 1 && !two) {
-    // one key tile: row tile 1 has nothing to do
+  if (warp < 8 && ((t == 1 && !two) || !__any_sync(kFull, owns()))) {
+    // one key tile (row tile 1 has nothing to do), or no row of this row tile
+    // in this warp's quadrant
   } else if (warp < 8) {
     // ================= softmax: row tile t takes key tiles t, t + 2, ... =================
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + t * 128;
     const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
     const float sc = p.qscale;
+    // this lane's record: (member, head) row of row tile t, half t of the chunk
+    const bool own = owns();
+    float* const rec = p.rec_out +
+                       ((((static_cast<int64_t>(g) * p.chunks + kc) * 2 + t) * p.Hkv + kvh) *
+                            p.rows + row0 + row_of()) *
+                           kPrefixRecStride;
     float m_used = -INFINITY;  // the maximum P is taken against (scaled logits)
     float l = 0.f;
     bool ok = true;
@@ -404,16 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fp32 record of this (member, head) and half: o / l, m, l
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* rec = p.rec_out +
-                   ((((static_cast<int64_t>(g) * p.chunks + kc) * 2 + t) * p.Hkv + kvh) * p.rows +
-                    r) *
-                       kPrefixRecStride;
 #pragma unroll
       for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
         uint32_t w[32];
         tmem_ld32(w, o_tm + c0);
         tmem_wait_ld(w);
-        if (valid) {
+        if (own) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             reinterpret_cast<float4*>(rec + c0)[q] =
@@ -422,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __uint_as_float(w[4 * q + 3]) * inv);
         }
       }
-      if (valid) {
+      if (own) {
         rec[128] = m_used;
         rec[129] = l;
       }
