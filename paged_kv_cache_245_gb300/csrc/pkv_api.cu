@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -330,13 +331,33 @@ static_assert(pkv::kPrefixRecStride == pkv::kRecStride, "one record layout for e
 constexpr int kMaxPrefixChunks = 8;  // chunks of a group's shared positions (bound)
 
 // Chunk of the shared positions for the prefix kernel: whole blocks, a
-// multiple of 128 positions, at least 4096 positions (a sweep of 1024 .. 8192
-// on the Yi-34B sharing workload: 154, 138, 129, 147 us), and at most
-// kMaxPrefixChunks chunks per group.
-int32_t prefix_chunk_blocks(int32_t max_blocks, int32_t block_size) {
+// multiple of 128 positions, at most kMaxPrefixChunks chunks per group.  A
+// CTA's start and drain are paid once per chunk, so chunks are as long as
+// possible, up to kMaxChunk positions, while there are still about 1.5 chunks
+// per SM, counting every group at the table's full length.  On the Yi-34B
+// sharing workload (32 groups x 8 KV heads, 1 K - 8 K shared positions, 152
+// SMs), chunks of 2048, 3072, 4096, 5120, 6144, 7168 and 8192 positions gave
+// 129.9, 122.1, 114.2, 114.2, 111.9, 109.9 and 109.0 us per call.
+// PKV_PREFIX_CHUNK (positions, 1024 .. 65536) fixes the length instead.
+int32_t prefix_chunk_blocks(int32_t max_blocks, int32_t block_size, int32_t num_groups,
+                            int32_t num_kv_heads, int sms) {
+  constexpr int64_t kMinChunk = 1024, kMaxChunk = 8192;
+  static const int64_t fixed = [] {
+    const char* v = getenv("PKV_PREFIX_CHUNK");
+    const long x = v != nullptr ? strtol(v, nullptr, 10) : 0;
+    return x >= 1024 && x <= 65536 ? static_cast<int64_t>(x) : int64_t{0};
+  }();
+  int64_t chunk = fixed;
+  if (chunk == 0) {
+    const int64_t slots = static_cast<int64_t>(num_groups) * num_kv_heads;  // CTAs per chunk
+    const int64_t want = (3 * static_cast<int64_t>(sms > 0 ? sms : 1) + 1) / 2;
+    const int64_t per_group = (want + slots - 1) / slots;
+    chunk = (static_cast<int64_t>(max_blocks) * block_size + per_group - 1) / per_group;
+    chunk = chunk < kMinChunk ? kMinChunk : (chunk > kMaxChunk ? kMaxChunk : chunk);
+  }
   auto up8 = [](int64_t x) { return static_cast<int32_t>((x + 7) / 8 * 8); };
   const int32_t a = up8((max_blocks + kMaxPrefixChunks - 1) / kMaxPrefixChunks);
-  const int32_t b = up8((4096 + block_size - 1) / block_size);
+  const int32_t b = up8((chunk + block_size - 1) / block_size);
   return a > b ? a : b;
 }
 
@@ -570,7 +591,8 @@ pkv_status pkv_paged_decode_attention_shared(
   c.num_groups = num_groups;
   c.bs = block_size;
   c.prefix_rows = sp.rows;
-  const int32_t chunk_blocks = prefix_chunk_blocks(max_blocks_per_seq, block_size);
+  const int32_t chunk_blocks = prefix_chunk_blocks(max_blocks_per_seq, block_size, num_groups,
+                                                   heads.num_kv_heads, sms);
   c.prefix_chunks = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
   c.prefix_chunk_keys = chunk_blocks * block_size;
   if (static_cast<int64_t>(num_groups) * c.prefix_chunks > 65535)
