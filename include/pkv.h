@@ -322,14 +322,18 @@ PKV_API pkv_status pkv_block_swap(const int64_t *pairs, int64_t n,
  * Same arguments and result as pkv_paged_decode_attention, minus the
  * workspace.  The split partials go to a fixed device array of
  * PKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
- * the process exits; nothing is allocated per call.  A batch whose partials
- * need more (pkv_decode_workspace_size above the maximum) is rejected with
- * PKV_ERR_WORKSPACE and a message in pkv_last_error.  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress) and
- * caches it; make that first call before any stream capture.  All calls on a
- * device share the one array: calls whose kernels overlap on the GPU (on
- * different streams, unordered) race and give wrong results.  The array
- * keeps the last call's contents; nothing in it needs to start at zero.
+ * the process exits; nothing is allocated per call.  The call picks its
+ * kernel as the regular call does; if that kernel needs more scratch than
+ * the maximum (the CUDA-core split kernel on a large batch of long contexts
+ * can), the call is rejected before anything is launched, with
+ * PKV_ERR_WORKSPACE and a message in pkv_last_error.  The first call in a
+ * device's context looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it, keyed by the context, under a lock
+ * (first calls from several host threads are safe); make that first call
+ * before any stream capture.  All calls on a device share the one array:
+ * calls whose kernels overlap on the GPU (on different streams, unordered)
+ * race and give wrong results.  The array keeps the last call's contents;
+ * nothing in it needs to start at zero.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 PKV_API pkv_status pkv_paged_decode_attention_noalloc(

@@ -76,3 +76,43 @@ class DeviceLayer:
     def assert_caches_equal(self):
         assert np.array_equal(W.to_u16(self.k_cache), self.h_k), "K cache differs"
         assert np.array_equal(W.to_u16(self.v_cache), self.h_v), "V cache differs"
+
+
+def shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed):
+    """Groups of consecutive sequences (sizes[g] members each) whose block
+    tables begin with the same whole prompt blocks, then each member's own
+    blocks; some members stop exactly at the shared blocks, singletons share
+    nothing.  Block size 16, physical blocks from a seeded permutation.
+    Returns (batch, group starts)."""
+    rng = np.random.default_rng(seed)
+    bs = 16
+    shape = W.ModelShape("s%d_%d" % (hq, hkv), 1, hq, hkv)
+    starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    B = int(starts[-1])
+    prompt = rng.integers(1, max_prompt_blocks, size=len(sizes)) * bs   # whole shared blocks
+    # a singleton shares nothing: all its positions are its own (keep them
+    # within the in-merge bound)
+    prompt[np.asarray(sizes) == 1] = np.minimum(prompt[np.asarray(sizes) == 1], 10 * bs)
+    own_pos = [rng.integers(0, 70, size=s) for s in sizes]
+    own_pos[int(np.argmax(np.asarray(sizes) > 1))][0] = 0  # a member with no own positions
+    ctx = np.concatenate([p + o for p, o in zip(prompt, own_pos)]).astype(np.int32)
+    ctx = np.maximum(ctx, 1)
+    max_blocks = int((ctx.max() + bs - 1) // bs)
+    nb = int(sum((c + bs - 1) // bs for c in ctx)) + 8
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.zeros((B, max_blocks), np.int32)
+    used = 0
+    for g, s in enumerate(sizes):
+        pb = int(prompt[g] // bs)
+        pblocks = perm[used:used + pb]
+        used += pb
+        for k in range(s):
+            i = int(starts[g]) + k
+            tables[i, :pb] = pblocks
+            rest = int((ctx[i] + bs - 1) // bs) - pb
+            tables[i, pb:pb + rest] = perm[used:used + rest]
+            used += rest
+    b = W.PagedBatch(shape=shape, seed=1, block_size=bs, num_blocks=nb, ctx_pre=ctx - 1, ctx=ctx,
+                     block_tables=tables, slot_mapping=np.full(B, -1, np.int64),
+                     req_ids=np.arange(B, dtype=np.int32), max_reqs=B)
+    return b, starts

@@ -179,7 +179,7 @@ def test_contiguous_layout_against_oracle(hq, hkv):
 
 def test_contiguous_prefill_on_memory_mapped_on_demand():
     # only the rows each request needs are backed; the output is the same
-    # bytes as on regular memory
+    # bytes as on regular memory and matches the oracle
     S = 16384
     kb, vb, req, ctx, cu, q = _contig_case(32, 8, S, 3, [0, 1, 2], [8000, 0, 12000],
                                            [192, 70, 300], seed=102)
@@ -197,6 +197,11 @@ def test_contiguous_prefill_on_memory_mapped_on_demand():
         out = pkv.contig_prefill_attention(qd, cud, vm.k, vm.v, *args)
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+        # and against the oracle, from the host inputs alone (request rows at
+        # reqId x S read as one-entry tables over blocks of S rows)
+        want = oracle.paged_prefill(W.to_u16(q), W.to_u16(kb), W.to_u16(vb), req[:, None], ctx,
+                                    cu, 128 ** -0.5)
+        assert_attention_close(out, want, "contiguous prefill on mapped memory")
     finally:
         torch.cuda.synchronize()
         vm.close()

@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_cache_245_gb300 as pkv
 import workloads as W
-from parity import DeviceLayer, assert_attention_close
+from parity import DeviceLayer, assert_attention_close, shared_groups_batch
 
 pytestmark = pytest.mark.gpu
 
@@ -67,39 +67,9 @@ def test_yi34b_sharing_scenario(step, own):
 
 
 def _synthetic(hq, hkv, own, sizes, max_prompt_blocks, seed):
-    rng = np.random.default_rng(seed)
-    bs = 16
-    shape = W.ModelShape("s%d_%d" % (hq, hkv), 1, hq, hkv)
-    starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
-    B = int(starts[-1])
-    prompt = rng.integers(1, max_prompt_blocks, size=len(sizes)) * bs   # whole shared blocks
-    # a singleton shares nothing: all its positions are its own (keep them
-    # within the in-merge bound)
-    prompt[np.asarray(sizes) == 1] = np.minimum(prompt[np.asarray(sizes) == 1], 10 * bs)
-    own_pos = [rng.integers(0, 70, size=s) for s in sizes]
-    own_pos[int(np.argmax(np.asarray(sizes) > 1))][0] = 0  # a member with no own positions
-    ctx = np.concatenate([p + o for p, o in zip(prompt, own_pos)]).astype(np.int32)
-    ctx = np.maximum(ctx, 1)
-    max_blocks = int((ctx.max() + bs - 1) // bs)
-    nb = int(sum((c + bs - 1) // bs for c in ctx)) + 8
-    perm = rng.permutation(nb).astype(np.int32)
-    tables = np.zeros((B, max_blocks), np.int32)
-    used = 0
-    for g, s in enumerate(sizes):
-        pb = int(prompt[g] // bs)
-        pblocks = perm[used:used + pb]
-        used += pb
-        for k in range(s):
-            i = int(starts[g]) + k
-            tables[i, :pb] = pblocks
-            rest = int((ctx[i] + bs - 1) // bs) - pb
-            tables[i, pb:pb + rest] = perm[used:used + rest]
-            used += rest
-    b = W.PagedBatch(shape=shape, seed=1, block_size=bs, num_blocks=nb, ctx_pre=ctx - 1, ctx=ctx,
-                     block_tables=tables, slot_mapping=np.full(B, -1, np.int64),
-                     req_ids=np.arange(B, dtype=np.int32), max_reqs=B)
+    b, starts = shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed)
     L = DeviceLayer(b, 0, DEV)
-    shared = shared_prefix_blocks(tables, ctx, bs, starts)
+    shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
     bound = own_bound(b, starts, shared)
     assert bound <= 256   # singletons keep whole contexts: within the in-merge bound
     out = _run(b, starts, shared, L, -1 if own == OWN[0] else bound)

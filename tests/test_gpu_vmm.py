@@ -1,6 +1,9 @@
 """Contiguous (reqId x S) K/V buffers whose physical memory is mapped on
-demand: decode attention and the decode step read and write them exactly
-as they do regular device memory (the same bytes out), pages are mapped as a
+demand ("Leveraging Low-Level CUDA APIs for vAttention's Dynamic Memory",
+5.2: reserve, create, map, set access; 5.2.3: a request's sub-tensor at
+reqId x S): decode attention and the decode step on them match the CPU
+oracle, and give the same bytes as on regular device memory; the append
+writes the same rows the oracle's append writes; pages are mapped as a
 request grows and unmapped when it ends, and released pages are reused.
 Every kernel call is preceded by a host check that the rows it can touch
 are backed."""
@@ -8,8 +11,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_245_gb300 as pkv
 import workloads as W
+from parity import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +37,7 @@ def _assert_backed(vm, ctx):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_attention_and_step_on_mapped_memory_match_regular_memory(variant):
+def test_attention_and_step_on_mapped_memory_match_oracle_and_regular_memory(variant):
     pkv.set_decode_variant(variant)
     shape = W.ModelShape("v32_8", 1, 32, 8)
     ctx = np.array([1, 17, 300, 1024, 2047, 2048, 5000, 9000], np.int32)
@@ -57,6 +62,12 @@ def test_attention_and_step_on_mapped_memory_match_regular_memory(variant):
         out = pkv.contig_decode_attention(li.q, vm.k, vm.v, req, ctx_d, int(ctx.max()), scale)
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+        # the oracle, from host copies of the inputs (nothing from the GPU path)
+        h_q = W.to_u16(li.q)
+        h_kb, h_vb = W.to_u16(kb).copy(), W.to_u16(vb).copy()
+        h_req = np.arange(b.B, dtype=np.int32)
+        assert_attention_close(out, oracle.contig_decode(h_q, h_kb, h_vb, h_req, ctx, scale),
+                               "attention on mapped memory")
         # one more token per request: back it, then append + attend in one call
         ctx2 = ctx + 1
         for r, c in enumerate(ctx2):
@@ -74,6 +85,13 @@ def test_attention_and_step_on_mapped_memory_match_regular_memory(variant):
         for r, c in enumerate(ctx2):
             assert torch.equal(vm.k[r, :, :c], kr[r, :, :c])
             assert torch.equal(vm.v[r, :, :c], vr[r, :, :c])
+        # the oracle's append into its host copies, then its attention
+        oracle.kv_append(slots.cpu().numpy(), W.to_u16(li.k_new), W.to_u16(li.v_new), h_kb, h_vb)
+        for r, c in enumerate(ctx2):
+            assert np.array_equal(W.to_u16(vm.k[r, :, :c]), h_kb[r, :, :c]), "K rows of %d" % r
+            assert np.array_equal(W.to_u16(vm.v[r, :, :c]), h_vb[r, :, :c]), "V rows of %d" % r
+        assert_attention_close(out2, oracle.contig_decode(h_q, h_kb, h_vb, h_req, ctx2, scale),
+                               "decode step on mapped memory")
     finally:
         vm.close()
 

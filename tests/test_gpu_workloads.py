@@ -42,12 +42,12 @@ def test_yi6b_batch64(layer):
     assert_attention_close(out, L.oracle_attend(), "Yi-6B layer %d" % layer)
 
 
+@pytest.mark.parametrize("layer", [0, 31])
 @pytest.mark.parametrize("B", W.LLAMA_SWEEP_BATCHES)
-def test_llama_sweep(B):
-    layer = 0 if B % 2 else 31
+def test_llama_sweep(B, layer):
     b = W.uniform_batch(W.LLAMA3_8B, B, 1024, 16, seed=W.SEED_LLAMA)
     L, out = _append_and_attend(b, layer)
-    assert_attention_close(out, L.oracle_attend(), "Llama b%d" % B)
+    assert_attention_close(out, L.oracle_attend(), "Llama b%d layer %d" % (B, layer))
 
 
 def test_llama_b64_bench_configuration():
@@ -65,15 +65,16 @@ def test_llama_b64_bench_configuration():
         assert_attention_close(out, L.oracle_attend(), "bench config layer %d" % layer)
 
 
+@pytest.mark.parametrize("layer", [0, 31])
 @pytest.mark.parametrize("bs", W.RAGGED_BLOCK_SIZES)
-def test_ragged_paged_and_contiguous(bs):
+def test_ragged_paged_and_contiguous(bs, layer):
     """Ragged serving batch (prompt ~ Exp(1024), output ~ Exp(256), max 8192)
     in the paged layout, and the same logical K/V in the contiguous layout at
     S = 8192 (reqId x S): paged matches the oracle, contiguous matches paged
-    bit for bit."""
+    bit for bit.  Layers 0 and 31 (first and last of the Llama-3-8B shape)."""
     b = W.ragged_batch(bs)
-    L, out = _append_and_attend(b, 0)
-    assert_attention_close(out, L.oracle_attend(), "ragged bs=%d" % bs)
+    L, out = _append_and_attend(b, layer)
+    assert_attention_close(out, L.oracle_attend(), "ragged bs=%d layer %d" % (bs, layer))
     if bs == 16:
         S = 8192
         kb = W.paged_to_contig(L.k_cache, b, S)
