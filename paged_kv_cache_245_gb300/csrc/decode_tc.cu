@@ -2,8 +2,11 @@
 // tensor-map encoding, batch chunking, kernel instantiations.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstdlib>
 #include <mutex>
+#include <random>
 
 #include "decode_tc.cuh"
 #include "decode_tc_launch.h"
@@ -46,6 +49,23 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
 
 namespace {
 
+// Record tags of the launches: a counter from a per-process random start, so
+// that consecutive launches differ and words left in reused memory (by
+// another process or any other data) rarely carry a launch's tag.  Never 0
+// (the value of a consumed record).
+uint32_t next_launch_tag() {
+  static std::atomic<uint32_t> counter{[] {
+    std::random_device rd;
+    uint64_t x = (static_cast<uint64_t>(rd()) << 32) ^ rd();
+    x ^= static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) *
+         0x9E3779B97F4A7C15ull;
+    return static_cast<uint32_t>(x ^ (x >> 32));
+  }()};
+  uint32_t t;
+  do t = counter.fetch_add(1, std::memory_order_relaxed); while (t == 0);
+  return t;
+}
+
 template <bool kContig, int W, int S, int NT = 1>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,
                        int num_ctas, cudaStream_t stream) {
@@ -79,20 +99,9 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
     // the first chunk of a decode step starts while the append runs
     p.early_inputs = s0 == 0 ? p0.early_inputs : 0;
+    p.tag = next_launch_tag();  // every launch writes its piece records under a fresh tag
     e = launch_pdl_if(p.early_inputs != 0 || pdl_enabled(), kernel, dim3(num_ctas), dim3(W * 32),
                       L::kTotal, stream, tk, tv, p);
-    if (e != cudaSuccess) return e;
-    if (num_ctas < 2) continue;  // one CTA: every pair was written whole
-    // The combine may be scheduled while the main kernel drains (it waits
-    // for it before reading the records); PKV_COMBINE_PDL=0 turns that off.
-    static const bool combine_pdl = [] {
-      const char* v = getenv("PKV_COMBINE_PDL");
-      return !(v != nullptr && v[0] == '0');
-    }();
-    const int64_t warps = static_cast<int64_t>(num_ctas - 1) * p.G;
-    e = launch_pdl_if(combine_pdl || pdl_enabled(), decode_tc_combine_kernel<kContig>,
-                      dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0, stream, p,
-                      num_ctas);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -100,8 +109,11 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
 
 }  // namespace
 
+// Per CTA: one piece record (its first segment, when that is part of a pair
+// that an earlier CTA's range began) of kTcRecHeads heads, kRecStride tagged
+// 64-bit words each.
 size_t tc_workspace_bytes(int num_ctas) {
-  return static_cast<size_t>(num_ctas) * 2 * kTcRecHeads * kRecStride * sizeof(float);
+  return static_cast<size_t>(num_ctas) * kTcRecHeads * kRecStride * sizeof(uint64_t);
 }
 
 TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, const void* v,
@@ -123,7 +135,7 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
     return x < 0 ? 0 : (x > 4096 ? 4096 : x);
   }();
   p.seg_cost = seg_cost;
-  p.rec = static_cast<float*>(workspace);
+  p.rec = static_cast<uint64_t*>(workspace);
   cudaError_t e;
   if (p.G > kTcHeads) {  // one n-tile of 8 query heads per KV head (the API allows G <= 8)
     e = cudaErrorInvalidValue;

@@ -15,9 +15,11 @@
 // pair it touches as seg_cost more (tc_unit_to_tile), whatever the context
 // lengths.  A CTA walks its run pair by pair ("segments"); its warps take
 // the segment's tiles round-robin.  A segment that covers a whole pair writes
-// the bf16 output directly; the at most two partial segments of a CTA (its
-// first and its last) write an fp32 record (o, m, l) that the combine kernel
-// merges.
+// the bf16 output directly.  The at most two partial segments of a CTA (its
+// first and its last: "pieces" of a pair cut by the ranges) are merged inside
+// the kernel: the CTA holding a pair's first tiles usually finishes its piece
+// last and merges the others' records, which were published with a flag long
+// before; a flag protocol without waiting covers every other order.
 //
 // Data movement.  K and V tiles (16 rows x 256 B) come in through the TMA
 // engine from a 2-D tensor map over the cache's rows, as two 64-column boxes
@@ -83,6 +85,166 @@ __device__ __forceinline__ int tc_context(const TcParams& p, int i, bool contig,
   return ctx;
 }
 
+__device__ __forceinline__ bool tc_range_nonempty(int cc, int64_t V, int64_t P) {
+  return tc_range_lo(cc, V, P) < tc_range_lo(cc + 1, V, P);
+}
+
+// One query head's result, from lane's four output elements: bf16 output,
+// or an (o, m, l) record in record mode.
+__device__ __forceinline__ void tc_write_out(const TcParams& p, int seq, int qh, int lane,
+                                             float4 o4, float M, float L) {
+  if (p.rec_out != nullptr) {
+    float* r = p.rec_out + (static_cast<int64_t>(seq) * p.Hq + qh) * kRecStride;
+    *reinterpret_cast<float4*>(r + lane * 4) = o4;
+    if (lane == 0) {
+      r[128] = M;
+      r[129] = L;
+    }
+    return;
+  }
+  const uint32_t lo16 = f32_to_bf16_bits(o4.x) | (uint32_t(f32_to_bf16_bits(o4.y)) << 16);
+  const uint32_t hi16 = f32_to_bf16_bits(o4.z) | (uint32_t(f32_to_bf16_bits(o4.w)) << 16);
+  *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(seq) * p.Hq + qh) * kHeadDim + lane * 4) =
+      make_uint2(lo16, hi16);
+}
+
+// Piece records.  Every 64-bit word of a record holds one fp32 value in its
+// low half and the launch's tag in its high half; naturally aligned 64-bit
+// stores and loads are single-copy atomic, so a reader that finds the tag in
+// every word of a record has read the whole record of this launch, with no
+// fence on either side.  The reader zeroes the tags once it has merged, so
+// every record is stale again when the launch ends: a launch replayed with
+// the same tag (a CUDA graph) never meets a word of an earlier replay, and a
+// word of any other origin matches a tag only by a 2^-32 accident per word.
+// Words 0..127: o (lane l owns 4l .. 4l + 3); 128: m; 129: l.
+__device__ __forceinline__ uint64_t tc_tagged(float x, uint32_t tag) {
+  return (static_cast<uint64_t>(tag) << 32) | __float_as_uint(x);
+}
+
+__device__ __forceinline__ void tc_store_piece(uint64_t* w, uint32_t tag, int lane, float4 o4, float M,
+                                               float L) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(w + lane * 4),
+               "l"(tc_tagged(o4.x, tag)), "l"(tc_tagged(o4.y, tag))
+               : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(w + lane * 4 + 2),
+               "l"(tc_tagged(o4.z, tag)), "l"(tc_tagged(o4.w, tag))
+               : "memory");
+  if (lane == 0)
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(w + 128),
+                 "l"(tc_tagged(M, tag)), "l"(tc_tagged(L, tag))
+                 : "memory");
+}
+
+// Lane's part of a piece record as read (o words, then m and l; the (m, l)
+// words are read by every lane).
+struct TcPieceWords {
+  uint64_t w[6];
+};
+
+__device__ __forceinline__ void tc_issue_piece(const uint64_t* w, int lane, TcPieceWords& pw) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+               : "=l"(pw.w[0]), "=l"(pw.w[1])
+               : "l"(w + lane * 4)
+               : "memory");
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+               : "=l"(pw.w[2]), "=l"(pw.w[3])
+               : "l"(w + lane * 4 + 2)
+               : "memory");
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+               : "=l"(pw.w[4]), "=l"(pw.w[5])
+               : "l"(w + 128)
+               : "memory");
+}
+
+// True if every word read carries `tag`; the values in o, m, l.
+__device__ __forceinline__ bool tc_parse_piece(const TcPieceWords& pw, uint32_t tag, float4* o4,
+                                               float* M, float* L) {
+  *o4 = make_float4(__uint_as_float(static_cast<uint32_t>(pw.w[0])),
+                    __uint_as_float(static_cast<uint32_t>(pw.w[1])),
+                    __uint_as_float(static_cast<uint32_t>(pw.w[2])),
+                    __uint_as_float(static_cast<uint32_t>(pw.w[3])));
+  *M = __uint_as_float(static_cast<uint32_t>(pw.w[4]));
+  *L = __uint_as_float(static_cast<uint32_t>(pw.w[5]));
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 6; ++k) ok = ok && static_cast<uint32_t>(pw.w[k] >> 32) == tag;
+  return ok;
+}
+
+__device__ __forceinline__ void tc_clear_piece(uint64_t* w, int lane) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %1};" ::"l"(w + lane * 4), "l"(0ull)
+               : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %1};" ::"l"(w + lane * 4 + 2), "l"(0ull)
+               : "memory");
+  if (lane == 0)
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %1};" ::"l"(w + 128), "l"(0ull) : "memory");
+}
+
+// Merge the pieces of a pair cut by the CTA ranges (CTAs cf .. cl) for query
+// head hh of the group and write the result; called by the CTA of the head
+// piece (cf), whose own piece comes from the caller's registers.  Every piece
+// is a normalised partial result (o, m, l) over its positions; softmax over
+// their union is
+//   M = max m_k,  w_k = l_k 2^(m_k - M),  o = sum w_k o_k / sum w_k,
+// folded here in CTA order with a running maximum.  A record not yet complete
+// (its CTA is still on that piece: rare, the head piece is the CTA's last
+// segment and the others are earlier segments of theirs) is read again until
+// it is, for at most kWaitLimitNs.  Every CTA of the grid is resident or
+// finishes without waiting (waits point only to higher CTAs, and the last
+// CTA's last segment is never a head piece), so the wait ends.  Returns
+// false if it gave up.
+__device__ __forceinline__ bool tc_merge_pieces(const TcParams& p, int seq, int qh, int hh, int cf,
+                                                int cl, int64_t V, int64_t P, int lane,
+                                                float4 o_own, float m_own, float l_own,
+                                                const TcPieceWords& next) {
+  constexpr unsigned kFull = 0xffffffffu;
+  const uint32_t tag = p.tag;
+  float Mr = -INFINITY, Wr = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fold = [&](float m, float l, float4 o) {
+    if (!(l > 0.f)) return;
+    if (m > Mr) {
+      const float s = fast_exp2(Mr - m);  // 0 while Mr is -inf
+      Wr *= s;
+      a.x *= s; a.y *= s; a.z *= s; a.w *= s;
+      Mr = m;
+    }
+    const float w = l * fast_exp2(m - Mr);
+    a.x = fmaf(w, o.x, a.x);
+    a.y = fmaf(w, o.y, a.y);
+    a.z = fmaf(w, o.z, a.z);
+    a.w = fmaf(w, o.w, a.w);
+    Wr += w;
+  };
+  fold(m_own, l_own, o_own);
+  bool ok = true;
+  for (int cc = cf + 1; cc <= cl; ++cc) {
+    if (!tc_range_nonempty(cc, V, P)) continue;
+    uint64_t* rec = p.rec + (static_cast<int64_t>(cc) * kTcRecHeads + hh) * kRecStride;
+    float m, l;
+    float4 o;
+    TcPieceWords pw;
+    if (cc == cf + 1) pw = next;  // read by the caller while the CTA merged its warps
+    else tc_issue_piece(rec, lane, pw);
+    if (!__all_sync(kFull, tc_parse_piece(pw, tag, &o, &m, &l))) {
+      const unsigned long long t0 = global_timer_ns();
+      bool have;
+      do {
+        __nanosleep(256);
+        tc_issue_piece(rec, lane, pw);
+        have = __all_sync(kFull, tc_parse_piece(pw, tag, &o, &m, &l));
+      } while (!have && global_timer_ns() - t0 < kWaitLimitNs);
+      if (!have) ok = false;
+    }
+    fold(m, l, o);
+    tc_clear_piece(rec, lane);
+  }
+  const float inv = Wr > 0.f ? 1.f / Wr : 0.f;
+  tc_write_out(p, seq, qh, lane, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv),
+               Wr > 0.f ? Mr : -INFINITY, Wr);
+  return ok;
+}
+
 // NT n-tiles of 8 query heads per KV head (instantiated with NT = 1: GQA
 // groups of up to 8 query heads).
 template <bool kContig, int W, int S, int NT>
@@ -119,9 +281,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   }
   // Programmatic dependent launch (no-ops without the launch attribute):
   // wait for the previous kernel in the stream to finish before reading any
-  // input, then let the combine kernel get scheduled.  In this order every
-  // input is complete by the time the combine starts, which lets it read
-  // context_lens before waiting for this kernel.  In a decode step whose
+  // input, then let the next kernel get scheduled.  In a decode step whose
   // previous kernel is the append (early_inputs), q, context_lens, req_ids
   // and the block tables were complete before it started and only the
   // caches are still being written: the prologue reads them at once and the
@@ -179,6 +339,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   }
   const int64_t lo = range[0];
   const int64_t hi = range[1];
+  const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);  // units of the whole partition
   if (lo >= hi) {  // uniform across the CTA
     if (p.early_inputs) grid_dependency_wait();  // never finish before the append
     return;
@@ -331,6 +492,14 @@ __global__ void __launch_bounds__(W * 32, 1)
       for (int i = 0; i < 8; ++i) acc[i][t][0] = acc[i][t][1] = acc[i][t][2] = acc[i][t][3] = 0.f;
     }
     const int ctx = ctx_s[seg.seq];
+    // A segment that is only part of its pair (the CTA ranges cut the pair)
+    // is a "piece"; the pair's CTAs are cf .. cl.  The piece of cf (the
+    // pair's first tiles, this CTA's last segment) usually finishes last:
+    // its CTA merges the pair (the head piece).
+    const bool whole = seg.x0 == seg.pstart && seg.x1 == seg.pend;
+    int cf = c, cl = c;
+    if (!whole) tc_pair_ctas(seg, prefix, p.Hkv, p.seg_cost, V, P, &cf, &cl);
+    const bool head_piece = !whole && cf == c;
 
     for (int64_t x = seg.x0 + warp; x < seg.x1 && !dead; x += W) {
       if (x == seg.x0 + warp) {  // this warp's first tile of the segment
@@ -446,6 +615,18 @@ __global__ void __launch_bounds__(W * 32, 1)
       }
     }
 
+    // ---- the head piece's merge warps request the next CTA's piece record
+    // of their heads now, so that it arrives while the warps are merged
+    TcPieceWords nxt[NT * 2];
+    if (head_piece && warp < kTcMergeHeads && cf + 1 <= cl && tc_range_nonempty(cf + 1, V, P)) {
+#pragma unroll
+      for (int k = 0; k < NT * 2; ++k)
+        if (warp + kTcMergeHeads * k < G)
+          tc_issue_piece(p.rec + (static_cast<int64_t>(cf + 1) * kTcRecHeads + warp + kTcMergeHeads * k) *
+                                     kRecStride,
+                         lane, nxt[k]);
+    }
+
     // ---- merge the warps' partial results for this segment (4 heads a pass)
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -462,11 +643,10 @@ __global__ void __launch_bounds__(W * 32, 1)
         ml[(warp * H + h + 1) * 2 + 1] = l1[t];
       }
     }
-    const bool whole = seg.x0 == seg.pstart && seg.x1 == seg.pend;
-    // record slot: 0 for a segment that began in an earlier CTA's range (it
-    // starts this range), 1 for one that starts the pair (and ends this range)
-    const int slot = seg.x0 > seg.pstart ? 0 : 1;
-    for (int h0 = 0; h0 < G; h0 += kTcMergeHeads) {
+#pragma unroll
+    for (int pass = 0; pass < NT * 2; ++pass) {
+      const int h0 = pass * kTcMergeHeads;
+      if (h0 >= G) break;
       // lanes whose head pair (8t + 2tq, + 1) falls in [h0, h0 + 4) write it
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
@@ -510,25 +690,18 @@ __global__ void __launch_bounds__(W * 32, 1)
           o4.z = fmaf(v.z, ww, o4.z);
           o4.w = fmaf(v.w, ww, o4.w);
         }
-        if (whole && p.rec_out != nullptr) {  // an (o, m, l) record per head
-          float* r = p.rec_out + (static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) * kRecStride;
-          *reinterpret_cast<float4*>(r + lane * 4) = o4;
-          if (lane == 0) {
-            r[128] = Ls > 0.f ? M : -INFINITY;
-            r[129] = Ls;
-          }
-        } else if (whole) {
-          const uint32_t lo16 = f32_to_bf16_bits(o4.x) | (uint32_t(f32_to_bf16_bits(o4.y)) << 16);
-          const uint32_t hi16 = f32_to_bf16_bits(o4.z) | (uint32_t(f32_to_bf16_bits(o4.w)) << 16);
-          *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(seg.seq) * p.Hq + seg.kvh * G + hh) *
-                                                kHeadDim + lane * 4) = make_uint2(lo16, hi16);
+        const float Mr = Ls > 0.f ? M : -INFINITY;
+        if (whole) {
+          tc_write_out(p, seg.seq, seg.kvh * G + hh, lane, o4, Mr, Ls);
+        } else if (head_piece) {
+          // this piece first, then the other pieces' records in CTA order
+          if (!tc_merge_pieces(p, seg.seq, seg.kvh * G + hh, hh, cf, cl, V, P, lane, o4, Mr, Ls,
+                               nxt[pass]) &&
+              lane == 0)
+            record_error(p.err, kErrTimeout);
         } else {
-          float* r = p.rec + ((static_cast<int64_t>(c) * 2 + slot) * kTcRecHeads + hh) * kRecStride;
-          *reinterpret_cast<float4*>(r + lane * 4) = o4;
-          if (lane == 0) {
-            r[128] = Ls > 0.f ? M : -INFINITY;
-            r[129] = Ls;
-          }
+          tc_store_piece(p.rec + (static_cast<int64_t>(c) * kTcRecHeads + hh) * kRecStride,
+                         p.tag, lane, o4, Mr, Ls);
         }
       }
       __syncthreads();
@@ -542,150 +715,6 @@ __global__ void __launch_bounds__(W * 32, 1)
     for (int k = consumed; k < issued; ++k)
       mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>(k / S) & 1u);
   }
-}
-
-// Split-pair combine.  One warp per (CTA boundary b = 1 .. P-1, query head
-// gi < G).  The warp finds the pair that holds the first tile of CTA b's
-// range; if b is the first boundary inside that pair (CTA b - 1 holds its
-// first tile), the warp merges the records of the CTAs cf .. cl that share
-// the pair:  M = max m_c,  w_c = l_c 2^(m_c - M),  out = sum w_c o_c / sum w_c.
-// Every other pair was written whole by the main kernel.  The classification
-// reads only context_lens (and req_ids), which were complete before this
-// kernel was launched (the main kernel lets it launch only after its own
-// dependency wait), so the warp classifies before waiting for the main
-// kernel; only the record loads and the merge follow the wait.
-template <bool kContig>
-__global__ void __launch_bounds__(128) decode_tc_combine_kernel(const TcParams p, int P) {
-  __shared__ int32_t prefix[kTcMaxSeqs + 1];
-  __shared__ int32_t wsum[4];
-  grid_dependency_trigger();
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int B = p.num_seqs;
-  // tile prefix over sequences, as the main kernel computes it (4 per thread)
-  int n4[4];
-  int tsum = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid * 4 + k;
-    n4[k] = i < B ? (tc_context(p, i, kContig, false) + 15) >> 4 : 0;
-    tsum += n4[k];
-  }
-  int incl = tsum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  int run = incl - tsum;
-  for (int w = 0; w < warp; ++w) run += wsum[w];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid * 4 + k;
-    if (i < B) prefix[i] = run;
-    run += n4[k];
-  }
-  if (tid == 127) prefix[B] = run;
-  __syncthreads();
-
-  // classify: does this warp merge a pair, and which
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  const int bnd = 1 + static_cast<int>(idx / p.G);
-  const int gi = static_cast<int>(idx % p.G);
-  const int alpha = p.seg_cost;
-  const int64_t V = tc_vseq(prefix, B, p.Hkv, alpha);
-  int seq = 0, kvh = 0, cf = 0, cl = 0;
-  const bool merge_it = tc_boundary_pair(bnd, prefix, B, p.Hkv, alpha, P, &seq, &kvh, &cf, &cl);
-  // Every thread waits here, so that the combine never completes before the
-  // main kernel (whose outputs later work in the stream may read).
-  grid_dependency_wait();
-  if (!merge_it) return;
-  uint2* dst = reinterpret_cast<uint2*>(
-      p.out + ((static_cast<int64_t>(seq) * p.Hq + kvh * p.G + gi) * kHeadDim) + lane * 4);
-  // CTA cc's record for this pair: slot 1 in cf (where the pair begins), slot
-  // 0 in the later CTAs (the pair began before their range); CTAs whose range
-  // is empty wrote nothing and are skipped.  Lane j loads record cf + j's
-  // (m, l) so that all records cost one round trip, then every lane loads its
-  // four output elements of the records four at a time.
-  constexpr unsigned kFull = 0xffffffffu;
-  auto record = [&](int cc) -> const float* {
-    // a CTA strictly between cf and cl with a non-empty range holds tiles of
-    // the pair (its units lie inside the pair's run of tiles)
-    if (tc_range_lo(cc, V, P) >= tc_range_lo(cc + 1, V, P)) return nullptr;
-    const int slot = cc == cf ? 1 : 0;
-    return p.rec + ((static_cast<int64_t>(cc) * 2 + slot) * kTcRecHeads + gi) * kRecStride;
-  };
-  const int K = cl - cf + 1;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float Wsum = 0.f;
-  float M = -INFINITY;
-  if (K <= 32) {
-    const float* rj = lane < K ? record(cf + lane) : nullptr;
-    const float mj = rj != nullptr ? __ldcg(rj + 128) : -INFINITY;
-    const float lj = rj != nullptr ? __ldcg(rj + 129) : 0.f;
-    M = lj > 0.f ? mj : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    const float wj = (lj > 0.f && M != -INFINITY) ? lj * fast_exp2(mj - M) : 0.f;
-    const unsigned long long rbits = reinterpret_cast<unsigned long long>(rj);
-    for (int j = 0; j < K; j += 4) {
-      float4 o[4];
-      float w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int jj = min(j + u, K - 1);
-        const float wu = __shfl_sync(kFull, wj, jj);
-        const float* r = reinterpret_cast<const float*>(__shfl_sync(kFull, rbits, jj));
-        w[u] = (j + u < K) ? wu : 0.f;
-        o[u] = w[u] > 0.f ? __ldcg(reinterpret_cast<const float4*>(r) + lane)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc.x = fmaf(w[u], o[u].x, acc.x);
-        acc.y = fmaf(w[u], o[u].y, acc.y);
-        acc.z = fmaf(w[u], o[u].z, acc.z);
-        acc.w = fmaf(w[u], o[u].w, acc.w);
-        Wsum += w[u];
-      }
-    }
-  } else {
-    // more than 32 CTAs share the pair (tiny batches): two passes
-    for (int cc = cf; cc <= cl; ++cc) {
-      const float* r = record(cc);
-      if (r != nullptr && r[129] > 0.f) M = fmaxf(M, r[128]);
-    }
-    if (M != -INFINITY) {
-      for (int cc = cf; cc <= cl; ++cc) {
-        const float* r = record(cc);
-        if (r == nullptr || !(r[129] > 0.f)) continue;
-        const float w = r[129] * fast_exp2(r[128] - M);
-        const float4 o = *reinterpret_cast<const float4*>(r + lane * 4);
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
-        Wsum += w;
-      }
-    }
-  }
-  const float inv = Wsum > 0.f ? 1.f / Wsum : 0.f;
-  if (p.rec_out != nullptr) {  // the pair's (o, m, l) record
-    float* r = p.rec_out + (static_cast<int64_t>(seq) * p.Hq + kvh * p.G + gi) * kRecStride;
-    *reinterpret_cast<float4*>(r + lane * 4) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (lane == 0) {
-      r[128] = Wsum > 0.f ? M : -INFINITY;
-      r[129] = Wsum;
-    }
-    return;
-  }
-  const uint32_t lo16 = f32_to_bf16_bits(acc.x * inv) | (uint32_t(f32_to_bf16_bits(acc.y * inv)) << 16);
-  const uint32_t hi16 = f32_to_bf16_bits(acc.z * inv) | (uint32_t(f32_to_bf16_bits(acc.w * inv)) << 16);
-  *dst = make_uint2(lo16, hi16);
 }
 
 }  // namespace pkv

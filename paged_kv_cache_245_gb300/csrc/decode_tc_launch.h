@@ -11,7 +11,7 @@ namespace pkv {
 
 constexpr int kTcMaxSeqs = 512;  // sequences per launch (larger batches run in chunks)
 constexpr int kRecStride = 132;  // floats per head record: o[128], m, l, pad
-constexpr int kTcRecHeads = 16;  // head slots per split record (up to two n-tiles)
+constexpr int kTcRecHeads = 16;  // head slots per piece record (up to two n-tiles)
 
 struct TcParams {
   const uint16_t* q;        // [B][Hq][128]
@@ -19,7 +19,8 @@ struct TcParams {
   const int32_t* ctx_lens;  // [B]
   const int32_t* block_tables;  // paged [B][max_blocks]
   const int32_t* req_ids;       // contig [B]
-  float* rec;               // [gridDim.x][2][kTcRecHeads][kRecStride]
+  uint64_t* rec;            // piece records [gridDim.x][kTcRecHeads][kRecStride] tagged words
+  uint32_t tag;             // this launch's record tag (never 0)
   float* rec_out;           // null: bf16 out; else [B][Hq][kRecStride] (o, m, l) records
   int32_t seg_cost;         // schedule weight of one segment, in tiles (alpha below)
   int64_t bs;               // paged block size (multiple of 16); contig S
@@ -125,29 +126,15 @@ __host__ __device__ inline TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_
   return s;
 }
 
-// The pair that the combine warp of CTA boundary bnd (1 <= bnd < P) merges:
-// the pair holding the first tile of CTA bnd's range, if bnd is the first
-// boundary inside it (CTA bnd - 1 holds its first tile).  Returns false if
-// that boundary merges nothing; else its sequence, KV head and the CTAs
-// cf .. cl whose ranges share the pair.
-__host__ __device__ inline bool tc_boundary_pair(int bnd, const int32_t* prefix, int B, int Hkv,
-                                                 int alpha, int64_t P, int* seq, int* kvh, int* cf,
-                                                 int* cl) {
-  if (bnd < 1 || bnd >= P) return false;
-  const int64_t V = tc_vseq(prefix, B, Hkv, alpha);
-  const int64_t T = static_cast<int64_t>(Hkv) * prefix[B];
-  const int64_t x = tc_unit_to_tile(tc_range_lo(bnd, V, P), prefix, B, Hkv, alpha);
-  if (x >= T) return false;
-  const TcSeg seg = tc_find_seg(x, T, prefix, B, Hkv);
-  if (seg.pstart == x) return false;  // a boundary between pairs cuts nothing
+// The CTAs cf .. cl whose ranges hold tiles of the pair that segment `seg`
+// belongs to (cf holds the pair's first tile, cl its last).  A CTA strictly
+// between them with a non-empty range holds tiles of the pair only.
+__host__ __device__ inline void tc_pair_ctas(const TcSeg& seg, const int32_t* prefix, int Hkv,
+                                             int alpha, int64_t V, int64_t P, int* cf, int* cl) {
   const int64_t n = seg.pend - seg.pstart;
-  // units of the pair's first and last tiles
   const int64_t u0 = tc_vseq(prefix, seg.seq, Hkv, alpha) + seg.kvh * (n + alpha) + alpha;
-  *seq = seg.seq;
-  *kvh = seg.kvh;
   *cf = static_cast<int>(tc_owner(u0, V, P));
   *cl = static_cast<int>(tc_owner(u0 + n - 1, V, P));
-  return *cf + 1 == bnd;
 }
 
 // A TMA tensor map over a K or V cache viewed as [rows][128] bf16: boxes of

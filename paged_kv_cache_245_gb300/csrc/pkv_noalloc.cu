@@ -129,8 +129,9 @@ extern "C" PKV_API pkv_status pkv_paged_decode_attention_noalloc(
   // The whole array is offered as the workspace.  The regular call picks its
   // kernel and checks that kernel's need against the size before anything
   // is launched, so a batch is turned away only when the kernel that would
-  // run needs more.  Every partial that kernel's combine reads is written by
-  // the same call first, so the scratch needs no clearing between calls.
+  // run needs more.  Every partial a kernel reads back is written by the same
+  // call first, and the tensor-core kernel leaves each of its flags at 0 (the
+  // array starts zeroed), so the scratch needs no clearing between calls.
   const pkv_status st = pkv_paged_decode_attention(
       q, k_cache, v_cache, block_tables, max_blocks_per_seq, num_blocks, context_lens, num_seqs,
       max_context, block_size, scale, heads, out, scratch,

@@ -5,12 +5,15 @@
 //    contexts), the CTAs' tile runs tile [0, T) exactly and in order, the unit
 //    owner of every tile is the CTA whose run holds it, and each CTA's cost
 //    (tiles + seg_cost per segment) stays within one pair of the even share;
-//  * records: walking every CTA's segments the way the kernel does, each
-//    partial segment takes a slot no other segment of its CTA takes, and the
-//    combine's lookup (cf..cl with its slot rule) names exactly the records
-//    written for every split pair, and no pair it treats as whole was split;
-//  * the combine's boundary warps: every split pair is merged exactly once,
-//    by the boundary just after the CTA holding its first tile.
+//  * pieces: walking every CTA's segments the way the kernel does, each
+//    partial segment (piece) takes a slot no other segment of its CTA takes;
+//    for every piece, tc_pair_ctas names the CTAs cf .. cl of its pair, and
+//    the merge's lookup (the non-empty CTAs of cf .. cl, slot 1 for cf and 0
+//    for the others) names exactly the records written for every split
+//    pair; no pair is both whole and split;
+//  * the head piece: a piece is the one the CTA merges without publishing
+//    (its pair's first tiles, slot 1) exactly when its CTA is cf, and it is
+//    always that CTA's last segment.
 #include <cstdio>
 #include <algorithm>
 #include <cstdlib>
@@ -117,6 +120,19 @@ static int check_weighted(const std::vector<int32_t>& n, int Hkv, int P, int alp
         if (used[slot]) return fail("slot reused", c, slot);
         used[slot] = true;
         written[q].insert({c, slot});
+        // the kernel's view of the piece: its pair's CTAs, and whether it is
+        // the head piece (merged by its own CTA)
+        const TcSeg seg = tc_find_seg(x, lo[c + 1], prefix.data(), B, Hkv);
+        if (seg.x0 != x || seg.x1 != x1 || seg.pstart != ps || seg.pend != pe)
+          return fail("segment", c, x);
+        int cf = -1, cl = -1;
+        tc_pair_ctas(seg, prefix.data(), Hkv, alpha, V, P, &cf, &cl);
+        const int ocf = static_cast<int>(tc_owner(pair_u0[q], V, P));
+        const int ocl = static_cast<int>(tc_owner(pair_u0[q] + pair_n[q] - 1, V, P));
+        if (cf != ocf || cl != ocl || c < cf || c > cl) return fail("pair ctas", c, cf);
+        const bool head = cf == c;
+        if (head != (slot == 1)) return fail("head piece slot", c, slot);
+        if (head && x1 != lo[c + 1]) return fail("head piece not last", c, x1);
       }
       x = x1;
     }
@@ -125,7 +141,7 @@ static int check_weighted(const std::vector<int32_t>& n, int Hkv, int P, int alp
     const int64_t longest = alpha + (B ? *std::max_element(n.begin(), n.end()) : 0);
     if (cost > share + 2 * longest + alpha) return fail("cost", c, cost);
   }
-  // the combine's lookup
+  // the merge's lookup of a split pair's records
   for (size_t r = 0; r < npairs; ++r) {
     if (pair_n[r] == 0) continue;
     const int cf = static_cast<int>(tc_owner(pair_u0[r], V, P));
@@ -141,22 +157,6 @@ static int check_weighted(const std::vector<int32_t>& n, int Hkv, int P, int alp
     }
     if (looked != written[r]) return fail("records", (long long)r, cf);
   }
-  // the combine's warps: each split pair is merged by exactly one CTA
-  // boundary (cf + 1), which names the pair and its CTAs; no other boundary
-  // merges anything
-  std::map<size_t, int> merged_by;
-  for (int bnd = 0; bnd <= P; ++bnd) {
-    int seq = -1, kvh = -1, bf = -1, bl = -1;
-    if (!tc_boundary_pair(bnd, prefix.data(), B, Hkv, alpha, P, &seq, &kvh, &bf, &bl)) continue;
-    const size_t r = static_cast<size_t>(seq) * Hkv + kvh;
-    const int cf = static_cast<int>(tc_owner(pair_u0[r], V, P));
-    const int cl = static_cast<int>(tc_owner(pair_u0[r] + pair_n[r] - 1, V, P));
-    if (cf == cl || bf != cf || bl != cl || bnd != cf + 1) return fail("boundary pair", bnd, cf);
-    if (merged_by.count(r)) return fail("pair merged twice", (long long)r, bnd);
-    merged_by[r] = bnd;
-  }
-  for (const auto& kv : written)
-    if (!merged_by.count(kv.first)) return fail("split pair not merged", (long long)kv.first, 0);
   return 0;
 }
 
