@@ -100,7 +100,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     // the first chunk of a decode step starts while the append runs
     p.early_inputs = s0 == 0 ? p0.early_inputs : 0;
     p.tag = next_launch_tag();  // every launch writes its piece records under a fresh tag
-    e = launch_pdl_if(p.early_inputs != 0 || pdl_enabled(), kernel, dim3(num_ctas), dim3(W * 32),
+    e = launch_pdl_if(p.early_inputs != 0 || pdl_decode_enabled(), kernel, dim3(num_ctas), dim3(W * 32),
                       L::kTotal, stream, tk, tv, p);
     if (e != cudaSuccess) return e;
   }
@@ -125,16 +125,19 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
   if (!encode_rows(&tk, k, rows_total) || !encode_rows(&tv, v, rows_total))
     return TcStatus::kEncodeFailed;
   TcParams p = p_in;
-  // The cost of a segment in tiles.  Measured per-CTA timelines grow by about
-  // 2-2.7 us per extra segment at 5.7-7 tiles/us per CTA (12-19 tiles); a
-  // sweep of 0..48 on GB300 was fastest at 24 (ragged batches gain most).
-  // PKV_TC_SEG_COST overrides it (0: an even split of the tiles alone).
+  // The cost of a segment in tiles, per pass of the segment merge (4 query
+  // heads a pass: one pass up to G = 4, two above).  Per-CTA timelines grow
+  // by about 2-3 us per extra segment; sweeps of 16..48 on GB300 were fastest
+  // at 24 for one pass (the ragged batch: 24 -> 16 or 32 costs 3-4 %, the
+  // Llama-3-8B shape moves by 0.6 %) and at 48 for two (the Yi-6B shape,
+  // G = 8: 31.7 -> 30.8 us).  PKV_TC_SEG_COST overrides the per-pass cost
+  // (0: an even split of the tiles alone).
   static const int seg_cost = [] {
     const char* v = getenv("PKV_TC_SEG_COST");
     const int x = v != nullptr ? atoi(v) : 24;
-    return x < 0 ? 0 : (x > 4096 ? 4096 : x);
+    return x < 0 ? 0 : (x > 2048 ? 2048 : x);
   }();
-  p.seg_cost = seg_cost;
+  p.seg_cost = seg_cost * ((p.G + kTcMergeHeads - 1) / kTcMergeHeads);
   p.rec = static_cast<uint64_t*>(workspace);
   cudaError_t e;
   if (p.G > kTcHeads) {  // one n-tile of 8 query heads per KV head (the API allows G <= 8)
