@@ -925,15 +925,41 @@ def run_reference(args, world, rank):
 
 def profile_case(args):
     """A small case for ncu: a few layers of the workload (about 1 GB at the
-    Llama shape; 2 layers of the sharing workload), a few attention calls
-    through the C ABI -- the shared-prefix call on the sharing workload."""
+    Llama shape; 2 layers of the ragged and sharing workloads;
+    --profile-layers overrides), a few attention calls through the C ABI --
+    the shared-prefix call on the sharing workload.  --profile-contig S lays
+    the workload's first --profile-requests requests out contiguously (offset
+    reqId x S) and runs the contiguous call instead."""
     import paged_kv_cache_245_gb300 as pkv
     from __graft_entry__ import build
     build()
     dev = torch.device("cuda", 0)
     b = rank_batch(args.workload, 0)
     shape, _, kind, bs, _ = WORKLOADS[args.workload]
-    nl = 2 if kind == "sharing" else 4
+    nl = 2 if kind in ("sharing", "ragged") else 4
+    if args.profile_layers > 0:
+        nl = args.profile_layers
+    if args.profile_contig > 0:
+        n = min(args.profile_requests or b.B, b.B)
+        S = args.profile_contig
+        sub = W.PagedBatch(shape=b.shape, seed=b.seed, block_size=b.block_size,
+                           num_blocks=b.num_blocks, ctx_pre=b.ctx_pre[:n], ctx=b.ctx[:n],
+                           block_tables=b.block_tables[:n], slot_mapping=b.slot_mapping[:n],
+                           req_ids=np.arange(n, dtype=np.int32), max_reqs=n)
+        bufs = []
+        for l in range(nl):
+            li = W.layer_inputs(b, l, device=dev, fast_cache=True)
+            bufs.append((li.q[:n].contiguous(), W.paged_to_contig(li.k_cache, sub, S),
+                         W.paged_to_contig(li.v_cache, sub, S)))
+            del li
+        req = torch.as_tensor(sub.req_ids, device=dev)
+        ctx = torch.as_tensor(sub.ctx, device=dev)
+        for i in range(args.profile_calls):
+            q, kb, vb = bufs[i % nl]
+            pkv.contig_decode_attention(q, kb, vb, req, ctx, int(sub.max_context),
+                                        W.default_scale(b.shape))
+        torch.cuda.synchronize(dev)
+        return
     layers = [W.layer_inputs(b, l, device=dev, fast_cache=True) for l in range(nl)]
     tables = torch.as_tensor(b.block_tables, device=dev)
     ctx = torch.as_tensor(b.ctx, device=dev)
@@ -995,6 +1021,13 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="profiling case: run this many paged attention calls over 4 layers "
                          "of the workload and exit (no timing, no JSON)")
+    ap.add_argument("--profile-layers", type=int, default=0,
+                    help="profiling case: layers to cycle over (default 4; 2 for the ragged "
+                         "and sharing workloads)")
+    ap.add_argument("--profile-contig", type=int, default=0,
+                    help="profiling case: contiguous layout with this S (tokens per request)")
+    ap.add_argument("--profile-requests", type=int, default=0,
+                    help="profiling case, contiguous layout: the first this many requests")
     ap.add_argument("--profile-prefill-calls", type=int, default=0,
                     help="profiling case: run this many prefill calls over 8 fresh 2048-token "
                          "prompts and exit (no timing, no JSON)")
