@@ -58,7 +58,7 @@ struct TcSmem {
   static constexpr int kReqOff = kCtxOff + kTcMaxSeqs * 4;
   static constexpr int kPrefixOff = kReqOff + kTcMaxSeqs * 4;
   static constexpr int kRangeOff = (kPrefixOff + (kTcMaxSeqs + 1) * 4 + 7) / 8 * 8;
-  static constexpr int kEnd = kRangeOff + 2 * 8;
+  static constexpr int kEnd = kRangeOff + 3 * 8;
   static constexpr int kTotal = kEnd + 1024;  // slack to align the base to 1 KiB
   static_assert(kTotal <= 232448, "shared memory per CTA exceeds 227 KiB");
 };
@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(W * 32, 1)
   int32_t* ctx_s = reinterpret_cast<int32_t*>(smem + L::kCtxOff);
   int32_t* req_s = reinterpret_cast<int32_t*>(smem + L::kReqOff);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L::kPrefixOff);
-  int64_t* range = reinterpret_cast<int64_t*>(smem + L::kRangeOff);  // this CTA's [lo, hi)
+  // this CTA's tiles [range[0], range[1]), and the sequence of its first tile
+  int64_t* range = reinterpret_cast<int64_t*>(smem + L::kRangeOff);
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -315,11 +316,77 @@ __global__ void __launch_bounds__(W * 32, 1)
       run += (ctx_s[i] + 15) >> 4;
     }
     if (lane == 31) prefix[B] = incl;
-    __syncwarp();
-    // this CTA's run of tiles, computed once: lane 0 its start, lane 1 its end
-    if (lane < 2) {
-      const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
-      range[lane] = tc_unit_to_tile(tc_range_lo(c + lane, V, P), prefix, B, p.Hkv, p.seg_cost);
+    // This CTA's run of tiles [range[0], range[1]) (tc_unit_to_tile of its
+    // first and past-the-end units) and the sequence holding its first tile
+    // (range[2]).  In 32-bit arithmetic, when the partition has fewer than
+    // 2^30 units (always, short of a million sequences of 128 K positions),
+    // the warp finds each sequence with one max-reduction over the lanes'
+    // own sequences instead of a serial search.
+    const int total = __shfl_sync(kFull, incl, 31);
+    const int64_t V64 = static_cast<int64_t>(p.Hkv) * (static_cast<int64_t>(total) +
+                                                      static_cast<int64_t>(p.seg_cost) * B);
+    if (V64 < (int64_t{1} << 30) && P < 1024) {
+      const uint32_t V = static_cast<uint32_t>(V64), hkv = static_cast<uint32_t>(p.Hkv);
+      const uint32_t alpha = static_cast<uint32_t>(p.seg_cost);
+      uint32_t u[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) u[k] = static_cast<uint32_t>(tc_range_lo(c + k, V, P));
+      // per unit: the last sequence whose units start at or before it
+      int best[2] = {-1, -1};
+      run = incl - sum;
+      for (int i = i0; i < i0 + per && i < B; ++i) {
+        const uint32_t vi = hkv * (static_cast<uint32_t>(run) + alpha * static_cast<uint32_t>(i));
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (vi <= u[k]) best[k] = i;
+        run += (ctx_s[i] + 15) >> 4;
+      }
+      int64_t tile[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int a = __reduce_max_sync(kFull, best[k]);
+        if (u[k] >= V || a < 0) {
+          tile[k] = static_cast<int64_t>(hkv) * total;
+        } else {
+          // the owner lane of sequence a holds its prefix; every lane reads
+          // it from shared memory (written above by that lane)
+          __syncwarp();
+          const uint32_t pa = static_cast<uint32_t>(prefix[a]);
+          const uint32_t n = static_cast<uint32_t>((ctx_s[a] + 15) >> 4);
+          const uint32_t r = u[k] - hkv * (pa + alpha * static_cast<uint32_t>(a));
+          const uint32_t h = r / (n + alpha);
+          const int32_t o = static_cast<int32_t>(r - h * (n + alpha)) - static_cast<int32_t>(alpha);
+          tile[k] = static_cast<int64_t>(hkv) * pa + h * n + (o > 0 ? o : 0);
+        }
+      }
+      // the sequence whose tiles hold tile[0]: the last with hkv * prefix <= tile[0]
+      int seq = -1;
+      run = incl - sum;
+      for (int i = i0; i < i0 + per && i < B; ++i) {
+        if (static_cast<int64_t>(hkv) * run <= tile[0]) seq = i;
+        run += (ctx_s[i] + 15) >> 4;
+      }
+      seq = __reduce_max_sync(kFull, seq);
+      if (lane == 0) {
+        range[0] = tile[0];
+        range[1] = tile[1];
+        range[2] = seq < 0 ? 0 : seq;
+      }
+    } else {
+      __syncwarp();
+      if (lane < 2) {
+        const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);
+        range[lane] = tc_unit_to_tile(tc_range_lo(c + lane, V, P), prefix, B, p.Hkv, p.seg_cost);
+      }
+      __syncwarp();
+      if (lane == 0) {  // the sequence holding the first tile
+        int a = 0, b = B - 1;
+        while (a < b) {
+          const int mid = (a + b + 1) >> 1;
+          if (static_cast<int64_t>(p.Hkv) * prefix[mid] <= range[0]) a = mid; else b = mid - 1;
+        }
+        range[2] = a;
+      }
     }
   }
   __syncthreads();
@@ -367,7 +434,8 @@ __global__ void __launch_bounds__(W * 32, 1)
   };
 
   // ---- this warp's tile stream: segment by segment, tiles x0 + warp, + W, ...
-  TcSeg iseg = tc_find_seg(lo, hi, prefix, B, p.Hkv);
+  const int seq_lo = static_cast<int>(range[2]);
+  TcSeg iseg = tc_seg_at(lo, hi, seq_lo, prefix, p.Hkv);
   int64_t ix = iseg.x0 + warp;
   bool ivalid = true;
   auto settle = [&]() {
@@ -482,7 +550,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   int consumed = 0;
   bool dead = false;
 
-  TcSeg seg = tc_find_seg(lo, hi, prefix, B, p.Hkv);
+  TcSeg seg = tc_seg_at(lo, hi, seq_lo, prefix, p.Hkv);
   while (true) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {

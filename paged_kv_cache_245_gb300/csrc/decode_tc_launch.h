@@ -103,15 +103,11 @@ struct TcSeg {
   int seq, kvh;
 };
 
-// Segment starting at tile x (x < hi <= T).  prefix[i] = tiles of sequences
-// before i; pair (i, h) holds tiles [Hkv*prefix[i] + h*n_i, + n_i).
-__host__ __device__ inline TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_t* prefix,
-                                             int B, int Hkv) {
-  int a = 0, b = B - 1;
-  while (a < b) {
-    const int mid = (a + b + 1) >> 1;
-    if (static_cast<int64_t>(Hkv) * prefix[mid] <= x) a = mid; else b = mid - 1;
-  }
+// Segment starting at tile x (x < hi <= T) of sequence a (the one whose
+// tiles hold x).  prefix[i] = tiles of sequences before i; pair (i, h) holds
+// tiles [Hkv*prefix[i] + h*n_i, + n_i).
+__host__ __device__ inline TcSeg tc_seg_at(int64_t x, int64_t hi, int a, const int32_t* prefix,
+                                           int Hkv) {
   const int64_t base = static_cast<int64_t>(Hkv) * prefix[a];
   const int n = prefix[a + 1] - prefix[a];  // > 0 because x < Hkv*prefix[a+1]
   TcSeg s;
@@ -124,6 +120,18 @@ __host__ __device__ inline TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_
   s.x0 = x;
   s.x1 = s.pend < hi ? s.pend : hi;
   return s;
+}
+
+// Segment starting at tile x (x < hi <= T): finds x's sequence first (the
+// last sequence whose tiles start at or before x).
+__host__ __device__ inline TcSeg tc_find_seg(int64_t x, int64_t hi, const int32_t* prefix,
+                                             int B, int Hkv) {
+  int a = 0, b = B - 1;
+  while (a < b) {
+    const int mid = (a + b + 1) >> 1;
+    if (static_cast<int64_t>(Hkv) * prefix[mid] <= x) a = mid; else b = mid - 1;
+  }
+  return tc_seg_at(x, hi, a, prefix, Hkv);
 }
 
 // The CTAs cf .. cl whose ranges hold tiles of the pair that segment `seg`
