@@ -389,7 +389,9 @@ def run_gpu(args, world, rank, local):
     _barrier(world)
     # ---- the attention calls alone (same calls, same data), for the roofline
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    attn_reps = max(args.steps // 2, 3)
+    # at least 50 replays (1,600 calls at 32 layers): the number that decides
+    # the roofline fraction is averaged over tens of milliseconds
+    attn_reps = max(args.steps // 2, 50)
     a0.record()
     for k in range(attn_reps):
         attn_graph.replay()
