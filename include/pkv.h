@@ -365,6 +365,16 @@ PKV_API int pkv_get_decode_variant(void);
 PKV_API void pkv_debug_stall_next_decode(void);
 
 /*
+ * Test hook for the bounded wait of the in-kernel pair merge.  In the next
+ * tensor-core decode call, CTA 1 does not write the record of its first
+ * piece (a pair whose first tiles belong to CTA 0): CTA 0's merge re-reads
+ * the record until its time limit (2 s), the call records
+ * PKV_DEVERR_TIMEOUT, that pair's output is undefined, and the context
+ * stays usable.
+ */
+PKV_API void pkv_debug_drop_next_piece_record(void);
+
+/*
  * Test-only gather: out[i][h][pos] (bf16 [num_seqs][Hkv][max_context][128])
  * = the cache row that the decode kernels read for position pos of sequence
  * i and KV head h, zeros for pos >= context_lens[i].  It locates rows with

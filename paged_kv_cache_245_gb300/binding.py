@@ -27,6 +27,7 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
             "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
+            "pkv_debug_drop_next_piece_record",
             "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
             "pkv_debug_gather_contig", "pkv_paged_decode_attention_shared",
             "pkv_shared_decode_workspace_size", "pkv_paged_prefill_attention",
@@ -88,6 +89,7 @@ def lib():
     L.pkv_set_checked.restype = None
     L.pkv_get_checked.restype = ctypes.c_int
     L.pkv_debug_stall_next_decode.restype = None
+    L.pkv_debug_drop_next_piece_record.restype = None
     L.pkv_set_decode_variant.argtypes = [ctypes.c_int]
     L.pkv_set_decode_variant.restype = None
     L.pkv_get_decode_variant.restype = ctypes.c_int

@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(W * 32, 1)
                                nxt[pass]) &&
               lane == 0)
             record_error(p.err, kErrTimeout);
-        } else {
+        } else if (!(p.drop_record_test && c == 1)) {
           tc_store_piece(p.rec + (static_cast<int64_t>(c) * kTcRecHeads + hh) * kRecStride,
                          p.tag, lane, o4, Mr, Ls);
         }

@@ -30,6 +30,7 @@ struct TcParams {
   float qscale;             // scale * log2(e)
   int32_t checked;
   int32_t stall_test;       // test hook: CTA 0's warp 0 expects 16 bytes that never come
+  int32_t drop_record_test; // test hook: CTA 1 writes no piece record
   int32_t early_inputs;     // previous kernel is the append: read inputs before the wait
   int* err;
 };

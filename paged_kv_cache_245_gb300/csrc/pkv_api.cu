@@ -25,6 +25,7 @@ std::atomic<int> g_split_tiles{0};
 // 0 automatic, 1 CUDA-core split kernel, 2 tensor-core 8x3, 3 tensor-core 12x2
 std::atomic<int> g_variant{0};
 std::atomic<int> g_stall_test{0};
+std::atomic<int> g_drop_record_test{0};
 thread_local char g_last_error[256] = "";
 
 // The device error word: one int per device (module-scope __device__).
@@ -226,6 +227,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     t.qscale = scale * 1.4426950408889634f;  // log2(e)
     t.checked = g_checked.load();
     t.stall_test = g_stall_test.exchange(0);
+    t.drop_record_test = g_drop_record_test.exchange(0);
     t.early_inputs = after_append ? 1 : 0;
     t.err = err;
     cudaError_t ce = cudaSuccess;
@@ -920,6 +922,7 @@ pkv_status pkv_block_swap(const int64_t* pairs, int64_t n, void* const* src_k,
 
 void pkv_set_checked(int enable) { g_checked.store(enable ? 1 : 0); }
 void pkv_debug_stall_next_decode(void) { g_stall_test.store(1); }
+void pkv_debug_drop_next_piece_record(void) { g_drop_record_test.store(1); }
 void pkv_set_decode_variant(int variant) { g_variant.store(variant >= 0 && variant <= 3 ? variant : 0); }
 int pkv_get_decode_variant(void) { return g_variant.load(); }
 int pkv_get_checked(void) { return g_checked.load(); }

@@ -374,6 +374,24 @@ def test_wait_limit_reports_timeout_and_context_survives():
     assert_attention_close(out, L.oracle_attend(), "after a timed-out call")
 
 
+def test_merge_wait_limit_reports_timeout_and_context_survives():
+    """The in-kernel merge of a pair cut by the CTA ranges re-reads a piece
+    record that is not there yet for at most 2 s.  Test hook: CTA 1 writes
+    no record in the next call, so CTA 0 (whose last segment holds the first
+    tiles of the pair it shares with CTA 1) gives up and reports a timeout;
+    the next call on the same context is correct."""
+    pkv.set_decode_variant(pkv.VARIANT_TC_12X2)
+    b = _batch(32, 8, [1024] * 64, 16, seed=37)
+    L = DeviceLayer(b, 0, DEV)
+    assert pkv.get_device_error() == "none"
+    pkv.lib().pkv_debug_drop_next_piece_record()
+    L.gpu_attend()
+    assert pkv.get_device_error() == "timeout"
+    out = L.gpu_attend()
+    assert pkv.get_device_error() == "none"
+    assert_attention_close(out, L.oracle_attend(), "after a merge that timed out")
+
+
 def test_cuda_graph_replay_matches_direct_calls():
     """The decode step (append + attention) captured in a CUDA graph and
     replayed gives the same bytes as direct calls."""
