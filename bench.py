@@ -188,9 +188,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# The sources the attention call's kernels (decode_tc_kernel and its
-# combine) are built from; the DRAM counters of a profile summary stand for
-# the kernel only while these are unchanged.
+# The sources the attention call's kernel (decode_tc_kernel, which merges
+# the pieces of cut pairs itself) is built from; the DRAM counters of a
+# profile summary stand for the kernel only while these are unchanged.
 DECODE_SOURCES = ("decode_tc.cu", "decode_tc.cuh", "decode_tc_launch.h", "pkv_device.cuh")
 
 
