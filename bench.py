@@ -6,9 +6,9 @@ One JSON line (rank 0):
   value       decode tokens/s per layer, whole job (all ranks), inputs resident
   e2e         the same metric with per-step inputs copied from pinned host
               memory and the outputs read back inside the timed region
-  roofline    achieved HBM bandwidth of the paged attention call (main +
-              split-combine kernels) from CUDA events in the timed region,
-              against the measured copy bandwidth of this GPU model
+  roofline    achieved HBM bandwidth of the paged attention call (its
+              kernels: one for the tensor-core path) from CUDA events in the
+              timed region, against the measured copy bandwidth of this GPU model
   cpu_baseline  the CPU fp64 oracle on a bounded sample of the same workload
   legs        contiguous-layout attention on the same logical KV, the append
               kernel alone, and a Yi-34B-shaped copy-on-write block copy
@@ -280,15 +280,30 @@ class DeviceWorkload:
     def uses_tc(self):
         return self.batch.block_size % 16 == 0 and self.pkv.get_decode_variant() != 1
 
+    def shared_kernels(self):
+        """The kernels of one shared-prefix call, by the library's launch count."""
+        n = (self.launches_per_step() - (0 if self.cow is None else 1)) // self.shape.num_layers - 1
+        return {1: "prefix_kernel alone: own positions as masked key tiles, output written there",
+                2: "prefix_kernel, then cascade_merge_kernel",
+                }.get(n, "cascade_prep_kernel, prefix_kernel, decode_tc_kernel over the own "
+                         "positions, cascade_merge_kernel")
+
     def launches_per_step(self):
-        # kv_append, the attention kernel and its combine kernel per layer,
-        # plus one block copy launch (all layers) when the step copies on write
+        # per layer kv_append and the attention call's kernels (the tensor-core
+        # kernel alone, merging its split pairs itself; the split kernel and its
+        # combine; the shared-prefix call's kernels as the library reports
+        # them), plus one block copy launch (all layers) when the step copies
+        # on write
         cow = 0 if self.cow is None else 1
         if self.groups is not None:
-            # append; the prefix kernel; the merge (own parts in the merge)
-            return self.shape.num_layers * 3 + cow
+            gs, sb, n, own = self.groups
+            b = self.batch
+            attn = self.pkv.shared_decode_launches(
+                b.B, int(gs.numel()) - 1, n, b.block_tables.shape[1], b.max_context,
+                b.block_size, own, self.shape.num_q_heads, self.shape.num_kv_heads)
+            return self.shape.num_layers * (1 + attn) + cow
         if self.uses_tc:
-            return self.shape.num_layers * 3 + cow
+            return self.shape.num_layers * 2 + cow
         return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0)) + cow
 
     def copy_on_write(self, pairs=None):
@@ -437,17 +452,16 @@ def run_gpu(args, world, rank, local):
                               "group's shared prompt blocks read once for all its branches)"
                               if wl.groups is not None
                               else "per layer: paged_decode_step = kv_append + "
-                              "paged_decode_attention (main + combine) in one C-ABI call")},
+                              "paged_decode_attention in one C-ABI call")},
         "hbm_tbs": round(achieved_gbs / 1e3, 4),
         "hbm_pct_of_8tbs": round(100 * achieved_gbs / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                      "traffic": _profiled_traffic(args.workload),
-                     "kernel": "paged_decode_attention_shared call (prefix_kernel, then "
-                               "cascade_merge_kernel with the own positions)"
+                     "kernel": "paged_decode_attention_shared call (%s)" % wl.shared_kernels()
                                if wl.groups is not None else
-                               "paged_decode_attention call (decode_tc_kernel + "
-                               "decode_tc_combine_kernel)" if wl.uses_tc else
+                               "paged_decode_attention call (decode_tc_kernel, merging the "
+                               "pairs its CTA ranges cut)" if wl.uses_tc else
                                "paged_decode_attention call (decode_attention_kernel + "
                                "decode_combine_kernel)",
                      "algorithmic_bytes_per_launch": alg,

@@ -200,15 +200,19 @@ PKV_API pkv_status pkv_contig_decode_step(
  * max_group_size sequences per group), and its members' block tables begin
  * with the same shared_blocks[g] entries (device int32 [num_groups]; every
  * member's context covers them).  Singleton groups with shared_blocks 0 are
- * plain sequences.  The shared positions are read once for every
- * ceil(16 / G) members (their query heads stacked into one tensor-core tile)
- * instead of once per member; each member's own later positions are read as
- * usual, and the two softmax parts are merged.  max_own_tokens is a host
- * bound on every sequence's own positions (context_lens[i] minus its group's
- * shared positions), or -1 if unknown: with a bound of at most 256 the own
- * positions are attended on CUDA cores inside the final merge instead of by
- * a second tensor-core pass (checked mode reports a sequence beyond the
- * bound, PKV_DEVERR_CONTEXT, and its later positions are left out).  Result:
+ * plain sequences.  The shared positions are read once per group (all its
+ * members' query heads are rows of one tensor-core tile) instead of once per
+ * member; each member's own later positions are read as usual, and the
+ * softmax parts are merged.  max_own_tokens is a host bound on every
+ * sequence's own positions (context_lens[i] minus its group's shared
+ * positions), or -1 if unknown.  With a bound of at most 256 the own
+ * positions are attended without a second tensor-core pass: as masked key
+ * tiles of the shared-prefix kernel when max_group_size times the bound
+ * (rounded up to whole boxes of gcd(block_size, 128) rows) fits 512 key
+ * slots -- and if the shared positions then take one chunk per group, that
+ * kernel writes the output and the call is one launch -- else on CUDA cores
+ * inside the final merge (checked mode reports a sequence beyond the bound,
+ * PKV_DEVERR_CONTEXT, and its later positions are left out).  Result:
  * the same attention as
  * pkv_paged_decode_attention within the attention tolerance (a different
  * summation order).  Other arguments as there; block_size must be a multiple
@@ -217,6 +221,16 @@ PKV_API pkv_status pkv_contig_decode_step(
  * max_blocks_per_seq, heads) bytes.  Checked mode also reports a member whose
  * context does not cover its group's shared blocks (PKV_DEVERR_CONTEXT).
  */
+/*
+ * Kernel launches one pkv_paged_decode_attention_shared call with these
+ * sizes makes on the current device (1 to 4, more for a tensor-core pass over
+ * a batch of many long sequences), or -1 for sizes the call rejects.  No
+ * counterpart in the pages: it reports which of the modes above a call runs.
+ */
+PKV_API int32_t pkv_shared_decode_launches(int32_t num_seqs, int32_t num_groups,
+                                           int32_t max_group_size, int32_t max_blocks_per_seq,
+                                           int32_t max_context, int32_t block_size,
+                                           int32_t max_own_tokens, pkv_heads heads);
 PKV_API size_t pkv_shared_decode_workspace_size(int32_t num_seqs, int32_t num_groups,
                                                 int32_t max_group_size,
                                                 int32_t max_blocks_per_seq, pkv_heads heads);

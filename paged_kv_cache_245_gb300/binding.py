@@ -30,7 +30,8 @@ EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size
             "pkv_debug_drop_next_piece_record",
             "pkv_paged_decode_step", "pkv_contig_decode_step", "pkv_debug_gather_paged",
             "pkv_debug_gather_contig", "pkv_paged_decode_attention_shared",
-            "pkv_shared_decode_workspace_size", "pkv_paged_prefill_attention",
+            "pkv_shared_decode_workspace_size", "pkv_shared_decode_launches",
+            "pkv_paged_prefill_attention",
             "pkv_contig_prefill_attention", "pkv_block_swap",
             "pkv_get_device_error", "pkv_status_string", "pkv_last_error")
 
@@ -80,6 +81,8 @@ def lib():
                                                ctypes.c_float, Heads, vp, vp]
     L.pkv_shared_decode_workspace_size.argtypes = [i32, i32, i32, i32, Heads]
     L.pkv_shared_decode_workspace_size.restype = sz
+    L.pkv_shared_decode_launches.argtypes = [i32, i32, i32, i32, i32, i32, i32, Heads]
+    L.pkv_shared_decode_launches.restype = i32
     L.pkv_paged_decode_attention_shared.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
                                                     vp, vp, i32, i32, i32, ctypes.c_float, Heads,
                                                     vp, vp, sz, vp]
@@ -163,6 +166,14 @@ def decode_num_splits(num_seqs, num_q_heads, num_kv_heads, max_context, head_dim
 def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, max_context, head_dim=128):
     return int(lib().pkv_decode_workspace_size(num_seqs, heads(num_q_heads, num_kv_heads,
                                                                head_dim), max_context))
+
+
+def shared_decode_launches(num_seqs, num_groups, max_group_size, max_blocks_per_seq, max_context,
+                           block_size, max_own_tokens, num_q_heads, num_kv_heads, head_dim=128):
+    """Kernel launches of one shared-prefix decode call with these sizes (-1: rejected)."""
+    return int(lib().pkv_shared_decode_launches(
+        num_seqs, num_groups, max_group_size, max_blocks_per_seq, max_context, block_size,
+        max_own_tokens, heads(num_q_heads, num_kv_heads, head_dim)))
 
 
 def _workspace(workspace, q, nbytes):

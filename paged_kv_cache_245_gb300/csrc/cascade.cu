@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   // Launched as a programmatic dependent of the prefix kernel when it attends
   // the own positions itself: those need only this call's inputs, so they
   // run before the wait, overlapping the prefix kernel's tail.
-  if (c.own_cap < 0) grid_dependency_wait();  // the own parts' records come from the previous kernel
+  const bool own_here = c.own_cap >= 0 && !c.own_in_prefix;
+  if (!own_here) grid_dependency_wait();  // the own parts come in records of the previous kernels
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
@@ -131,7 +132,11 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   const float* rs = c.rec_s + idx * kRecStride;
   float ms, ls;
   float4 os;
-  if (c.own_cap >= 0) {
+  if (c.own_in_prefix) {  // in the prefix records
+    ms = -INFINITY;
+    ls = 0.f;
+    os = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else if (c.own_cap >= 0) {
     int n = c.ctx[i] - sb * c.bs;
     if (n > c.own_cap) {
       if (c.checked && (threadIdx.x & 31) == 0) record_error(c.err, kErrContext);
@@ -146,10 +151,12 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
     os = ls > 0.f ? __ldcg(reinterpret_cast<const float4*>(rs) + lane)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (c.own_cap >= 0) grid_dependency_wait();  // the prefix records are complete
+  if (own_here) grid_dependency_wait();  // the prefix records are complete
   grid_dependency_trigger();
   // Fold in the prefix records, two per chunk of the shared positions (even
-  // and odd key tiles; the second only if the chunk has more than one tile).
+  // and odd key tiles; the second only if the chunk has more than one tile,
+  // always when the own tiles follow the last chunk: a group then has at
+  // least one chunk and the prefix kernel writes every half).
   // A member beyond the group size bound has none: the caller broke the
   // contract, nothing is read.  Lane k loads record k's (m, l), all at once;
   // every lane loads its four o values of four records at a time; then
@@ -158,12 +165,14 @@ __global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeParams 
   constexpr int kMaxRec = 16;  // 2 records per chunk, at most 8 chunks
   const bool member = kg >= 0 && kg * c.G < c.prefix_rows;
   const int shared = sb * c.bs;
-  const int chunks = member ? min((shared + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys,
+  const int nch = (shared + c.prefix_chunk_keys - 1) / c.prefix_chunk_keys;
+  const int chunks = member ? min(c.own_in_prefix ? max(nch, 1) : nch,
                                   min(c.prefix_chunks, kMaxRec / 2))
                             : 0;
   auto used = [&](int kh) {
     return kh < 2 * chunks &&
-           ((kh & 1) == 0 || min(c.prefix_chunk_keys, shared - (kh >> 1) * c.prefix_chunk_keys) > 128);
+           (c.own_in_prefix || (kh & 1) == 0 ||
+            min(c.prefix_chunk_keys, shared - (kh >> 1) * c.prefix_chunk_keys) > 128);
   };
   auto rec = [&](int kh) {
     return c.rec_p + ((((static_cast<int64_t>(g) * c.prefix_chunks + (kh >> 1)) * 2 + (kh & 1)) *

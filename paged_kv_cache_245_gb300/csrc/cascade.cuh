@@ -28,6 +28,9 @@ struct CascadeParams {
   const uint16_t* v_cache;
   float qscale;                  // scale * log2(e)
   int32_t own_cap;
+  // own positions attended by the prefix kernel as extra key tiles of each
+  // group's last chunk: its records hold them, nothing is attended here
+  int32_t own_in_prefix;
   // workspace
   int32_t* tables_s;  // [B][max_blocks]
   int32_t* ctx_s;     // [B]

@@ -66,6 +66,20 @@ uint32_t next_launch_tag() {
   return t;
 }
 
+}  // namespace
+
+// Batches above kTcMaxSeqs run as consecutive chunks reusing the workspace;
+// a chunk's tile prefix (int32) must hold chunk * ceil(max_context / 16).
+int tc_chunk_seqs(int max_context) {
+  const int64_t max_tiles = (static_cast<int64_t>(max_context) + 15) / 16;
+  int chunk = kTcMaxSeqs;
+  if (max_tiles > 0 && static_cast<int64_t>(chunk) * max_tiles > 0x7fffffffLL)
+    chunk = static_cast<int>(0x7fffffffLL / max_tiles);
+  return chunk < 1 ? 1 : chunk;
+}
+
+namespace {
+
 template <bool kContig, int W, int S, int NT = 1>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,
                        int num_ctas, cudaStream_t stream) {
@@ -81,13 +95,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
   }
-  // Batches above kTcMaxSeqs run as consecutive chunks reusing the workspace;
-  // a chunk's tile prefix (int32) must hold chunk * ceil(max_context / 16).
-  const int64_t max_tiles = (static_cast<int64_t>(p0.max_context) + 15) / 16;
-  int chunk = kTcMaxSeqs;
-  if (max_tiles > 0 && static_cast<int64_t>(chunk) * max_tiles > 0x7fffffffLL)
-    chunk = static_cast<int>(0x7fffffffLL / max_tiles);
-  if (chunk < 1) chunk = 1;
+  const int chunk = tc_chunk_seqs(p0.max_context);
   for (int s0 = 0; s0 < p0.num_seqs; s0 += chunk) {
     TcParams p = p0;
     p.num_seqs = (p0.num_seqs - s0) < chunk ? (p0.num_seqs - s0) : chunk;

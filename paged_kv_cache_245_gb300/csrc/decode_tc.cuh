@@ -17,9 +17,11 @@
 // the segment's tiles round-robin.  A segment that covers a whole pair writes
 // the bf16 output directly.  The at most two partial segments of a CTA (its
 // first and its last: "pieces" of a pair cut by the ranges) are merged inside
-// the kernel: the CTA holding a pair's first tiles usually finishes its piece
-// last and merges the others' records, which were published with a flag long
-// before; a flag protocol without waiting covers every other order.
+// the kernel: the CTA holding a pair's first tiles (its last segment)
+// merges the others' records, which their CTAs wrote as their first
+// segments, usually long before; the records validate themselves (a launch
+// tag in every word), and a record not yet complete is read again, for a
+// bounded time (tc_merge_pieces).
 //
 // Data movement.  K and V tiles (16 rows x 256 B) come in through the TMA
 // engine from a 2-D tensor map over the cache's rows, as two 64-column boxes

@@ -153,6 +153,9 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows);
 // Workspace bytes for the per-CTA partial records.
 size_t tc_workspace_bytes(int num_ctas);
 
+// Sequences per launch (a larger batch runs as consecutive launches).
+int tc_chunk_seqs(int max_context);
+
 // cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages.  A group
 // of more than 8 query heads per KV head (p.G <= 16, paged only) runs with
 // two n-tiles of heads on 8 warps x 3 stages whatever cfg says.

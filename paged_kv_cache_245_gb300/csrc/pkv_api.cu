@@ -2,6 +2,7 @@
 // split policy, launches, checked mode and the per-device error word.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -322,6 +323,8 @@ pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const 
 
 // Own parts of at most this many positions are attended in the merge kernel.
 constexpr int32_t kInlineOwnMax = 256;
+constexpr int64_t kPrefixRowTile = 128;  // rows of a prefix-kernel row block
+constexpr int64_t kOwnTileSlots = 512;   // own key slots per prefix row block (4 key tiles)
 
 // Shared-prefix plan: prefix entries stack the heads of m sequences (m * G
 // <= 16 query heads per KV head); workspace regions, 256-byte aligned.
@@ -388,6 +391,41 @@ SharedPlan shared_plan(int32_t B, int32_t num_groups, int32_t max_group_size, in
   s.tc = take(pkv::tc_workspace_bytes(tc_ctas(sms)));
   s.total = at;
   return s;
+}
+
+// How a shared-prefix call runs: the chunks of the shared positions and
+// where the own positions (after a group's shared blocks) are attended.
+struct SharedModes {
+  int32_t chunk_blocks = 0, prefix_chunks = 0;
+  int32_t run_rows = 0;    // rows per TMA box of the prefix kernel: gcd(block_size, 128)
+  int32_t own_cap = -1;    // a host bound of at most kInlineOwnMax own positions, else -1
+  int32_t own_slots = 0;   // > 0: own positions as masked key tiles of the prefix kernel
+  bool fused = false;      // the prefix kernel writes the output: the call is one launch
+};
+
+SharedModes shared_modes(int32_t max_blocks, int32_t block_size, int32_t num_groups,
+                         int32_t max_group_size, int32_t max_own_tokens, const pkv_heads& h,
+                         int sms) {
+  SharedModes m;
+  const int32_t G = h.num_q_heads / h.num_kv_heads;
+  m.chunk_blocks = prefix_chunk_blocks(max_blocks, block_size, num_groups, h.num_kv_heads, sms);
+  m.prefix_chunks = (max_blocks + m.chunk_blocks - 1) / m.chunk_blocks;
+  m.run_rows = 128;
+  while (block_size % m.run_rows != 0) m.run_rows >>= 1;
+  // short own parts are attended without a second tensor-core pass
+  m.own_cap = max_own_tokens >= 0 && max_own_tokens <= kInlineOwnMax ? max_own_tokens : -1;
+  // Own parts of at most kOwnTileSlots slots per row block (slots: the bound
+  // rounded up to whole boxes, times the members a row block can hold) ride
+  // as masked key tiles of the prefix kernel; with one chunk per group that
+  // kernel then writes the output itself and the merge is not launched.
+  // Otherwise the merge kernel attends them on CUDA cores.
+  if (m.own_cap >= 0) {
+    const int64_t slots = (static_cast<int64_t>(m.own_cap) + m.run_rows - 1) / m.run_rows * m.run_rows;
+    const int64_t members = std::min<int64_t>(max_group_size, kPrefixRowTile / G + 2);
+    if (slots > 0 && members * slots <= kOwnTileSlots) m.own_slots = static_cast<int32_t>(slots);
+  }
+  m.fused = m.own_slots > 0 && m.prefix_chunks == 1;
+  return m;
 }
 
 pkv_status gather_common(const void* cache, const int32_t* block_tables, int32_t max_blocks,
@@ -523,6 +561,24 @@ pkv_status pkv_contig_decode_attention(const void* q, const void* k_buf, const v
                        stream);
 }
 
+int32_t pkv_shared_decode_launches(int32_t num_seqs, int32_t num_groups, int32_t max_group_size,
+                                   int32_t max_blocks_per_seq, int32_t max_context,
+                                   int32_t block_size, int32_t max_own_tokens, pkv_heads heads) {
+  int sms = 0;
+  if (device_info(nullptr, nullptr, &sms) != PKV_OK) return -1;
+  if (check_heads(heads) != PKV_OK || num_seqs <= 0 || num_groups <= 0 || max_group_size <= 0 ||
+      max_blocks_per_seq <= 0 || max_context < 0 || block_size <= 0 || block_size % 16 != 0)
+    return -1;
+  const SharedModes m = shared_modes(max_blocks_per_seq, block_size, num_groups, max_group_size,
+                                     max_own_tokens, heads, sms);
+  if (m.fused) return 1;          // the prefix kernel
+  if (m.own_cap >= 0) return 2;   // the prefix kernel, the merge
+  // the prep, the prefix kernel, the tensor-core pass (one launch per chunk of
+  // sequences), the merge
+  const int chunk = pkv::tc_chunk_seqs(max_context);
+  return 3 + (num_seqs + chunk - 1) / chunk;
+}
+
 size_t pkv_shared_decode_workspace_size(int32_t num_seqs, int32_t num_groups,
                                         int32_t max_group_size, int32_t max_blocks_per_seq,
                                         pkv_heads heads) {
@@ -593,10 +649,10 @@ pkv_status pkv_paged_decode_attention_shared(
   c.num_groups = num_groups;
   c.bs = block_size;
   c.prefix_rows = sp.rows;
-  const int32_t chunk_blocks = prefix_chunk_blocks(max_blocks_per_seq, block_size, num_groups,
-                                                   heads.num_kv_heads, sms);
-  c.prefix_chunks = (max_blocks_per_seq + chunk_blocks - 1) / chunk_blocks;
-  c.prefix_chunk_keys = chunk_blocks * block_size;
+  const SharedModes sm = shared_modes(max_blocks_per_seq, block_size, num_groups, max_group_size,
+                                      max_own_tokens, heads, sms);
+  c.prefix_chunks = sm.prefix_chunks;
+  c.prefix_chunk_keys = sm.chunk_blocks * block_size;
   if (static_cast<int64_t>(num_groups) * c.prefix_chunks > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "too many groups");
   c.checked = g_checked.load();
@@ -604,8 +660,11 @@ pkv_status pkv_paged_decode_attention_shared(
   c.k_cache = static_cast<const uint16_t*>(k_cache);
   c.v_cache = static_cast<const uint16_t*>(v_cache);
   c.qscale = scale * 1.4426950408889634f;  // log2(e)
-  // short own parts are attended in the merge kernel (no second launch)
-  c.own_cap = max_own_tokens >= 0 && max_own_tokens <= kInlineOwnMax ? max_own_tokens : -1;
+  c.own_cap = sm.own_cap;
+  c.own_in_prefix = sm.own_slots > 0;
+  const int32_t own_slots = sm.own_slots;
+  const int run_rows = sm.run_rows;
+  const bool fused = sm.fused;
   c.tables_s = reinterpret_cast<int32_t*>(ws + sp.tables_s);
   c.ctx_s = reinterpret_cast<int32_t*>(ws + sp.ctx_s);
   c.rec_p = reinterpret_cast<float*>(ws + sp.rec_p);
@@ -620,8 +679,6 @@ pkv_status pkv_paged_decode_attention_shared(
   // a group against its shared blocks on the tcgen05 prefill kernel (no
   // causal mask), records out.
   {
-    int run_rows = 128;  // gcd(block_size, 128)
-    while (block_size % run_rows != 0) run_rows >>= 1;
     alignas(64) CUtensorMap tk;
     alignas(64) CUtensorMap tv;
     if (!pkv::encode_prefill_runs(&tk, k_cache, rows_total, run_rows) ||
@@ -646,6 +703,10 @@ pkv_status pkv_paged_decode_attention_shared(
     pf.chunk_keys = c.prefix_chunk_keys;
     pf.run_rows = run_rows;
     pf.qscale = c.qscale;
+    pf.ctx = context_lens;
+    pf.own_slots = own_slots;
+    pf.own_cap = c.own_cap;
+    pf.out = fused ? c.out : nullptr;
     pf.checked = c.checked;
     pf.err = err;
     ce = pkv::launch_prefix(tk, tv, pf, s);
@@ -676,6 +737,7 @@ pkv_status pkv_paged_decode_attention_shared(
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
     if (ts != pkv::TcStatus::kOk) return cuda_fail(ce, "prefix-sharing decode launch");
   }
+  if (fused) return PKV_OK;  // the prefix kernel wrote the output
   ce = pkv::launch_cascade_merge(c, s);
   if (ce != cudaSuccess) return cuda_fail(ce, "prefix-sharing merge launch");
   return PKV_OK;

@@ -18,6 +18,14 @@
 // next loads ahead of the chain S -> softmax -> P V.  K and V have a producer
 // warp each.  Tensor memory as in prefill.cu: S_t in columns 128t .., O_t in
 // 256 + 128t ..; P over S in place; lazy rescale.
+//
+// Own positions (with a host bound on them): a group's last chunk takes
+// extra key tiles holding every member's own positions, own_slots key slots
+// per member, and a row sees only its member's slots (a per-row window in
+// the softmax mask; V rows of empty slots are zeroed).  The records then
+// hold the whole attention, split in parts.  With one chunk per group the
+// CTA also merges its two halves and writes the bf16 output: the call is
+// this one launch.
 #include "pkv_device.cuh"
 #include "prefix.cuh"
 #include "umma.cuh"
@@ -32,7 +40,20 @@ constexpr int kStages = 3;
 constexpr int kOffK = kOpBytes;                       // after the one Q tile
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 224 KiB
-constexpr int kSmemBytes = kTilesBytes + 256 + 1024;
+constexpr int kOwnLenOff = kTilesBytes + 256;                // [members of the row block] own lengths
+constexpr int kOwnLenBytes = 576;                           // up to 144 members
+constexpr int kSmemBytes = kOwnLenOff + kOwnLenBytes + 1024;
+// The fused ending's exchange of the two halves' rows, [2][kRowTile][kPrefixRecStride]
+// fp32, in the K/V stages (idle by then).
+static_assert(2 * kRowTile * kPrefixRecStride * 4 <= kStages * kStageBytes, "exchange area");
+
+// Bits [a, b) of a 32-bit word, 0 <= a, b <= 32.
+__device__ __forceinline__ uint32_t bit_range(int a, int b) {
+  if (b <= a) return 0u;
+  const uint32_t below_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
+  const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+  return below_b & ~below_a;
+}
 constexpr int kThreads = 352;  // 8 softmax warps, K producer, MMA issuer, V producer
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -56,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(bars + 20);
 
   int* pick = reinterpret_cast<int*>(bars + 22);  // [2] the chosen key-tile count, chunk
+  int* own_len = reinterpret_cast<int*>(smem + kOwnLenOff);  // own positions of the members here
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -142,13 +164,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = (p.group_start[g + 1] - seq) * G;
   const int row0 = blockIdx.x * kRowTile;
   if (row0 >= rows) return;  // past the group's rows (uniform)
-  const int sb = min(max(p.shared_blocks[g], 0), p.max_blocks);
+  const int sb_in = p.shared_blocks[g];
+  const int sb = min(max(sb_in, 0), p.max_blocks);
   const int ctx = sb * static_cast<int>(p.bs);  // the shared positions
   const int kbase = kc * p.chunk_keys;
-  if (kbase >= ctx) return;  // a chunk past them (uniform)
+  // the group's chunks (at least one when own tiles follow: the last takes them)
+  const int nch = (ctx + p.chunk_keys - 1) / p.chunk_keys;
+  const int nch_all = p.own_slots > 0 ? max(nch, 1) : nch;
+  if (kc >= nch_all) return;  // a chunk past them (uniform)
   const int kend = min(ctx, kbase + p.chunk_keys);
-  const int ntiles = (kend - kbase + kKeys - 1) / kKeys;
+  const int nts = kend > kbase ? (kend - kbase + kKeys - 1) / kKeys : 0;  // shared key tiles
+  const int rows_here = min(rows - row0, kRowTile);
+  const int m_first = row0 / G;  // the row block's members: m_first .. + members_here - 1
+  const int members_here = (row0 + rows_here - 1) / G - m_first + 1;
+  const int nto = p.own_slots > 0 && kc == nch_all - 1
+                      ? (members_here * p.own_slots + kKeys - 1) / kKeys
+                      : 0;  // own key tiles
+  const int ntiles = nts + nto;
   const bool two = ntiles > 1;  // row tile 1 has odd tiles to take
+  const bool fused = p.out != nullptr;
 
   // Producers: warp 8 copies K, warp 10 copies V, each on its own stage
   // schedule -- K of tile j waits only for the S product of tile j - 3, not
@@ -157,17 +191,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t policy = l2_policy_evict_first();  // read once
   const int run = p.run_rows;    // rows per box (16 .. 128, divides 128 and bs)
   const int runs = kKeys / run;  // boxes per tile and tensor (<= 8)
+  // Tile j < nts: shared positions kbase + 128 j ..; else own slots
+  // 128 (j - nts) .. (member k's own position o at slot k * own_slots + o).
+  // A run of rows never crosses a block: own_slots and every run start are
+  // multiples of run, which divides bs.
   auto entry = [&](int j) -> int32_t {
-    const int kpos = kbase + j * kKeys + lane * run;
     int32_t e = -1;
-    if (j < ntiles && lane < runs && kpos < ctx) {
-      e = p.block_tables[static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs];
-      if (p.checked && (e < 0 || e >= p.num_blocks)) {
-        record_error(p.err, kErrBlockId);
-        e = -1;  // skip the copy: stale rows, undefined output, no fault
+    if (j < ntiles && lane < runs) {
+      int64_t at = -1;  // index into the block tables
+      if (j < nts) {
+        const int kpos = kbase + j * kKeys + lane * run;
+        if (kpos < ctx) at = static_cast<int64_t>(seq) * p.max_blocks + kpos / p.bs;
+      } else {
+        const int s0 = (j - nts) * kKeys + lane * run;
+        const int k = s0 / p.own_slots, o = s0 - k * p.own_slots;
+        if (k < members_here && o < own_len[k])
+          at = static_cast<int64_t>(seq + m_first + k) * p.max_blocks + sb + o / p.bs;
+      }
+      if (at >= 0) {
+        e = p.block_tables[at];
+        if (p.checked && (e < 0 || e >= p.num_blocks)) {
+          record_error(p.err, kErrBlockId);
+          e = -1;  // skip the copy: stale rows, undefined output, no fault
+        }
       }
     }
     return e;
+  };
+  auto run_offset = [&](int j) -> int {  // in-block offset of this lane's run of tile j
+    if (j < nts) return (kbase + j * kKeys + lane * run) % static_cast<int>(p.bs);
+    const int s0 = (j - nts) * kKeys + lane * run;
+    return (s0 % p.own_slots) % static_cast<int>(p.bs);
   };
   const bool is_v = warp == 10;
   const CUtensorMap* tm = is_v ? &tmv : &tmk;
@@ -180,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = j % kStages;
       const uint32_t u = static_cast<uint32_t>(j / kStages);  // use of the stage
       const uint32_t loaded = __popc(__ballot_sync(kFull, e >= 0));
-      const int off = (kbase + j * kKeys + lane * run) % p.bs;
+      const int off = run_offset(j);
       const int32_t grp =
           e >= 0 ? static_cast<int32_t>(cache_row(e, kvh, p.Hkv, p.bs, off) >> 3) : 0;
       unsigned char* dst =
@@ -212,7 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Softmax warps whose quadrant holds none of their row tile's rows idle.
   const int t = (warp >> 2) & 1;
   const int lr = tid & (kRowTile - 1);  // Q row / TMEM lane
-  const int rows_here = min(rows - row0, kRowTile);
   const int nq = (rows_here + 31) / 32;                  // quadrants of a row tile at work
   const int shift = two && nq <= 2 ? 32 * nq : 0;
   const int qr = shift > 0 && lr >= shift && lr < 2 * shift ? lr - shift : lr;  // row of Q lane lr
@@ -224,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rt = row_of();
     return rt >= 0 && rt < rows_here && (t == 1 || shift == 0 || lr < shift);
   };
-  const int pos = ctx - 1;                               // every shared position is visible
 
   if (warp == 8) {
     if (lane == 0) {
@@ -234,6 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_barrier_init();
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
+    }
+    if (nto > 0) {
+      // own positions of the row block's members (read before their tiles'
+      // entries need them), clamped to the bound and to the table
+      const int cap = min(min(p.own_cap, p.own_slots),
+                          (p.max_blocks - sb) * static_cast<int>(p.bs));
+      for (int k = lane; k < members_here; k += 32) {
+        const int n = p.ctx[seq + m_first + k] - ctx;
+        if (p.checked && (n < 0 || n > cap || sb != sb_in)) record_error(p.err, kErrContext);
+        own_len[k] = min(max(n, 0), cap);
+      }
     }
     __syncwarp();
     e = entry(0);
@@ -260,9 +323,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = smem_addr(smem);
 
+  // a softmax lane's (l, m) and whether its O is complete, for the fused ending
+  float fin_l = 0.f, fin_m = -INFINITY;
+  bool fin_ok = false;
+  auto record_of = [&](int half) {  // this lane's record: (member, head) row, half of the chunk
+    return p.rec_out + ((((static_cast<int64_t>(g) * p.chunks + kc) * 2 + half) * p.Hkv + kvh) *
+                            p.rows + row0 + row_of()) *
+                           kPrefixRecStride;
+  };
+
   if (warp < 8 && ((t == 1 && !two) || !__any_sync(kFull, owns()))) {
     // one key tile (row tile 1 has nothing to do), or no row of this row tile
-    // in this warp's quadrant
+    // in this warp's quadrant.  With own tiles the merge reads both halves of
+    // every chunk: half 1 of a one-tile chunk is an empty record.
+    if (t == 1 && !two && p.own_slots > 0 && !fused && owns()) {
+      float* rec = record_of(1);
+#pragma unroll
+      for (int q = 0; q < kHeadDim / 4; ++q)
+        reinterpret_cast<float4*>(rec)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      rec[128] = -INFINITY;
+      rec[129] = 0.f;
+    }
   } else if (warp < 8) {
     // ================= softmax: row tile t takes key tiles t, t + 2, ... =================
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -271,10 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sc = p.qscale;
     // this lane's record: (member, head) row of row tile t, half t of the chunk
     const bool own = owns();
-    float* const rec = p.rec_out +
-                       ((((static_cast<int64_t>(g) * p.chunks + kc) * 2 + t) * p.Hkv + kvh) *
-                            p.rows + row0 + row_of()) *
-                           kPrefixRecStride;
+    // the keys this lane's row sees: shared positions [0, ctx), then its
+    // member's own slots [own_lo, own_hi) of the own tiles
+    const int own_k = (row0 + min(max(row_of(), 0), rows_here - 1)) / G - m_first;  // member
     float m_used = -INFINITY;  // the maximum P is taken against (scaled logits)
     float l = 0.f;
     bool ok = true;
@@ -282,8 +362,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(kFull, wait_or_abort(&sfull[t], n & 1, abort, p.err));
       if (!ok) break;
       tc_fence_after();
-      const int k0 = kbase + j * kKeys;
-      const bool diag = k0 + kKeys - 1 > pos;  // some key of the tile lies past the row
+      // tile keys k0 .. k0 + 127 against the row's window [wlo, whi)
+      const bool own_tile = j >= nts;
+      const int k0 = own_tile ? (j - nts) * kKeys : kbase + j * kKeys;
+      const int wlo = own_tile ? own_k * p.own_slots : 0;
+      const int whi = own_tile ? wlo + own_len[own_k] : ctx;
+      const bool diag = k0 < wlo || k0 + kKeys > whi;  // some key of the tile is not seen
       // general: a masked tile in this warp, or a negative scale (the maximum
       // of the scaled logits is then not the scaled maximum)
       const bool general = __any_sync(kFull, diag) || !(sc >= 0.f);
@@ -322,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const float x = __uint_as_float(c < 32 ? a[c] : b[c - 32]) * sc;
-            mx[c & 7] = fmaxf(mx[c & 7], !diag || k0 + 64 * h + c <= pos ? x : -INFINITY);
+            const int key = k0 + 64 * h + c;
+            mx[c & 7] = fmaxf(mx[c & 7], !diag || (key >= wlo && key < whi) ? x : -INFINITY);
           }
         }
         tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -330,7 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_new = fmaxf(m_used, tmax);
       if (n == 0) {
-        m_used = m_new;  // finite: the tile's first key is visible to every row
+        // -inf for a row that sees none of the tile's keys (an own tile of
+        // another member): its P is all zero by the mask, and the first
+        // tile it sees scales the empty O and l by 2^-inf = 0
+        m_used = m_new;
       } else {
         const bool grow = m_new > m_used + kRescaleLog2;
         if (__any_sync(kFull, grow)) {
@@ -394,11 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(b, s_tm + 64 * h + 32);
           tmem_wait_ld(a);
           tmem_ready(b);
-          // keys of this half the row sees: bit c of (lo, hi) for key 64h + c
-          const int seen = diag ? min(max(pos - k0 - 64 * h + 1, 0), 64) : 64;
-          const uint32_t lo = seen >= 32 ? 0xffffffffu : (1u << seen) - 1u;
-          const uint32_t hi =
-              seen >= 64 ? 0xffffffffu : (seen <= 32 ? 0u : (1u << (seen - 32)) - 1u);
+          // keys of this half the row sees, [a, b): bit c of (lo, hi) for key 64h + c
+          const int kh = k0 + 64 * h;
+          const int ka = diag ? min(max(wlo - kh, 0), 64) : 0;
+          const int kb = diag ? min(max(whi - kh, 0), 64) : 64;
+          const uint32_t lo = bit_range(min(ka, 32), min(kb, 32));
+          const uint32_t hi = bit_range(max(ka - 32, 0), max(kb - 32, 0));
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
@@ -422,8 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&pfull[t]);
     }
     if (ok) ok = __all_sync(kFull, wait_or_abort(&ofull[t], 0, abort, p.err));
-    if (ok) {
+    fin_l = l;
+    fin_m = m_used;
+    fin_ok = ok;
+    if (ok && !fused) {
       // fp32 record of this (member, head) and half: o / l, m, l
+      float* const rec = record_of(t);
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -492,13 +585,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t c = static_cast<uint32_t>(j >> 1);    // the row tile's tile count
       ok = __all_sync(kFull, wait_or_abort(&vfull[s], u & 1, abort, p.err));
       if (!ok) break;
-      const int k0 = kbase + j * kKeys;
-      if (k0 + kKeys > ctx) {  // zero V rows at or past the shared positions
-        unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
-        const int first = ctx - k0;
-        for (int idx = lane; idx < (kKeys - first) * 16; idx += 32)
-          *reinterpret_cast<uint4*>(vt + kv_chunk_offset(first + (idx >> 4), idx & 15)) =
-              make_uint4(0u, 0u, 0u, 0u);
+      // V rows that hold no key of the tile (stale bytes, maybe NaN) must
+      // not meet a zero P: zero them
+      unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
+      if (j < nts) {
+        const int k0 = kbase + j * kKeys;
+        if (k0 + kKeys > ctx) {  // rows at or past the shared positions
+          const int first = ctx - k0;
+          for (int idx = lane; idx < (kKeys - first) * 16; idx += 32)
+            *reinterpret_cast<uint4*>(vt + kv_chunk_offset(first + (idx >> 4), idx & 15)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+      } else {  // own slots past their member's own positions, or past the members
+        for (int r = lane; r < kKeys; r += 32) {
+          const int slot = (j - nts) * kKeys + r;
+          const int k = slot / p.own_slots, o = slot - k * p.own_slots;
+          if (k >= members_here || o >= own_len[k]) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              *reinterpret_cast<uint4*>(vt + kv_chunk_offset(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
       }
@@ -532,11 +641,75 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Fused ending (one chunk per group, own positions included): the two
+  // halves of every row meet in shared memory (the K/V stages: every copy
+  // has landed and every product has completed) and the row's output is
+  //   M = max(m_0, m_1),  w_t = l_t 2^(m_t - M),  o = (w_0 o_0 + w_1 o_1) / (w_0 + w_1)
+  // with o_t the half's normalised O.  An abort leaves the output unwritten.
+  const bool finish = fused && *abort == 0;  // uniform: nothing sets abort past the barrier
+  float* xo = reinterpret_cast<float*>(smem + kOffK);  // [2][kRowTile][kPrefixRecStride]
+  if (finish) {
+    if (fin_ok) {  // a softmax warp that ran (uniform over the warp)
+      tc_fence_after();
+      const uint32_t o_tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 + t * 128;
+      const float inv = fin_l > 0.f ? 1.f / fin_l : 0.f;
+      float* dst = xo + (t * kRowTile + row_of()) * kPrefixRecStride;
+      const bool own = owns();
+#pragma unroll
+      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(w, o_tm + c0);
+        tmem_wait_ld(w);
+        if (own) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(dst + c0)[q] =
+                make_float4(__uint_as_float(w[4 * q]) * inv, __uint_as_float(w[4 * q + 1]) * inv,
+                            __uint_as_float(w[4 * q + 2]) * inv,
+                            __uint_as_float(w[4 * q + 3]) * inv);
+        }
+      }
+      if (own) {
+        dst[128] = fin_m;
+        dst[129] = fin_l;
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 9) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
+  }
+  if (finish) {
+    for (int r = warp; r < rows_here; r += kThreads / 32) {  // a warp per row, 4 dims a lane
+      const float* h0 = xo + r * kPrefixRecStride;
+      const float* h1 = xo + (kRowTile + r) * kPrefixRecStride;
+      const float l0 = h0[129], l1 = two ? h1[129] : 0.f;
+      const float m0 = l0 > 0.f ? h0[128] : -INFINITY, m1 = l1 > 0.f ? h1[128] : -INFINITY;
+      const float M = fmaxf(m0, m1);
+      const float w0 = l0 > 0.f ? l0 * fast_exp2(m0 - M) : 0.f;
+      const float w1 = l1 > 0.f ? l1 * fast_exp2(m1 - M) : 0.f;
+      const float W = w0 + w1;
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (w0 > 0.f) {
+        const float4 a = reinterpret_cast<const float4*>(h0)[lane];
+        o = make_float4(a.x * w0, a.y * w0, a.z * w0, a.w * w0);
+      }
+      if (w1 > 0.f) {
+        const float4 b = reinterpret_cast<const float4*>(h1)[lane];
+        o = make_float4(fmaf(b.x, w1, o.x), fmaf(b.y, w1, o.y), fmaf(b.z, w1, o.z),
+                        fmaf(b.w, w1, o.w));
+      }
+      const int rr = row0 + r;
+      const int64_t orow = (static_cast<int64_t>(seq) + rr / G) * p.Hq + kvh * G + rr % G;
+      const uint32_t lo16 = f32_to_bf16_bits(o.x * inv) | (uint32_t(f32_to_bf16_bits(o.y * inv)) << 16);
+      const uint32_t hi16 = f32_to_bf16_bits(o.z * inv) | (uint32_t(f32_to_bf16_bits(o.w * inv)) << 16);
+      *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + lane * 4) = make_uint2(lo16, hi16);
+    }
   }
 }
 

@@ -27,6 +27,17 @@ struct PrefixParams {
   int32_t chunk_keys;            // positions per chunk, a multiple of 128
   int32_t run_rows;              // rows per TMA box: gcd(bs, 128)
   float qscale;                  // scale * log2(e)
+  // Own positions (a member's positions after its group's shared blocks),
+  // attended as extra key tiles of a group's last chunk when own_slots > 0:
+  // member k of the row block (k = row / G - first member) owns key slots
+  // [k * own_slots, k * own_slots + n_k) of those tiles, n_k = ctx - shared
+  // positions (at most own_cap), and its rows see only those slots.
+  const int32_t* ctx;            // [B] context lengths (own_slots > 0)
+  int32_t own_slots;             // slots per member, a multiple of run_rows; 0: none
+  int32_t own_cap;               // host bound on n_k (checked mode reports a larger one)
+  // fused (own_slots > 0 and one chunk per group): the CTA merges its two
+  // halves and writes the bf16 output [B][Hq][128] here instead of records
+  uint16_t* out;
   int32_t checked;
   int* err;
 };

@@ -78,11 +78,13 @@ class DeviceLayer:
         assert np.array_equal(W.to_u16(self.v_cache), self.h_v), "V cache differs"
 
 
-def shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed):
+def shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed, own_max=70,
+                        singleton_blocks=10):
     """Groups of consecutive sequences (sizes[g] members each) whose block
     tables begin with the same whole prompt blocks, then each member's own
-    blocks; some members stop exactly at the shared blocks, singletons share
-    nothing.  Block size 16, physical blocks from a seeded permutation.
+    blocks (0 .. own_max - 1 positions); some members stop exactly at the
+    shared blocks, singletons share nothing (at most singleton_blocks blocks
+    of their own).  Block size 16, physical blocks from a seeded permutation.
     Returns (batch, group starts)."""
     rng = np.random.default_rng(seed)
     bs = 16
@@ -92,8 +94,9 @@ def shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed):
     prompt = rng.integers(1, max_prompt_blocks, size=len(sizes)) * bs   # whole shared blocks
     # a singleton shares nothing: all its positions are its own (keep them
     # within the in-merge bound)
-    prompt[np.asarray(sizes) == 1] = np.minimum(prompt[np.asarray(sizes) == 1], 10 * bs)
-    own_pos = [rng.integers(0, 70, size=s) for s in sizes]
+    prompt[np.asarray(sizes) == 1] = np.minimum(prompt[np.asarray(sizes) == 1],
+                                                singleton_blocks * bs)
+    own_pos = [rng.integers(0, own_max, size=s) for s in sizes]
     own_pos[int(np.argmax(np.asarray(sizes) > 1))][0] = 0  # a member with no own positions
     ctx = np.concatenate([p + o for p, o in zip(prompt, own_pos)]).astype(np.int32)
     ctx = np.maximum(ctx, 1)

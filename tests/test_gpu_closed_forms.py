@@ -18,8 +18,9 @@ reduces to something a reader can check by eye when:
 
 Each case runs every kernel: the automatic choice, the CUDA-core split
 kernel, both tensor-core CTA shapes, the contiguous layout on the split and
-the tensor-core kernels, and the shared-prefix call in both of its
-own-position modes.  The output is compared with the closed form and with
+the tensor-core kernels, and the shared-prefix call in each of its
+own-position modes (a second tensor-core pass, CUDA cores in the merge, and
+masked key tiles of the prefix kernel, which then writes the output).  The output is compared with the closed form and with
 the fp64 oracle at |err| <= 1e-2 + 1e-2 |ref| per element; the closed form
 is first checked against the oracle, so the inputs really realise it.
 Expected values are computed from the host inputs alone."""
@@ -38,12 +39,12 @@ DEV = torch.device("cuda:0")
 
 FORMS = ["identical_keys", "zero_query", "zero_scale", "constant_v", "dominant_logit", "scale_2"]
 MODES = ["auto", "split", "tc_8x3", "tc_12x2", "contig_split", "contig_tc", "shared_tc_pass",
-         "shared_in_merge"]
+         "shared_in_merge", "shared_own_tiles"]
 HEADS = [(32, 8), (56, 8), (32, 4)]
 VARIANT = {"auto": pkv.VARIANT_AUTO, "split": pkv.VARIANT_SPLIT, "tc_8x3": pkv.VARIANT_TC_8X3,
            "tc_12x2": pkv.VARIANT_TC_12X2, "contig_split": pkv.VARIANT_SPLIT,
            "contig_tc": pkv.VARIANT_TC_12X2, "shared_tc_pass": pkv.VARIANT_AUTO,
-           "shared_in_merge": pkv.VARIANT_AUTO}
+           "shared_in_merge": pkv.VARIANT_AUTO, "shared_own_tiles": pkv.VARIANT_AUTO}
 # contexts from one position to many tiles; with a tensor-core variant forced
 # the few tiles spread over every SM, so pairs are cut by many CTA ranges
 CTX = [1, 2, 15, 16, 17, 100, 257, 700, 1500]
@@ -141,7 +142,7 @@ def _run(mode, L, b, starts, scale):
     if mode.startswith("shared"):
         shared = W.shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
         own = -1
-        if mode == "shared_in_merge":
+        if mode in ("shared_in_merge", "shared_own_tiles"):
             per_seq = np.repeat(shared, np.diff(starts)) * b.block_size
             own = int((b.ctx - per_seq).max())
         out = pkv.paged_decode_attention_shared(
@@ -160,7 +161,12 @@ def _run(mode, L, b, starts, scale):
 @pytest.mark.parametrize("form", FORMS)
 def test_closed_form(form, mode, hq, hkv):
     seed = 1000 + 17 * FORMS.index(form) + hq + hkv
-    if mode.startswith("shared"):
+    if mode == "shared_own_tiles":
+        # few own positions: they ride as masked key tiles of the prefix
+        # kernel, which (one chunk per group here) writes the output itself
+        b, starts = shared_groups_batch(hq, hkv, [1, 2, 3, 4], 40, seed, own_max=20,
+                                        singleton_blocks=1)
+    elif mode.startswith("shared"):
         # groups of 1..4 sequences over shared prompt blocks of up to 40 blocks
         b, starts = shared_groups_batch(hq, hkv, [1, 2, 3, 4], 40, seed)
     else:

@@ -49,16 +49,21 @@ def _run(b, starts, shared, L, own=-1):
 OWN = ["tensor_core_pass", "in_merge"]
 
 
-@pytest.mark.parametrize("own", OWN)
+@pytest.mark.parametrize("own", OWN + ["own_tiles"])
 @pytest.mark.parametrize("step", [0, 1, 63])
 def test_yi34b_sharing_scenario(step, own):
+    """The exact own bound (<= 79 positions, 4 members) puts the own positions
+    in masked key tiles of the prefix kernel, which with one chunk per group
+    writes the output itself; a loose bound of 256 keeps them in the merge."""
     sc = W.sharing_scenario()
     b = sc.steps[step]
     L = DeviceLayer(b, 0, DEV, fast_cache=True)
     starts = np.arange(0, b.B + 1, sc.n)
     shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
     assert shared.min() > 0
-    out = _run(b, starts, shared, L, -1 if own == OWN[0] else own_bound(b, starts, shared))
+    bound = {"tensor_core_pass": -1, "in_merge": 256,
+             "own_tiles": own_bound(b, starts, shared)}[own]
+    out = _run(b, starts, shared, L, bound)
     ref = L.gpu_attend()
     torch.cuda.synchronize()
     assert_attention_close(out, ref.float().cpu().numpy().astype(np.float64), "vs regular call")
@@ -67,7 +72,11 @@ def test_yi34b_sharing_scenario(step, own):
 
 
 def _synthetic(hq, hkv, own, sizes, max_prompt_blocks, seed):
-    b, starts = shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed)
+    if own == "own_tiles":  # few own positions: masked key tiles of the prefix kernel
+        b, starts = shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed, own_max=12,
+                                        singleton_blocks=0)
+    else:
+        b, starts = shared_groups_batch(hq, hkv, sizes, max_prompt_blocks, seed)
     L = DeviceLayer(b, 0, DEV)
     shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
     bound = own_bound(b, starts, shared)
@@ -77,7 +86,7 @@ def _synthetic(hq, hkv, own, sizes, max_prompt_blocks, seed):
                            % (hq // hkv, sizes))
 
 
-@pytest.mark.parametrize("own", OWN)
+@pytest.mark.parametrize("own", OWN + ["own_tiles"])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (28, 4), (32, 4)])
 def test_synthetic_groups(hq, hkv, own):
     """Groups of 1..5 sequences over one prompt each: members have their own
@@ -86,7 +95,7 @@ def test_synthetic_groups(hq, hkv, own):
     _synthetic(hq, hkv, own, [1, 2, 3, 4, 5, 1, 3], 40, hq * 10 + hkv)
 
 
-@pytest.mark.parametrize("own", OWN)
+@pytest.mark.parametrize("own", OWN + ["own_tiles"])
 def test_large_groups_and_long_shared_prompts(own):
     """A group of 24 members at G = 8 (192 rows: two row blocks of the prefix
     kernel) and shared prompts of up to 600 blocks (several chunks of the
@@ -94,16 +103,18 @@ def test_large_groups_and_long_shared_prompts(own):
     _synthetic(32, 4, own, [24, 2, 1, 5], 600, 77)
 
 
-def test_checked_mode_reports_an_uncovered_member():
+@pytest.mark.parametrize("own", ["tensor_core_pass", "own_tiles"])
+def test_checked_mode_reports_an_uncovered_member(own):
     pkv.set_checked(True)
     sc = W.sharing_scenario(num_prompts=4, decode_steps=1)
     b = sc.steps[0]
     L = DeviceLayer(b, 0, DEV, fast_cache=True)
     starts = np.arange(0, b.B + 1, sc.n)
     shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
+    bound = own_bound(b, starts, shared)
     shared[0] = int(b.ctx[:sc.n].max() // b.block_size) + 1   # beyond every member's context
     assert pkv.get_device_error() == "none"
-    _run(b, starts, shared, L)
+    _run(b, starts, shared, L, -1 if own == "tensor_core_pass" else bound)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == "context"
 
@@ -123,3 +134,25 @@ def test_checked_mode_reports_an_own_part_beyond_the_bound():
     _run(b, starts, shared, L, bound - 1)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == "context"
+
+
+def test_launch_count_follows_the_own_mode():
+    """The Yi-34B sharing step: the exact own bound makes the call one launch
+    (own key tiles, one chunk per group), a loose bound of 256 two (prefix
+    kernel, merge), no bound four (prep, prefix kernel, tensor-core pass,
+    merge); a rejected shape reports -1."""
+    sc = W.sharing_scenario()
+    b = sc.steps[0]
+    starts = np.arange(0, b.B + 1, sc.n)
+    shared = shared_prefix_blocks(b.block_tables, b.ctx, b.block_size, starts)
+    sh = b.shape
+
+    def launches(own, bs=b.block_size):
+        return pkv.shared_decode_launches(b.B, len(starts) - 1, sc.n, b.block_tables.shape[1],
+                                          b.max_context, bs, own, sh.num_q_heads,
+                                          sh.num_kv_heads)
+
+    assert launches(own_bound(b, starts, shared)) == 1
+    assert launches(256) == 2
+    assert launches(-1) == 4
+    assert launches(16, bs=8) == -1
