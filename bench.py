@@ -289,11 +289,11 @@ class DeviceWorkload:
                          "positions, cascade_merge_kernel")
 
     def launches_per_step(self):
-        # per layer kv_append and the attention call's kernels (the tensor-core
-        # kernel alone, merging its split pairs itself; the split kernel and its
-        # combine; the shared-prefix call's kernels as the library reports
-        # them), plus one block copy launch (all layers) when the step copies
-        # on write
+        # per layer: the decode step's kernels (the tensor-core kernel alone,
+        # which does the append and merges its split pairs itself; else the
+        # append, the split kernel and its combine), or the append and the
+        # shared-prefix call's kernels as the library reports them; plus one
+        # block copy launch (all layers) when the step copies on write
         cow = 0 if self.cow is None else 1
         if self.groups is not None:
             gs, sb, n, own = self.groups
@@ -303,7 +303,7 @@ class DeviceWorkload:
                 b.block_size, own, self.shape.num_q_heads, self.shape.num_kv_heads)
             return self.shape.num_layers * (1 + attn) + cow
         if self.uses_tc:
-            return self.shape.num_layers * 2 + cow
+            return self.shape.num_layers + cow
         return self.shape.num_layers * (2 + (1 if self.nsplit > 1 else 0)) + cow
 
     def copy_on_write(self, pairs=None):
@@ -451,8 +451,9 @@ def run_gpu(args, world, rank, local):
                            + ("per layer: kv_append + paged_decode_attention_shared (each "
                               "group's shared prompt blocks read once for all its branches)"
                               if wl.groups is not None
-                              else "per layer: paged_decode_step = kv_append + "
-                              "paged_decode_attention in one C-ABI call")},
+                              else "per layer: paged_decode_step (kv_append + "
+                              "paged_decode_attention; with the tensor-core kernel one launch "
+                              "that also appends)")},
         "hbm_tbs": round(achieved_gbs / 1e3, 4),
         "hbm_pct_of_8tbs": round(100 * achieved_gbs / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,

@@ -165,13 +165,19 @@ PKV_API pkv_status pkv_contig_decode_attention(
  *   pkv_paged_decode_attention(q, k_cache, v_cache, ..., stream);
  * (contiguous: block_size = S, num_slots = max_reqs * S and
  * pkv_contig_decode_attention), with one new token per sequence (k_new,
- * v_new [num_seqs][Hkv][128]).  All arguments are checked before anything is
- * launched.  The attention kernel starts while the append runs: it reads q,
- * context_lens and block_tables (req_ids) at once and waits for the append
- * only before it loads K/V, so none of those, nor out, may alias k_new, v_new
- * or the caches (they never do in a decode step).  Errors as for the two
- * calls.  The pages have no counterpart beyond the two operations it
- * combines.
+ * v_new [num_seqs][Hkv][128]), as long as slot_mapping[i] is the slot of
+ * sequence i's newest position context_lens[i] - 1, or negative (no new
+ * token): when the tensor-core kernel runs (the automatic choice for all
+ * but small batches), it does the append itself, in the same launch, and
+ * takes that position's K and V from k_new / v_new instead of from the
+ * cache (the same bytes); checked mode reports a slot that is not that
+ * position's (PKV_DEVERR_SLOT).  Otherwise the append kernel runs first and
+ * the attention kernel starts while it runs: it reads q, context_lens and
+ * block_tables (req_ids) at once and waits for the append only before it
+ * loads K/V.  Either way none of those, nor out, may alias k_new, v_new or
+ * the caches (they never do in a decode step).  All arguments are checked
+ * before anything is launched.  Errors as for the two calls.  The pages
+ * have no counterpart beyond the two operations it combines.
  */
 PKV_API pkv_status pkv_paged_decode_step(
     const int64_t *slot_mapping, const void *k_new, const void *v_new,

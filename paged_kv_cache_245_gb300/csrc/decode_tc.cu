@@ -80,7 +80,7 @@ int tc_chunk_seqs(int max_context) {
 
 namespace {
 
-template <bool kContig, int W, int S, int NT = 1>
+template <bool kContig, int W, int S, bool kFuse, int NT = 1>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,
                        int num_ctas, cudaStream_t stream) {
   using L = TcSmem<W, S, NT>;
@@ -89,7 +89,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  auto kernel = decode_tc_kernel<kContig, W, S, NT>;
+  auto kernel = decode_tc_kernel<kContig, W, S, NT, kFuse>;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
     if (e != cudaSuccess) return e;
@@ -103,6 +103,11 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     p.out += static_cast<int64_t>(s0) * p.Hq * kHeadDim;
     if (p.rec_out != nullptr) p.rec_out += static_cast<int64_t>(s0) * p.Hq * kRecStride;
     p.ctx_lens += s0;
+    if (p.slot_mapping != nullptr) {
+      p.slot_mapping += s0;
+      p.k_new += static_cast<int64_t>(s0) * p.Hkv * kHeadDim;
+      p.v_new += static_cast<int64_t>(s0) * p.Hkv * kHeadDim;
+    }
     if (kContig) p.req_ids += s0;
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
     // the first chunk of a decode step starts while the append runs
@@ -150,12 +155,19 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
   cudaError_t e;
   if (p.G > kTcHeads) {  // one n-tile of 8 query heads per KV head (the API allows G <= 8)
     e = cudaErrorInvalidValue;
+  } else if (p.slot_mapping != nullptr) {  // the decode step with its append
+    if (contig)
+      e = cfg == 1 ? launch_cfg<true, 12, 2, true>(tk, tv, p, num_ctas, stream)
+                   : launch_cfg<true, 8, 3, true>(tk, tv, p, num_ctas, stream);
+    else
+      e = cfg == 1 ? launch_cfg<false, 12, 2, true>(tk, tv, p, num_ctas, stream)
+                   : launch_cfg<false, 8, 3, true>(tk, tv, p, num_ctas, stream);
   } else if (contig) {
-    e = cfg == 1 ? launch_cfg<true, 12, 2>(tk, tv, p, num_ctas, stream)
-                 : launch_cfg<true, 8, 3>(tk, tv, p, num_ctas, stream);
+    e = cfg == 1 ? launch_cfg<true, 12, 2, false>(tk, tv, p, num_ctas, stream)
+                 : launch_cfg<true, 8, 3, false>(tk, tv, p, num_ctas, stream);
   } else {
-    e = cfg == 1 ? launch_cfg<false, 12, 2>(tk, tv, p, num_ctas, stream)
-                 : launch_cfg<false, 8, 3>(tk, tv, p, num_ctas, stream);
+    e = cfg == 1 ? launch_cfg<false, 12, 2, false>(tk, tv, p, num_ctas, stream)
+                 : launch_cfg<false, 8, 3, false>(tk, tv, p, num_ctas, stream);
   }
   *cuda_err = e;
   return e == cudaSuccess ? TcStatus::kOk : TcStatus::kCudaError;

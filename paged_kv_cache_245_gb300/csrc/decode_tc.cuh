@@ -91,6 +91,19 @@ __device__ __forceinline__ bool tc_range_nonempty(int cc, int64_t V, int64_t P) 
   return tc_range_lo(cc, V, P) < tc_range_lo(cc + 1, V, P);
 }
 
+// Asynchronous global -> shared copies (cp.async, generic proxy): 16, 8 and
+// 4 bytes, aligned to their size; wait_all waits for this thread's own.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // One query head's result, from lane's four output elements: bf16 output,
 // or an (o, m, l) record in record mode.
 __device__ __forceinline__ void tc_write_out(const TcParams& p, int seq, int qh, int lane,
@@ -248,8 +261,9 @@ __device__ __forceinline__ bool tc_merge_pieces(const TcParams& p, int seq, int 
 }
 
 // NT n-tiles of 8 query heads per KV head (instantiated with NT = 1: GQA
-// groups of up to 8 query heads).
-template <bool kContig, int W, int S, int NT>
+// groups of up to 8 query heads).  kFuse: the decode step's append is done
+// here too (p.slot_mapping).
+template <bool kContig, int W, int S, int NT, bool kFuse>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const TcParams p) {
@@ -404,6 +418,22 @@ __global__ void __launch_bounds__(W * 32, 1)
     } else {
       uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(i) * p.Hq * kHeadDim);
       for (int k = tid; k < p.Hq * kHeadDim / 8; k += W * 32) o[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (kFuse) {  // the fused append of a sequence with no tile to take it
+      const int64_t slot = p.slot_mapping[i];
+      if (slot >= 0 && p.checked && slot >= p.num_slots) {
+        if (tid == 0) record_error(p.err, kErrSlot);
+      } else if (slot >= 0) {
+        for (int k = tid; k < p.Hkv * 32; k += W * 32) {  // (KV head, tensor, 16-byte chunk)
+          const int h = k >> 5, ch = k & 15;
+          const bool is_v = (k & 16) != 0;
+          *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) +
+                                    cache_row(slot / p.bs, h, p.Hkv, p.bs, slot % p.bs) * kHeadDim +
+                                    ch * 8) =
+              ld_global_nc_v4((is_v ? p.v_new : p.k_new) +
+                              (static_cast<int64_t>(i) * p.Hkv + h) * kHeadDim + ch * 8);
+        }
+      }
     }
   }
   const int64_t lo = range[0];
@@ -571,6 +601,25 @@ __global__ void __launch_bounds__(W * 32, 1)
     if (!whole) tc_pair_ctas(seg, prefix, p.Hkv, p.seg_cost, V, P, &cf, &cl);
     const bool head_piece = !whole && cf == c;
 
+    // The fused append (slot_mapping): the warp that takes the pair's last
+    // tile (position ctx - 1) brings the new rows into its merge slot, idle
+    // until the segment's end (lanes 0-15 K, 16-31 V, 16 bytes each; then the
+    // slot and, checked, the table entry of position ctx - 1), writes them to
+    // the cache and over that row of the tile.
+    const int64_t x_last = seg.pend - 1;
+    const bool own_last = kFuse && x_last >= seg.x0 && x_last < seg.x1 &&
+                          (x_last - seg.x0) % W == warp;
+    unsigned char* fuse_s = reinterpret_cast<unsigned char*>(merge + warp * kTcMergeHeads * kRecStride);
+    if (own_last) {
+      const int64_t pr = static_cast<int64_t>(seg.seq) * p.Hkv + seg.kvh;
+      cp_async_16(fuse_s + lane * 16,
+                  (lane < 16 ? p.k_new : p.v_new) + pr * kHeadDim + (lane & 15) * 8);
+      if (lane == 0) cp_async_8(fuse_s + 512, p.slot_mapping + seg.seq);
+      if (lane == 1 && p.checked && !kContig)
+        cp_async_4(fuse_s + 520,
+                   p.block_tables + static_cast<int64_t>(seg.seq) * p.max_blocks + (ctx - 1) / p.bs);
+    }
+
     for (int64_t x = seg.x0 + warp; x < seg.x1 && !dead; x += W) {
       if (x == seg.x0 + warp) {  // this warp's first tile of the segment
         if (qn_pair == seg.pstart) {
@@ -598,6 +647,35 @@ __global__ void __launch_bounds__(W * 32, 1)
       const uint32_t kaddr = smem_addr(st);
       const uint32_t vaddr = kaddr + 2 * kBoxBytes;
       const int nvalid = min(16, ctx - static_cast<int>((x - seg.pstart) * 16));
+      if (own_last && x == x_last) {  // the new rows: into the cache and over row nvalid - 1
+        cp_async_wait_all();
+        __syncwarp();
+        const int64_t slot = *reinterpret_cast<const int64_t*>(fuse_s + 512);
+        bool ok = slot >= 0;
+        if (ok && p.checked) {
+          int64_t want;  // the slot of position ctx - 1
+          if (kContig) {
+            want = static_cast<int64_t>(req_s[seg.seq]) * p.bs + ctx - 1;
+          } else {
+            want = static_cast<int64_t>(*reinterpret_cast<const int32_t*>(fuse_s + 520)) * p.bs +
+                   (ctx - 1) % p.bs;
+          }
+          if (slot >= p.num_slots || slot != want) {
+            if (lane == 0) record_error(p.err, kErrSlot);
+            ok = false;
+          }
+        }
+        if (ok) {
+          const uint4 v = *reinterpret_cast<const uint4*>(fuse_s + lane * 16);
+          const int r = nvalid - 1, ch = lane & 15;
+          *reinterpret_cast<uint4*>((lane < 16 ? p.k_cache : p.v_cache) +
+                                    cache_row(slot / p.bs, seg.kvh, p.Hkv, p.bs, slot % p.bs) *
+                                        kHeadDim + ch * 8) = v;
+          *reinterpret_cast<uint4*>(st + (lane < 16 ? 0 : 2 * kBoxBytes) + (ch >> 3) * kBoxBytes +
+                                    r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+        }
+        __syncwarp();
+      }
 
       if (nvalid < 16) {  // rows past the context must not feed p.V (0 * NaN)
         for (int idx = lane; idx < (16 - nvalid) * 16; idx += 32) {

@@ -32,6 +32,18 @@ struct TcParams {
   int32_t stall_test;       // test hook: CTA 0's warp 0 expects 16 bytes that never come
   int32_t drop_record_test; // test hook: CTA 1 writes no piece record
   int32_t early_inputs;     // previous kernel is the append: read inputs before the wait
+  // The decode step's append, fused (slot_mapping non-null): sequence i's
+  // new K/V rows k_new / v_new [B][Hkv][128] go to slot slot_mapping[i]
+  // (negative: none) of the caches, and its attention reads them for
+  // position ctx_i - 1 from the inputs rather than from the cache -- the same
+  // bytes, so the same result as the append followed by the attention, as
+  // long as the slot is that position's (checked mode verifies it).
+  const int64_t* slot_mapping;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_cache;        // the caches (written: the new rows only)
+  uint16_t* v_cache;
+  int64_t num_slots;        // checked mode: slots in [0, num_slots)
   int* err;
 };
 

@@ -149,15 +149,27 @@ size_t decode_workspace_need(int32_t num_seqs, const pkv_heads& h, int32_t max_c
   return split > tc ? split : tc;
 }
 
+// A decode step's append, for the tensor-core kernel to do itself.
+struct FusedAppend {
+  const int64_t* slot_mapping;
+  const void* k_new;
+  const void* v_new;
+  int64_t num_slots;
+};
+
 // Validates a decode call and, unless dry_run, launches it.  after_append: the
 // previous kernel in the stream is this step's append (plain launch), so the
-// tensor-core kernel may read its inputs before waiting for it.
+// tensor-core kernel may read its inputs before waiting for it.  fused (the
+// tensor-core kernel only): the step's append done by the attention kernel.
+// *tc_out: whether the tensor-core kernel is (or would be) the one launched.
 pkv_status decode_common(bool contig, const void* q, const void* k, const void* v,
                          const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
                          const int32_t* req_ids, int32_t max_reqs, const int32_t* context_lens,
                          int32_t num_seqs, int32_t max_context, int64_t bs_or_S, float scale,
                          pkv_heads h, void* out, void* workspace, size_t workspace_bytes,
-                         void* stream, bool dry_run = false, bool after_append = false) {
+                         void* stream, bool dry_run = false, bool after_append = false,
+                         bool* tc_out = nullptr, const FusedAppend* fused = nullptr) {
+  if (tc_out) *tc_out = false;
   pkv_status st = check_heads(h);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_context < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
@@ -203,6 +215,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
                              ((static_cast<int64_t>(max_context) + 15) / 16);
   const bool tc_pick = variant >= 2 || (variant == 0 && tile_bound >= 32LL * tc_ctas(sms));
   if (tc_pick && tc_ok) {
+    if (tc_out) *tc_out = true;
     const size_t need = pkv::tc_workspace_bytes(tc_ctas(sms));
     if (!workspace || workspace_bytes < need)
       return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need,
@@ -230,6 +243,14 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     t.stall_test = g_stall_test.exchange(0);
     t.drop_record_test = g_drop_record_test.exchange(0);
     t.early_inputs = after_append ? 1 : 0;
+    if (fused != nullptr) {
+      t.slot_mapping = fused->slot_mapping;
+      t.k_new = static_cast<const uint16_t*>(fused->k_new);
+      t.v_new = static_cast<const uint16_t*>(fused->v_new);
+      t.k_cache = static_cast<uint16_t*>(const_cast<void*>(k));
+      t.v_cache = static_cast<uint16_t*>(const_cast<void*>(v));
+      t.num_slots = fused->num_slots;
+    }
     t.err = err;
     cudaError_t ce = cudaSuccess;
     const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total,
@@ -287,7 +308,8 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
 // PKV_PDL says (the append of a decode step).
 pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const void* k,
                          const void* v, void* k_cache, void* v_cache, int64_t num_slots,
-                         int64_t block_size, pkv_heads heads, void* stream, bool plain) {
+                         int64_t block_size, pkv_heads heads, void* stream, bool plain,
+                         bool dry_run = false) {
   if (heads.num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads must be positive");
   if (heads.head_dim != pkv::kHeadDim)
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (only 128 is built)", heads.head_dim);
@@ -316,6 +338,7 @@ pkv_status append_common(const int64_t* slot_mapping, int64_t num_tokens, const 
   p.err = err;
   const int64_t rows = 2 * num_tokens * heads.num_kv_heads;
   if ((rows + 15) / 16 > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens");
+  if (dry_run) return PKV_OK;
   const cudaError_t e = pkv::launch_kv_append(p, static_cast<cudaStream_t>(stream), plain);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return PKV_OK;
@@ -492,14 +515,25 @@ pkv_status pkv_paged_decode_step(const int64_t* slot_mapping, const void* k_new,
                                  int32_t num_seqs, int32_t max_context, int32_t block_size,
                                  float scale, pkv_heads heads, void* out, void* workspace,
                                  size_t workspace_bytes, void* stream) {
+  bool tc = false;
   pkv_status st = decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                 num_blocks, nullptr, 0, context_lens, num_seqs, max_context,
                                 block_size, scale, heads, out, workspace, workspace_bytes, stream,
-                                true);
+                                true, false, &tc);
   if (st != PKV_OK || num_seqs == 0) return st;
-  st = append_common(slot_mapping, num_seqs, k_new, v_new, k_cache, v_cache,
-                     static_cast<int64_t>(num_blocks) * block_size, block_size, heads, stream,
-                     true);
+  const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
+  if (tc) {  // one launch: the tensor-core kernel does the append too
+    st = append_common(slot_mapping, num_seqs, k_new, v_new, k_cache, v_cache, num_slots,
+                       block_size, heads, stream, true, true);
+    if (st != PKV_OK) return st;
+    const FusedAppend fa{slot_mapping, k_new, v_new, num_slots};
+    return decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                         num_blocks, nullptr, 0, context_lens, num_seqs, max_context, block_size,
+                         scale, heads, out, workspace, workspace_bytes, stream, false, false,
+                         nullptr, &fa);
+  }
+  st = append_common(slot_mapping, num_seqs, k_new, v_new, k_cache, v_cache, num_slots,
+                     block_size, heads, stream, true);
   if (st != PKV_OK) return st;
   return decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq, num_blocks,
                        nullptr, 0, context_lens, num_seqs, max_context, block_size, scale, heads,
@@ -513,12 +547,23 @@ pkv_status pkv_contig_decode_step(const int64_t* slot_mapping, const void* k_new
                                   int32_t max_context, int64_t S, float scale, pkv_heads heads,
                                   void* out, void* workspace, size_t workspace_bytes,
                                   void* stream) {
+  bool tc = false;
   pkv_status st = decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs,
                                 context_lens, num_seqs, max_context, S, scale, heads, out,
-                                workspace, workspace_bytes, stream, true);
+                                workspace, workspace_bytes, stream, true, false, &tc);
   if (st != PKV_OK || num_seqs == 0) return st;
-  st = append_common(slot_mapping, num_seqs, k_new, v_new, k_buf, v_buf,
-                     static_cast<int64_t>(max_reqs) * S, S, heads, stream, true);
+  const int64_t num_slots = static_cast<int64_t>(max_reqs) * S;
+  if (tc) {  // one launch: the tensor-core kernel does the append too
+    st = append_common(slot_mapping, num_seqs, k_new, v_new, k_buf, v_buf, num_slots, S, heads,
+                       stream, true, true);
+    if (st != PKV_OK) return st;
+    const FusedAppend fa{slot_mapping, k_new, v_new, num_slots};
+    return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
+                         num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
+                         stream, false, false, nullptr, &fa);
+  }
+  st = append_common(slot_mapping, num_seqs, k_new, v_new, k_buf, v_buf, num_slots, S, heads,
+                     stream, true);
   if (st != PKV_OK) return st;
   return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
                        num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,

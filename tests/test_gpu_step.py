@@ -147,3 +147,46 @@ def test_bad_attention_argument_launches_nothing():
                               L.ctx, too_long, L.scale)
     torch.cuda.synchronize()
     assert torch.equal(L.k_cache, k0) and torch.equal(L.v_cache, v0)
+
+
+@pytest.mark.parametrize("variant", [pkv.VARIANT_TC_8X3, pkv.VARIANT_TC_12X2])
+def test_step_with_sequences_without_a_new_token(variant):
+    """With the tensor-core kernel the step is one launch that also does the
+    append; a negative slot means no new token for that sequence: its
+    attention then reads the cache as it stands, as after the two calls."""
+    pkv.set_decode_variant(variant)
+    b, _ = _case("small")
+    L = DeviceLayer(b, 0, DEV)
+    slots = L.slots.clone()
+    slots[1::2] = -1
+    k0, v0 = L.k_cache.clone(), L.v_cache.clone()
+    pkv.kv_append(slots, L.k_new, L.v_new, L.k_cache, L.v_cache)
+    ref = pkv.paged_decode_attention(L.q, L.k_cache, L.v_cache, L.tables, L.ctx, b.max_context,
+                                     L.scale)
+    torch.cuda.synchronize()
+    kr, vr = L.k_cache.clone(), L.v_cache.clone()
+    L.k_cache.copy_(k0)
+    L.v_cache.copy_(v0)
+    out = pkv.paged_decode_step(slots, L.k_new, L.v_new, L.q, L.k_cache, L.v_cache, L.tables,
+                                L.ctx, b.max_context, L.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(L.k_cache, kr) and torch.equal(L.v_cache, vr), "caches differ"
+    assert torch.equal(out, ref), "output differs from the two calls"
+
+
+def test_step_reports_a_slot_that_is_not_the_last_position():
+    """Checked mode: with the append inside the tensor-core kernel, a slot in
+    range that is not the sequence's position ctx - 1 is reported (the
+    attention would read the new token there)."""
+    pkv.set_checked(True)
+    pkv.set_decode_variant(pkv.VARIANT_TC_12X2)
+    b, _ = _case("small")
+    L = DeviceLayer(b, 0, DEV)
+    slots = L.slots.clone()
+    i = int(np.argmax(b.ctx > 100))   # a sequence with several blocks
+    slots[i] = slots[i] - 1           # the position before its last
+    assert pkv.get_device_error() == "none"
+    pkv.paged_decode_step(slots, L.k_new, L.v_new, L.q, L.k_cache, L.v_cache, L.tables, L.ctx,
+                          b.max_context, L.scale)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == "slot"
