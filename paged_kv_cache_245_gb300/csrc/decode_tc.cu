@@ -110,10 +110,8 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcPar
     }
     if (kContig) p.req_ids += s0;
     else p.block_tables += static_cast<int64_t>(s0) * p.max_blocks;
-    // the first chunk of a decode step starts while the append runs
-    p.early_inputs = s0 == 0 ? p0.early_inputs : 0;
     p.tag = next_launch_tag();  // every launch writes its piece records under a fresh tag
-    e = launch_pdl_if(p.early_inputs != 0 || pdl_decode_enabled(), kernel, dim3(num_ctas), dim3(W * 32),
+    e = launch_pdl_if(pdl_decode_enabled(), kernel, dim3(num_ctas), dim3(W * 32),
                       L::kTotal, stream, tk, tv, p);
     if (e != cudaSuccess) return e;
   }

@@ -298,15 +298,9 @@ __global__ void __launch_bounds__(W * 32, 1)
   }
   // Programmatic dependent launch (no-ops without the launch attribute):
   // wait for the previous kernel in the stream to finish before reading any
-  // input, then let the next kernel get scheduled.  In a decode step whose
-  // previous kernel is the append (early_inputs), q, context_lens, req_ids
-  // and the block tables were complete before it started and only the
-  // caches are still being written: the prologue reads them at once and the
-  // wait comes just before the first K/V load.
-  if (!p.early_inputs) {
-    grid_dependency_wait();
-    grid_dependency_trigger();
-  }
+  // input, then let the next kernel get scheduled.
+  grid_dependency_wait();
+  grid_dependency_trigger();
 
   // ---- tile counts and their prefix over sequences (every CTA, once)
   for (int i = tid; i < B; i += W * 32) {
@@ -439,10 +433,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   const int64_t lo = range[0];
   const int64_t hi = range[1];
   const int64_t V = tc_vseq(prefix, B, p.Hkv, p.seg_cost);  // units of the whole partition
-  if (lo >= hi) {  // uniform across the CTA
-    if (p.early_inputs) grid_dependency_wait();  // never finish before the append
-    return;
-  }
+  if (lo >= hi) return;  // uniform across the CTA
 
   const uint64_t policy = l2_policy_evict_first();
   unsigned char* stage0 = smem + L::kStagesOff + warp * S * kTcStageBytes;
@@ -551,10 +542,6 @@ __global__ void __launch_bounds__(W * 32, 1)
         cx = cs.x0 + warp;
       }
     }
-  }
-  if (p.early_inputs) {
-    grid_dependency_wait();
-    grid_dependency_trigger();
   }
   for (int s = 0; s < S && ivalid; ++s) {
     issue(s, __shfl_sync(kFull, pre_entry, s));

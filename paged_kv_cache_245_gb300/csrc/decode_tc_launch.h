@@ -31,7 +31,6 @@ struct TcParams {
   int32_t checked;
   int32_t stall_test;       // test hook: CTA 0's warp 0 expects 16 bytes that never come
   int32_t drop_record_test; // test hook: CTA 1 writes no piece record
-  int32_t early_inputs;     // previous kernel is the append: read inputs before the wait
   // The decode step's append, fused (slot_mapping non-null): sequence i's
   // new K/V rows k_new / v_new [B][Hkv][128] go to slot slot_mapping[i]
   // (negative: none) of the caches, and its attention reads them for

@@ -157,9 +157,7 @@ struct FusedAppend {
   int64_t num_slots;
 };
 
-// Validates a decode call and, unless dry_run, launches it.  after_append: the
-// previous kernel in the stream is this step's append (plain launch), so the
-// tensor-core kernel may read its inputs before waiting for it.  fused (the
+// Validates a decode call and, unless dry_run, launches it.  fused (the
 // tensor-core kernel only): the step's append done by the attention kernel.
 // *tc_out: whether the tensor-core kernel is (or would be) the one launched.
 pkv_status decode_common(bool contig, const void* q, const void* k, const void* v,
@@ -167,8 +165,8 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
                          const int32_t* req_ids, int32_t max_reqs, const int32_t* context_lens,
                          int32_t num_seqs, int32_t max_context, int64_t bs_or_S, float scale,
                          pkv_heads h, void* out, void* workspace, size_t workspace_bytes,
-                         void* stream, bool dry_run = false, bool after_append = false,
-                         bool* tc_out = nullptr, const FusedAppend* fused = nullptr) {
+                         void* stream, bool dry_run = false, bool* tc_out = nullptr,
+                         const FusedAppend* fused = nullptr) {
   if (tc_out) *tc_out = false;
   pkv_status st = check_heads(h);
   if (st != PKV_OK) return st;
@@ -242,7 +240,6 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     t.checked = g_checked.load();
     t.stall_test = g_stall_test.exchange(0);
     t.drop_record_test = g_drop_record_test.exchange(0);
-    t.early_inputs = after_append ? 1 : 0;
     if (fused != nullptr) {
       t.slot_mapping = fused->slot_mapping;
       t.k_new = static_cast<const uint16_t*>(fused->k_new);
@@ -519,7 +516,7 @@ pkv_status pkv_paged_decode_step(const int64_t* slot_mapping, const void* k_new,
   pkv_status st = decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                 num_blocks, nullptr, 0, context_lens, num_seqs, max_context,
                                 block_size, scale, heads, out, workspace, workspace_bytes, stream,
-                                true, false, &tc);
+                                true, &tc);
   if (st != PKV_OK || num_seqs == 0) return st;
   const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
   if (tc) {  // one launch: the tensor-core kernel does the append too
@@ -529,15 +526,15 @@ pkv_status pkv_paged_decode_step(const int64_t* slot_mapping, const void* k_new,
     const FusedAppend fa{slot_mapping, k_new, v_new, num_slots};
     return decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                          num_blocks, nullptr, 0, context_lens, num_seqs, max_context, block_size,
-                         scale, heads, out, workspace, workspace_bytes, stream, false, false,
-                         nullptr, &fa);
+                         scale, heads, out, workspace, workspace_bytes, stream, false, nullptr,
+                         &fa);
   }
   st = append_common(slot_mapping, num_seqs, k_new, v_new, k_cache, v_cache, num_slots,
                      block_size, heads, stream, true);
   if (st != PKV_OK) return st;
   return decode_common(false, q, k_cache, v_cache, block_tables, max_blocks_per_seq, num_blocks,
                        nullptr, 0, context_lens, num_seqs, max_context, block_size, scale, heads,
-                       out, workspace, workspace_bytes, stream, false, true);
+                       out, workspace, workspace_bytes, stream);
 }
 
 pkv_status pkv_contig_decode_step(const int64_t* slot_mapping, const void* k_new,
@@ -550,7 +547,7 @@ pkv_status pkv_contig_decode_step(const int64_t* slot_mapping, const void* k_new
   bool tc = false;
   pkv_status st = decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs,
                                 context_lens, num_seqs, max_context, S, scale, heads, out,
-                                workspace, workspace_bytes, stream, true, false, &tc);
+                                workspace, workspace_bytes, stream, true, &tc);
   if (st != PKV_OK || num_seqs == 0) return st;
   const int64_t num_slots = static_cast<int64_t>(max_reqs) * S;
   if (tc) {  // one launch: the tensor-core kernel does the append too
@@ -560,14 +557,14 @@ pkv_status pkv_contig_decode_step(const int64_t* slot_mapping, const void* k_new
     const FusedAppend fa{slot_mapping, k_new, v_new, num_slots};
     return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
                          num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
-                         stream, false, false, nullptr, &fa);
+                         stream, false, nullptr, &fa);
   }
   st = append_common(slot_mapping, num_seqs, k_new, v_new, k_buf, v_buf, num_slots, S, heads,
                      stream, true);
   if (st != PKV_OK) return st;
   return decode_common(true, q, k_buf, v_buf, nullptr, 0, 0, req_ids, max_reqs, context_lens,
                        num_seqs, max_context, S, scale, heads, out, workspace, workspace_bytes,
-                       stream, false, true);
+                       stream);
 }
 
 int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads, int32_t max_context) {
