@@ -80,16 +80,16 @@ int tc_chunk_seqs(int max_context) {
 
 namespace {
 
-template <bool kContig, int W, int S, bool kFuse, int NT = 1>
+template <bool kContig, int W, int S, bool kFuse, int MH = kTcMergeHeads, int NT = 1>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p0,
                        int num_ctas, cudaStream_t stream) {
-  using L = TcSmem<W, S, NT>;
+  using L = TcSmem<W, S, NT, MH>;
   static unsigned long long done_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  auto kernel = decode_tc_kernel<kContig, W, S, NT, kFuse>;
+  auto kernel = decode_tc_kernel<kContig, W, S, NT, kFuse, MH>;
   if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
     if (e != cudaSuccess) return e;
@@ -137,36 +137,37 @@ TcStatus launch_decode_tc(const TcParams& p_in, bool contig, const void* k, cons
     return TcStatus::kEncodeFailed;
   TcParams p = p_in;
   // The cost of a segment in tiles, per pass of the segment merge (4 query
-  // heads a pass: one pass up to G = 4, two above).  Per-CTA timelines grow
-  // by about 2-3 us per extra segment; sweeps of 16..48 on GB300 were fastest
-  // at 24 for one pass (the ragged batch: 24 -> 16 or 32 costs 3-4 %, the
-  // Llama-3-8B shape moves by 0.6 %) and at 48 for two (the Yi-6B shape,
-  // G = 8: 31.7 -> 30.8 us).  PKV_TC_SEG_COST overrides the per-pass cost
-  // (0: an even split of the tiles alone).
+  // heads a pass, or 8 with cfg 2).  Per-CTA timelines grow by about 2-3 us
+  // per extra segment; sweeps of 16..48 on GB300 were fastest at 24 for one
+  // pass (the ragged batch: 24 -> 16 or 32 costs 3-4 %, the Llama-3-8B shape
+  // moves by 0.6 %; the Yi-6B shape in one pass of 8 heads: 29.0 / 28.8 /
+  // 29.0 us at 16 / 24 / 32) and at 48 for two.  PKV_TC_SEG_COST overrides
+  // the per-pass cost (0: an even split of the tiles alone).
   static const int seg_cost = [] {
     const char* v = getenv("PKV_TC_SEG_COST");
     const int x = v != nullptr ? atoi(v) : 24;
     return x < 0 ? 0 : (x > 2048 ? 2048 : x);
   }();
-  p.seg_cost = seg_cost * ((p.G + kTcMergeHeads - 1) / kTcMergeHeads);
+  // cfg 2 (groups of more than 4 query heads): 10 warps x 2 stages, whose
+  // shared memory holds every warp's partials of all 8 heads: one merge pass
+  const int mh = cfg == 2 && p.G > kTcMergeHeads ? 8 : kTcMergeHeads;
+  p.seg_cost = seg_cost * ((p.G + mh - 1) / mh);
   p.rec = static_cast<uint64_t*>(workspace);
   cudaError_t e;
+  const bool fuse = p.slot_mapping != nullptr;  // the decode step with its append
+#define PKV_TC_LAUNCH(C, W, S, F, M) launch_cfg<C, W, S, F, M>(tk, tv, p, num_ctas, stream)
+#define PKV_TC_PICK(C, F)                                                             \
+  (mh == 8 ? PKV_TC_LAUNCH(C, 10, 2, F, 8)                                            \
+           : (cfg == 0 ? PKV_TC_LAUNCH(C, 8, 3, F, 4) : PKV_TC_LAUNCH(C, 12, 2, F, 4)))
   if (p.G > kTcHeads) {  // one n-tile of 8 query heads per KV head (the API allows G <= 8)
     e = cudaErrorInvalidValue;
-  } else if (p.slot_mapping != nullptr) {  // the decode step with its append
-    if (contig)
-      e = cfg == 1 ? launch_cfg<true, 12, 2, true>(tk, tv, p, num_ctas, stream)
-                   : launch_cfg<true, 8, 3, true>(tk, tv, p, num_ctas, stream);
-    else
-      e = cfg == 1 ? launch_cfg<false, 12, 2, true>(tk, tv, p, num_ctas, stream)
-                   : launch_cfg<false, 8, 3, true>(tk, tv, p, num_ctas, stream);
-  } else if (contig) {
-    e = cfg == 1 ? launch_cfg<true, 12, 2, false>(tk, tv, p, num_ctas, stream)
-                 : launch_cfg<true, 8, 3, false>(tk, tv, p, num_ctas, stream);
+  } else if (fuse) {
+    e = contig ? PKV_TC_PICK(true, true) : PKV_TC_PICK(false, true);
   } else {
-    e = cfg == 1 ? launch_cfg<false, 12, 2, false>(tk, tv, p, num_ctas, stream)
-                 : launch_cfg<false, 8, 3, false>(tk, tv, p, num_ctas, stream);
+    e = contig ? PKV_TC_PICK(true, false) : PKV_TC_PICK(false, false);
   }
+#undef PKV_TC_PICK
+#undef PKV_TC_LAUNCH
   *cuda_err = e;
   return e == cudaSuccess ? TcStatus::kOk : TcStatus::kCudaError;
 }

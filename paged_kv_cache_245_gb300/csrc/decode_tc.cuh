@@ -45,17 +45,17 @@
 namespace pkv {
 
 constexpr int kTcHeads = 8;           // mma N of one n-tile: query heads of one KV head, padded
-constexpr int kTcMergeHeads = 4;      // heads merged per pass through shared memory
+constexpr int kTcMergeHeads = 4;      // heads merged per pass through shared memory (or 8: MH)
 constexpr int kTcStageBytes = 8192;   // K tile 4 KiB, V tile 4 KiB
 constexpr int kBoxBytes = 2048;       // 16 rows x 128 B: half a head_dim row
 
 
-template <int W, int S, int NT = 1>
+template <int W, int S, int NT = 1, int MH = kTcMergeHeads>
 struct TcSmem {
   static constexpr int kStagesOff = 0;
   static constexpr int kBarsOff = W * S * kTcStageBytes;
   static constexpr int kMergeOff = kBarsOff + W * S * 8;
-  static constexpr int kMLOff = kMergeOff + W * kTcMergeHeads * kRecStride * 4;
+  static constexpr int kMLOff = kMergeOff + W * MH * kRecStride * 4;
   static constexpr int kCtxOff = kMLOff + W * kTcHeads * NT * 2 * 4;
   static constexpr int kReqOff = kCtxOff + kTcMaxSeqs * 4;
   static constexpr int kPrefixOff = kReqOff + kTcMaxSeqs * 4;
@@ -262,12 +262,13 @@ __device__ __forceinline__ bool tc_merge_pieces(const TcParams& p, int seq, int 
 
 // NT n-tiles of 8 query heads per KV head (instantiated with NT = 1: GQA
 // groups of up to 8 query heads).  kFuse: the decode step's append is done
-// here too (p.slot_mapping).
-template <bool kContig, int W, int S, int NT, bool kFuse>
+// here too (p.slot_mapping).  MH: query heads merged per pass (4, or 8 when
+// the shared memory holds every warp's 8 partials: one pass at G = 8).
+template <bool kContig, int W, int S, int NT, bool kFuse, int MH>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const TcParams p) {
-  using L = TcSmem<W, S, NT>;
+  using L = TcSmem<W, S, NT, MH>;
   constexpr int H = kTcHeads * NT;  // padded query heads per KV head
   constexpr unsigned kFull = 0xffffffffu;
   extern __shared__ unsigned char smem_raw[];
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int64_t x_last = seg.pend - 1;
     const bool own_last = kFuse && x_last >= seg.x0 && x_last < seg.x1 &&
                           (x_last - seg.x0) % W == warp;
-    unsigned char* fuse_s = reinterpret_cast<unsigned char*>(merge + warp * kTcMergeHeads * kRecStride);
+    unsigned char* fuse_s = reinterpret_cast<unsigned char*>(merge + warp * MH * kRecStride);
     if (own_last) {
       const int64_t pr = static_cast<int64_t>(seg.seq) * p.Hkv + seg.kvh;
       cp_async_16(fuse_s + lane * 16,
@@ -753,11 +754,11 @@ __global__ void __launch_bounds__(W * 32, 1)
     // ---- the head piece's merge warps request the next CTA's piece record
     // of their heads now, so that it arrives while the warps are merged
     TcPieceWords nxt[NT * 2];
-    if (head_piece && warp < kTcMergeHeads && cf + 1 <= cl && tc_range_nonempty(cf + 1, V, P)) {
+    if (head_piece && warp < MH && cf + 1 <= cl && tc_range_nonempty(cf + 1, V, P)) {
 #pragma unroll
       for (int k = 0; k < NT * 2; ++k)
-        if (warp + kTcMergeHeads * k < G)
-          tc_issue_piece(p.rec + (static_cast<int64_t>(cf + 1) * kTcRecHeads + warp + kTcMergeHeads * k) *
+        if (warp + MH * k < G)
+          tc_issue_piece(p.rec + (static_cast<int64_t>(cf + 1) * kTcRecHeads + warp + MH * k) *
                                      kRecStride,
                          lane, nxt[k]);
     }
@@ -780,14 +781,14 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
 #pragma unroll
     for (int pass = 0; pass < NT * 2; ++pass) {
-      const int h0 = pass * kTcMergeHeads;
+      const int h0 = pass * MH;
       if (h0 >= G) break;
       // lanes whose head pair (8t + 2tq, + 1) falls in [h0, h0 + 4) write it
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const int h = 8 * t + 2 * tq;
-        if (h >= h0 && h < h0 + kTcMergeHeads) {
-          float* mb = merge + (warp * kTcMergeHeads + (h - h0)) * kRecStride;
+        if (h >= h0 && h < h0 + MH) {
+          float* mb = merge + (warp * MH + (h - h0)) * kRecStride;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             mb[16 * i + g] = acc[i][t][0];
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(W * 32, 1)
       // warp hl merges head h0 + hl: lane j < W derives warp j's weight
       // 2^(m_j - M) / sum_k l_k 2^(m_k - M) once, then every lane sums its four
       // output elements over the W partials
-      const int nh = min(kTcMergeHeads, G - h0);
+      const int nh = min(MH, G - h0);
       if (warp < nh) {
         const int hh = h0 + warp;
         const float mj = lane < W ? ml[(lane * H + hh) * 2] : -INFINITY;
@@ -819,7 +820,7 @@ __global__ void __launch_bounds__(W * 32, 1)
         for (int w = 0; w < W; ++w) {
           const float ww = __shfl_sync(kFull, wj, w);
           const float4 v =
-              *reinterpret_cast<const float4*>(merge + (w * kTcMergeHeads + warp) * kRecStride + lane * 4);
+              *reinterpret_cast<const float4*>(merge + (w * MH + warp) * kRecStride + lane * 4);
           o4.x = fmaf(v.x, ww, o4.x);
           o4.y = fmaf(v.y, ww, o4.y);
           o4.z = fmaf(v.z, ww, o4.z);

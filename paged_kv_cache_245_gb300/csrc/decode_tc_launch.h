@@ -167,9 +167,9 @@ size_t tc_workspace_bytes(int num_ctas);
 // Sequences per launch (a larger batch runs as consecutive launches).
 int tc_chunk_seqs(int max_context);
 
-// cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages.  A group
-// of more than 8 query heads per KV head (p.G <= 16, paged only) runs with
-// two n-tiles of heads on 8 warps x 3 stages whatever cfg says.
+// cfg 0: 8 warps x 3 stages per CTA; cfg 1: 12 warps x 2 stages; cfg 2:
+// 10 warps x 2 stages with one merge pass for groups of 5..8 query heads
+// (else as cfg 1).
 TcStatus launch_decode_tc(const TcParams& p, bool contig, const void* k, const void* v,
                           int64_t rows_total, int cfg, int num_ctas, void* workspace,
                           cudaStream_t stream, cudaError_t* cuda_err);

@@ -250,8 +250,11 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
     }
     t.err = err;
     cudaError_t ce = cudaSuccess;
-    const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total,
-                                                   variant == 2 ? 0 : 1, tc_ctas(sms), workspace,
+    // 8 x 3 when forced; 12 x 2 when forced or for up to 4 query heads per KV
+    // head, else 10 x 2 (one merge pass for all 8 heads)
+    const int cfg = variant == 2 ? 0 : (variant == 0 && group > 4 ? 2 : 1);
+    const pkv::TcStatus ts = pkv::launch_decode_tc(t, contig, k, v, rows_total, cfg,
+                                                   tc_ctas(sms), workspace,
                                                    static_cast<cudaStream_t>(stream), &ce);
     if (ts == pkv::TcStatus::kEncodeFailed)
       return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V cache");
