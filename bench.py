@@ -678,8 +678,8 @@ def measure_prefill(wl, dev, reps):
         del li
     res["peak_tflops"] = peak
     res["peak_source"] = peak_src
-    res["kernel"] = ("prefill_kernel (tcgen05.mma 128x128x16 bf16, S and O in tensor memory, "
-                     "256 query rows per CTA)")
+    res["kernel"] = ("prefill_kernel (tcgen05.mma 128x128x16 bf16, S and O in tensor memory; "
+                     "persistent, one CTA per SM over items of 256 query rows)")
     return res
 
 

@@ -20,6 +20,7 @@ struct PrefillParams {
   int32_t max_q;                 // host bound on any chunk's length
   int32_t run_rows;              // rows per TMA box: gcd(bs, 128), one box per block run
   float qscale;                  // scale * log2(e)
+  int32_t q_tma;                 // Q tiles by TMA through the q map (G divides 128), else cp.async
   int32_t checked;
   int* err;
 };
@@ -31,8 +32,15 @@ struct PrefillParams {
 // driver rejects the map.
 bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int run_rows);
 
-// One CTA per (256 query rows, KV head, sequence).
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                           cudaStream_t stream);
+// q ([num_tokens][Hq][128] bf16) as a 4-D tensor (64 columns, 2 column
+// halves, Hq heads, tokens) whose box of 128 / G tokens x G heads x 64
+// columns lands as one column half of a 128-row Q tile, 128-byte swizzled.
+// False when G does not divide 128 or the driver rejects the map.
+bool encode_prefill_q(CUtensorMap* map, const void* q, int64_t num_tokens, int Hq, int G);
+
+// A persistent grid (one CTA per SM) over the (256 query rows, KV head,
+// sequence) items.
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                           const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace pkv

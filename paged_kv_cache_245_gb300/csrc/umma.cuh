@@ -171,6 +171,26 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// The same for a role with slack (the producers): between polls the thread
+// sleeps about sleep_ns, leaving its SM sub-partition's issue slots to the
+// softmax warps.
+__device__ __forceinline__ bool wait_or_abort_idle(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort, int* err,
+                                                   unsigned sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_error(err, kErrTimeout);
+      return false;
+    }
+    __nanosleep(sleep_ns);
+  }
+  return true;
+}
+
 // Byte offset of 16-byte chunk c (0..15) of row r in the Q tile: two
 // 64-column halves of 128 rows x 128 bytes, 128-byte swizzled.
 __device__ __forceinline__ int q_chunk_offset(int r, int c) {
@@ -190,7 +210,26 @@ __device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, in
       "l"(tmap), "r"(0), "r"(0), "r"(0), "r"(group), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
+// The same at coordinates (c0, c1, c2, c3), innermost first.
+__device__ __forceinline__ void tma_load_4d_at(void* dst_smem, const void* tmap, int32_t c0,
+                                               int32_t c1, int32_t c2, int32_t c3, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst_smem)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
 
+// A 16-byte global -> shared copy (cp.async, generic proxy, L2 only) that
+// reads src_bytes (16 or 0) and fills the rest with zeros; drain waits for
+// every such copy of this thread.
+__device__ __forceinline__ void cp_async_zfill_16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_drain() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 }  // namespace umma
 }  // namespace pkv
