@@ -64,7 +64,8 @@ constexpr int kStages = 2;
 constexpr int kQSlots = 2;                            // Q tiles (two: a third measured slower)
 constexpr int kOffK = kQSlots * kOpBytes;             // after the Q slots
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
-constexpr int kTilesBytes = kOffK + kStages * kStageBytes;  // 192 KiB
+constexpr int kOffOut = kOffK + kStages * kStageBytes;  // output staging, 4 KiB per softmax warp
+constexpr int kTilesBytes = kOffOut + 8 * 4096;       // 224 KiB
 constexpr int kSmemBytes = kTilesBytes + 512 + 1024;  // + barriers and item ring, alignment
 constexpr int kThreads = 352;
 constexpr int kRing = 4;                              // item descriptors in flight
@@ -97,7 +98,8 @@ struct PBars {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv,
-                   const __grid_constant__ CUtensorMap tmq, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tmo, const PrefillParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint64_t* bar0 = reinterpret_cast<uint64_t*>(smem + kTilesBytes);
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
       if (p.q_tma) prefetch_tensormap(&tmq);
+      if (p.out_tma) prefetch_tensormap(&tmo);
     }
   } else if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -450,26 +453,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = waitb(&B.pfull[0], np0 & 1);
       ++np0;
+      if (ok && !last) ok = waitb(&B.kfull[s ^ 1], ((g + 1) >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
         issue_pv(0, s, j > 0);
         if (last) umma_commit(&B.ofull[0]);
         if (!two) umma_commit(&B.vempty[s]);
-      }
-      __syncwarp();
-      if (!last) {
-        ok = waitb(&B.kfull[s ^ 1], ((g + 1) >> 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
+        if (!last) {
           issue_s(0, nq % kQSlots, s ^ 1);
           umma_commit(&B.sfull[0]);
           if (qlast) umma_commit(&B.qempty[nq % kQSlots]);
           if (!two) umma_commit(&B.kempty[s ^ 1]);
         }
-        __syncwarp();
       }
+      __syncwarp();
       if (two) {
         ok = waitb(&B.pfull[1], np1 & 1);
         ++np1;
@@ -682,26 +680,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_t only after these warps hand over its first P
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * kHeadDim);
+      const int wrow0 = it.row0 + t * kRowTile + 32 * (warp & 3);  // this warp's first row
+      if (p.out_tma && wrow0 + 32 <= it.rows) {
+        // G divides 32: the warp's 32 rows are 32 / G whole tokens.  Each
+        // column half goes through the warp's 4 KiB of staging (row = lane,
+        // 128-byte swizzled) and one tensor store.
+        unsigned char* stg = smem + kOffOut + warp * 4096;
+        const int tokw = it.q0 + wrow0 / G;
 #pragma unroll
-      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-        uint32_t w[32];
-        tmem_ld32(w, o_tm + c0);
-        tmem_wait_ld(w);
-        if (valid) {
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w[32], w2[32];
+          tmem_ld32(w, o_tm + 64 * h);
+          tmem_ld32(w2, o_tm + 64 * h + 32);
+          if (lane == 0) bulk_wait_read();  // the warp's last store has read the staging
+          __syncwarp();
+          tmem_wait_ld(w);
+          tmem_ready(w2);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* x = c < 4 ? w + 8 * c : w2 + 8 * (c - 4);
             uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]) * inv, __uint_as_float(w[8 * q + 1]) * inv);
-            o.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]) * inv, __uint_as_float(w[8 * q + 3]) * inv);
-            o.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]) * inv, __uint_as_float(w[8 * q + 5]) * inv);
-            o.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]) * inv, __uint_as_float(w[8 * q + 7]) * inv);
-            dst[c0 / 8 + q] = o;
+            o.x = pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv);
+            o.y = pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
+            o.z = pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv);
+            o.w = pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv);
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();  // the tensor store reads the staging through the async proxy
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d_at(&tmo, stg, 0, h, it.kvh * G, tokw);
+            bulk_commit();
+          }
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * kHeadDim);
+#pragma unroll
+        for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+          uint32_t w[32];
+          tmem_ld32(w, o_tm + c0);
+          tmem_wait_ld(w);
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]) * inv, __uint_as_float(w[8 * q + 1]) * inv);
+              o.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]) * inv, __uint_as_float(w[8 * q + 3]) * inv);
+              o.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]) * inv, __uint_as_float(w[8 * q + 5]) * inv);
+              o.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]) * inv, __uint_as_float(w[8 * q + 7]) * inv);
+              dst[c0 / 8 + q] = o;
+            }
           }
         }
       }
       tc_fence_before();
     }
+    if (lane == 0) bulk_wait_done();  // the warp's tensor stores completed
   }
 
   tc_fence_before();
@@ -748,16 +782,19 @@ bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int r
   return r == CUDA_SUCCESS;
 }
 
-bool encode_prefill_q(CUtensorMap* map, const void* q, int64_t num_tokens, int Hq, int G) {
+bool encode_prefill_rows(CUtensorMap* map, const void* base, int64_t num_tokens, int Hq, int G,
+                         int box_rows) {
   auto enc = prefill_map_encoder();
-  if (enc == nullptr || G <= 0 || 128 % G != 0 || Hq < G || num_tokens <= 0) return false;
+  if (enc == nullptr || G <= 0 || box_rows % G != 0 || box_rows > 128 || Hq < G || num_tokens <= 0)
+    return false;
   const cuuint64_t dims[4] = {64u, 2u, static_cast<cuuint64_t>(Hq),
                               static_cast<cuuint64_t>(num_tokens)};
   const cuuint64_t strides[3] = {128u, static_cast<cuuint64_t>(kRowBytes),
                                  static_cast<cuuint64_t>(Hq) * kRowBytes};
-  const cuuint32_t box[4] = {64u, 1u, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  const cuuint32_t box[4] = {64u, 1u, static_cast<cuuint32_t>(G),
+                            static_cast<cuuint32_t>(box_rows / G)};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims,
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -765,7 +802,7 @@ bool encode_prefill_q(CUtensorMap* map, const void* q, int64_t num_tokens, int H
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                           const PrefillParams& p, cudaStream_t stream) {
+                           const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   static std::atomic<bool> attr_done{false};  // repeated calls are harmless
   if (!attr_done.load()) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -790,7 +827,7 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const C
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < n ? items : n);
   return launch_pdl(prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, tk, tv, tq,
-                    p);
+                    to, p);
 }
 
 }  // namespace pkv

@@ -21,6 +21,7 @@ struct PrefillParams {
   int32_t run_rows;              // rows per TMA box: gcd(bs, 128), one box per block run
   float qscale;                  // scale * log2(e)
   int32_t q_tma;                 // Q tiles by TMA through the q map (G divides 128), else cp.async
+  int32_t out_tma;               // output rows by tensor stores (G divides 32), else plain stores
   int32_t checked;
   int* err;
 };
@@ -32,15 +33,18 @@ struct PrefillParams {
 // driver rejects the map.
 bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int run_rows);
 
-// q ([num_tokens][Hq][128] bf16) as a 4-D tensor (64 columns, 2 column
-// halves, Hq heads, tokens) whose box of 128 / G tokens x G heads x 64
-// columns lands as one column half of a 128-row Q tile, 128-byte swizzled.
-// False when G does not divide 128 or the driver rejects the map.
-bool encode_prefill_q(CUtensorMap* map, const void* q, int64_t num_tokens, int Hq, int G);
+// q or out ([num_tokens][Hq][128] bf16) as a 4-D tensor (64 columns, 2
+// column halves, Hq heads, tokens) whose box of box_rows / G tokens x G heads
+// x 64 columns is one column half of box_rows rows (token major, head
+// minor), 128-byte swizzled: a Q tile's half (box_rows 128) or one warp's
+// output rows (32).  False when G does not divide box_rows or the driver
+// rejects the map.
+bool encode_prefill_rows(CUtensorMap* map, const void* base, int64_t num_tokens, int Hq, int G,
+                         int box_rows);
 
 // A persistent grid (one CTA per SM) over the (256 query rows, KV head,
 // sequence) items.
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                           const PrefillParams& p, cudaStream_t stream);
+                           const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace pkv

@@ -221,6 +221,28 @@ __device__ __forceinline__ void tma_load_4d_at(void* dst_smem, const void* tmap,
       : "memory");
 }
 
+// Tensor store from shared memory (box at coordinates c0..c3, innermost
+// first) in this thread's bulk group; commit closes the group, and
+// wait_read / wait_done wait until every committed group of this thread has
+// read its shared memory / completed.
+__device__ __forceinline__ void tma_store_4d_at(const void* tmap, const void* src_smem, int32_t c0,
+                                                int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          tmap),
+      "r"(smem_addr(src_smem)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_done() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // A 16-byte global -> shared copy (cp.async, generic proxy, L2 only) that
 // reads src_bytes (16 or 0) and fills the rest with zeros; drain waits for
 // every such copy of this thread.
