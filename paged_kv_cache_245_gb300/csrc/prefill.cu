@@ -542,16 +542,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         float tmax;
         if (!general) {
           float mx[4];
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < 4; ++u) mx[u] = -INFINITY;
-  #pragma unroll
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t a[32], b[32];
             tmem_ld32(a, s_tm + 64 * h);
             tmem_ld32(b, s_tm + 64 * h + 32);
             tmem_wait_ld(a);
             tmem_ready(b);
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 16; ++c) {
               mx[c & 3] = fmax3(mx[c & 3], __uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1]));
               mx[(c + 2) & 3] =
@@ -561,16 +561,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
         } else {
           float mx[8];
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-  #pragma unroll
+          // (not unrolled: the masked path runs once per item, and a smaller kernel
+          // measured faster)
+#pragma unroll 1
           for (int h = 0; h < 2; ++h) {
             uint32_t a[32], b[32];
             tmem_ld32(a, s_tm + 64 * h);
             tmem_ld32(b, s_tm + 64 * h + 32);
             tmem_wait_ld(a);
             tmem_ready(b);
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 64; ++c) {
               const float x = __uint_as_float(c < 32 ? a[c] : b[c - 32]) * sc;
               mx[c & 7] = fmaxf(mx[c & 7], !diag || k0 + 64 * h + c <= pos ? x : -INFINITY);
@@ -590,12 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               l *= alpha;
               m_used = m_new;
             }
-  #pragma unroll
+#pragma unroll
             for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
               uint32_t w[32];
               tmem_ld32(w, o_tm + c0);
               tmem_wait_ld(w);
-  #pragma unroll
+#pragma unroll
               for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * alpha);
               tmem_st32(o_tm + c0, w);
             }
@@ -607,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t sc2 = f2_pack(__float_as_uint(sc), __float_as_uint(sc));
           const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
           uint64_t ls2[4];
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < 4; ++u) ls2[u] = 0ull;  // (+0, +0)
-  #pragma unroll
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t a[32], b[32];
             tmem_ld32(a, s_tm + 64 * h);
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld(a);
             tmem_ready(b);
             uint32_t pk[32];
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 32; ++c) {
               const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
               const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
@@ -636,9 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           l += (l0 + l2) + (l1 + l3);
         } else {
           float ls[8];
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-  #pragma unroll
+          // (not unrolled: the masked path runs once per item, and a smaller kernel
+          // measured faster)
+#pragma unroll 1
           for (int h = 0; h < 2; ++h) {
             uint32_t a[32], b[32];
             tmem_ld32(a, s_tm + 64 * h);
@@ -651,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t hi =
                 seen >= 64 ? 0xffffffffu : (seen <= 32 ? 0u : (1u << (seen - 32)) - 1u);
             uint32_t pk[32];
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 32; ++c) {
               const uint32_t u0 = c < 16 ? a[2 * c] : b[2 * c - 32];
               const uint32_t u1 = c < 16 ? a[2 * c + 1] : b[2 * c - 31];
@@ -715,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * kHeadDim);
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
           uint32_t w[32];
           tmem_ld32(w, o_tm + c0);
