@@ -396,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-#pragma unroll
+        // (not unrolled: masked tiles are few, and a smaller kernel measured faster)
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t a[32], b[32];
           tmem_ld32(a, s_tm + 64 * h);
@@ -427,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
             m_used = m_new;
           }
-#pragma unroll
+          // (not unrolled: the rescale is rare, and a smaller kernel measured faster)
+#pragma unroll 1
           for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
             uint32_t w[32];
             tmem_ld32(w, o_tm + c0);
@@ -475,7 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ls[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-#pragma unroll
+        // (not unrolled: masked tiles are few, and a smaller kernel measured faster)
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           uint32_t a[32], b[32];
           tmem_ld32(a, s_tm + 64 * h);
