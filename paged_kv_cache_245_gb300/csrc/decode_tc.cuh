@@ -753,10 +753,11 @@ __global__ void __launch_bounds__(W * 32, 1)
 
     // ---- the head piece's merge warps request the next CTA's piece record
     // of their heads now, so that it arrives while the warps are merged
-    TcPieceWords nxt[NT * 2];
+    constexpr int kPasses = (NT * 8 + MH - 1) / MH;  // merge passes that can hold heads
+    TcPieceWords nxt[kPasses];
     if (head_piece && warp < MH && cf + 1 <= cl && tc_range_nonempty(cf + 1, V, P)) {
 #pragma unroll
-      for (int k = 0; k < NT * 2; ++k)
+      for (int k = 0; k < kPasses; ++k)
         if (warp + MH * k < G)
           tc_issue_piece(p.rec + (static_cast<int64_t>(cf + 1) * kTcRecHeads + warp + MH * k) *
                                      kRecStride,
@@ -780,7 +781,7 @@ __global__ void __launch_bounds__(W * 32, 1)
       }
     }
 #pragma unroll
-    for (int pass = 0; pass < NT * 2; ++pass) {
+    for (int pass = 0; pass < kPasses; ++pass) {
       const int h0 = pass * MH;
       if (h0 >= G) break;
       // lanes whose head pair (8t + 2tq, + 1) falls in [h0, h0 + 4) write it
