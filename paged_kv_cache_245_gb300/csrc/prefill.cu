@@ -8,11 +8,13 @@
 // 0 .. ctx - Lq + j ("Running Out of Cache": a block table maps positions to
 // blocks; a chunk of one token is the decode step).
 //
-// Work items: (256 query rows, KV head, sequence).  The rows are the chunk's
+// Work items: (two row tiles, KV head, sequence).  The rows are the chunk's
 // (token, query head) pairs of the KV head's group, token major (row r: token
-// r / G, head r % G), so every K/V tile serves the whole group.  An item's
-// rows form two tiles of 128 (the M of one tcgen05.mma), each with its own
-// softmax warpgroup.  The grid is persistent, one CTA per SM, and each CTA
+// r / G, head r % G), so every K/V tile serves the whole group.  A row tile
+// is the M = 128 of one tcgen05.mma and holds TR = (128 / G) G rows, whole
+// tokens (128, or 126 / 125 when G does not divide 128; the rest is zero
+// padding), so that its Q rows are TMA boxes of whole tokens; each row tile
+// has its own softmax warpgroup.  The grid is persistent, one CTA per SM, and each CTA
 // walks a fixed list of items: heaviest (latest rows) first, dealt to the
 // CTAs in rounds whose direction alternates, which balances the CTAs about as
 // well as a dynamic queue would (no shared counter, nothing to reset).  The
@@ -25,7 +27,7 @@
 //              128-byte swizzled atoms ordered (row group, column half)
 //   warp 9     tensor-memory owner and MMA issuer (one thread)
 //   warp 10    the item list (descriptors into a 4-slot ring) and the Q rows,
-//              by TMA (or cp.async when G does not divide 128) into two
+//              by TMA (cp.async should the map be refused) into two or three
 //              rotating 32 KiB slots
 //
 // Tensor memory (512 columns, lane = query row of the tile): S_t = Q_t K^T in
@@ -61,8 +63,10 @@ using namespace umma;
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kQSlots = 2;                            // Q tiles (two: a third measured slower)
-constexpr int kOffK = kQSlots * kOpBytes;             // after the Q slots
+// Q tiles rotate over two slots, or three when the output staging is unused
+// (its space is the third, with plain stores: G not dividing 32)
+constexpr int kQSlotsMax = 3;
+constexpr int kOffK = 2 * kOpBytes;                   // after the two fixed Q slots
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kOffOut = kOffK + kStages * kStageBytes;  // output staging, 4 KiB per softmax warp
 constexpr int kTilesBytes = kOffOut + 8 * 4096;       // 224 KiB
@@ -75,6 +79,20 @@ constexpr int kRingUsers = 10;                        // readers: softmax warps,
 // the list.
 struct PItem {
   int32_t seq, kvh, row0, rows, base, ntiles, q0, ctx;
+};
+
+// A Q tile's slot in the rotation and the phase of that slot's barriers.
+struct QCursor {
+  int slot;
+  uint32_t phase;
+  __device__ QCursor next(int nslots) const {
+    QCursor c = *this;
+    if (++c.slot == nslots) {
+      c.slot = 0;
+      c.phase ^= 1u;
+    }
+    return c;
+  }
 };
 
 // The mbarriers after the tiles.
@@ -112,11 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.pfull = bar0 + 10;
   B.ofull = bar0 + 12;
   B.qfull = bar0 + 14;
-  B.qempty = B.qfull + kQSlots;
-  B.ifull = B.qempty + kQSlots;
+  B.qempty = B.qfull + kQSlotsMax;
+  B.ifull = B.qempty + kQSlotsMax;
   B.iempty = B.ifull + kRing;
   B.drain = B.iempty + kRing;
-  constexpr int kNumBars = 15 + 2 * kQSlots + 2 * kRing;
+  constexpr int kNumBars = 15 + 2 * kQSlotsMax + 2 * kRing;
   static_assert(kNumBars * 8 + 8 <= 256, "barriers, tensor-memory address and abort flag");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar0 + kNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(bar0 + kNumBars) + 1;
@@ -126,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int G = p.G;
+  const int TR = p.tile_rows;  // rows of a row tile: whole tokens, (128 / G) G
+  const int nqs = p.out_tma ? 2 : kQSlotsMax;  // Q slots in rotation
+  auto q_off = [](int slot) { return slot < 2 ? slot * kOpBytes : kOffOut; };
 
   grid_dependency_wait();
   grid_dependency_trigger();
@@ -154,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&B.pfull[s], 4);  // one arrival per softmax warp
         mbar_init(&B.ofull[s], 1);
       }
-      for (int s = 0; s < kQSlots; ++s) {
+      for (int s = 0; s < kQSlotsMax; ++s) {
         mbar_init(&B.qfull[s], 32);  // every lane of the Q warp
         mbar_init(&B.qempty[s], 1);
       }
@@ -170,6 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.q_tma) prefetch_tensormap(&tmq);
       if (p.out_tma) prefetch_tensormap(&tmo);
     }
+  } else if (warp == 10 && TR < kRowTile) {
+    // rows TR .. 127 of every Q slot are padding that no copy writes: zero
+    for (int slot = 0; slot < nqs; ++slot)
+      for (int x = lane; x < (kRowTile - TR) * 16; x += 32)
+        *reinterpret_cast<uint4*>(smem + q_off(slot) + q_chunk_offset(TR + (x >> 4), x & 15)) =
+            make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   } else if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
@@ -265,12 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 0 of an item, then row tile 1 if it has rows) goes to slot n % 2 once
     // the last S product reading tile n - 2 completed.
     const int P = gridDim.x;
-    const int R = (p.max_q * G + 2 * kRowTile - 1) / (2 * kRowTile);
+    const int R = (p.max_q * G + 2 * TR - 1) / (2 * TR);
     const int per = p.num_seqs * p.Hkv;
     const int total = R * per;
     const uint64_t qpolicy = l2_policy_evict_first();  // every Q row is read once
     int published = 0;
-    uint32_t nq = 0;
+    uint32_t nq = 0;      // Q tiles loaded
+    QCursor qc = {0, 0};  // slot of Q tile nq and its phase
+    uint32_t last_phase = 0;  // bit s: phase of the last load into slot s
     bool ok = true;
     auto publish = [&](const PItem& it) -> bool {
       const int slot = published & (kRing - 1);
@@ -305,10 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       it.rows = Lq * G;
-      it.row0 = rt * 2 * kRowTile;
+      it.row0 = rt * 2 * TR;
       if (it.row0 >= it.rows) continue;  // this item's rows lie past the chunk
       it.base = it.ctx - Lq;             // position of the chunk's first token
-      const int last_row = min(it.row0 + 2 * kRowTile, it.rows) - 1;
+      const int last_row = min(it.row0 + 2 * TR, it.rows) - 1;
       const int kend = it.base + last_row / G + 1;  // keys the item needs
       if (kend <= 0) continue;  // only when ctx < Lq (caught in checked mode)
       it.ntiles = (kend + kKeys - 1) / kKeys;
@@ -316,24 +346,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      const int nt = it.rows > it.row0 + kRowTile ? 2 : 1;
-      for (int t = 0; t < nt; ++t, ++nq) {
-        const int qs = nq % kQSlots;
-        if (nq >= kQSlots &&
-            !__all_sync(kFull, wait_or_abort(&B.qempty[qs], ((nq / kQSlots) - 1) & 1, abort,
-                                             p.err))) {
+      const int nt = it.rows > it.row0 + TR ? 2 : 1;
+      for (int t = 0; t < nt; ++t, ++nq, qc = qc.next(nqs)) {
+        const int qs = qc.slot;
+        if (nq >= static_cast<uint32_t>(nqs) &&
+            !__all_sync(kFull, wait_or_abort(&B.qempty[qs], qc.phase ^ 1u, abort, p.err))) {
           ok = false;
           break;
         }
-        unsigned char* dst = smem + qs * kOpBytes;
+        last_phase = (last_phase & ~(1u << qs)) | (qc.phase << qs);
+        unsigned char* dst = smem + q_off(qs);
         if (p.q_tma) {
-          // G divides 128: the tile is 128 / G whole tokens, each column half
-          // one box of (tokens, G heads, 64 columns); rows past the chunk
-          // bring the next tokens' rows (or zeros past the tensor) and are
-          // never written out
-          const int tok0 = it.q0 + (it.row0 + t * kRowTile) / G;
+          // the tile is TR / G whole tokens, each column half one box of
+          // (tokens, G heads, 64 columns); rows past the chunk bring the next
+          // tokens' rows (or zeros past the tensor) and are never written out
+          const int tok0 = it.q0 + (it.row0 + t * TR) / G;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&B.qfull[qs], kOpBytes);
+            // two column halves of TR rows x 128 bytes
+            mbar_arrive_expect_tx(&B.qfull[qs], static_cast<uint32_t>(TR) * kRowBytes);
             tma_load_4d_at(dst, &tmq, 0, 0, it.kvh * G, tok0, &B.qfull[qs], qpolicy);
             tma_load_4d_at(dst + kHalfBytes, &tmq, 0, 1, it.kvh * G, tok0, &B.qfull[qs], qpolicy);
           } else {
@@ -342,11 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // lanes 0-15 and 16-31 take the 16-byte chunks of rows 2i and 2i + 1
           const int ch = lane & 15;
-          int rr = it.row0 + t * kRowTile + (lane >> 4);
+          int rr = it.row0 + t * TR + (lane >> 4);
           int tok = rr / G;
           int h = rr - tok * G;
           for (int r = lane >> 4; r < kRowTile; r += 2) {
-            const bool valid = rr < it.rows;  // padding rows are zero
+            const bool valid = r < TR && rr < it.rows;  // padding rows are zero
             const uint16_t* src =
                 valid ? p.q + ((static_cast<int64_t>(it.q0) + tok) * p.Hq + it.kvh * G + h) *
                                   kHeadDim + ch * 8
@@ -371,13 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (*abort && p.q_tma && lane == 0) {
       // let the Q copies in flight land before the shared memory is released
-      for (uint32_t n = nq >= kQSlots ? nq - kQSlots : 0; n < nq; ++n)
-        mbar_wait_bounded(&B.qfull[n % kQSlots], (n / kQSlots) & 1);
+      for (int qs = 0; qs < nqs && static_cast<uint32_t>(qs) < nq; ++qs)
+        mbar_wait_bounded(&B.qfull[qs], (last_phase >> qs) & 1u);
     }
   } else if (warp == 9) {
     // ================= MMA issuer (lane 0 issues) =================
     auto issue_s = [&](int t, int qs, int stage) {  // S_t = Q K^T
-      const uint32_t q_addr = smem_base + qs * kOpBytes;
+      const uint32_t q_addr = smem_base + q_off(qs);
       const uint32_t k_addr = smem_base + kOffK + stage * kStageBytes;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -396,26 +426,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto waitb = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(kFull, wait_or_abort(b, parity, abort, p.err));
     };
-    auto has_two = [](const PItem& it) { return it.rows > it.row0 + kRowTile; };
-    // S products of an item's first tile, global tile g, its Q tiles from nqi
-    auto first_s = [&](const PItem& it, uint32_t nqi, int g) -> bool {
-      if (!waitb(&B.kfull[g & 1], (g >> 1) & 1) ||
-          !waitb(&B.qfull[nqi % kQSlots], (nqi / kQSlots) & 1))
+    auto has_two = [TR](const PItem& it) { return it.rows > it.row0 + TR; };
+    // S products of an item's first tile, global tile g, its Q tiles at qa, qb
+    auto first_s = [&](const PItem& it, QCursor qa, QCursor qb, int g) -> bool {
+      if (!waitb(&B.kfull[g & 1], (g >> 1) & 1) || !waitb(&B.qfull[qa.slot], qa.phase))
         return false;
       tc_fence_after();
       if (lane == 0) {
-        issue_s(0, nqi % kQSlots, g & 1);
+        issue_s(0, qa.slot, g & 1);
         umma_commit(&B.sfull[0]);
-        if (it.ntiles == 1) umma_commit(&B.qempty[nqi % kQSlots]);
+        if (it.ntiles == 1) umma_commit(&B.qempty[qa.slot]);
       }
       __syncwarp();
       if (has_two(it)) {
-        if (!waitb(&B.qfull[(nqi + 1) % kQSlots], ((nqi + 1) / kQSlots) & 1)) return false;
+        if (!waitb(&B.qfull[qb.slot], qb.phase)) return false;
         tc_fence_after();
         if (lane == 0) {
-          issue_s(1, (nqi + 1) % kQSlots, g & 1);
+          issue_s(1, qb.slot, g & 1);
           umma_commit(&B.sfull[1]);
-          if (it.ntiles == 1) umma_commit(&B.qempty[(nqi + 1) % kQSlots]);
+          if (it.ntiles == 1) umma_commit(&B.qempty[qb.slot]);
         }
         __syncwarp();
       }
@@ -426,10 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nread = 0;
     PItem cur;
     bool ok = read_item(nread++, cur);
-    uint32_t nq = 0;            // Q tiles of the items before cur
+    QCursor q0 = {0, 0};        // cur's Q tiles: row tile 0 at q0, row tile 1 at q1
+    QCursor q1 = q0.next(nqs);
     int g = 0;                  // tile index over all items (ring stage g & 1)
     uint32_t np0 = 0, np1 = 0;  // P hand-overs taken per row tile
-    if (ok && cur.ntiles > 0) ok = first_s(cur, nq, g);
+    if (ok && cur.ntiles > 0) ok = first_s(cur, q0, q1, g);
     // Tile g, (cur, j): within an item PV_0(j) S_0(j+1) | PV_1(j) S_1(j+1);
     // at an item's last tile both P V products go first, then the next
     // item's first S products, so the current item never waits on the next.
@@ -461,9 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last) umma_commit(&B.ofull[0]);
         if (!two) umma_commit(&B.vempty[s]);
         if (!last) {
-          issue_s(0, nq % kQSlots, s ^ 1);
+          issue_s(0, q0.slot, s ^ 1);
           umma_commit(&B.sfull[0]);
-          if (qlast) umma_commit(&B.qempty[nq % kQSlots]);
+          if (qlast) umma_commit(&B.qempty[q0.slot]);
           if (!two) umma_commit(&B.kempty[s ^ 1]);
         }
       }
@@ -478,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (last) umma_commit(&B.ofull[1]);
           umma_commit(&B.vempty[s]);  // the producer reuses the stage
           if (!last) {
-            issue_s(1, (nq + 1) % kQSlots, s ^ 1);
+            issue_s(1, q1.slot, s ^ 1);
             umma_commit(&B.sfull[1]);
-            if (qlast) umma_commit(&B.qempty[(nq + 1) % kQSlots]);
+            if (qlast) umma_commit(&B.qempty[q1.slot]);
             umma_commit(&B.kempty[s ^ 1]);
           }
         }
@@ -491,10 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         PItem nx;
         ok = read_item(nread++, nx);
         if (!ok) break;
-        nq += two ? 2 : 1;
+        q0 = two ? q1.next(nqs) : q1;  // the next item's Q tiles follow cur's
+        q1 = q0.next(nqs);
         cur = nx;
         j = 0;
-        if (cur.ntiles > 0) ok = first_s(cur, nq, g);
+        if (cur.ntiles > 0) ok = first_s(cur, q0, q1, g);
       } else {
         ++j;
       }
@@ -518,9 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; ok; ++n) {
       PItem it;
       if (!read_item(n, it) || it.ntiles == 0) break;
-      if (t == 1 && it.rows <= it.row0 + kRowTile) continue;  // row tile 1 holds no rows
-      const int r = it.row0 + t * kRowTile + lr;  // row of the chunk
-      const bool valid = r < it.rows;
+      if (t == 1 && it.rows <= it.row0 + TR) continue;  // row tile 1 holds no rows
+      const int r = it.row0 + t * TR + lr;  // row of the chunk
+      const bool valid = lr < TR && r < it.rows;
       const int rr = valid ? r : it.rows - 1;     // padding rows mirror the last row
       const int tok = rr / G;
       const int head = it.kvh * G + rr % G;
@@ -684,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_t only after these warps hand over its first P
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int wrow0 = it.row0 + t * kRowTile + 32 * (warp & 3);  // this warp's first row
-      if (p.out_tma && wrow0 + 32 <= it.rows) {
+      const int wrow0 = it.row0 + t * TR + 32 * (warp & 3);  // this warp's first row
+      if (p.out_tma && 32 * (warp & 3) + 32 <= TR && wrow0 + 32 <= it.rows) {
         // G divides 32: the warp's 32 rows are 32 / G whole tokens.  Each
         // column half goes through the warp's 4 KiB of staging (row = lane,
         // 128-byte swizzled) and one tensor store.
@@ -789,7 +820,8 @@ bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int r
 bool encode_prefill_rows(CUtensorMap* map, const void* base, int64_t num_tokens, int Hq, int G,
                          int box_rows) {
   auto enc = prefill_map_encoder();
-  if (enc == nullptr || G <= 0 || box_rows % G != 0 || box_rows > 128 || Hq < G || num_tokens <= 0)
+  if (enc == nullptr || G <= 0 || box_rows % G != 0 || box_rows > 128 || box_rows / G > 256 ||
+      Hq < G || num_tokens <= 0)
     return false;
   const cuuint64_t dims[4] = {64u, 2u, static_cast<cuuint64_t>(Hq),
                               static_cast<cuuint64_t>(num_tokens)};
@@ -825,7 +857,10 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const C
     if (e != cudaSuccess) return e;
     if (dev < 64) sms[dev].store(n);
   }
-  const int64_t row_tiles = (static_cast<int64_t>(p.max_q) * p.G + 2 * kRowTile - 1) / (2 * kRowTile);
+  if (p.tile_rows <= 0 || p.tile_rows > kRowTile || p.tile_rows % p.G != 0)
+    return cudaErrorInvalidValue;
+  const int64_t row_tiles =
+      (static_cast<int64_t>(p.max_q) * p.G + 2 * p.tile_rows - 1) / (2 * p.tile_rows);
   const int64_t items = row_tiles * p.Hkv * p.num_seqs;
   if (items <= 0) return cudaSuccess;
   if (items > INT32_MAX) return cudaErrorInvalidValue;

@@ -19,8 +19,9 @@ struct PrefillParams {
   int32_t max_blocks, num_seqs, Hq, Hkv, G;
   int32_t max_q;                 // host bound on any chunk's length
   int32_t run_rows;              // rows per TMA box: gcd(bs, 128), one box per block run
+  int32_t tile_rows;             // query rows of a row tile: whole tokens, (128 / G) G
   float qscale;                  // scale * log2(e)
-  int32_t q_tma;                 // Q tiles by TMA through the q map (G divides 128), else cp.async
+  int32_t q_tma;                 // Q tiles by TMA through the q map (boxes of TR rows), else cp.async
   int32_t out_tma;               // output rows by tensor stores (G divides 32), else plain stores
   int32_t checked;
   int* err;
@@ -42,8 +43,8 @@ bool encode_prefill_runs(CUtensorMap* map, const void* base, int64_t rows, int r
 bool encode_prefill_rows(CUtensorMap* map, const void* base, int64_t num_tokens, int Hq, int G,
                          int box_rows);
 
-// A persistent grid (one CTA per SM) over the (256 query rows, KV head,
-// sequence) items.
+// A persistent grid (one CTA per SM) over the (two row tiles of tile_rows
+// query rows, KV head, sequence) items.
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                            const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
 
