@@ -851,15 +851,15 @@ pkv_status prefill_common(const void* q, const int32_t* cu_seqlens_q, int32_t nu
   p.qscale = scale * 1.4426950408889634f;  // log2(e)
   p.checked = g_checked.load();
   p.err = err;
-  // Q tiles by TMA (boxes of whole tokens; the kernel's cp.async path should
-  // the driver refuse the map), and the output by tensor stores when G
-  // divides 32 (else plain stores)
+  // Q tiles by TMA (boxes of whole tokens), and the output by tensor stores
+  // when G divides 32 (else plain stores)
   alignas(64) CUtensorMap tq;
   alignas(64) CUtensorMap to;
   std::memset(&tq, 0, sizeof tq);
   std::memset(&to, 0, sizeof to);
   p.tile_rows = (128 / G) * G;  // a row tile holds whole tokens
-  p.q_tma = pkv::encode_prefill_rows(&tq, q, num_tokens, heads.num_q_heads, G, p.tile_rows) ? 1 : 0;
+  if (!pkv::encode_prefill_rows(&tq, q, num_tokens, heads.num_q_heads, G, p.tile_rows))
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
   p.out_tma = pkv::encode_prefill_rows(&to, out, num_tokens, heads.num_q_heads, G, 32) ? 1 : 0;
   const cudaError_t e =
       pkv::launch_prefill(tk, tv, tq, to, p, static_cast<cudaStream_t>(stream));

@@ -27,8 +27,7 @@
 //              128-byte swizzled atoms ordered (row group, column half)
 //   warp 9     tensor-memory owner and MMA issuer (one thread)
 //   warp 10    the item list (descriptors into a 4-slot ring) and the Q rows,
-//              by TMA (cp.async should the map be refused) into two or three
-//              rotating 32 KiB slots
+//              by TMA into two or three rotating 32 KiB slots
 //
 // Tensor memory (512 columns, lane = query row of the tile): S_t = Q_t K^T in
 // columns 128t .. 128t+127, O_t in columns 256 + 128t ..  For key tile j the
@@ -188,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_barrier_init();
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
-      if (p.q_tma) prefetch_tensormap(&tmq);
+      prefetch_tensormap(&tmq);
       if (p.out_tma) prefetch_tensormap(&tmo);
     }
   } else if (warp == 10 && TR < kRowTile) {
@@ -356,41 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         last_phase = (last_phase & ~(1u << qs)) | (qc.phase << qs);
         unsigned char* dst = smem + q_off(qs);
-        if (p.q_tma) {
-          // the tile is TR / G whole tokens, each column half one box of
-          // (tokens, G heads, 64 columns); rows past the chunk bring the next
-          // tokens' rows (or zeros past the tensor) and are never written out
-          const int tok0 = it.q0 + (it.row0 + t * TR) / G;
-          if (lane == 0) {
-            // two column halves of TR rows x 128 bytes
-            mbar_arrive_expect_tx(&B.qfull[qs], static_cast<uint32_t>(TR) * kRowBytes);
-            tma_load_4d_at(dst, &tmq, 0, 0, it.kvh * G, tok0, &B.qfull[qs], qpolicy);
-            tma_load_4d_at(dst + kHalfBytes, &tmq, 0, 1, it.kvh * G, tok0, &B.qfull[qs], qpolicy);
-          } else {
-            mbar_arrive(&B.qfull[qs]);
-          }
+        // the tile is TR / G whole tokens, each column half one box of
+        // (tokens, G heads, 64 columns); rows past the chunk bring the next
+        // tokens' rows (or zeros past the tensor) and are never written out
+        const int tok0 = it.q0 + (it.row0 + t * TR) / G;
+        if (lane == 0) {
+          // two column halves of TR rows x 128 bytes
+          mbar_arrive_expect_tx(&B.qfull[qs], static_cast<uint32_t>(TR) * kRowBytes);
+          tma_load_4d_at(dst, &tmq, 0, 0, it.kvh * G, tok0, &B.qfull[qs], qpolicy);
+          tma_load_4d_at(dst + kHalfBytes, &tmq, 0, 1, it.kvh * G, tok0, &B.qfull[qs], qpolicy);
         } else {
-          // lanes 0-15 and 16-31 take the 16-byte chunks of rows 2i and 2i + 1
-          const int ch = lane & 15;
-          int rr = it.row0 + t * TR + (lane >> 4);
-          int tok = rr / G;
-          int h = rr - tok * G;
-          for (int r = lane >> 4; r < kRowTile; r += 2) {
-            const bool valid = r < TR && rr < it.rows;  // padding rows are zero
-            const uint16_t* src =
-                valid ? p.q + ((static_cast<int64_t>(it.q0) + tok) * p.Hq + it.kvh * G + h) *
-                                  kHeadDim + ch * 8
-                      : p.q;
-            cp_async_zfill_16(dst + q_chunk_offset(r, ch), src, valid ? 16u : 0u);
-            rr += 2;
-            h += 2;
-            while (h >= G) {
-              h -= G;
-              ++tok;
-            }
-          }
-          cp_async_drain();
-          fence_proxy_async_smem();  // the MMAs read the slot through the async proxy
           mbar_arrive(&B.qfull[qs]);
         }
       }
@@ -399,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       PItem end = {};  // ntiles 0: the end of this CTA's list
       publish(end);
     }
-    if (*abort && p.q_tma && lane == 0) {
+    if (*abort && lane == 0) {
       // let the Q copies in flight land before the shared memory is released
       for (int qs = 0; qs < nqs && static_cast<uint32_t>(qs) < nq; ++qs)
         mbar_wait_bounded(&B.qfull[qs], (last_phase >> qs) & 1u);

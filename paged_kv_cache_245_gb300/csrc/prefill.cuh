@@ -21,7 +21,6 @@ struct PrefillParams {
   int32_t run_rows;              // rows per TMA box: gcd(bs, 128), one box per block run
   int32_t tile_rows;             // query rows of a row tile: whole tokens, (128 / G) G
   float qscale;                  // scale * log2(e)
-  int32_t q_tma;                 // Q tiles by TMA through the q map (boxes of TR rows), else cp.async
   int32_t out_tma;               // output rows by tensor stores (G divides 32), else plain stores
   int32_t checked;
   int* err;

@@ -243,15 +243,6 @@ __device__ __forceinline__ void bulk_wait_done() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// A 16-byte global -> shared copy (cp.async, generic proxy, L2 only) that
-// reads src_bytes (16 or 0) and fills the rest with zeros; drain waits for
-// every such copy of this thread.
-__device__ __forceinline__ void cp_async_zfill_16(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_drain() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 }  // namespace umma
 }  // namespace pkv

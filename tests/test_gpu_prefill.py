@@ -95,10 +95,13 @@ def test_long_chunks_span_many_row_and_key_tiles():
     assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "long chunks")
 
 
-def test_group_of_seven_splits_tokens_across_row_tiles():
-    # G = 7 (Yi-34B heads): 128-row tiles and 256-row CTAs cut through tokens
-    b, li, q, cu = _case(56, 8, [5, 0, 130], [100, 300, 37], 16, seed=95)
-    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "G=7")
+@pytest.mark.parametrize("hq,hkv", [(56, 8), (24, 8), (40, 8), (12, 2)])
+def test_groups_that_do_not_divide_128(hq, hkv):
+    # G = 7 (Yi-34B heads), 3, 5 and 6: row tiles of whole tokens (126 or 125
+    # rows and zero padding), chunks that end inside a row tile and in the
+    # second row tile of an item
+    b, li, q, cu = _case(hq, hkv, [5, 0, 130], [100, 300, 37], 16, seed=95 + hq)
+    assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "G=%d" % (hq // hkv))
 
 
 @pytest.mark.parametrize("scale", [0.5, 2.0, 0.0, -0.3])
