@@ -27,7 +27,7 @@
 //              128-byte swizzled atoms ordered (row group, column half)
 //   warp 9     tensor-memory owner and MMA issuer (one thread)
 //   warp 10    the item list (descriptors into a 4-slot ring) and the Q rows,
-//              by TMA into two or three rotating 32 KiB slots
+//              by TMA into two rotating 32 KiB slots
 //
 // Tensor memory (512 columns, lane = query row of the tile): S_t = Q_t K^T in
 // columns 128t .. 128t+127, O_t in columns 256 + 128t ..  For key tile j the
@@ -62,10 +62,8 @@ using namespace umma;
 namespace {
 
 constexpr int kStages = 2;
-// Q tiles rotate over two slots, or three when the output staging is unused
-// (its space is the third, with plain stores: G not dividing 32)
-constexpr int kQSlotsMax = 3;
-constexpr int kOffK = 2 * kOpBytes;                   // after the two fixed Q slots
+constexpr int kQSlots = 2;                            // Q tiles in rotation (a third measured slower)
+constexpr int kOffK = kQSlots * kOpBytes;             // after the Q slots
 constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kOffOut = kOffK + kStages * kStageBytes;  // output staging, 4 KiB per softmax warp
 constexpr int kTilesBytes = kOffOut + 8 * 4096;       // 224 KiB
@@ -129,11 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.pfull = bar0 + 10;
   B.ofull = bar0 + 12;
   B.qfull = bar0 + 14;
-  B.qempty = B.qfull + kQSlotsMax;
-  B.ifull = B.qempty + kQSlotsMax;
+  B.qempty = B.qfull + kQSlots;
+  B.ifull = B.qempty + kQSlots;
   B.iempty = B.ifull + kRing;
   B.drain = B.iempty + kRing;
-  constexpr int kNumBars = 15 + 2 * kQSlotsMax + 2 * kRing;
+  constexpr int kNumBars = 15 + 2 * kQSlots + 2 * kRing;
   static_assert(kNumBars * 8 + 8 <= 256, "barriers, tensor-memory address and abort flag");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar0 + kNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(bar0 + kNumBars) + 1;
@@ -144,8 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int G = p.G;
   const int TR = p.tile_rows;  // rows of a row tile: whole tokens, (128 / G) G
-  const int nqs = p.out_tma ? 2 : kQSlotsMax;  // Q slots in rotation
-  auto q_off = [](int slot) { return slot < 2 ? slot * kOpBytes : kOffOut; };
+  auto q_off = [](int slot) { return slot * kOpBytes; };
 
   grid_dependency_wait();
   grid_dependency_trigger();
@@ -174,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&B.pfull[s], 4);  // one arrival per softmax warp
         mbar_init(&B.ofull[s], 1);
       }
-      for (int s = 0; s < kQSlotsMax; ++s) {
+      for (int s = 0; s < kQSlots; ++s) {
         mbar_init(&B.qfull[s], 32);  // every lane of the Q warp
         mbar_init(&B.qempty[s], 1);
       }
@@ -192,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 10 && TR < kRowTile) {
     // rows TR .. 127 of every Q slot are padding that no copy writes: zero
-    for (int slot = 0; slot < nqs; ++slot)
+    for (int slot = 0; slot < kQSlots; ++slot)
       for (int x = lane; x < (kRowTile - TR) * 16; x += 32)
         *reinterpret_cast<uint4*>(smem + q_off(slot) + q_chunk_offset(TR + (x >> 4), x & 15)) =
             make_uint4(0u, 0u, 0u, 0u);
@@ -346,9 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int nt = it.rows > it.row0 + TR ? 2 : 1;
-      for (int t = 0; t < nt; ++t, ++nq, qc = qc.next(nqs)) {
+      for (int t = 0; t < nt; ++t, ++nq, qc = qc.next(kQSlots)) {
         const int qs = qc.slot;
-        if (nq >= static_cast<uint32_t>(nqs) &&
+        if (nq >= static_cast<uint32_t>(kQSlots) &&
             !__all_sync(kFull, wait_or_abort(&B.qempty[qs], qc.phase ^ 1u, abort, p.err))) {
           ok = false;
           break;
@@ -375,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (*abort && lane == 0) {
       // let the Q copies in flight land before the shared memory is released
-      for (int qs = 0; qs < nqs && static_cast<uint32_t>(qs) < nq; ++qs)
+      for (int qs = 0; qs < kQSlots && static_cast<uint32_t>(qs) < nq; ++qs)
         mbar_wait_bounded(&B.qfull[qs], (last_phase >> qs) & 1u);
     }
   } else if (warp == 9) {
@@ -430,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     PItem cur;
     bool ok = read_item(nread++, cur);
     QCursor q0 = {0, 0};        // cur's Q tiles: row tile 0 at q0, row tile 1 at q1
-    QCursor q1 = q0.next(nqs);
+    QCursor q1 = q0.next(kQSlots);
     int g = 0;                  // tile index over all items (ring stage g & 1)
     uint32_t np0 = 0, np1 = 0;  // P hand-overs taken per row tile
     if (ok && cur.ntiles > 0) ok = first_s(cur, q0, q1, g);
@@ -495,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         PItem nx;
         ok = read_item(nread++, nx);
         if (!ok) break;
-        q0 = two ? q1.next(nqs) : q1;  // the next item's Q tiles follow cur's
-        q1 = q0.next(nqs);
+        q0 = two ? q1.next(kQSlots) : q1;  // the next item's Q tiles follow cur's
+        q1 = q0.next(kQSlots);
         cur = nx;
         j = 0;
         if (cur.ntiles > 0) ok = first_s(cur, q0, q1, g);
