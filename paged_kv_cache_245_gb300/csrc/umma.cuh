@@ -171,26 +171,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return true;
 }
 
-// The same for a role with slack (the producers): between polls the thread
-// sleeps about sleep_ns, leaving its SM sub-partition's issue slots to the
-// softmax warps.
-__device__ __forceinline__ bool wait_or_abort_idle(uint64_t* bar, uint32_t parity,
-                                                   volatile int* abort, int* err,
-                                                   unsigned sleep_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      record_error(err, kErrTimeout);
-      return false;
-    }
-    __nanosleep(sleep_ns);
-  }
-  return true;
-}
-
 // Byte offset of 16-byte chunk c (0..15) of row r in the Q tile: two
 // 64-column halves of 128 rows x 128 bytes, 128-byte swizzled.
 __device__ __forceinline__ int q_chunk_offset(int r, int c) {
