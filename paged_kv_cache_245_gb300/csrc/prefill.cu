@@ -68,6 +68,7 @@ constexpr int kStageBytes = 2 * kOpBytes;             // K then V
 constexpr int kOffOut = kOffK + kStages * kStageBytes;  // output staging, 4 KiB per softmax warp
 constexpr int kTilesBytes = kOffOut + 8 * 4096;       // 224 KiB
 constexpr int kSmemBytes = kTilesBytes + 512 + 1024;  // + barriers and item ring, alignment
+static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KiB");
 constexpr int kThreads = 352;
 constexpr int kRing = 4;                              // item descriptors in flight
 constexpr int kRingUsers = 10;                        // readers: softmax warps, K/V and MMA warps
