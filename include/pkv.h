@@ -261,10 +261,13 @@ PKV_API pkv_status pkv_paged_decode_attention_shared(
  *   out[row][h] = sum_{p <= ctx_i - Lq_i + j} softmax_p(scale * q[row][h] . K_p) V_p
  * with K_p, V_p found through block_tables[i] as in pkv_paged_decode_attention
  * (a chunk of one token is exactly that call).  q, out: bf16 [num_tokens][Hq][128].
- * max_q_tokens is a host bound on every chunk's length (it sizes the grid);
- * block_size must be a multiple of 16.  Accumulation in fp32, output bf16.
- * Checked mode reports a chunk longer than its context or than max_q_tokens,
- * or a context beyond the block table (PKV_DEVERR_CONTEXT), and bad block ids.
+ * max_q_tokens is a host bound on every chunk's length (it sizes the list of
+ * work items; the grid is one CTA per SM at most); block_size must be a
+ * multiple of 16.  Accumulation in fp32, output bf16.  q is read through a
+ * tensor map of exactly num_tokens rows, so no read leaves q.  Returns
+ * PKV_ERR_CUDA when the driver refuses a tensor map.  Checked mode reports a
+ * chunk longer than its context or than max_q_tokens, or a context beyond the
+ * block table (PKV_DEVERR_CONTEXT), and bad block ids.
  */
 PKV_API pkv_status pkv_paged_prefill_attention(
     const void *q, const int32_t *cu_seqlens_q, int32_t num_tokens,
