@@ -861,6 +861,7 @@ pkv_status prefill_common(const void* q, const int32_t* cu_seqlens_q, int32_t nu
   if (!pkv::encode_prefill_rows(&tq, q, num_tokens, heads.num_q_heads, G, p.tile_rows))
     return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
   p.out_tma = pkv::encode_prefill_rows(&to, out, num_tokens, heads.num_q_heads, G, 32) ? 1 : 0;
+  p.out_v8 = aligned(out, 32) ? 1 : 0;
   const cudaError_t e =
       pkv::launch_prefill(tk, tv, tq, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

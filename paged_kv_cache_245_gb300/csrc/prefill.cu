@@ -728,14 +728,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(w, o_tm + c0);
           tmem_wait_ld(w);
           if (valid) {
+            uint4 o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]) * inv, __uint_as_float(w[8 * q + 1]) * inv);
-              o.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]) * inv, __uint_as_float(w[8 * q + 3]) * inv);
-              o.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]) * inv, __uint_as_float(w[8 * q + 5]) * inv);
-              o.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]) * inv, __uint_as_float(w[8 * q + 7]) * inv);
-              dst[c0 / 8 + q] = o;
+              o[q].x = pack_bf16x2(__uint_as_float(w[8 * q + 0]) * inv, __uint_as_float(w[8 * q + 1]) * inv);
+              o[q].y = pack_bf16x2(__uint_as_float(w[8 * q + 2]) * inv, __uint_as_float(w[8 * q + 3]) * inv);
+              o[q].z = pack_bf16x2(__uint_as_float(w[8 * q + 4]) * inv, __uint_as_float(w[8 * q + 5]) * inv);
+              o[q].w = pack_bf16x2(__uint_as_float(w[8 * q + 6]) * inv, __uint_as_float(w[8 * q + 7]) * inv);
+            }
+            if (p.out_v8) {  // out 32-byte aligned: whole 32-byte sectors
+              st_global_v8(dst + c0 / 8, o[0], o[1]);
+              st_global_v8(dst + c0 / 8 + 2, o[2], o[3]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dst[c0 / 8 + q] = o[q];
             }
           }
         }

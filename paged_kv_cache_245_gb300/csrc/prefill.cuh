@@ -22,6 +22,7 @@ struct PrefillParams {
   int32_t tile_rows;             // query rows of a row tile: whole tokens, (128 / G) G
   float qscale;                  // scale * log2(e)
   int32_t out_tma;               // output rows by tensor stores (G divides 32), else plain stores
+  int32_t out_v8;                // plain stores of 32 bytes (out 32-byte aligned), else 16
   int32_t checked;
   int* err;
 };

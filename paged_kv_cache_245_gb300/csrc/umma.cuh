@@ -213,6 +213,13 @@ __device__ __forceinline__ void tma_store_4d_at(const void* tmap, const void* sr
       "r"(smem_addr(src_smem)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// A 32-byte store (a whole sector) of a then b; the address 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -104,6 +104,23 @@ def test_groups_that_do_not_divide_128(hq, hkv):
     assert_attention_close(_gpu(b, li, q, cu), _oracle(b, li, q, cu), "G=%d" % (hq // hkv))
 
 
+def test_output_only_16_byte_aligned():
+    # G = 7 writes rows with plain stores, 32 bytes at a time when out is
+    # 32-byte aligned; an out 16 bytes off that uses 16-byte stores, same bytes
+    b, li, q, cu = _case(56, 8, [5, 0], [100, 37], 16, seed=90)
+    args = (q.to(DEV), torch.as_tensor(cu, device=DEV), li.k_cache.to(DEV), li.v_cache.to(DEV),
+            torch.as_tensor(b.block_tables, device=DEV), torch.as_tensor(b.ctx, device=DEV),
+            int(np.diff(cu).max()), W.default_scale(b.shape))
+    ref = pkv.paged_prefill_attention(*args)
+    flat = torch.zeros(q.numel() + 8, dtype=torch.bfloat16, device=DEV)
+    out = flat[8:].view(q.shape)
+    assert out.data_ptr() % 32 == 16
+    pkv.paged_prefill_attention(*args, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert_attention_close(ref, _oracle(b, li, q, cu), "G=7, 32-byte stores")
+
+
 @pytest.mark.parametrize("scale", [0.5, 2.0, 0.0, -0.3])
 def test_growing_maxima_and_degenerate_scale(scale):
     # large scales make the running maximum jump between key tiles (the
