@@ -278,7 +278,10 @@ class DeviceWorkload:
 
     @property
     def uses_tc(self):
-        return self.batch.block_size % 16 == 0 and self.pkv.get_decode_variant() != 1
+        # the library's own choice for this batch (variant, block size, tiles per SM)
+        return self.pkv.decode_uses_tensor_cores(self.batch.B, self.shape.num_q_heads,
+                                                 self.shape.num_kv_heads, self.batch.max_context,
+                                                 self.batch.block_size, self.shape.head_dim)
 
     def shared_kernels(self):
         """The kernels of one shared-prefix call, by the library's launch count."""

@@ -107,6 +107,16 @@ PKV_API pkv_status pkv_kv_append(const int64_t *slot_mapping, int64_t num_tokens
  * device's SM count and pkv_set_split_tiles; both decode calls use the same
  * rule.  The size covers whichever decode kernel the call selects.
  */
+/*
+ * Whether the decode calls (paged with this block_size, or contiguous with
+ * block_size 0) run the tensor-core kernel (1) or the split kernel (0) for
+ * num_seqs sequences of at most max_context positions, under the current
+ * pkv_set_decode_variant; -1 on bad arguments.  (The paged call also needs
+ * fewer than 2^31 cache rows for the tensor-core kernel.)
+ */
+PKV_API int32_t pkv_decode_uses_tensor_cores(int32_t num_seqs, pkv_heads heads,
+                                             int32_t max_context, int32_t block_size);
+
 PKV_API int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads,
                               int32_t max_context);
 PKV_API size_t pkv_decode_workspace_size(int32_t num_seqs, pkv_heads heads,
@@ -368,7 +378,7 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
 /*
  * Which decode kernel later calls use: 0 automatic (the default: the
  * tensor-core kernel wherever it applies -- contiguous layout, or a paged
- * block size that is a multiple of 16 -- and the batch holds at least 32
+ * block size that is a multiple of 16 -- and the batch holds at least 8
  * sixteen-token tiles per SM when every context is max_context long; else
  * the split kernel, which fills the GPU better for small batches), 1 always the
  * split (CUDA-core) kernel, 2 / 3 the tensor-core kernel with 8 warps x 3

@@ -6,7 +6,8 @@ library with ``build.build()``."""
 from .binding import (BlockManager, PkvError, VmmBuffer, block_copy, block_swap,
                       BM_RETIRED, BM_RUNNING, BM_SWAPPED, BM_RECOMPUTE, PREEMPT_RECOMPUTE,
                       PREEMPT_SWAP, contig_decode_attention, contig_decode_step,
-                      decode_num_splits, paged_decode_step, paged_decode_attention_shared,
+                      decode_num_splits, decode_uses_tensor_cores, paged_decode_step,
+                      paged_decode_attention_shared,
                       shared_decode_launches,
                       paged_prefill_attention, contig_prefill_attention,
                       decode_workspace_size, get_checked, get_device_error, kv_append, lib,
@@ -19,7 +20,7 @@ __all__ = ["BlockManager", "PkvError", "VmmBuffer", "block_copy", "block_swap", 
            "contig_decode_attention", "contig_decode_step",
            "paged_decode_step", "paged_decode_attention_shared", "paged_prefill_attention",
            "contig_prefill_attention",
-           "decode_num_splits", "shared_decode_launches",
+           "decode_num_splits", "decode_uses_tensor_cores", "shared_decode_launches",
            "decode_workspace_size", "get_checked", "get_device_error", "kv_append", "lib",
            "paged_decode_attention", "set_checked", "set_split_tiles", "set_decode_variant",
            "get_decode_variant", "VARIANT_AUTO", "VARIANT_SPLIT", "VARIANT_TC_8X3",

@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
 DEVERR_NAMES = {0: "none", 1: "block_id", 2: "slot", 3: "req_id", 4: "context",
                 5: "copy_pair", 6: "timeout"}
 
-EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_workspace_size",
+EXPORTED = ("pkv_kv_append", "pkv_decode_num_splits", "pkv_decode_uses_tensor_cores",
+            "pkv_decode_workspace_size",
             "pkv_paged_decode_attention", "pkv_contig_decode_attention", "pkv_block_copy",
             "pkv_set_checked", "pkv_get_checked", "pkv_set_split_tiles",
             "pkv_set_decode_variant", "pkv_get_decode_variant", "pkv_debug_stall_next_decode",
@@ -63,6 +64,8 @@ def lib():
     L.pkv_kv_append.argtypes = [vp, i64, vp, vp, vp, vp, i64, i64, Heads, vp]
     L.pkv_decode_num_splits.argtypes = [i32, Heads, i32]
     L.pkv_decode_num_splits.restype = i32
+    L.pkv_decode_uses_tensor_cores.argtypes = [i32, Heads, i32, i32]
+    L.pkv_decode_uses_tensor_cores.restype = i32
     L.pkv_decode_workspace_size.argtypes = [i32, Heads, i32]
     L.pkv_decode_workspace_size.restype = sz
     L.pkv_paged_decode_attention.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
@@ -161,6 +164,17 @@ def kv_append(slot_mapping, k, v, k_cache, v_cache):
 def decode_num_splits(num_seqs, num_q_heads, num_kv_heads, max_context, head_dim=128):
     return int(lib().pkv_decode_num_splits(num_seqs, heads(num_q_heads, num_kv_heads, head_dim),
                                            max_context))
+
+
+def decode_uses_tensor_cores(num_seqs, num_q_heads, num_kv_heads, max_context, block_size,
+                             head_dim=128):
+    """True when the decode calls run the tensor-core kernel for this batch
+    (block_size 0: the contiguous layout)."""
+    r = int(lib().pkv_decode_uses_tensor_cores(num_seqs, heads(num_q_heads, num_kv_heads, head_dim),
+                                               max_context, block_size))
+    if r < 0:
+        raise ValueError("bad arguments")
+    return r == 1
 
 
 def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, max_context, head_dim=128):

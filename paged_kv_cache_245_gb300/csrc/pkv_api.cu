@@ -160,6 +160,18 @@ struct FusedAppend {
 // Validates a decode call and, unless dry_run, launches it.  fused (the
 // tensor-core kernel only): the step's append done by the attention kernel.
 // *tc_out: whether the tensor-core kernel is (or would be) the one launched.
+// Automatic choice: the persistent tensor-core kernel needs enough tiles to
+// spread over one CTA per SM; for batches whose upper-bound tile count (all
+// contexts at max_context) is under 8 tiles per SM the many-CTA split kernel
+// finishes sooner.  Llama-3-8B shape, context 1024, on GB300: batch 1 (3.4
+// tiles per SM) 10.6 us split / 14.4 tensor-core, batch 2 (6.7) 11.9 / 11.4,
+// batch 4 (13.5) 12.8 / 11.1, batch 8 15.9 / 13.8.
+bool tc_enough_tiles(int32_t num_seqs, const pkv_heads& h, int32_t max_context, int sms) {
+  const int64_t tile_bound = static_cast<int64_t>(num_seqs) * h.num_kv_heads *
+                             ((static_cast<int64_t>(max_context) + 15) / 16);
+  return tile_bound >= 8LL * tc_ctas(sms);
+}
+
 pkv_status decode_common(bool contig, const void* q, const void* k, const void* v,
                          const int32_t* block_tables, int32_t max_blocks, int64_t num_blocks,
                          const int32_t* req_ids, int32_t max_reqs, const int32_t* context_lens,
@@ -205,13 +217,7 @@ pkv_status decode_common(bool contig, const void* q, const void* k, const void* 
   const int variant = g_variant.load();
   if (variant >= 2 && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "tensor-core kernel needs block_size %% 16 == 0 and < 2^31 rows");
-  // Automatic choice: the persistent tensor-core kernel needs enough tiles
-  // to spread over one CTA per SM; for batches whose upper-bound tile count
-  // (all contexts at max_context) is under 32 tiles per SM the many-CTA
-  // split kernel finishes sooner.
-  const int64_t tile_bound = static_cast<int64_t>(num_seqs) * h.num_kv_heads *
-                             ((static_cast<int64_t>(max_context) + 15) / 16);
-  const bool tc_pick = variant >= 2 || (variant == 0 && tile_bound >= 32LL * tc_ctas(sms));
+  const bool tc_pick = variant >= 2 || (variant == 0 && tc_enough_tiles(num_seqs, h, max_context, sms));
   if (tc_pick && tc_ok) {
     if (tc_out) *tc_out = true;
     const size_t need = pkv::tc_workspace_bytes(tc_ctas(sms));
@@ -575,6 +581,17 @@ int32_t pkv_decode_num_splits(int32_t num_seqs, pkv_heads heads, int32_t max_con
   if (device_info(nullptr, nullptr, &sms) != PKV_OK) return -1;
   if (check_heads(heads) != PKV_OK || num_seqs < 0 || max_context < 0) return -1;
   return plan_splits(num_seqs, heads, max_context, sms).nsplit;
+}
+
+int32_t pkv_decode_uses_tensor_cores(int32_t num_seqs, pkv_heads heads, int32_t max_context,
+                                     int32_t block_size) {
+  int sms = 0;
+  if (device_info(nullptr, nullptr, &sms) != PKV_OK) return -1;
+  if (check_heads(heads) != PKV_OK || num_seqs < 0 || max_context < 0) return -1;
+  const int variant = g_variant.load();
+  if (variant == 1 || (block_size > 0 && block_size % 16 != 0)) return 0;
+  if (variant >= 2) return 1;
+  return tc_enough_tiles(num_seqs, heads, max_context, sms) ? 1 : 0;
 }
 
 size_t pkv_decode_workspace_size(int32_t num_seqs, pkv_heads heads, int32_t max_context) {
