@@ -377,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&B.qfull[qs], (last_phase >> qs) & 1u);
     }
   } else if (warp == 9) {
-    // ================= MMA issuer (lane 0 issues) =================
+    // ================= MMA issuer: lane 0 alone =================
+    // One thread issues every product, waits on single-lane barrier checks
+    // and never votes or reconverges with the other lanes inside the loop.
+    if (lane == 0) {
     auto issue_s = [&](int t, int qs, int stage) {  // S_t = Q K^T
       const uint32_t q_addr = smem_base + q_off(qs);
       const uint32_t k_addr = smem_base + kOffK + stage * kStageBytes;
@@ -396,7 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 smem_desc(v_addr + kk * 4096, 1024, 2048), kIdescPV, (acc || kk > 0));
     };
     auto waitb = [&](uint64_t* b, uint32_t parity) -> bool {
-      return __all_sync(kFull, wait_or_abort(b, parity, abort, p.err));
+      return wait_or_abort(b, parity, abort, p.err);
+    };
+    auto read_item1 = [&](int n, PItem& it) -> bool {
+      const int slot = n & (kRing - 1);
+      if (!wait_or_abort(&B.ifull[slot], (n / kRing) & 1, abort, p.err)) return false;
+      it = ring[slot];
+      mbar_arrive(&B.iempty[slot]);
+      return true;
     };
     auto has_two = [TR](const PItem& it) { return it.rows > it.row0 + TR; };
     // S products of an item's first tile, global tile g, its Q tiles at qa, qb
@@ -404,29 +414,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waitb(&B.kfull[g & 1], (g >> 1) & 1) || !waitb(&B.qfull[qa.slot], qa.phase))
         return false;
       tc_fence_after();
-      if (lane == 0) {
+      {
         issue_s(0, qa.slot, g & 1);
         umma_commit(&B.sfull[0]);
         if (it.ntiles == 1) umma_commit(&B.qempty[qa.slot]);
       }
-      __syncwarp();
       if (has_two(it)) {
         if (!waitb(&B.qfull[qb.slot], qb.phase)) return false;
         tc_fence_after();
-        if (lane == 0) {
+        {
           issue_s(1, qb.slot, g & 1);
           umma_commit(&B.sfull[1]);
           if (it.ntiles == 1) umma_commit(&B.qempty[qb.slot]);
         }
-        __syncwarp();
       }
-      if (lane == 0) umma_commit(&B.kempty[g & 1]);  // both S products of tile g issued
-      __syncwarp();
+      umma_commit(&B.kempty[g & 1]);  // both S products of tile g issued
       return true;
     };
     int nread = 0;
     PItem cur;
-    bool ok = read_item(nread++, cur);
+    bool ok = read_item1(nread++, cur);
     QCursor q0 = {0, 0};        // cur's Q tiles: row tile 0 at q0, row tile 1 at q1
     QCursor q1 = q0.next(kQSlots);
     int g = 0;                  // tile index over all items (ring stage g & 1)
@@ -447,18 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k0 + kKeys > cur.ctx) {  // zero V rows at or past the context (0 x stale bytes)
         unsigned char* vt = smem + kOffK + s * kStageBytes + kOpBytes;
         const int first = cur.ctx - k0;
-        for (int idx = lane; idx < (kKeys - first) * 16; idx += 32)
+        for (int idx = 0; idx < (kKeys - first) * 16; ++idx)
           *reinterpret_cast<uint4*>(vt + kv_chunk_offset(first + (idx >> 4), idx & 15)) =
               make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
-        __syncwarp();
       }
       ok = waitb(&B.pfull[0], np0 & 1);
       ++np0;
       if (ok && !last) ok = waitb(&B.kfull[s ^ 1], ((g + 1) >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
-      if (lane == 0) {
+      {
         issue_pv(0, s, j > 0);
         if (last) umma_commit(&B.ofull[0]);
         if (!two) umma_commit(&B.vempty[s]);
@@ -469,13 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!two) umma_commit(&B.kempty[s ^ 1]);
         }
       }
-      __syncwarp();
       if (two) {
         ok = waitb(&B.pfull[1], np1 & 1);
         ++np1;
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
+        {
           issue_pv(1, s, j > 0);
           if (last) umma_commit(&B.ofull[1]);
           umma_commit(&B.vempty[s]);  // the producer reuses the stage
@@ -486,12 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&B.kempty[s ^ 1]);
           }
         }
-        __syncwarp();
       }
       ++g;
       if (last) {
         PItem nx;
-        ok = read_item(nread++, nx);
+        ok = read_item1(nread++, nx);
         if (!ok) break;
         q0 = two ? q1.next(kQSlots) : q1;  // the next item's Q tiles follow cur's
         q1 = q0.next(kQSlots);
@@ -502,7 +506,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++j;
       }
     }
-    if (lane == 0) {
       // every MMA issued has completed before the tensor memory is released
       umma_commit(B.drain);
       mbar_wait_bounded(B.drain, 0);
