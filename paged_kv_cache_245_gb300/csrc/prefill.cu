@@ -573,6 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // measured faster)
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
+            // a half whose keys no row of the warp sees adds nothing to the maximum
+            if (!__any_sync(kFull, !diag || k0 + 64 * h <= pos)) continue;
             uint32_t a[32], b[32];
             tmem_ld32(a, s_tm + 64 * h);
             tmem_ld32(b, s_tm + 64 * h + 32);
@@ -650,6 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // measured faster)
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
+            if (!__any_sync(kFull, !diag || k0 + 64 * h <= pos)) {
+              // no row of the warp sees a key of this half: its P is zero
+              uint32_t pz[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) pz[c] = 0u;
+              tmem_st32(s_tm + 32 * h, pz);
+              continue;
+            }
             uint32_t a[32], b[32];
             tmem_ld32(a, s_tm + 64 * h);
             tmem_ld32(b, s_tm + 64 * h + 32);
