@@ -707,15 +707,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 128-byte swizzled) and one tensor store.
         unsigned char* stg = smem + kOffOut + warp * 4096;
         const int tokw = it.q0 + wrow0 / G;
+        // the row's 128 columns in one tensor-memory round trip
+        uint32_t wa[32], wb[32], wc[32], wd[32];
+        tmem_ld32(wa, o_tm);
+        tmem_ld32(wb, o_tm + 32);
+        tmem_ld32(wc, o_tm + 64);
+        tmem_ld32(wd, o_tm + 96);
+        tmem_wait_ld(wa);
+        tmem_ready(wb);
+        tmem_ready(wc);
+        tmem_ready(wd);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t w[32], w2[32];
-          tmem_ld32(w, o_tm + 64 * h);
-          tmem_ld32(w2, o_tm + 64 * h + 32);
+          const uint32_t* w = h == 0 ? wa : wc;
+          const uint32_t* w2 = h == 0 ? wb : wd;
           if (lane == 0) bulk_wait_read();  // the warp's last store has read the staging
           __syncwarp();
-          tmem_wait_ld(w);
-          tmem_ready(w2);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t* x = c < 4 ? w + 8 * c : w2 + 8 * (c - 4);
